@@ -1,0 +1,370 @@
+"""Plain CPU oracle of one GPT2 training step: forward, backward, AdamW.
+
+TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+baseline leg use this module; the library never calls it, and it shares no
+code with the CUDA path (it imports numpy only).
+
+What it computes is the untiled definition of the step the NNTile pages
+describe: the tile-wise task graph only reorders this arithmetic
+("NNTile: a machine learning framework ..." review page, section "What carries
+the argument": every tensor split into tiles, every layer -- embedding, linear,
+layer norm, softmax, attention, cross-entropy, Adam -- written as tasks on
+tiles). The model is GPT2 (title of the first page) with pre-LN blocks (its
+reference "On Layer Normalization in the Transformer Architecture"), Layer
+Normalization (reference "Layer Normalization"), scaled dot-product causal
+attention (reference "Attention Is All You Need"), mean cross-entropy over all
+tokens (README "Minimal working GPT example", flag --loss-reduction=mean) and
+decoupled weight decay AdamW (reference "Decoupled Weight Decay
+Regularization"; README flags --optimizer=fusedadamw, --optimizer-eps=1e-8,
+--weight-decay=0.1, --lr=3e-4).
+
+Readings where the pages are silent (each also listed in the design notes):
+  * LayerNorm eps 1e-5, biased variance.
+  * GELU: the tanh approximation used by GPT2.
+  * attention scale 1/sqrt(head_dim); causal mask = probability exactly 0.
+  * no dropout, no gradient clipping, constant lr, AdamW betas (0.9, 0.999).
+  * weight decay applied to every parameter (one --weight-decay flag, no
+    exclusion list on the pages).
+  * tied LM head (wte used as the output projection, no LM bias); the two
+    gradient contributions to wte are summed.
+  * targets are the next token: window ``[B, S+1]``, inputs ``[:, :S]``,
+    targets ``[:, 1:]``.
+
+Arithmetic runs in ``dtype`` (float64 by default). Weight matrices are stored
+``[out, in]``; a linear layer is ``y = x W^T + b``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class GPT2Config:
+    n_layer: int
+    d_model: int
+    n_head: int
+    d_ff: int
+    vocab: int
+    seq: int
+    batch: int
+    ln_eps: float = 1e-5
+
+    @property
+    def head_dim(self) -> int:
+        return self.d_model // self.n_head
+
+
+@dataclass(frozen=True)
+class AdamWHyper:
+    lr: float = 3e-4
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+
+
+def param_order(cfg: GPT2Config):
+    """Names and shapes in the fixed parameter order (weights ``[out, in]``)."""
+    d, f = cfg.d_model, cfg.d_ff
+    out = [("wte", (cfg.vocab, d)), ("wpe", (cfg.seq, d))]
+    for l in range(cfg.n_layer):
+        p = f"h{l}."
+        out += [(p + "ln1.g", (d,)), (p + "ln1.b", (d,)),
+                (p + "qkv.w", (3 * d, d)), (p + "qkv.b", (3 * d,)),
+                (p + "o.w", (d, d)), (p + "o.b", (d,)),
+                (p + "ln2.g", (d,)), (p + "ln2.b", (d,)),
+                (p + "fc.w", (f, d)), (p + "fc.b", (f,)),
+                (p + "proj.w", (d, f)), (p + "proj.b", (d,))]
+    out += [("ln_f.g", (d,)), ("ln_f.b", (d,))]
+    return out
+
+
+# --------------------------------------------------------------------------
+# single operations
+# --------------------------------------------------------------------------
+
+def embedding_forward(ids, wte, wpe):
+    """x[b, s, :] = wte[ids[b, s], :] + wpe[s, :] (one add, in the arrays' dtype)."""
+    S = ids.shape[1]
+    return wte[ids.astype(np.int64)] + wpe[:S][None, :, :]
+
+
+def embedding_backward(dx, ids, dwte, dwpe):
+    """Scatter-add of the embedding gradient, returning updated copies.
+
+    ``dwte[ids[t]] += dx[t]`` for flat token index t = b*S + s taken in
+    increasing order, and ``dwpe[s] += dx[b, s]`` for b in increasing order.
+    The additions happen one at a time in the arrays' dtype, so a float32 call
+    fixes the exact rounding sequence.
+    """
+    B, S, d = dx.shape
+    dwte = dwte.copy()
+    dwpe = dwpe.copy()
+    flat_ids = ids.reshape(-1).astype(np.int64)
+    flat_dx = dx.reshape(B * S, d)
+    for t in range(B * S):
+        v = flat_ids[t]
+        dwte[v] = dwte[v] + flat_dx[t]
+    for b in range(B):
+        dwpe[:S] = dwpe[:S] + dx[b]
+    return dwte, dwpe
+
+
+def layernorm_forward(x, gamma, beta, eps):
+    """Layer normalisation over the last axis (biased variance).
+
+    Returns ``y = gamma * xhat + beta``, the mean and ``rstd = 1/sqrt(var + eps)``.
+    """
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (x - mu) * rstd
+    return gamma * xhat + beta, mu[..., 0], rstd[..., 0]
+
+
+def layernorm_backward(dy, x, mu, rstd, gamma):
+    """Gradients of :func:`layernorm_forward`.
+
+    With ``g = gamma * dy``: ``dx = rstd * (g - mean(g) - xhat * mean(g * xhat))``;
+    ``dgamma = sum over rows of dy * xhat``; ``dbeta = sum over rows of dy``.
+    """
+    xhat = (x - mu[..., None]) * rstd[..., None]
+    g = gamma * dy
+    dx = rstd[..., None] * (g - g.mean(axis=-1, keepdims=True)
+                            - xhat * (g * xhat).mean(axis=-1, keepdims=True))
+    rows = tuple(range(dy.ndim - 1))
+    return dx, (dy * xhat).sum(axis=rows), dy.sum(axis=rows)
+
+
+GELU_C = math.sqrt(2.0 / math.pi)
+GELU_A = 0.044715
+
+
+def gelu_forward(u):
+    """tanh-form GELU: 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3)))."""
+    return 0.5 * u * (1.0 + np.tanh(GELU_C * (u + GELU_A * u ** 3)))
+
+
+def gelu_backward(dg, u):
+    """dL/du for :func:`gelu_forward`, by the product and chain rules."""
+    t = np.tanh(GELU_C * (u + GELU_A * u ** 3))
+    dt_du = (1.0 - t * t) * GELU_C * (1.0 + 3.0 * GELU_A * u * u)
+    return dg * (0.5 * (1.0 + t) + 0.5 * u * dt_du)
+
+
+def causal_softmax_forward(scores):
+    """Row softmax over the last axis with key index > query index masked out.
+
+    ``scores[..., q, k]``; masked entries get probability exactly 0.
+    """
+    S_q, S_k = scores.shape[-2:]
+    mask = np.triu(np.ones((S_q, S_k), dtype=bool), k=1)
+    s = np.where(mask, -np.inf, scores)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def causal_softmax_backward(dP, P):
+    """dS = P * (dP - rowsum(dP * P)); masked entries (P = 0) give 0."""
+    return P * (dP - (dP * P).sum(axis=-1, keepdims=True))
+
+
+def split_heads(t, n_head):
+    B, S, d = t.shape
+    return t.reshape(B, S, n_head, d // n_head).transpose(0, 2, 1, 3)
+
+
+def merge_heads(t):
+    B, H, S, hd = t.shape
+    return t.transpose(0, 2, 1, 3).reshape(B, S, H * hd)
+
+
+def attention_forward(qkv, n_head):
+    """Causal multi-head attention on the fused ``[B, S, 3d]`` projection.
+
+    Columns ``[0, d)`` are queries, ``[d, 2d)`` keys, ``[2d, 3d)`` values; head h
+    owns columns ``h*hd .. h*hd+hd-1`` of each part.
+    Returns the merged output ``[B, S, d]`` and the probabilities ``[B, H, S, S]``.
+    """
+    d = qkv.shape[-1] // 3
+    q = split_heads(qkv[..., :d], n_head)
+    k = split_heads(qkv[..., d:2 * d], n_head)
+    v = split_heads(qkv[..., 2 * d:], n_head)
+    scale = 1.0 / math.sqrt(d // n_head)
+    P = causal_softmax_forward((q @ k.transpose(0, 1, 3, 2)) * scale)
+    return merge_heads(P @ v), P
+
+
+def attention_backward(do, qkv, P, n_head):
+    """Gradient of :func:`attention_forward` w.r.t. the fused projection."""
+    d = qkv.shape[-1] // 3
+    q = split_heads(qkv[..., :d], n_head)
+    k = split_heads(qkv[..., d:2 * d], n_head)
+    v = split_heads(qkv[..., 2 * d:], n_head)
+    scale = 1.0 / math.sqrt(d // n_head)
+    dO = split_heads(do, n_head)
+    dv = P.transpose(0, 1, 3, 2) @ dO
+    dP = dO @ v.transpose(0, 1, 3, 2)
+    dS = causal_softmax_backward(dP, P) * scale
+    dq = dS @ k
+    dk = dS.transpose(0, 1, 3, 2) @ q
+    return np.concatenate([merge_heads(dq), merge_heads(dk), merge_heads(dv)], axis=-1)
+
+
+def linear_forward(x, w, b=None):
+    """y = x W^T (+ b), W stored ``[out, in]``."""
+    y = x @ w.T
+    return y if b is None else y + b
+
+
+def cross_entropy_forward_backward(z, targets):
+    """Mean next-token cross-entropy and its gradient w.r.t. the logits.
+
+    ``loss = (1/T) sum_t [logsumexp(z_t) - z_t[y_t]]`` over all T tokens;
+    ``dz = (softmax(z) - onehot(y)) / T``.
+    """
+    T = z.shape[0]
+    m = z.max(axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    ssum = e.sum(axis=-1, keepdims=True)
+    lse = (m + np.log(ssum))[:, 0]
+    rows = np.arange(T)
+    loss = (lse - z[rows, targets]).sum() / T
+    dz = e / ssum
+    dz[rows, targets] -= 1.0
+    return loss, dz / T
+
+
+def adamw_update(w, g, m, v, step, hp: AdamWHyper):
+    """One decoupled-weight-decay Adam update (PyTorch AdamW order).
+
+    m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; mhat = m/(1-b1^t);
+    vhat = v/(1-b2^t); w <- w - lr*wd*w - lr*mhat/(sqrt(vhat)+eps), both terms
+    using the pre-update w.
+    """
+    m = hp.beta1 * m + (1.0 - hp.beta1) * g
+    v = hp.beta2 * v + (1.0 - hp.beta2) * g * g
+    mhat = m / (1.0 - hp.beta1 ** step)
+    vhat = v / (1.0 - hp.beta2 ** step)
+    w = w - hp.lr * hp.weight_decay * w - hp.lr * mhat / (np.sqrt(vhat) + hp.eps)
+    return w, m, v
+
+
+# --------------------------------------------------------------------------
+# whole step
+# --------------------------------------------------------------------------
+
+def _cast(params, dtype):
+    return {k: np.asarray(v, dtype=dtype) for k, v in params.items()}
+
+
+def forward(cfg: GPT2Config, params, windows, dtype=np.float64, keep=True):
+    """Forward pass; returns ``(loss, cache)``. ``windows`` is ``[B, S+1]``."""
+    p = _cast(params, dtype)
+    ids = windows[:, :cfg.seq].astype(np.int64)
+    tgt = windows[:, 1:cfg.seq + 1].astype(np.int64)
+    B, S, d = cfg.batch, cfg.seq, cfg.d_model
+    cache = {"ids": ids, "layers": []}
+    x = embedding_forward(ids, p["wte"], p["wpe"])
+    for l in range(cfg.n_layer):
+        q = f"h{l}."
+        c = {"x_in": x}
+        h1, c["mu1"], c["r1"] = layernorm_forward(x, p[q + "ln1.g"], p[q + "ln1.b"], cfg.ln_eps)
+        qkv = linear_forward(h1, p[q + "qkv.w"], p[q + "qkv.b"])
+        o, P = attention_forward(qkv, cfg.n_head)
+        x = x + linear_forward(o, p[q + "o.w"], p[q + "o.b"])
+        c["x_mid"] = x
+        h2, c["mu2"], c["r2"] = layernorm_forward(x, p[q + "ln2.g"], p[q + "ln2.b"], cfg.ln_eps)
+        u = linear_forward(h2, p[q + "fc.w"], p[q + "fc.b"])
+        g = gelu_forward(u)
+        x = x + linear_forward(g, p[q + "proj.w"], p[q + "proj.b"])
+        if keep:
+            c.update(h1=h1, qkv=qkv, o=o, P=P, h2=h2, u=u, g=g)
+            cache["layers"].append(c)
+    cache["x_L"] = x
+    y, cache["muf"], cache["rf"] = layernorm_forward(x, p["ln_f.g"], p["ln_f.b"], cfg.ln_eps)
+    cache["y"] = y
+    z = linear_forward(y.reshape(B * S, d), p["wte"])
+    loss, dz = cross_entropy_forward_backward(z, tgt.reshape(-1))
+    cache["z"] = z
+    cache["dz"] = dz
+    return loss, cache
+
+
+def backward(cfg: GPT2Config, params, cache, dtype=np.float64):
+    """Reverse-mode gradients of the mean loss w.r.t. every parameter."""
+    p = _cast(params, dtype)
+    B, S, d = cfg.batch, cfg.seq, cfg.d_model
+    grads = {}
+    dz = cache["dz"]
+    y = cache["y"].reshape(B * S, d)
+    dwte = dz.T @ y
+    dy = (dz @ p["wte"]).reshape(B, S, d)
+    dx, grads["ln_f.g"], grads["ln_f.b"] = layernorm_backward(
+        dy, cache["x_L"], cache["muf"], cache["rf"], p["ln_f.g"])
+    for l in reversed(range(cfg.n_layer)):
+        q = f"h{l}."
+        c = cache["layers"][l]
+        dg = dx @ p[q + "proj.w"]
+        grads[q + "proj.w"] = dx.reshape(B * S, d).T @ c["g"].reshape(B * S, -1)
+        grads[q + "proj.b"] = dx.sum(axis=(0, 1))
+        du = gelu_backward(dg, c["u"])
+        grads[q + "fc.w"] = du.reshape(B * S, -1).T @ c["h2"].reshape(B * S, d)
+        grads[q + "fc.b"] = du.sum(axis=(0, 1))
+        dh2 = du @ p[q + "fc.w"]
+        dln, grads[q + "ln2.g"], grads[q + "ln2.b"] = layernorm_backward(
+            dh2, c["x_mid"], c["mu2"], c["r2"], p[q + "ln2.g"])
+        dx = dx + dln
+        do = dx @ p[q + "o.w"]
+        grads[q + "o.w"] = dx.reshape(B * S, d).T @ c["o"].reshape(B * S, d)
+        grads[q + "o.b"] = dx.sum(axis=(0, 1))
+        dqkv = attention_backward(do, c["qkv"], c["P"], cfg.n_head)
+        grads[q + "qkv.w"] = dqkv.reshape(B * S, -1).T @ c["h1"].reshape(B * S, d)
+        grads[q + "qkv.b"] = dqkv.sum(axis=(0, 1))
+        dh1 = dqkv @ p[q + "qkv.w"]
+        dln, grads[q + "ln1.g"], grads[q + "ln1.b"] = layernorm_backward(
+            dh1, c["x_in"], c["mu1"], c["r1"], p[q + "ln1.g"])
+        dx = dx + dln
+    dwpe = np.zeros_like(p["wpe"])
+    grads["wte"], grads["wpe"] = embedding_backward(dx, cache["ids"], dwte, dwpe)
+    return grads
+
+
+def adamw_step(params, grads, m, v, step, hp: AdamWHyper, dtype=np.float64):
+    """AdamW over every parameter; returns new (params, m, v) dictionaries."""
+    new_p, new_m, new_v = {}, {}, {}
+    for k in params:
+        w = np.asarray(params[k], dtype=dtype)
+        mk = np.zeros_like(w) if m is None else np.asarray(m[k], dtype=dtype)
+        vk = np.zeros_like(w) if v is None else np.asarray(v[k], dtype=dtype)
+        new_p[k], new_m[k], new_v[k] = adamw_update(w, np.asarray(grads[k], dtype=dtype),
+                                                    mk, vk, step, hp)
+    return new_p, new_m, new_v
+
+
+def train_step(cfg: GPT2Config, params, windows, hp: AdamWHyper = AdamWHyper(),
+               m=None, v=None, step=1, dtype=np.float64):
+    """forward + backward + AdamW; returns (loss, grads, new_params, new_m, new_v)."""
+    loss, cache = forward(cfg, params, windows, dtype)
+    grads = backward(cfg, params, cache, dtype)
+    new_p, new_m, new_v = adamw_step(params, grads, m, v, step, hp, dtype)
+    return loss, grads, new_p, new_m, new_v
+
+
+def step_flops(cfg: GPT2Config) -> float:
+    """Algorithmic FLOPs of one step: 3x the forward matmuls plus causal attention.
+
+    Forward matmuls per token: 2*(d*3d + d*d + 2*d*f) per layer plus 2*d*V for
+    the LM head; attention QK^T and PV count only the causal half
+    (S(S+1)/2 key positions per query row, 2*hd flops each, two products).
+    Backward is twice the forward. Elementwise work is not counted.
+    """
+    d, f, V, S, B, L = cfg.d_model, cfg.d_ff, cfg.vocab, cfg.seq, cfg.batch, cfg.n_layer
+    T = B * S
+    dense = 2.0 * T * (L * (3 * d * d + d * d + 2 * d * f) + d * V)
+    attn = L * B * cfg.n_head * 2 * (2.0 * cfg.head_dim * S * (S + 1) / 2)
+    return 3.0 * (dense + attn)

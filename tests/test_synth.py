@@ -1,0 +1,37 @@
+"""Seeded input generators: splitmix64 against its published sequence, recipes."""
+import numpy as np
+
+from tile_task_transformer_gb300 import synth
+
+
+def test_splitmix64_published_sequence():
+    # sequence of the splitmix64 generator seeded with 1234567 (state advanced by
+    # the golden-ratio increment before each output), as published with the
+    # algorithm's reference implementations
+    g = 0x9E3779B97F4A7C15
+    got = [int(synth.splitmix64(np.uint64((1234567 + k * g) % 2 ** 64))) for k in range(5)]
+    assert got == [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                   4593380528125082431, 16408922859458223821]
+
+
+def test_normal_statistics_and_determinism():
+    a = synth.normal_f32(5, 3, 200001, 0.02)
+    assert a.dtype == np.float32
+    assert abs(a.mean()) < 3e-4 and abs(a.std() - 0.02) < 3e-4
+    np.testing.assert_array_equal(a[:1000], synth.normal_f32(5, 3, 1000, 0.02))
+
+
+def test_token_windows_range_and_shape():
+    w = synth.token_windows(1, 4, 1024, 50257)
+    assert w.shape == (4, 1025) and w.dtype == np.uint16
+    assert w.max() < 50257
+    # roughly uniform
+    assert abs(w.astype(np.float64).mean() - 25128) < 600
+
+
+def test_param_recipe():
+    p = synth.gpt2_params(0, 2, 64, 256, 256, 32)
+    names = [n for n, _ in synth.param_names_shapes(2, 64, 256, 256, 32)]
+    assert list(p) == names and len(names) == 2 + 12 * 2 + 2
+    assert np.all(p["h0.ln1.g"] == 1) and np.all(p["ln_f.b"] == 0)
+    assert sum(v.size for v in p.values()) == 118528
