@@ -1,0 +1,196 @@
+"""Whole training step through the C ABI against the CPU oracle (GPU).
+
+Tolerances: loss within 1e-3 absolute; gradients, AdamW moments and updated
+weights within 2e-2 normwise max relative error (max|gpu - ref| / max|ref| per
+tensor); the AdamW weight change also within 2e-2 of the oracle's change on
+the elements whose gradient is clearly resolved.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import gpt2 as O  # noqa: E402
+from tile_task_transformer_gb300 import nnt, synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TINY = O.GPT2Config(n_layer=2, d_model=64, n_head=4, d_ff=256, vocab=256, seq=32, batch=2)
+TINY_TILES = {"seq_tile": 16, "embd_tile": 32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nnt.lib()
+
+
+def relerr(a, r):
+    return float(np.abs(np.asarray(a, np.float64) - r).max() / max(np.abs(r).max(), 1e-30))
+
+
+def make(cfg, dtype, tiles, **kw):
+    return nnt.Model(cfg.n_layer, cfg.d_model, cfg.n_head, cfg.d_ff, cfg.vocab, cfg.seq, cfg.batch,
+                     dtype=dtype, tiles=tiles, **kw)
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_step(cfg, seed):
+    key = (cfg, seed)
+    if key not in _ORACLE_CACHE:
+        params = synth.gpt2_params(seed, cfg.n_layer, cfg.d_model, cfg.d_ff, cfg.vocab, cfg.seq)
+        win = synth.token_windows(seed, cfg.batch, cfg.seq, cfg.vocab)
+        loss, grads, new_p, new_m, new_v = O.train_step(cfg, params, win)
+        _ORACLE_CACHE[key] = (params, win, loss, grads, new_p, new_m, new_v)
+    return _ORACLE_CACHE[key]
+
+
+def run_step(cfg, dtype, tiles, seed=0, **kw):
+    params, win, *_ = oracle_step(cfg, seed)
+    m = make(cfg, dtype, tiles, **kw)
+    m.set_params(params)
+    loss = m.forward(win)
+    m.backward()
+    grads = m.grads()
+    m.adamw_step()
+    out = dict(loss=loss, grads=grads, params=m.params(),
+               m={n: m.get_adam_state(i, 0) for i, n in enumerate(m.names)},
+               v={n: m.get_adam_state(i, 1) for i, n in enumerate(m.names)})
+    m.close()
+    return out
+
+
+def check_step(cfg, got, seed=0, tol=2e-2, lr=3e-4):
+    """Loss, gradients, moments and updated weights against the oracle.
+
+    Updated weights: normwise within `tol` for tensors that start non-zero; the
+    weight change within `tol` on elements whose oracle gradient is resolved
+    (|g| > 0.2 max|g|); and everywhere within 2*lr*(1 + tol) + tol*max|w| -- the
+    most a sign flip of an unresolved near-zero gradient can move a weight in
+    one AdamW step (at t = 1 each element moves by about lr*sign(g)).
+    """
+    params, win, loss, grads, new_p, new_m, new_v = oracle_step(cfg, seed)
+    assert abs(got["loss"] - loss) < 1e-3, (got["loss"], loss)
+    for n in grads:
+        assert relerr(got["grads"][n], grads[n]) < tol, (n, relerr(got["grads"][n], grads[n]))
+        assert relerr(got["m"][n], new_m[n]) < tol, n
+        assert relerr(got["v"][n], new_v[n]) < 2 * tol, n
+        w_gpu = got["params"][n].astype(np.float64)
+        if np.abs(params[n]).max() > 0:
+            assert relerr(w_gpu, new_p[n]) < tol, n
+        bound = 2 * lr * (1 + tol) + tol * np.abs(new_p[n]).max()
+        assert np.abs(w_gpu - new_p[n]).max() <= bound, n
+        g = grads[n]
+        sel = np.abs(g) > 0.2 * np.abs(g).max()
+        if sel.any():
+            dw_ref = (new_p[n] - params[n])[sel]
+            dw = (w_gpu - params[n])[sel]
+            assert relerr(dw, dw_ref) < tol, n
+
+
+def test_tiny_fp32_step_matches_oracle():
+    got = run_step(TINY, nnt.F32, TINY_TILES)
+    check_step(TINY, got, tol=1e-4)
+
+
+@pytest.mark.parametrize("tiles", [
+    {},
+    {"seq_tile": 8},
+    {"seq_tile": 16, "embd_tile": 48, "inner_tile": 96, "head_tile": 2, "vocab_tile": 80},
+    {"batch_tile": 1, "seq_tile": 32, "embd_tile": 16, "head_tile": 1},
+])
+def test_tiny_fp32_tile_invariance(tiles):
+    ref = run_step(TINY, nnt.F32, TINY_TILES)
+    got = run_step(TINY, nnt.F32, tiles)
+    assert abs(got["loss"] - ref["loss"]) < 1e-5
+    for n in ref["grads"]:
+        assert relerr(got["grads"][n], ref["grads"][n].astype(np.float64)) < 1e-4, n
+    # embedding bookkeeping is order-fixed: the gradient of wpe sums the same
+    # fp32 values in the same order under every tiling of the token axis
+    np.testing.assert_array_equal(got["grads"]["wpe"], ref["grads"]["wpe"])
+
+
+@pytest.mark.parametrize("n_streams,graph", [(1, False), (4, False), (3, True)])
+def test_tiny_fp32_streams_and_graphs(n_streams, graph):
+    got = run_step(TINY, nnt.F32, TINY_TILES, n_streams=n_streams, use_cuda_graph=graph)
+    check_step(TINY, got, tol=1e-4)
+
+
+def test_tiny_bf16_step_matches_oracle():
+    got = run_step(TINY, nnt.BF16, TINY_TILES)
+    check_step(TINY, got)
+
+
+def test_tiny_bf16_cuda_core_and_tensor_core_agree():
+    a = run_step(TINY, nnt.BF16, TINY_TILES, gemm_backend=0)
+    b = run_step(TINY, nnt.BF16, TINY_TILES, gemm_backend=1)
+    assert abs(a["loss"] - b["loss"]) < 1e-3
+    for n in a["grads"]:
+        assert relerr(a["grads"][n], b["grads"][n].astype(np.float64)) < 2e-2, n
+
+
+def test_call_order_and_bad_tokens():
+    m = make(TINY, nnt.F32, TINY_TILES)
+    with pytest.raises(nnt.NNTError) as e:
+        m.backward()
+    assert e.value.status == nnt.ERR_STATE
+    with pytest.raises(nnt.NNTError) as e:
+        m.adamw_step()
+    assert e.value.status == nnt.ERR_STATE
+    bad = synth.token_windows(0, TINY.batch, TINY.seq, TINY.vocab)
+    bad[1, 5] = 300
+    with pytest.raises(nnt.NNTError) as e:
+        m.forward(bad)
+    assert e.value.status == nnt.ERR_INVALID_ARG
+    # the model stays usable
+    loss = m.forward(synth.token_windows(0, TINY.batch, TINY.seq, TINY.vocab))
+    assert np.isfinite(loss)
+    m.backward()
+    m.adamw_step()
+    m.close()
+
+
+def test_device_init_matches_host_generator():
+    m = make(TINY, nnt.F32, TINY_TILES, seed=123)
+    host = synth.gpt2_params(123, TINY.n_layer, TINY.d_model, TINY.d_ff, TINY.vocab, TINY.seq)
+    for i, n in enumerate(m.names):
+        d = m.get_param(i)
+        # same generator on both sides; the device's double log/sincos may differ
+        # from the host's in the last double bit, which can move the fp32 rounding
+        diff = np.abs(d - host[n])
+        assert (diff <= np.spacing(np.abs(host[n]).astype(np.float32))).all(), n
+        assert (diff == 0).mean() > 0.99, n
+    m.close()
+
+
+def test_zero_embedding_gives_log_vocab():
+    params = synth.gpt2_params(0, TINY.n_layer, TINY.d_model, TINY.d_ff, TINY.vocab, TINY.seq)
+    m = make(TINY, nnt.BF16, TINY_TILES)
+    m.set_params(params)
+    m.set_param(0, np.zeros_like(params["wte"]))
+    loss = m.forward(synth.token_windows(0, TINY.batch, TINY.seq, TINY.vocab))
+    assert abs(loss - np.log(TINY.vocab)) < 1e-5
+    m.close()
+
+
+def test_multi_step_loss_decreases_and_tracks_oracle():
+    cfg = TINY
+    params = synth.gpt2_params(5, cfg.n_layer, cfg.d_model, cfg.d_ff, cfg.vocab, cfg.seq)
+    win = synth.token_windows(5, cfg.batch, cfg.seq, cfg.vocab)
+    m = make(cfg, nnt.F32, TINY_TILES, use_cuda_graph=True)
+    m.set_params(params)
+    p, mm, vv = params, None, None
+    hp = O.AdamWHyper(lr=1e-2)
+    losses, ref = [], []
+    for step in range(1, 6):
+        losses.append(m.forward(win))
+        m.backward()
+        m.adamw_step(lr=1e-2)
+        l, g, p, mm, vv = O.train_step(cfg, p, win, hp, mm, vv, step)
+        ref.append(l)
+    m.close()
+    assert losses[-1] < losses[0] - 0.05
+    np.testing.assert_allclose(losses, ref, atol=1e-3)

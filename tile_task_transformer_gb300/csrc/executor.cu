@@ -1,0 +1,227 @@
+// Tile-task executor: dependency inference, stream schedule, launch, trace.
+#include <algorithm>
+#include <unordered_map>
+
+#include "common.cuh"
+#include "executor.h"
+
+namespace nnt {
+
+int Program::add(Task t) {
+  tasks_.push_back(std::move(t));
+  return (int)tasks_.size() - 1;
+}
+
+void Program::finalize(int n_streams) {
+  n_streams_ = std::max(1, n_streams);
+  const size_t n = tasks_.size();
+  deps_.assign(n, {});
+  struct TileState {
+    int writer = -1;
+    std::vector<int> readers;
+  };
+  std::unordered_map<int64_t, TileState> state;
+  std::unordered_map<int64_t, int> modes;
+  for (size_t i = 0; i < n; ++i) {
+    modes.clear();
+    for (const TileUse& u : tasks_[i].uses) modes[u.tile] |= u.mode;
+    std::vector<int>& d = deps_[i];
+    for (const auto& kv : modes) {
+      TileState& s = state[kv.first];
+      if (s.writer >= 0) d.push_back(s.writer);              // RAW, WAW
+      if (kv.second & ACC_W) d.insert(d.end(), s.readers.begin(), s.readers.end());  // WAR
+    }
+    for (const auto& kv : modes) {
+      TileState& s = state[kv.first];
+      if (kv.second & ACC_W) {
+        s.writer = (int)i;
+        s.readers.clear();
+      } else {
+        s.readers.push_back((int)i);
+      }
+    }
+    std::sort(d.begin(), d.end());
+    d.erase(std::unique(d.begin(), d.end()), d.end());
+    d.erase(std::remove(d.begin(), d.end(), (int)i), d.end());
+  }
+
+  bool has_copy = false;
+  for (const Task& t : tasks_) has_copy |= t.copy_engine != 0;
+  const int ns = n_streams_ + (has_copy ? 1 : 0);
+  const int copy_stream = n_streams_;
+  std::vector<int> last_on(ns, -1);
+  std::vector<std::vector<int>> frontier(n, std::vector<int>(ns, -1));
+  n_edges_ = 0;
+  std::vector<char> used(ns, 0);
+  for (size_t i = 0; i < n; ++i) {
+    Task& t = tasks_[i];
+    int s;
+    if (t.copy_engine) {
+      s = copy_stream;
+    } else {
+      // continue the stream whose latest task is one of our dependencies
+      s = -1;
+      for (int c = 0; c < n_streams_; ++c) {
+        if (last_on[c] < 0) continue;
+        if (std::binary_search(deps_[i].begin(), deps_[i].end(), last_on[c]) &&
+            (s < 0 || last_on[c] > last_on[s]))
+          s = c;
+      }
+      if (s < 0) {  // least recently used compute stream
+        s = 0;
+        for (int c = 1; c < n_streams_; ++c)
+          if (last_on[c] < last_on[s]) s = c;
+      }
+    }
+    t.stream = s;
+    used[s] = 1;
+    std::vector<int> F(ns, -1);
+    if (last_on[s] >= 0) {
+      F = frontier[last_on[s]];
+      F[s] = std::max(F[s], last_on[s]);
+    }
+    t.waits.clear();
+    for (auto it = deps_[i].rbegin(); it != deps_[i].rend(); ++it) {
+      const int dep = *it;
+      const int sd = tasks_[dep].stream;
+      if (dep <= F[sd]) continue;  // already implied
+      t.waits.push_back(dep);
+      tasks_[dep].record = true;
+      ++n_edges_;
+      for (int c = 0; c < ns; ++c) F[c] = std::max(F[c], frontier[dep][c]);
+      F[sd] = std::max(F[sd], dep);
+    }
+    frontier[i] = F;
+    last_on[s] = (int)i;
+  }
+  n_streams_used_ = 0;
+  for (char u : used) n_streams_used_ += u;
+}
+
+Executor::~Executor() {
+  for (auto g : graphs_)
+    if (g) cudaGraphExecDestroy(g);
+  for (auto e : task_events_) cudaEventDestroy(e);
+  for (auto e : t0_) cudaEventDestroy(e);
+  for (auto e : t1_) cudaEventDestroy(e);
+  for (auto e : fork_join_) cudaEventDestroy(e);
+  for (size_t i = 1; i < streams_.size(); ++i) cudaStreamDestroy(streams_[i]);
+}
+
+nnt_status Executor::init(cudaStream_t main, int n_streams, bool need_copy_stream, bool trace,
+                          int n_types) {
+  main_ = main;
+  n_compute_ = std::max(1, n_streams);
+  trace_ = trace;
+  streams_.assign(1, main);
+  const int total = n_compute_ + (need_copy_stream ? 1 : 0);
+  for (int i = 1; i < total; ++i) {
+    cudaStream_t s;
+    NNT_CUDA_TRY(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    streams_.push_back(s);
+  }
+  if (need_copy_stream && total == 1) {
+    cudaStream_t s;
+    NNT_CUDA_TRY(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    streams_.push_back(s);
+  }
+  fork_join_.resize(streams_.size() + 1);
+  for (auto& e : fork_join_) NNT_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  graphs_.assign(8, nullptr);
+  n_types_ = n_types;
+  reset_trace();
+  return NNT_OK;
+}
+
+void Executor::reset_trace() {
+  type_launches_.assign(n_types_, 0);
+  type_ms_.assign(n_types_, 0.0);
+  type_flops_.assign(n_types_, 0.0);
+  type_bytes_.assign(n_types_, 0.0);
+}
+
+nnt_status Executor::ensure_events(size_t n) {
+  while (task_events_.size() < n) {
+    cudaEvent_t e;
+    NNT_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    task_events_.push_back(e);
+  }
+  if (trace_) {
+    while (t0_.size() < n) {
+      cudaEvent_t a, b;
+      NNT_CUDA_TRY(cudaEventCreate(&a));
+      NNT_CUDA_TRY(cudaEventCreate(&b));
+      t0_.push_back(a);
+      t1_.push_back(b);
+    }
+  }
+  return NNT_OK;
+}
+
+nnt_status Executor::launch_all(Program& p, bool traced) {
+  NNT_TRY(ensure_events(p.size()));
+  const int ns = (int)streams_.size();
+  NNT_CUDA_TRY(cudaEventRecord(fork_join_[0], main_));
+  for (int s = 1; s < ns; ++s) NNT_CUDA_TRY(cudaStreamWaitEvent(streams_[s], fork_join_[0], 0));
+  for (size_t i = 0; i < p.tasks_.size(); ++i) {
+    Task& t = p.tasks_[i];
+    cudaStream_t s = streams_[std::min(t.stream, ns - 1)];
+    for (int w : t.waits) NNT_CUDA_TRY(cudaStreamWaitEvent(s, task_events_[w], 0));
+    if (traced) NNT_CUDA_TRY(cudaEventRecord(t0_[i], s));
+    NNT_TRY(t.fn(s));
+    if (traced) NNT_CUDA_TRY(cudaEventRecord(t1_[i], s));
+    if (t.record) NNT_CUDA_TRY(cudaEventRecord(task_events_[i], s));
+  }
+  for (int s = 1; s < ns; ++s) {
+    NNT_CUDA_TRY(cudaEventRecord(fork_join_[s], streams_[s]));
+    NNT_CUDA_TRY(cudaStreamWaitEvent(main_, fork_join_[s], 0));
+  }
+  return NNT_OK;
+}
+
+nnt_status Executor::run(Program& p, int graph_slot) {
+  if (graph_slot < 0 || trace_) return launch_all(p, trace_);
+  if ((size_t)graph_slot >= graphs_.size()) graphs_.resize(graph_slot + 1, nullptr);
+  if (!graphs_[graph_slot]) {
+    cudaGraph_t g = nullptr;
+    NNT_CUDA_TRY(cudaStreamBeginCapture(main_, cudaStreamCaptureModeThreadLocal));
+    nnt_status st = launch_all(p, false);
+    cudaError_t e = cudaStreamEndCapture(main_, &g);
+    if (st != NNT_OK) {
+      if (g) cudaGraphDestroy(g);
+      return st;
+    }
+    if (e != cudaSuccess) {
+      set_thread_error("graph capture failed: %s", cudaGetErrorString(e));
+      return NNT_ERR_CUDA;
+    }
+    cudaGraphExec_t ge = nullptr;
+    e = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      set_thread_error("graph instantiate failed: %s", cudaGetErrorString(e));
+      return NNT_ERR_CUDA;
+    }
+    graphs_[graph_slot] = ge;
+  }
+  NNT_CUDA_TRY(cudaGraphLaunch(graphs_[graph_slot], main_));
+  return NNT_OK;
+}
+
+nnt_status Executor::collect_trace(const Program& p) {
+  if (!trace_) return NNT_OK;
+  for (size_t i = 0; i < p.tasks_.size(); ++i) {
+    const Task& t = p.tasks_[i];
+    float ms = 0.f;
+    NNT_CUDA_TRY(cudaEventElapsedTime(&ms, t0_[i], t1_[i]));
+    if (t.type >= 0 && t.type < n_types_) {
+      type_launches_[t.type] += 1;
+      type_ms_[t.type] += ms;
+      type_flops_[t.type] += t.flops;
+      type_bytes_[t.type] += t.bytes;
+    }
+  }
+  return NNT_OK;
+}
+
+}  // namespace nnt

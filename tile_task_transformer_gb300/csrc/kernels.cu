@@ -1,0 +1,997 @@
+// Memory-bound tile kernels of the GPT2 step: embedding gather/scatter, layer
+// norm, causal softmax, GELU, cross-entropy, AdamW, column sums, init.
+//
+// The operations are the tile-wise layers the NNTile review page lists
+// (pith.science, "What carries the argument": embedding, layer norm, softmax,
+// attention, cross-entropy, Adam). All of them stream HBM once: rows are held
+// in registers between the reduction and the write, loads and stores are
+// 16-byte vectors, and reductions use warp shuffles. Reductions that produce
+// parameter gradients write per-CTA partials that a second kernel sums in a
+// fixed order, so results do not depend on scheduling.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+
+#include "kernels.cuh"
+
+namespace nnt {
+
+static __device__ uint32_t g_device_error = 0;
+
+uint32_t* device_error_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<uint32_t*>(p);
+}
+
+// Copies the word to pinned-free host memory; synchronises `st`.
+nnt_status read_and_clear_device_error(uint32_t* code_host, cudaStream_t st) {
+  uint32_t zero = 0;
+  NNT_CUDA_TRY(cudaMemcpyFromSymbolAsync(code_host, g_device_error, 4, 0, cudaMemcpyDeviceToHost, st));
+  NNT_CUDA_TRY(cudaMemcpyToSymbolAsync(g_device_error, &zero, 4, 0, cudaMemcpyHostToDevice, st));
+  NNT_CUDA_TRY(cudaStreamSynchronize(st));
+  return NNT_OK;
+}
+
+static thread_local char t_err[512] = "";
+void set_thread_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof t_err, fmt, ap);
+  va_end(ap);
+}
+const char* thread_error() { return t_err; }
+
+static inline nnt_status launch_check(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_thread_error("launch of %s failed: %s", what, cudaGetErrorString(e));
+    return NNT_ERR_CUDA;
+  }
+  return NNT_OK;
+}
+
+static constexpr float kLog2e = 1.4426950408889634f;
+
+// =====================================================================
+// embedding
+// =====================================================================
+
+// x[row(b,s), :] = wte[id(b,s), :] + wpe[s, :]; one thread per 4 columns.
+__global__ void embedding_fwd_kernel(const uint16_t* __restrict__ ids, int64_t ids_stride,
+                                     const float* __restrict__ wte, const float* __restrict__ wpe,
+                                     float* __restrict__ x, int d, int vocab, TokMap tm, int b0,
+                                     int nb, int s0, int ns) {
+  const int nv = d >> 2;
+  const int64_t total = (int64_t)nb * ns * nv;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % nv);
+    const int64_t tok = i / nv;
+    const int b = b0 + (int)(tok / ns), s = s0 + (int)(tok % ns);
+    const int id = ids[(int64_t)b * ids_stride + s];
+    float4 out;
+    if (id < vocab) {
+      float4 e = load4(wte + (int64_t)id * d + 4 * c);
+      float4 p = load4(wpe + (int64_t)s * d + 4 * c);
+      out = make_float4(e.x + p.x, e.y + p.y, e.z + p.z, e.w + p.w);
+    } else {
+      if (c == 0) atomicOr(&g_device_error, DEVERR_TOKEN_RANGE);
+      out = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    store4(x + tm.row(b, s) * d + 4 * c, out);
+  }
+}
+
+nnt_status launch_embedding_fwd(const uint16_t* ids, int64_t ids_stride, const float* wte,
+                                const float* wpe, float* x, int d, int vocab, TokMap tm, int b0,
+                                int nb, int s0, int ns, cudaStream_t st) {
+  NNT_CHECK_ARG(d % 4 == 0 && d > 0, "embedding: d must be a positive multiple of 4");
+  int64_t total = (int64_t)nb * ns * (d / 4);
+  if (total == 0) return NNT_OK;
+  int grid = (int)std::min<int64_t>(ceil_div(total, 256), 152 * 16);
+  embedding_fwd_kernel<<<grid, 256, 0, st>>>(ids, ids_stride, wte, wpe, x, d, vocab, tm, b0, nb, s0,
+                                             ns);
+  return launch_check("embedding_fwd");
+}
+
+// One CTA sorts the keys id*T + t (t = b*S + s) of all T tokens with a bitonic
+// network in shared memory. Keys are unique, so the order of tokens that share
+// an id is their token order.
+__global__ void token_sort_kernel(const uint16_t* __restrict__ ids, int64_t ids_stride, int B,
+                                  int S, uint32_t* __restrict__ keys_out, int npow2) {
+  extern __shared__ uint32_t sk[];
+  const int T = B * S;
+  for (int i = threadIdx.x; i < npow2; i += blockDim.x) {
+    uint32_t k = 0xFFFFFFFFu;
+    if (i < T) {
+      int b = i / S, s = i % S;
+      k = (uint32_t)ids[(int64_t)b * ids_stride + s] * (uint32_t)T + (uint32_t)i;
+    }
+    sk[i] = k;
+  }
+  __syncthreads();
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < npow2 / 2; i += blockDim.x) {
+        int lo = 2 * i - (i & (stride - 1));
+        int hi = lo + stride;
+        bool up = ((lo & size) == 0);
+        uint32_t a = sk[lo], c = sk[hi];
+        if ((a > c) == up) {
+          sk[lo] = c;
+          sk[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < T; i += blockDim.x) keys_out[i] = sk[i];
+}
+
+nnt_status launch_token_sort(const uint16_t* ids, int64_t ids_stride, int B, int S,
+                             uint32_t* keys_out, cudaStream_t st) {
+  const int T = B * S;
+  NNT_CHECK_ARG(T > 0 && T <= 16384, "token sort: batch*seq must be in [1, 16384] (got %d)", T);
+  int npow2 = 1;
+  while (npow2 < T) npow2 <<= 1;
+  size_t smem = (size_t)npow2 * 4;
+  if (smem > 48 * 1024)
+    NNT_CUDA_TRY(cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem));
+  token_sort_kernel<<<1, 1024, smem, st>>>(ids, ids_stride, B, S, keys_out, npow2);
+  return launch_check("token_sort");
+}
+
+// CTA i handles sorted position i when it starts a run of equal ids: it adds the
+// dx rows of that run, in token order, onto dwte[id].
+__global__ void embedding_scatter_kernel(const uint32_t* __restrict__ keys, int T,
+                                         const float* __restrict__ dx, TokMap tm, int S,
+                                         float* __restrict__ dwte, int d, int vocab) {
+  const int i = blockIdx.x;
+  const uint32_t id = keys[i] / (uint32_t)T;
+  if (i > 0 && keys[i - 1] / (uint32_t)T == id) return;
+  if (id >= (uint32_t)vocab) return;
+  int j_end = i + 1;
+  while (j_end < T && keys[j_end] / (uint32_t)T == id) ++j_end;
+  const int nv = d >> 2;
+  for (int c = threadIdx.x; c < nv; c += blockDim.x) {
+    float4 acc = load4(dwte + (int64_t)id * d + 4 * c);
+    for (int j = i; j < j_end; ++j) {
+      int t = (int)(keys[j] % (uint32_t)T);
+      float4 g = load4(dx + tm.row(t / S, t % S) * d + 4 * c);
+      acc.x += g.x;
+      acc.y += g.y;
+      acc.z += g.z;
+      acc.w += g.w;
+    }
+    store4(dwte + (int64_t)id * d + 4 * c, acc);
+  }
+}
+
+nnt_status launch_embedding_scatter(const uint32_t* keys, int T, const float* dx, TokMap tm, int S,
+                                    float* dwte, int d, int vocab, cudaStream_t st) {
+  NNT_CHECK_ARG(d % 4 == 0, "embedding scatter: d must be a multiple of 4");
+  if (T == 0) return NNT_OK;
+  int threads = std::min(256, std::max(32, (d / 4 + 31) / 32 * 32));
+  embedding_scatter_kernel<<<T, threads, 0, st>>>(keys, T, dx, tm, S, dwte, d, vocab);
+  return launch_check("embedding_scatter");
+}
+
+__global__ void wpe_grad_kernel(const float* __restrict__ dx, TokMap tm, int B, int s0, int ns,
+                                int d, float* __restrict__ dwpe, int accumulate) {
+  const int nv = d >> 2;
+  const int64_t total = (int64_t)ns * nv;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int s = s0 + (int)(i / nv), c = (int)(i % nv);
+    float4 acc = accumulate ? load4(dwpe + (int64_t)s * d + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b = 0; b < B; ++b) {
+      float4 g = load4(dx + tm.row(b, s) * d + 4 * c);
+      acc.x += g.x;
+      acc.y += g.y;
+      acc.z += g.z;
+      acc.w += g.w;
+    }
+    store4(dwpe + (int64_t)s * d + 4 * c, acc);
+  }
+}
+
+nnt_status launch_wpe_grad(const float* dx, TokMap tm, int B, int s0, int ns, int d, float* dwpe,
+                           int accumulate, cudaStream_t st) {
+  int64_t total = (int64_t)ns * (d / 4);
+  if (total == 0) return NNT_OK;
+  int grid = (int)std::min<int64_t>(ceil_div(total, 256), 152 * 8);
+  wpe_grad_kernel<<<grid, 256, 0, st>>>(dx, tm, B, s0, ns, d, dwpe, accumulate);
+  return launch_check("wpe_grad");
+}
+
+// =====================================================================
+// layer norm (reference "Layer Normalization"; pre-LN blocks)
+// =====================================================================
+
+// TPR threads per row, each holding up to MAXV float4 of the row in registers.
+template <int TPR, int MAXV, typename T>
+__global__ void ln_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g,
+                              const float* __restrict__ b, T* __restrict__ y,
+                              float* __restrict__ mean, float* __restrict__ rstd, int64_t rows,
+                              int cols, float eps) {
+  __shared__ float red[32];
+  const int rpc = blockDim.x / TPR;
+  const int lane = threadIdx.x % TPR;
+  const int64_t row = (int64_t)blockIdx.x * rpc + threadIdx.x / TPR;
+  const bool active = row < rows;
+  const int nv = cols >> 2;
+  const float* xr = x + (active ? row : 0) * cols;
+  float4 v[MAXV];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (active && c < nv) {
+      v[i] = load4(xr + 4 * c);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    } else {
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  s = group_sum<TPR>(s, red);
+  const float mu = s / (float)cols;
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (active && c < nv) {
+      float a = v[i].x - mu, bb = v[i].y - mu, cc = v[i].z - mu, dd = v[i].w - mu;
+      ss += (a * a + bb * bb) + (cc * cc + dd * dd);
+    }
+  }
+  ss = group_sum<TPR>(ss, red);
+  const float rs = 1.0f / sqrtf(ss / (float)cols + eps);
+  if (!active) return;
+  T* yr = y + row * cols;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (c < nv) {
+      float4 gv = load4(g + 4 * c), bv = load4(b + 4 * c);
+      float4 o;
+      o.x = (v[i].x - mu) * rs * gv.x + bv.x;
+      o.y = (v[i].y - mu) * rs * gv.y + bv.y;
+      o.z = (v[i].z - mu) * rs * gv.z + bv.z;
+      o.w = (v[i].w - mu) * rs * gv.w + bv.w;
+      store4(yr + 4 * c, o);
+    }
+  }
+  if (lane == 0) {
+    mean[row] = mu;
+    rstd[row] = rs;
+  }
+}
+
+// Pick threads-per-row so that a row fits in <= 8 float4 per thread.
+static int row_tpr(int cols) {
+  int nv = cols / 4;
+  int tpr = 32;
+  while (tpr * 8 < nv && tpr < 1024) tpr <<= 1;
+  return tpr;
+}
+
+#define NNT_TPR_DISPATCH(tpr, ...)                          \
+  switch (tpr) {                                            \
+    case 32: { constexpr int TPR = 32; __VA_ARGS__; } break;     \
+    case 64: { constexpr int TPR = 64; __VA_ARGS__; } break;     \
+    case 128: { constexpr int TPR = 128; __VA_ARGS__; } break;   \
+    case 256: { constexpr int TPR = 256; __VA_ARGS__; } break;   \
+    case 512: { constexpr int TPR = 512; __VA_ARGS__; } break;   \
+    default: { constexpr int TPR = 1024; __VA_ARGS__; } break;   \
+  }
+
+nnt_status launch_layernorm_fwd(const float* x, const float* g, const float* b, void* y,
+                                float* mean, float* rstd, int64_t rows, int cols, float eps,
+                                int act_dtype, cudaStream_t st) {
+  NNT_CHECK_ARG(cols % 4 == 0 && cols > 0 && cols <= 32768,
+                "layernorm: cols must be a multiple of 4 in [4, 32768] (got %d)", cols);
+  if (rows == 0) return NNT_OK;
+  const int tpr = row_tpr(cols);
+  const int block = std::max(256, tpr);
+  const int rpc = block / tpr;
+  const int64_t grid = ceil_div(rows, rpc);
+  NNT_TPR_DISPATCH(tpr, {
+    if (act_dtype == NNT_BF16)
+      ln_fwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>(x, g, b, (bf16*)y, mean, rstd, rows, cols, eps);
+    else
+      ln_fwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>(x, g, b, (float*)y, mean, rstd, rows, cols, eps);
+  });
+  return launch_check("layernorm_fwd");
+}
+
+static int ln_bwd_grid(int64_t rows, int cols) {
+  const int tpr = row_tpr(cols);
+  const int rpc = std::max(256, tpr) / tpr;
+  return (int)std::min<int64_t>(ceil_div(rows, rpc), 256);
+}
+int ln_bwd_nparts(int64_t rows, int cols) { return ln_bwd_grid(rows, cols); }
+
+// dx = rstd*(gdy - mean(gdy) - xhat*mean(gdy*xhat)) (+ resid), gdy = g*dy.
+// Each CTA walks rows with a grid stride, keeps per-column sums of dy*xhat and
+// dy for the columns its threads own, combines its row groups in shared memory
+// and writes one partial row per CTA.
+template <int TPR, int MAXV, typename T>
+__global__ void ln_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
+                              const float* __restrict__ mean, const float* __restrict__ rstd,
+                              const float* __restrict__ g, const float* resid,
+                              float* dx, T* __restrict__ dx_act,
+                              float* __restrict__ part_g, float* __restrict__ part_b, int64_t rows,
+                              int cols) {
+  __shared__ float red[32];
+  extern __shared__ float comb[];  // [rpc][cols] x 2 when rpc > 1
+  const int rpc = blockDim.x / TPR;
+  const int grp = threadIdx.x / TPR;
+  const int lane = threadIdx.x % TPR;
+  const int nv = cols >> 2;
+  float4 pg[MAXV], pb[MAXV], gam[MAXV];
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    pg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    pb[i] = pg[i];
+    const int c = lane + i * TPR;
+    gam[i] = (c < nv) ? load4(g + 4 * c) : pg[i];
+  }
+  const float inv_n = 1.0f / (float)cols;
+  for (int64_t row0 = (int64_t)blockIdx.x * rpc; row0 < rows; row0 += (int64_t)gridDim.x * rpc) {
+    const int64_t row = row0 + grp;
+    const bool active = row < rows;
+    const int64_t r = active ? row : 0;
+    const float mu = mean[r], rs = rstd[r];
+    float4 xh[MAXV], gd[MAXV];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int c = lane + i * TPR;
+      if (active && c < nv) {
+        float4 dv = load4(dy + r * cols + 4 * c);
+        float4 xv = load4(x + r * cols + 4 * c);
+        xh[i] = make_float4((xv.x - mu) * rs, (xv.y - mu) * rs, (xv.z - mu) * rs, (xv.w - mu) * rs);
+        gd[i] = make_float4(gam[i].x * dv.x, gam[i].y * dv.y, gam[i].z * dv.z, gam[i].w * dv.w);
+        s1 += (gd[i].x + gd[i].y) + (gd[i].z + gd[i].w);
+        s2 += (gd[i].x * xh[i].x + gd[i].y * xh[i].y) + (gd[i].z * xh[i].z + gd[i].w * xh[i].w);
+        pg[i].x += dv.x * xh[i].x;
+        pg[i].y += dv.y * xh[i].y;
+        pg[i].z += dv.z * xh[i].z;
+        pg[i].w += dv.w * xh[i].w;
+        pb[i].x += dv.x;
+        pb[i].y += dv.y;
+        pb[i].z += dv.z;
+        pb[i].w += dv.w;
+      } else {
+        xh[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gd[i] = xh[i];
+      }
+    }
+    s1 = group_sum<TPR>(s1, red) * inv_n;
+    s2 = group_sum<TPR>(s2, red) * inv_n;
+    if (active) {
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) {
+        const int c = lane + i * TPR;
+        if (c < nv) {
+          float4 o;
+          o.x = rs * (gd[i].x - s1 - xh[i].x * s2);
+          o.y = rs * (gd[i].y - s1 - xh[i].y * s2);
+          o.z = rs * (gd[i].z - s1 - xh[i].z * s2);
+          o.w = rs * (gd[i].w - s1 - xh[i].w * s2);
+          if (resid) {
+            float4 q = load4(resid + r * cols + 4 * c);
+            o.x += q.x;
+            o.y += q.y;
+            o.z += q.z;
+            o.w += q.w;
+          }
+          store4(dx + r * cols + 4 * c, o);
+          if (dx_act) store4(dx_act + r * cols + 4 * c, o);
+        }
+      }
+    }
+  }
+  if (!part_g) return;
+  if (rpc == 1) {
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int c = lane + i * TPR;
+      if (c < nv) {
+        store4(part_g + (int64_t)blockIdx.x * cols + 4 * c, pg[i]);
+        store4(part_b + (int64_t)blockIdx.x * cols + 4 * c, pb[i]);
+      }
+    }
+    return;
+  }
+  float* cg = comb;
+  float* cb = comb + rpc * cols;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (c < nv) {
+      store4(cg + grp * cols + 4 * c, pg[i]);
+      store4(cb + grp * cols + 4 * c, pb[i]);
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+    float a = 0.f, bsum = 0.f;
+    for (int j = 0; j < rpc; ++j) {
+      a += cg[j * cols + c];
+      bsum += cb[j * cols + c];
+    }
+    part_g[(int64_t)blockIdx.x * cols + c] = a;
+    part_b[(int64_t)blockIdx.x * cols + c] = bsum;
+  }
+}
+
+nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* mean,
+                                const float* rstd, const float* g, const float* resid, float* dx,
+                                void* dx_act, float* part_g, float* part_b, int64_t rows, int cols,
+                                int act_dtype, cudaStream_t st) {
+  NNT_CHECK_ARG(cols % 4 == 0 && cols > 0 && cols <= 32768,
+                "layernorm bwd: cols must be a multiple of 4 in [4, 32768] (got %d)", cols);
+  if (rows == 0) return NNT_OK;
+  const int tpr = row_tpr(cols);
+  const int block = std::max(256, tpr);
+  const int rpc = block / tpr;
+  const int grid = ln_bwd_grid(rows, cols);
+  const size_t smem = (rpc > 1 && part_g) ? (size_t)2 * rpc * cols * sizeof(float) : 0;
+  NNT_TPR_DISPATCH(tpr, {
+    if (act_dtype == NNT_BF16) {
+      auto k = ln_bwd_kernel<TPR, 8, bf16>;
+      if (smem > 48 * 1024) NNT_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      k<<<grid, block, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, part_g, part_b, rows, cols);
+    } else {
+      auto k = ln_bwd_kernel<TPR, 8, float>;
+      if (smem > 48 * 1024) NNT_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      k<<<grid, block, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, part_g, part_b, rows, cols);
+    }
+  });
+  return launch_check("layernorm_bwd");
+}
+
+// out[c] (+)= sum_p part[p*ld + c], p ascending.
+__global__ void sum_parts_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
+                                 int64_t ld, float* __restrict__ out, int accumulate) {
+  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s = 0.f;
+  for (int64_t p = 0; p < nparts; ++p) s += part[p * ld + c];
+  out[c] = accumulate ? out[c] + s : s;
+}
+
+nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,
+                            float* out, int accumulate, cudaStream_t st) {
+  if (cols == 0) return NNT_OK;
+  sum_parts_kernel<<<(unsigned)ceil_div(cols, 256), 256, 0, st>>>(part, nparts, cols, ld, out,
+                                                                   accumulate);
+  return launch_check("sum_parts");
+}
+
+// Column sums in two fixed-order stages: CTA (cb, rb) sums rows
+// [rb*kColRows, +kColRows) of columns [cb*256, +256) into part[rb][c].
+static constexpr int kColRows = 64;
+int64_t colsum_nparts(int64_t rows) { return ceil_div(rows, kColRows); }
+
+template <typename T>
+__global__ void colsum_part_kernel(const T* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
+                                   float* __restrict__ part) {
+  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int64_t r0 = (int64_t)blockIdx.y * kColRows;
+  const int64_t r1 = r0 + kColRows < rows ? r0 + kColRows : rows;
+  float s = 0.f;
+  for (int64_t r = r0; r < r1; ++r) s += to_f(a[r * ld + c]);
+  part[(int64_t)blockIdx.y * cols + c] = s;
+}
+
+nnt_status launch_colsum(const void* a, int a_dtype, int64_t rows, int64_t cols, int64_t ld,
+                         float* part, float* out, int accumulate, cudaStream_t st) {
+  if (cols == 0) return NNT_OK;
+  const int64_t np = colsum_nparts(rows);
+  NNT_CHECK_ARG(np < 65536, "colsum: too many rows");
+  dim3 grid((unsigned)ceil_div(cols, 256), (unsigned)np);
+  if (a_dtype == NNT_BF16)
+    colsum_part_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)a, rows, cols, ld, part);
+  else
+    colsum_part_kernel<float><<<grid, 256, 0, st>>>((const float*)a, rows, cols, ld, part);
+  NNT_TRY(launch_check("colsum_part"));
+  return launch_sum_parts(part, np, cols, cols, out, accumulate, st);
+}
+
+// =====================================================================
+// causal softmax over score rows (scores already scaled by 1/sqrt(hd))
+// =====================================================================
+
+template <int TPR, int MAXV, typename T>
+__global__ void softmax_fwd_kernel(const float* __restrict__ s, T* __restrict__ p, int64_t S,
+                                   ZMap zm, int nz, int q0, int nq) {
+  __shared__ float red[32];
+  const int rpc = blockDim.x / TPR;
+  const int lane = threadIdx.x % TPR;
+  const int64_t r = (int64_t)blockIdx.x * rpc + threadIdx.x / TPR;
+  const bool active = r < (int64_t)nz * nq;
+  const int64_t rr = active ? r : 0;
+  const int q = q0 + (int)(rr % nq);
+  const int64_t z = zm.z((int)(rr / nq));
+  const float* sr = s + (z * S + q) * S;
+  T* pr = p + (z * S + q) * S;
+  const int valid = q + 1;
+  const int wend = (int)std::min<int64_t>(S, round_up(valid, kCausalBlock));
+  const int nvv = (valid + 3) >> 2;
+  float4 v[MAXV];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (active && c < nvv) {
+      v[i] = load4_stream(sr + 4 * c);
+      if (4 * c + 1 > q) v[i].y = -INFINITY;
+      if (4 * c + 2 > q) v[i].z = -INFINITY;
+      if (4 * c + 3 > q) v[i].w = -INFINITY;
+      mx = fmaxf(mx, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
+    } else {
+      v[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+  }
+  mx = group_max<TPR>(mx, red);
+  const float ms = mx * kLog2e;
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    v[i].x = exp2f(v[i].x * kLog2e - ms);
+    v[i].y = exp2f(v[i].y * kLog2e - ms);
+    v[i].z = exp2f(v[i].z * kLog2e - ms);
+    v[i].w = exp2f(v[i].w * kLog2e - ms);
+    sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+  sum = group_sum<TPR>(sum, red);
+  if (!active) return;
+  const float inv = 1.0f / sum;
+  const int nw = wend >> 2;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (c < nw) {
+      float4 o = make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv);
+      store4(pr + 4 * c, o);  // masked lanes hold exp2(-inf) = 0
+    }
+  }
+}
+
+template <int TPR, int MAXV, typename T>
+__global__ void softmax_bwd_kernel(const T* __restrict__ p, const float* __restrict__ dp,
+                                   T* __restrict__ ds, int64_t S, ZMap zm, int nz, int q0, int nq,
+                                   float scale) {
+  __shared__ float red[32];
+  const int rpc = blockDim.x / TPR;
+  const int lane = threadIdx.x % TPR;
+  const int64_t r = (int64_t)blockIdx.x * rpc + threadIdx.x / TPR;
+  const bool active = r < (int64_t)nz * nq;
+  const int64_t rr = active ? r : 0;
+  const int q = q0 + (int)(rr % nq);
+  const int64_t z = zm.z((int)(rr / nq));
+  const int64_t off = (z * S + q) * S;
+  const int valid = q + 1;
+  const int wend = (int)std::min<int64_t>(S, round_up(valid, kCausalBlock));
+  const int nvv = (valid + 3) >> 2;
+  float4 pv[MAXV], dv[MAXV];
+  float dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (active && c < nvv) {
+      pv[i] = load4(p + off + 4 * c);
+      dv[i] = load4_stream(dp + off + 4 * c);
+      // P is exactly 0 beyond q; clear dP there too so 0*garbage cannot leak in
+      if (4 * c + 1 > q) { pv[i].y = 0.f; dv[i].y = 0.f; }
+      if (4 * c + 2 > q) { pv[i].z = 0.f; dv[i].z = 0.f; }
+      if (4 * c + 3 > q) { pv[i].w = 0.f; dv[i].w = 0.f; }
+      dot += (pv[i].x * dv[i].x + pv[i].y * dv[i].y) + (pv[i].z * dv[i].z + pv[i].w * dv[i].w);
+    } else {
+      pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dv[i] = pv[i];
+    }
+  }
+  dot = group_sum<TPR>(dot, red);
+  if (!active) return;
+  const int nw = wend >> 2;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + i * TPR;
+    if (c < nw) {
+      float4 o;
+      o.x = scale * pv[i].x * (dv[i].x - dot);
+      o.y = scale * pv[i].y * (dv[i].y - dot);
+      o.z = scale * pv[i].z * (dv[i].z - dot);
+      o.w = scale * pv[i].w * (dv[i].w - dot);
+      store4(ds + off + 4 * c, o);
+    }
+  }
+}
+
+static int softmax_tpr(int64_t S) {
+  int tpr = 32;
+  while ((int64_t)tpr * 8 * 4 < S && tpr < 1024) tpr <<= 1;
+  return tpr;
+}
+
+nnt_status launch_softmax_fwd(const float* s, void* p, int64_t S, ZMap zm, int nz, int q0, int nq,
+                              int act_dtype, cudaStream_t st) {
+  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 32768, "softmax: seq must be a multiple of 4 <= 32768");
+  const int64_t rows = (int64_t)nz * nq;
+  if (rows == 0) return NNT_OK;
+  const int tpr = softmax_tpr(S);
+  const int block = std::max(256, tpr);
+  const int64_t grid = ceil_div(rows, block / tpr);
+  NNT_TPR_DISPATCH(tpr, {
+    if (act_dtype == NNT_BF16)
+      softmax_fwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>(s, (bf16*)p, S, zm, nz, q0, nq);
+    else
+      softmax_fwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>(s, (float*)p, S, zm, nz, q0, nq);
+  });
+  return launch_check("softmax_fwd");
+}
+
+nnt_status launch_softmax_bwd(const void* p, const float* dp, void* ds, int64_t S, ZMap zm, int nz,
+                              int q0, int nq, float scale, int act_dtype, cudaStream_t st) {
+  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 32768, "softmax bwd: seq must be a multiple of 4 <= 32768");
+  const int64_t rows = (int64_t)nz * nq;
+  if (rows == 0) return NNT_OK;
+  const int tpr = softmax_tpr(S);
+  const int block = std::max(256, tpr);
+  const int64_t grid = ceil_div(rows, block / tpr);
+  NNT_TPR_DISPATCH(tpr, {
+    if (act_dtype == NNT_BF16)
+      softmax_bwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>((const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
+    else
+      softmax_bwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>((const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
+  });
+  return launch_check("softmax_bwd");
+}
+
+// =====================================================================
+// GELU (tanh form)
+// =====================================================================
+
+__device__ __forceinline__ float gelu_f(float u) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  return 0.5f * u * (1.0f + tanhf(c * (u + a * u * u * u)));
+}
+__device__ __forceinline__ float gelu_grad_f(float u) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float t = tanhf(c * (u + a * u * u * u));
+  return 0.5f * (1.0f + t) + 0.5f * u * (1.0f - t * t) * c * (1.0f + 3.0f * a * u * u);
+}
+
+template <typename T>
+__global__ void gelu_fwd_kernel(const float* __restrict__ u, T* __restrict__ g, int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 x = load4_stream(u + 4 * i);
+    store4(g + 4 * i, make_float4(gelu_f(x.x), gelu_f(x.y), gelu_f(x.z), gelu_f(x.w)));
+  }
+}
+template <typename T>
+__global__ void gelu_bwd_kernel(const T* __restrict__ dg, const float* __restrict__ u,
+                                T* __restrict__ du, int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 x = load4_stream(u + 4 * i);
+    float4 d = load4(dg + 4 * i);
+    store4(du + 4 * i, make_float4(d.x * gelu_grad_f(x.x), d.y * gelu_grad_f(x.y),
+                                   d.z * gelu_grad_f(x.z), d.w * gelu_grad_f(x.w)));
+  }
+}
+
+static int elementwise_grid(int64_t n4) {
+  return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n4, 256), 152 * 8));
+}
+
+nnt_status launch_gelu_fwd(const float* u, void* g, int64_t n, int act_dtype, cudaStream_t st) {
+  NNT_CHECK_ARG(n % 4 == 0, "gelu: n must be a multiple of 4");
+  if (n == 0) return NNT_OK;
+  if (act_dtype == NNT_BF16)
+    gelu_fwd_kernel<bf16><<<elementwise_grid(n / 4), 256, 0, st>>>(u, (bf16*)g, n / 4);
+  else
+    gelu_fwd_kernel<float><<<elementwise_grid(n / 4), 256, 0, st>>>(u, (float*)g, n / 4);
+  return launch_check("gelu_fwd");
+}
+nnt_status launch_gelu_bwd(const void* dg, const float* u, void* du, int64_t n, int act_dtype,
+                           cudaStream_t st) {
+  NNT_CHECK_ARG(n % 4 == 0, "gelu bwd: n must be a multiple of 4");
+  if (n == 0) return NNT_OK;
+  if (act_dtype == NNT_BF16)
+    gelu_bwd_kernel<bf16><<<elementwise_grid(n / 4), 256, 0, st>>>((const bf16*)dg, u, (bf16*)du, n / 4);
+  else
+    gelu_bwd_kernel<float><<<elementwise_grid(n / 4), 256, 0, st>>>((const float*)dg, u, (float*)du, n / 4);
+  return launch_check("gelu_bwd");
+}
+
+// =====================================================================
+// cross-entropy (mean over tokens) + dlogits
+// =====================================================================
+
+// One CTA per row: pass 1 keeps a running (max, sum of exp) per thread and
+// merges them across the CTA; pass 2 re-reads the row (from L2) and writes
+// dz = (exp(z - lse) - onehot) * inv_rows, zero in the padding columns.
+template <typename T>
+__global__ void __launch_bounds__(512) cross_entropy_kernel(
+    const float* __restrict__ z, int64_t ldz, int64_t r0, int64_t cols,
+    const uint16_t* __restrict__ tok_ids, TokMap tm, const uint16_t* __restrict__ tgt,
+    int64_t tgt_stride, T* __restrict__ dz, int64_t lddz, float* __restrict__ row_loss,
+    float inv_rows) {
+  __shared__ float red_m[32], red_s[32];
+  const int64_t r = r0 + blockIdx.x;
+  const float* zr = z + r * ldz;
+  const int64_t n4 = cols >> 2;  // full float4s
+  float m = -INFINITY, s = 0.f;
+  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 v = load4(zr + 4 * i);
+    float lm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (lm > m) {
+      s *= exp2f((m - lm) * kLog2e);
+      m = lm;
+    }
+    s += exp2f((v.x - m) * kLog2e) + exp2f((v.y - m) * kLog2e) + exp2f((v.z - m) * kLog2e) +
+         exp2f((v.w - m) * kLog2e);
+  }
+  for (int64_t c = 4 * n4 + threadIdx.x; c < cols; c += blockDim.x) {
+    float v = zr[c];
+    if (v > m) {
+      s *= exp2f((m - v) * kLog2e);
+      m = v;
+    }
+    s += exp2f((v - m) * kLog2e);
+  }
+  // merge (m, s) over the CTA
+  float wm = warp_max(m);
+  s = (m == -INFINITY) ? 0.f : s * exp2f((m - wm) * kLog2e);
+  s = warp_sum(s);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red_m[w] = wm;
+    red_s[w] = s;
+  }
+  __syncthreads();
+  float M = -INFINITY;
+  for (int i = 0; i < nw; ++i) M = fmaxf(M, red_m[i]);
+  float SUM = 0.f;
+  for (int i = 0; i < nw; ++i) SUM += red_s[i] * exp2f((red_m[i] - M) * kLog2e);
+  const float lse = M + logf(SUM);
+  int y;
+  if (tok_ids) {
+    int b, sq;
+    tm.bs(r, b, sq);
+    y = tok_ids[(int64_t)b * (tm.S + 1) + sq + 1];
+  } else {
+    y = tgt[r * tgt_stride];
+  }
+  if (y >= cols) {
+    if (threadIdx.x == 0) atomicOr(&g_device_error, DEVERR_TOKEN_RANGE);
+    y = 0;
+  }
+  if (threadIdx.x == 0) row_loss[r] = lse - zr[y];
+  const float ls = lse * kLog2e;
+  T* dr = dz + r * lddz;
+  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 v = load4(zr + 4 * i);
+    float4 o;
+    o.x = exp2f(v.x * kLog2e - ls);
+    o.y = exp2f(v.y * kLog2e - ls);
+    o.z = exp2f(v.z * kLog2e - ls);
+    o.w = exp2f(v.w * kLog2e - ls);
+    const int64_t c0 = 4 * i;
+    if (y >= c0 && y < c0 + 4) {
+      const int k = (int)(y - c0);
+      if (k == 0) o.x -= 1.f;
+      else if (k == 1) o.y -= 1.f;
+      else if (k == 2) o.z -= 1.f;
+      else o.w -= 1.f;
+    }
+    o.x *= inv_rows;
+    o.y *= inv_rows;
+    o.z *= inv_rows;
+    o.w *= inv_rows;
+    store4(dr + c0, o);
+  }
+  for (int64_t c = 4 * n4 + threadIdx.x; c < lddz; c += blockDim.x) {
+    float o = 0.f;
+    if (c < cols) o = (exp2f(zr[c] * kLog2e - ls) - (c == y ? 1.f : 0.f)) * inv_rows;
+    dr[c] = from_f<T>(o);
+  }
+}
+
+nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t nrows,
+                                int64_t cols, const uint16_t* tok_ids, TokMap tm,
+                                const uint16_t* tgt, int64_t tgt_stride, void* dz, int64_t lddz,
+                                float* row_loss, float inv_rows, int act_dtype, cudaStream_t st) {
+  NNT_CHECK_ARG(ldz % 4 == 0 && lddz % 4 == 0 && ldz >= cols && lddz >= cols,
+                "cross entropy: leading dimensions must be multiples of 4 and >= cols");
+  if (nrows == 0) return NNT_OK;
+  if (act_dtype == NNT_BF16)
+    cross_entropy_kernel<bf16><<<(unsigned)nrows, 512, 0, st>>>(
+        z, ldz, r0, cols, tok_ids, tm, tgt, tgt_stride, (bf16*)dz, lddz, row_loss, inv_rows);
+  else
+    cross_entropy_kernel<float><<<(unsigned)nrows, 512, 0, st>>>(
+        z, ldz, r0, cols, tok_ids, tm, tgt, tgt_stride, (float*)dz, lddz, row_loss, inv_rows);
+  return launch_check("cross_entropy");
+}
+
+// loss = (sum of row losses in a fixed order, in double) / rows
+__global__ void mean_loss_kernel(const float* __restrict__ row_loss, int64_t rows,
+                                 float* __restrict__ loss) {
+  __shared__ double red[1024];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) s += (double)row_loss[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = (float)(red[0] / (double)rows);
+}
+
+nnt_status launch_mean_loss(const float* row_loss, int64_t rows, float* loss, cudaStream_t st) {
+  mean_loss_kernel<<<1, 1024, 0, st>>>(row_loss, rows, loss);
+  return launch_check("mean_loss");
+}
+
+// =====================================================================
+// AdamW (decoupled weight decay), fp32 state, optional bf16 copy out
+// =====================================================================
+
+__device__ __forceinline__ void adamw_one(float& w, float g, float& m, float& v, float lr, float b1,
+                                          float b2, float eps, float wd, float bc1, float bc2) {
+  m = b1 * m + (1.f - b1) * g;
+  v = b2 * v + (1.f - b2) * g * g;
+  const float mhat = m / bc1;
+  const float vhat = v / bc2;
+  w = w - lr * wd * w - lr * mhat / (sqrtf(vhat) + eps);
+}
+
+// hyper (optional, device): lr, beta1, beta2, eps, wd, bc1, bc2 -- overrides the
+// by-value arguments so a captured graph can be replayed with new values.
+__global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
+                             float* __restrict__ m, float* __restrict__ v, bf16* __restrict__ wb,
+                             int64_t n, float lr, float b1, float b2, float eps, float wd,
+                             float bc1, float bc2, const float* __restrict__ hyper) {
+  if (hyper) {
+    lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; eps = hyper[3]; wd = hyper[4];
+    bc1 = hyper[5]; bc2 = hyper[6];
+  }
+  const int64_t n4 = n >> 2;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 W = load4_stream(w + 4 * i), G = load4_stream(g + 4 * i);
+    float4 M = load4_stream(m + 4 * i), V = load4_stream(v + 4 * i);
+    adamw_one(W.x, G.x, M.x, V.x, lr, b1, b2, eps, wd, bc1, bc2);
+    adamw_one(W.y, G.y, M.y, V.y, lr, b1, b2, eps, wd, bc1, bc2);
+    adamw_one(W.z, G.z, M.z, V.z, lr, b1, b2, eps, wd, bc1, bc2);
+    adamw_one(W.w, G.w, M.w, V.w, lr, b1, b2, eps, wd, bc1, bc2);
+    store4_stream(w + 4 * i, W);
+    store4_stream(m + 4 * i, M);
+    store4_stream(v + 4 * i, V);
+    if (wb) store4(wb + 4 * i, W);
+  }
+  // tail
+  const int64_t t = 4 * n4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t < n) {
+    float W = w[t], M = m[t], V = v[t];
+    adamw_one(W, g[t], M, V, lr, b1, b2, eps, wd, bc1, bc2);
+    w[t] = W;
+    m[t] = M;
+    v[t] = V;
+    if (wb) wb[t] = __float2bfloat16_rn(W);
+  }
+}
+
+nnt_status launch_adamw(float* w, const float* g, float* m, float* v, bf16* w_bf16, int64_t n,
+                        float lr, float b1, float b2, float eps, float wd, float bc1, float bc2,
+                        cudaStream_t st) {
+  if (n == 0) return NNT_OK;
+  NNT_CHECK_ARG(((uintptr_t)w | (uintptr_t)g | (uintptr_t)m | (uintptr_t)v) % 16 == 0 &&
+                    ((uintptr_t)w_bf16) % 8 == 0,
+                "adamw: buffers must be 16-byte aligned (bf16 copy 8-byte)");
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
+  adamw_kernel<<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, lr, b1, b2, eps, wd, bc1, bc2, nullptr);
+  return launch_check("adamw");
+}
+
+nnt_status launch_adamw_dev(float* w, const float* g, float* m, float* v, bf16* w_bf16, int64_t n,
+                            const float* hyper_dev, cudaStream_t st) {
+  if (n == 0) return NNT_OK;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
+  adamw_kernel<<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
+  return launch_check("adamw");
+}
+
+// =====================================================================
+// init: splitmix64 counter stream + Box-Muller (same recipe as the host
+// generator: key = sm(sm(seed) ^ stream), bits_i = sm(key + i),
+// u = ((bits >> 11) + 0.5) * 2^-53, pairs (2j, 2j+1) -> cos / sin branch)
+// =====================================================================
+
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__global__ void init_normal_kernel(float* __restrict__ w, int64_t n, uint64_t key, double std) {
+  const int64_t npairs = (n + 1) / 2;
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < npairs;
+       j += (int64_t)gridDim.x * blockDim.x) {
+    const uint64_t b1 = splitmix64(key + (uint64_t)(2 * j));
+    const uint64_t b2 = splitmix64(key + (uint64_t)(2 * j + 1));
+    const double u1 = ((double)(b1 >> 11) + 0.5) * 0x1.0p-53;
+    const double u2 = ((double)(b2 >> 11) + 0.5) * 0x1.0p-53;
+    const double r = sqrt(-2.0 * log(u1));
+    const double th = 6.283185307179586 * u2;
+    double sn, cs;
+    sincos(th, &sn, &cs);
+    w[2 * j] = (float)(r * cs * std);
+    if (2 * j + 1 < n) w[2 * j + 1] = (float)(r * sn * std);
+  }
+}
+
+static uint64_t host_splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+nnt_status launch_init_normal(float* w, int64_t n, uint64_t seed, uint64_t stream_id, double std,
+                              cudaStream_t st) {
+  if (n == 0) return NNT_OK;
+  const uint64_t key = host_splitmix64(host_splitmix64(seed) ^ stream_id);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div((n + 1) / 2, 256), 152 * 16));
+  init_normal_kernel<<<grid, 256, 0, st>>>(w, n, key, std);
+  return launch_check("init_normal");
+}
+
+__global__ void fill_kernel(float* __restrict__ w, int64_t n, float value) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    w[i] = value;
+}
+nnt_status launch_fill(float* w, int64_t n, float value, cudaStream_t st) {
+  if (n == 0) return NNT_OK;
+  fill_kernel<<<(int)std::min<int64_t>(ceil_div(n, 256), 152 * 16), 256, 0, st>>>(w, n, value);
+  return launch_check("fill");
+}
+
+__global__ void cast_bf16_kernel(const float* __restrict__ s, bf16* __restrict__ d, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    d[i] = __float2bfloat16_rn(s[i]);
+}
+nnt_status launch_cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t st) {
+  if (n == 0) return NNT_OK;
+  cast_bf16_kernel<<<(int)std::min<int64_t>(ceil_div(n, 256), 152 * 16), 256, 0, st>>>(src, dst, n);
+  return launch_check("cast_bf16");
+}
+
+__global__ void check_tokens_kernel(const uint16_t* __restrict__ ids, int64_t n, int vocab) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    if (ids[i] >= vocab) atomicOr(&g_device_error, DEVERR_TOKEN_RANGE);
+}
+nnt_status launch_check_tokens(const uint16_t* ids, int64_t n, int vocab, cudaStream_t st) {
+  if (n == 0) return NNT_OK;
+  check_tokens_kernel<<<(int)std::min<int64_t>(ceil_div(n, 256), 152), 256, 0, st>>>(ids, n, vocab);
+  return launch_check("check_tokens");
+}
+
+}  // namespace nnt

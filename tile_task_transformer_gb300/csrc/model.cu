@@ -1,0 +1,1361 @@
+// GPT2 training step as a static tile-task program, behind the C ABI of nnt.h.
+//
+// Model: GPT2 with pre-LN blocks, causal multi-head attention, tanh-GELU MLP,
+// final LayerNorm and a tied LM head, mean next-token cross-entropy, AdamW
+// with decoupled weight decay (first page: title and "Builds on" references
+// -- Attention Is All You Need, Layer Normalization, On Layer Normalization in
+// the Transformer Architecture, Decoupled Weight Decay Regularization; README
+// "Minimal working GPT example": GPT2 config, tile flags, fusedadamw flags,
+// --loss-reduction=mean).
+//
+// Tiling (README flag descriptions): tokens are tiled by batch_tile x
+// seq_tile, features by embd_tile / inner_tile, heads by head_tile, the
+// vocabulary by vocab_tile. Every layer is emitted as tasks over those tiles
+// that declare the tiles they read and write; the executor derives the
+// dependency graph and the stream schedule once, at creation.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <chrono>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "common.cuh"
+#include "executor.h"
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+using namespace nnt;
+
+namespace {
+
+enum TaskType : int {
+  TT_EMBED = 0, TT_LN_FWD, TT_GEMM_QKV, TT_GEMM_QK, TT_SOFTMAX_FWD, TT_GEMM_PV, TT_GEMM_ATTN_O,
+  TT_GEMM_FC, TT_GEMM_MLP_PROJ, TT_GEMM_LM_HEAD, TT_XENT, TT_LOSS,
+  TT_GEMM_LM_DX, TT_GEMM_LM_DW, TT_LN_BWD, TT_LN_PARTS, TT_GEMM_DX, TT_GEMM_DW, TT_COLSUM,
+  TT_GEMM_ATTN_BWD, TT_SOFTMAX_BWD, TT_EMB_SORT, TT_EMB_SCATTER, TT_WPE_GRAD, TT_ADAMW,
+  TT_COUNT
+};
+const char* kTaskNames[TT_COUNT] = {
+    "embedding_fwd", "layernorm_fwd", "gemm_qkv", "gemm_qk", "softmax_fwd", "gemm_pv",
+    "gemm_attn_out", "gemm_fc_gelu", "gemm_mlp_proj", "gemm_lm_head", "cross_entropy",
+    "mean_loss", "gemm_lm_dx", "gemm_lm_dw", "layernorm_bwd", "layernorm_param_grads",
+    "gemm_dx", "gemm_dw", "bias_grads", "gemm_attn_bwd", "softmax_bwd", "token_sort",
+    "embedding_scatter", "wpe_grad", "adamw"};
+
+
+struct ParamInfo {
+  std::string name;
+  int64_t shape0, shape1;  // shape1 = 0 for vectors
+  int64_t off, n;
+  int kind;  // 0 weight (normal), 1 bias (normal or 0), 2 ln gain (1), 3 ln bias (0)
+};
+
+// A tensor's tile grid: up to 4 tile axes, tile id = base + linear index.
+struct TGrid {
+  int64_t base = 0;
+  int g[4] = {1, 1, 1, 1};
+};
+
+struct AdamHyperDev {
+  float lr, b1, b2, eps, wd, bc1, bc2, pad;
+};
+
+thread_local std::string t_model_err;
+
+}  // namespace
+
+struct nnt_model {
+  nnt_gpt2_config cfg;
+  nnt_tiles tiles;
+  nnt_options opts;
+  int act = NNT_BF16;
+  size_t act_size = 2;
+  int L, d, H, hd, f, V, S, B, T;
+  int tb, ts, te, ti, th, tv;
+  int n_bt, n_st, n_ht, n_tok, TT, nce, ncf, ncv;
+  TokMap tm;
+  int64_t ldz, lddz;
+  int backend = 0;
+  std::string err;
+
+  // memory
+  std::vector<void*> dev_allocs;
+  uint64_t device_bytes = 0, host_bytes = 0;
+
+  // parameters (flat fp32 buffers + bf16 copy, same offsets)
+  std::vector<ParamInfo> params;
+  int64_t n_flat = 0, n_scalar = 0;
+  float *master = nullptr, *grad = nullptr, *mom1 = nullptr, *mom2 = nullptr;
+  bf16* wbf = nullptr;
+  AdamHyperDev* hyper_dev = nullptr;
+  AdamHyperDev hyper_host{};
+
+  // activations
+  uint16_t* tokens_dev = nullptr;
+  std::vector<float*> x, xmid, mu1, r1, mu2, r2, u;
+  std::vector<void*> h1, qkvh, P, O, h2, g;
+  float* scores = nullptr;  // [B*H][S][S] fp32, reused by every layer (fwd scores, bwd dP)
+  void* y = nullptr;
+  float *muf = nullptr, *rf = nullptr;
+  float* z = nullptr;
+  void* dz = nullptr;
+  float *row_loss = nullptr, *loss_dev = nullptr;
+  float* loss_host = nullptr;  // pinned
+  // backward scratch
+  float* dres = nullptr;
+  void* dres_act = nullptr;
+  float* dtmp = nullptr;
+  void* du = nullptr;
+  void* dOh = nullptr;
+  void* dqkv = nullptr;
+  float *ln_part_g = nullptr, *ln_part_b = nullptr;
+  float* col_part = nullptr;
+  uint32_t* sort_keys = nullptr;
+
+  // tile grids
+  std::vector<TGrid> gx, gxmid, gh1, gqkvh, gP, gO, gh2, gu, gg, gstat1, gstat2;
+  TGrid gscores, gy, gstatf, gz, gdz, grow_loss, gloss, gtok;
+  TGrid gdres, gdres_act, gdtmp, gdu, gdOh, gdqkv, gln_part, gcol_part, gkeys;
+  std::vector<TGrid> gparam, ggrad;
+  int64_t next_tile = 0;
+
+  Program fwd, bwd, opt;
+  Executor ex;
+  cudaEvent_t done_event = nullptr;
+  int state = 0;  // 0: created, 1: forward done, 2: backward done
+  int64_t step = 0;
+  double last_fwd_ms = 0, last_bwd_ms = 0, last_opt_ms = 0;
+};
+
+namespace {
+
+nnt_status fail(nnt_model* m, nnt_status s) {
+  if (m) m->err = thread_error();
+  t_model_err = thread_error();
+  return s;
+}
+
+template <typename Ptr>
+nnt_status dalloc(nnt_model* m, Ptr*& p, size_t bytes) {
+  void* q = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_thread_error("cudaMalloc of %zu bytes failed (%s); %llu bytes already held", bytes,
+                     cudaGetErrorString(e), (unsigned long long)m->device_bytes);
+    return NNT_ERR_OOM;
+  }
+  m->dev_allocs.push_back(q);
+  m->device_bytes += bytes;
+  p = static_cast<Ptr*>(q);
+  return NNT_OK;
+}
+
+TGrid new_grid(nnt_model* m, int a, int b = 1, int c = 1, int d = 1) {
+  TGrid t;
+  t.base = m->next_tile;
+  t.g[0] = a;
+  t.g[1] = b;
+  t.g[2] = c;
+  t.g[3] = d;
+  m->next_tile += (int64_t)a * b * c * d;
+  return t;
+}
+
+// Add the tiles of box [a0,a1) x [b0,b1) x [c0,c1) x [d0,d1) (-1 = whole axis).
+void box(std::vector<TileUse>& u, const TGrid& t, int mode, int a0 = 0, int a1 = -1, int b0 = 0,
+         int b1 = -1, int c0 = 0, int c1 = -1, int d0 = 0, int d1 = -1) {
+  if (a1 < 0) a1 = t.g[0];
+  if (b1 < 0) b1 = t.g[1];
+  if (c1 < 0) c1 = t.g[2];
+  if (d1 < 0) d1 = t.g[3];
+  for (int a = a0; a < a1; ++a)
+    for (int b = b0; b < b1; ++b)
+      for (int c = c0; c < c1; ++c)
+        for (int d = d0; d < d1; ++d)
+          u.push_back({t.base + (((int64_t)a * t.g[1] + b) * t.g[2] + c) * t.g[3] + d, mode});
+}
+
+int tiles_of(int n, int t) { return (int)ceil_div(n, t); }
+int tile_lo(int i, int t) { return i * t; }
+int tile_hi(int i, int t, int n) { return std::min(n, (i + 1) * t); }
+
+double causal_rows(int q0, int nq) {  // sum_{q=q0}^{q0+nq-1} (q+1)
+  return (double)nq * q0 + (double)nq * (nq + 1) / 2.0;
+}
+
+// ------------------------------------------------------------ model build
+
+nnt_status validate(const nnt_gpt2_config* c, const nnt_tiles* t) {
+  NNT_CHECK_ARG(c, "NULL config");
+  NNT_CHECK_ARG(c->n_layer >= 0 && c->d_model > 0 && c->n_head > 0 && c->d_ff > 0 && c->vocab > 0 &&
+                    c->n_ctx > 0 && c->batch > 0,
+                "config sizes must be positive");
+  NNT_CHECK_ARG(c->dtype == NNT_F32 || c->dtype == NNT_BF16, "dtype must be NNT_F32 or NNT_BF16");
+  NNT_CHECK_ARG(c->d_model % c->n_head == 0, "d_model %% n_head != 0");
+  NNT_CHECK_ARG(c->d_model % 8 == 0 && c->d_ff % 8 == 0,
+                "d_model and d_ff must be multiples of 8");
+  const int hd = c->d_model / c->n_head;
+  NNT_CHECK_ARG(hd % 8 == 0, "head size must be a multiple of 8");
+  NNT_CHECK_ARG(c->dtype == NNT_F32 || hd % 16 == 0, "bf16 needs a head size multiple of 16");
+  NNT_CHECK_ARG(c->vocab <= 65536, "vocab must be <= 65536 (uint16 token ids)");
+  NNT_CHECK_ARG(c->n_ctx % 4 == 0, "n_ctx must be a multiple of 4");
+  NNT_CHECK_ARG((int64_t)c->batch * c->n_ctx <= 16384, "batch*n_ctx must be <= 16384");
+  NNT_CHECK_ARG(c->d_model <= 32768, "d_model must be <= 32768");
+  if (t) {
+    NNT_CHECK_ARG(t->batch_tile >= 0 && t->seq_tile >= 0 && t->embd_tile >= 0 && t->inner_tile >= 0 &&
+                      t->head_tile >= 0 && t->vocab_tile >= 0,
+                  "tile sizes must be >= 0");
+    const int tb = t->batch_tile ? t->batch_tile : c->batch;
+    const int ts = t->seq_tile ? t->seq_tile : c->n_ctx;
+    const int th = t->head_tile ? t->head_tile : c->n_head;
+    NNT_CHECK_ARG(c->batch % tb == 0, "batch %% batch_tile != 0");
+    NNT_CHECK_ARG(c->n_ctx % ts == 0, "n_ctx %% seq_tile != 0 (sequence length must be divisible by seq-tile)");
+    NNT_CHECK_ARG(c->n_head % th == 0, "n_head %% head_tile != 0");
+    NNT_CHECK_ARG(ts % 4 == 0 || ts == c->n_ctx, "seq_tile must be a multiple of 4");
+    const int te = t->embd_tile ? t->embd_tile : c->d_model;
+    const int ti = t->inner_tile ? t->inner_tile : c->d_ff;
+    const int tv = t->vocab_tile ? t->vocab_tile : c->vocab;
+    NNT_CHECK_ARG(te % 8 == 0 || te >= c->d_model, "embd_tile must be a multiple of 8");
+    NNT_CHECK_ARG(ti % 8 == 0 || ti >= c->d_ff, "inner_tile must be a multiple of 8");
+    NNT_CHECK_ARG(tv % 8 == 0 || tv >= c->vocab, "vocab_tile must be a multiple of 8");
+  }
+  return NNT_OK;
+}
+
+nnt_status alloc_all(nnt_model* m) {
+  const int L = m->L, d = m->d, f = m->f, T = m->T, H = m->H, S = m->S, B = m->B;
+  const size_t as = m->act_size;
+  // parameters: each tensor starts on a 64-element boundary
+  auto add_param = [&](const std::string& name, int64_t s0, int64_t s1, int kind) {
+    ParamInfo p;
+    p.name = name;
+    p.shape0 = s0;
+    p.shape1 = s1;
+    p.n = s0 * (s1 ? s1 : 1);
+    p.off = m->n_flat;
+    p.kind = kind;
+    m->n_flat += round_up(p.n, 64);
+    m->n_scalar += p.n;
+    m->params.push_back(p);
+  };
+  add_param("wte", m->V, d, 0);
+  add_param("wpe", S, d, 0);
+  for (int l = 0; l < L; ++l) {
+    std::string p = "h" + std::to_string(l) + ".";
+    add_param(p + "ln1.g", d, 0, 2);
+    add_param(p + "ln1.b", d, 0, 3);
+    add_param(p + "qkv.w", 3 * d, d, 0);
+    add_param(p + "qkv.b", 3 * d, 0, 1);
+    add_param(p + "o.w", d, d, 0);
+    add_param(p + "o.b", d, 0, 1);
+    add_param(p + "ln2.g", d, 0, 2);
+    add_param(p + "ln2.b", d, 0, 3);
+    add_param(p + "fc.w", f, d, 0);
+    add_param(p + "fc.b", f, 0, 1);
+    add_param(p + "proj.w", d, f, 0);
+    add_param(p + "proj.b", d, 0, 1);
+  }
+  add_param("ln_f.g", d, 0, 2);
+  add_param("ln_f.b", d, 0, 3);
+  const size_t pf = (size_t)m->n_flat * 4;
+  NNT_TRY(dalloc(m, m->master, pf));
+  NNT_TRY(dalloc(m, m->grad, pf));
+  NNT_TRY(dalloc(m, m->mom1, pf));
+  NNT_TRY(dalloc(m, m->mom2, pf));
+  NNT_TRY(dalloc(m, m->wbf, (size_t)m->n_flat * 2));
+  NNT_TRY(dalloc(m, m->hyper_dev, sizeof(AdamHyperDev)));
+  NNT_CUDA_TRY(cudaMemset(m->master, 0, pf));
+  NNT_CUDA_TRY(cudaMemset(m->grad, 0, pf));
+  NNT_CUDA_TRY(cudaMemset(m->mom1, 0, pf));
+  NNT_CUDA_TRY(cudaMemset(m->mom2, 0, pf));
+  NNT_CUDA_TRY(cudaMemset(m->wbf, 0, (size_t)m->n_flat * 2));
+
+  NNT_TRY(dalloc(m, m->tokens_dev, (size_t)B * (S + 1) * 2));
+  m->x.resize(L + 1);
+  m->xmid.resize(L);
+  m->mu1.resize(L);
+  m->r1.resize(L);
+  m->mu2.resize(L);
+  m->r2.resize(L);
+  m->u.resize(L);
+  m->h1.resize(L);
+  m->qkvh.resize(L);
+  m->P.resize(L);
+  m->O.resize(L);
+  m->h2.resize(L);
+  m->g.resize(L);
+  const size_t Td = (size_t)T * d;
+  for (int l = 0; l <= L; ++l) NNT_TRY(dalloc(m, m->x[l], Td * 4));
+  for (int l = 0; l < L; ++l) {
+    NNT_TRY(dalloc(m, m->xmid[l], Td * 4));
+    NNT_TRY(dalloc(m, m->mu1[l], (size_t)T * 4));
+    NNT_TRY(dalloc(m, m->r1[l], (size_t)T * 4));
+    NNT_TRY(dalloc(m, m->mu2[l], (size_t)T * 4));
+    NNT_TRY(dalloc(m, m->r2[l], (size_t)T * 4));
+    NNT_TRY(dalloc(m, m->h1[l], Td * as));
+    NNT_TRY(dalloc(m, m->qkvh[l], 3 * Td * as));
+    NNT_TRY(dalloc(m, m->P[l], (size_t)B * H * S * S * as));
+    NNT_TRY(dalloc(m, m->O[l], Td * as));
+    NNT_TRY(dalloc(m, m->h2[l], Td * as));
+    NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * 4));
+    NNT_TRY(dalloc(m, m->g[l], (size_t)T * f * as));
+  }
+  NNT_TRY(dalloc(m, m->scores, (size_t)B * H * S * S * 4));
+  NNT_TRY(dalloc(m, m->y, Td * as));
+  NNT_TRY(dalloc(m, m->muf, (size_t)T * 4));
+  NNT_TRY(dalloc(m, m->rf, (size_t)T * 4));
+  NNT_TRY(dalloc(m, m->z, (size_t)T * m->ldz * 4));
+  NNT_TRY(dalloc(m, m->dz, (size_t)T * m->lddz * as));
+  NNT_TRY(dalloc(m, m->row_loss, (size_t)T * 4));
+  NNT_TRY(dalloc(m, m->loss_dev, 16));
+  NNT_TRY(dalloc(m, m->dres, Td * 4));
+  NNT_TRY(dalloc(m, m->dres_act, Td * as));
+  NNT_TRY(dalloc(m, m->dtmp, Td * 4));
+  NNT_TRY(dalloc(m, m->du, (size_t)T * f * as));
+  NNT_TRY(dalloc(m, m->dOh, Td * as));
+  NNT_TRY(dalloc(m, m->dqkv, 3 * Td * as));
+  const int lnp = ln_bwd_nparts(m->TT, d);
+  NNT_TRY(dalloc(m, m->ln_part_g, (size_t)m->n_tok * lnp * d * 4));
+  NNT_TRY(dalloc(m, m->ln_part_b, (size_t)m->n_tok * lnp * d * 4));
+  const int64_t maxcols = std::max<int64_t>(3 * d, f);
+  NNT_TRY(dalloc(m, m->col_part, (size_t)colsum_nparts(T) * maxcols * 4));
+  NNT_TRY(dalloc(m, m->sort_keys, (size_t)T * 4));
+  // padding columns of the logits must stay finite: zero them once
+  NNT_CUDA_TRY(cudaMemset(m->z, 0, (size_t)T * m->ldz * 4));
+  NNT_CUDA_TRY(cudaMemset(m->dz, 0, (size_t)T * m->lddz * as));
+  void* lh = nullptr;
+  NNT_CUDA_TRY(cudaMallocHost(&lh, 64));
+  m->loss_host = (float*)lh;
+  m->host_bytes += 64;
+  return NNT_OK;
+}
+
+nnt_status init_params(nnt_model* m, cudaStream_t st) {
+  const double std = m->opts.init_std > 0 ? (double)m->opts.init_std : 0.02;
+  for (size_t i = 0; i < m->params.size(); ++i) {
+    const ParamInfo& p = m->params[i];
+    float* w = m->master + p.off;
+    if (p.kind == 2) NNT_TRY(launch_fill(w, p.n, 1.f, st));
+    else if (p.kind == 3 || (p.kind == 1 && m->opts.init_zero_bias)) NNT_TRY(launch_fill(w, p.n, 0.f, st));
+    else NNT_TRY(launch_init_normal(w, p.n, m->opts.init_seed, (uint64_t)i, std, st));
+  }
+  NNT_TRY(launch_cast_bf16(m->master, m->wbf, m->n_flat, st));
+  return NNT_OK;
+}
+
+const ParamInfo& P_(nnt_model* m, int l, int which) {  // which: index within a layer block
+  return m->params[2 + 12 * l + which];
+}
+enum { LN1G = 0, LN1B, QKVW, QKVB, OW, OB, LN2G, LN2B, FCW, FCB, PROJW, PROJB };
+
+// pointer helpers
+float* pm(nnt_model* m, const ParamInfo& p) { return m->master + p.off; }
+float* pg(nnt_model* m, const ParamInfo& p) { return m->grad + p.off; }
+const void* pw(nnt_model* m, const ParamInfo& p) {  // GEMM operand copy of a weight
+  if (m->act == NNT_BF16) return m->wbf + p.off;
+  return m->master + p.off;
+}
+
+struct Builder {
+  nnt_model* m;
+  int row0(int rt) const { return rt * m->TT; }
+  int bt_of(int rt) const { return rt / m->n_st; }
+  int st_of(int rt) const { return rt % m->n_st; }
+
+  // GEMM task helper
+  void gemm_task(Program& P, int type, const GemmArgs& g, std::vector<TileUse> uses, double flops) {
+    Task t;
+    t.type = type;
+    t.uses = std::move(uses);
+    t.flops = flops;
+    const int be = m->backend;
+    t.fn = [g, be](cudaStream_t s) { return gemm(g, be, s); };
+    P.add(std::move(t));
+  }
+  GemmArgs base() const {
+    GemmArgs g;
+    g.op_dtype = m->act;
+    g.tm = m->tm;
+    return g;
+  }
+  // column tiles of the qkv axis: part-major, te-sized inside each part
+  void qkv_cols(int ct, int& c0, int& c1) const {
+    const int part = ct / m->nce, c = ct % m->nce;
+    c0 = part * m->d + tile_lo(c, m->te);
+    c1 = part * m->d + tile_hi(c, m->te, m->d);
+  }
+  // head-tile range overlapped by columns [c0, c1) of one part (c relative to part)
+  void head_tiles(int c0, int c1, int& h0, int& h1) const {
+    const int hl = c0 / m->hd, hh = (c1 + m->hd - 1) / m->hd;
+    h0 = hl / m->th;
+    h1 = (hh - 1) / m->th + 1;
+  }
+};
+
+// -------------------------------------------------------------- forward
+void build_forward(nnt_model* m) {
+  Builder b{m};
+  Program& P = m->fwd;
+  const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
+  const size_t as = m->act_size;
+  const float eps = m->cfg.ln_eps > 0 ? m->cfg.ln_eps : 1e-5f;
+  const int act = m->act;
+
+  // embedding per token tile
+  for (int rt = 0; rt < m->n_tok; ++rt) {
+    Task t;
+    t.type = TT_EMBED;
+    box(t.uses, m->gtok, ACC_R);
+    box(t.uses, m->gx[0], ACC_W, rt, rt + 1);
+    const int b0 = b.bt_of(rt) * m->tb, s0 = b.st_of(rt) * m->ts;
+    t.bytes = (double)m->TT * d * 12 + m->TT * 2.0;
+    t.fn = [m, b0, s0](cudaStream_t s) {
+      return launch_embedding_fwd(m->tokens_dev, m->S + 1, m->master + m->params[0].off,
+                                  m->master + m->params[1].off, m->x[0], m->d, m->V, m->tm, b0,
+                                  m->tb, s0, m->ts, s);
+    };
+    P.add(std::move(t));
+  }
+
+  auto ln_fwd_task = [&](int type, const float* const* xin, const TGrid& gxin, const ParamInfo* pgm,
+                         const ParamInfo* pbt, void* const* yout, const TGrid& gyout, float* const* mu,
+                         float* const* rs, const TGrid& gst, int rt) {
+    Task t;
+    t.type = type;
+    box(t.uses, gxin, ACC_R, rt, rt + 1);
+    box(t.uses, gyout, ACC_W, rt, rt + 1);
+    box(t.uses, gst, ACC_W, rt, rt + 1);
+    t.bytes = (double)m->TT * d * (4 + as) + 8.0 * m->TT;
+    const int64_t r0 = (int64_t)rt * m->TT;
+    t.fn = [=](cudaStream_t s) {
+      return launch_layernorm_fwd(*xin + r0 * d, pm(m, *pgm), pm(m, *pbt),
+                                  (char*)*yout + r0 * d * as, *mu + r0, *rs + r0, m->TT, d, eps,
+                                  act, s);
+    };
+    P.add(std::move(t));
+  };
+
+  for (int l = 0; l < m->L; ++l) {
+    // LN1
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      ln_fwd_task(TT_LN_FWD, &m->x[l], m->gx[l], &P_(m, l, LN1G), &P_(m, l, LN1B), &m->h1[l],
+                  m->gh1[l], &m->mu1[l], &m->r1[l], m->gstat1[l], rt);
+    // QKV projection, epilogue writes head-major q/k/v
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < 3 * m->nce; ++ct) {
+        int c0, c1;
+        b.qkv_cols(ct, c0, c1);
+        GemmArgs g = b.base();
+        g.M = T; g.N = 3 * d; g.K = d;
+        g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+        g.A = m->h1[l]; g.lda = d; g.a_trans = 0;
+        g.B = pw(m, P_(m, l, QKVW)); g.ldb = d; g.b_trans = 0;
+        g.C = m->qkvh[l]; g.c_dtype = act; g.out_mode = OUT_HEADSPLIT;
+        g.hs_B = m->B; g.hs_H = H; g.hs_S = S; g.hs_hd = hd; g.hs_d = d;
+        g.bias = pm(m, P_(m, l, QKVB));
+        std::vector<TileUse> u;
+        box(u, m->gh1[l], ACC_R, rt, rt + 1);
+        const int part = ct / m->nce;
+        int h0, h1;
+        b.head_tiles(c0 - part * d, c1 - part * d, h0, h1);
+        box(u, m->gqkvh[l], ACC_W, part, part + 1, b.bt_of(rt), b.bt_of(rt) + 1, h0, h1,
+            b.st_of(rt), b.st_of(rt) + 1);
+        b.gemm_task(P, TT_GEMM_QKV, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
+      }
+    // attention per (batch tile, head tile, query tile)
+    const size_t zq = (size_t)S * hd;  // elements of one head's q (or k, v)
+    const char* qkv_base = (const char*)m->qkvh[l];
+    const int64_t BH = (int64_t)m->B * H;
+    for (int bt = 0; bt < m->n_bt; ++bt)
+      for (int ht = 0; ht < m->n_ht; ++ht)
+        for (int st = 0; st < m->n_st; ++st) {
+          const int nz = m->tb * m->th;
+          ZMap zm{bt * m->tb, ht * m->th, m->th, H};
+          const int q0 = st * m->ts, nq = m->ts;
+          // scores = Q K^T / sqrt(hd), causal tiles only
+          {
+            GemmArgs g = b.base();
+            g.M = S; g.N = S; g.K = hd; g.nbatch = nz; g.zm = zm;
+            g.m0 = q0; g.mt = nq; g.n0 = 0; g.nt = std::min<int>(S, (int)round_up(q0 + nq, kCausalBlock));
+            g.A = qkv_base; g.lda = hd; g.a_zs = zq; g.a_trans = 0;
+            g.B = qkv_base + BH * zq * as; g.ldb = hd; g.b_zs = zq; g.b_trans = 0;
+            g.C = m->scores; g.ldc = S; g.c_zs = (int64_t)S * S; g.c_dtype = NNT_F32;
+            g.alpha = 1.0f / sqrtf((float)hd);
+            g.causal = CAUSAL_TILES;
+            std::vector<TileUse> u;
+            box(u, m->gqkvh[l], ACC_R, 0, 2, bt, bt + 1, ht, ht + 1);
+            box(u, m->gscores, ACC_W, bt, bt + 1, ht, ht + 1, st, st + 1);
+            b.gemm_task(P, TT_GEMM_QK, g, std::move(u), 2.0 * hd * causal_rows(q0, nq) * nz);
+          }
+          {
+            Task t;
+            t.type = TT_SOFTMAX_FWD;
+            box(t.uses, m->gscores, ACC_R, bt, bt + 1, ht, ht + 1, st, st + 1);
+            box(t.uses, m->gP[l], ACC_W, bt, bt + 1, ht, ht + 1, st, st + 1);
+            t.bytes = causal_rows(q0, nq) * nz * (4 + as);
+            void* Pl = m->P[l];
+            t.fn = [=](cudaStream_t s) {
+              return launch_softmax_fwd(m->scores, Pl, S, zm, nz, q0, nq, act, s);
+            };
+            P.add(std::move(t));
+          }
+          // O = P V, merged back to token-major [T, d]
+          {
+            GemmArgs g = b.base();
+            g.M = S; g.N = hd; g.K = S; g.nbatch = nz; g.zm = zm;
+            g.m0 = q0; g.mt = nq; g.n0 = 0; g.nt = hd;
+            g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 0;
+            g.B = qkv_base + 2 * BH * zq * as; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
+            g.C = m->O[l]; g.ldc = d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
+            g.hs_hd = hd;
+            g.causal = CAUSAL_K_UPPER;
+            std::vector<TileUse> u;
+            box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1, st, st + 1);
+            box(u, m->gqkvh[l], ACC_R, 2, 3, bt, bt + 1, ht, ht + 1);
+            box(u, m->gO[l], ACC_W, bt * m->n_st + st, bt * m->n_st + st + 1);
+            b.gemm_task(P, TT_GEMM_PV, g, std::move(u), 2.0 * hd * causal_rows(q0, nq) * nz);
+          }
+        }
+    // attention output projection + residual: xmid = x + O Wo^T + bo
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->nce; ++ct) {
+        const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+        GemmArgs g = b.base();
+        g.M = T; g.N = d; g.K = d;
+        g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+        g.A = m->O[l]; g.lda = d;
+        g.B = pw(m, P_(m, l, OW)); g.ldb = d;
+        g.C = m->xmid[l]; g.ldc = d; g.c_dtype = NNT_F32;
+        g.bias = pm(m, P_(m, l, OB));
+        g.resid = m->x[l]; g.ld_resid = d;
+        std::vector<TileUse> u;
+        box(u, m->gO[l], ACC_R, rt, rt + 1);
+        box(u, m->gx[l], ACC_R, rt, rt + 1, ct, ct + 1);
+        box(u, m->gxmid[l], ACC_W, rt, rt + 1, ct, ct + 1);
+        b.gemm_task(P, TT_GEMM_ATTN_O, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
+      }
+    // LN2
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      ln_fwd_task(TT_LN_FWD, &m->xmid[l], m->gxmid[l], &P_(m, l, LN2G), &P_(m, l, LN2B), &m->h2[l],
+                  m->gh2[l], &m->mu2[l], &m->r2[l], m->gstat2[l], rt);
+    // FC + GELU: u = h2 W1^T + b1 (kept, fp32), g = gelu(u)
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->ncf; ++ct) {
+        const int c0 = tile_lo(ct, m->ti), c1 = tile_hi(ct, m->ti, f);
+        GemmArgs g = b.base();
+        g.M = T; g.N = f; g.K = d;
+        g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+        g.A = m->h2[l]; g.lda = d;
+        g.B = pw(m, P_(m, l, FCW)); g.ldb = d;
+        g.C = m->g[l]; g.ldc = f; g.c_dtype = act;
+        g.bias = pm(m, P_(m, l, FCB));
+        g.epi = EPI_GELU; g.aux = m->u[l]; g.ld_aux = f;
+        std::vector<TileUse> u;
+        box(u, m->gh2[l], ACC_R, rt, rt + 1);
+        box(u, m->gu[l], ACC_W, rt, rt + 1, ct, ct + 1);
+        box(u, m->gg[l], ACC_W, rt, rt + 1, ct, ct + 1);
+        b.gemm_task(P, TT_GEMM_FC, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
+      }
+    // MLP projection + residual: x[l+1] = xmid + g W2^T + b2
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->nce; ++ct) {
+        const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+        GemmArgs g = b.base();
+        g.M = T; g.N = d; g.K = f;
+        g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+        g.A = m->g[l]; g.lda = f;
+        g.B = pw(m, P_(m, l, PROJW)); g.ldb = f;
+        g.C = m->x[l + 1]; g.ldc = d; g.c_dtype = NNT_F32;
+        g.bias = pm(m, P_(m, l, PROJB));
+        g.resid = m->xmid[l]; g.ld_resid = d;
+        std::vector<TileUse> u;
+        box(u, m->gg[l], ACC_R, rt, rt + 1);
+        box(u, m->gxmid[l], ACC_R, rt, rt + 1, ct, ct + 1);
+        box(u, m->gx[l + 1], ACC_W, rt, rt + 1, ct, ct + 1);
+        b.gemm_task(P, TT_GEMM_MLP_PROJ, g, std::move(u), 2.0 * m->TT * (c1 - c0) * f);
+      }
+  }
+  // final LN
+  const ParamInfo& lnfg = m->params[2 + 12 * m->L];
+  const ParamInfo& lnfb = m->params[3 + 12 * m->L];
+  for (int rt = 0; rt < m->n_tok; ++rt)
+    ln_fwd_task(TT_LN_FWD, &m->x[m->L], m->gx[m->L], &lnfg, &lnfb, &m->y, m->gy, &m->muf, &m->rf,
+                m->gstatf, rt);
+  // tied LM head: z = y wte^T (fp32 logits)
+  for (int rt = 0; rt < m->n_tok; ++rt)
+    for (int vt = 0; vt < m->ncv; ++vt) {
+      const int c0 = tile_lo(vt, m->tv), c1 = tile_hi(vt, m->tv, V);
+      GemmArgs g = b.base();
+      g.M = T; g.N = V; g.K = d;
+      g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+      g.A = m->y; g.lda = d;
+      g.B = pw(m, m->params[0]); g.ldb = d;
+      g.C = m->z; g.ldc = m->ldz; g.c_dtype = NNT_F32;
+      std::vector<TileUse> u;
+      box(u, m->gy, ACC_R, rt, rt + 1);
+      box(u, m->gz, ACC_W, rt, rt + 1, vt, vt + 1);
+      b.gemm_task(P, TT_GEMM_LM_HEAD, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
+    }
+  // cross-entropy + dlogits per token tile (over every vocab tile)
+  const float inv_T = 1.0f / (float)T;
+  for (int rt = 0; rt < m->n_tok; ++rt) {
+    Task t;
+    t.type = TT_XENT;
+    box(t.uses, m->gz, ACC_R, rt, rt + 1);
+    box(t.uses, m->gtok, ACC_R);
+    box(t.uses, m->gdz, ACC_W, rt, rt + 1);
+    box(t.uses, m->grow_loss, ACC_W, rt, rt + 1);
+    t.bytes = (double)m->TT * V * (4 + as) + 2.0 * m->TT;
+    const int64_t r0 = (int64_t)rt * m->TT;
+    t.fn = [=](cudaStream_t s) {
+      return launch_cross_entropy(m->z, m->ldz, r0, m->TT, V, m->tokens_dev, m->tm, nullptr, 0,
+                                  m->dz, m->lddz, m->row_loss, inv_T, act, s);
+    };
+    P.add(std::move(t));
+  }
+  {
+    Task t;
+    t.type = TT_LOSS;
+    box(t.uses, m->grow_loss, ACC_R);
+    box(t.uses, m->gloss, ACC_W);
+    t.bytes = 4.0 * T;
+    t.fn = [m](cudaStream_t s) { return launch_mean_loss(m->row_loss, m->T, m->loss_dev, s); };
+    P.add(std::move(t));
+  }
+}
+
+// -------------------------------------------------------------- backward
+void build_backward(nnt_model* m) {
+  Builder b{m};
+  Program& P = m->bwd;
+  const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
+  const size_t as = m->act_size;
+  const int act = m->act;
+  const int lnp = ln_bwd_nparts(m->TT, d);
+
+  // dX tasks: out[rows rt, cols ct] = dY[rt] * W  (W [out, in], K = out); the
+  // caller lists the tiles read and written.
+  auto dx_gemm = [&](int type, const void* dY, int64_t ldy, int K, const ParamInfo& W, int64_t ldw,
+                     void* out, int out_dtype, int N, int tileN, int rt, int ct, GemmArgs proto,
+                     std::vector<TileUse> uses) {
+    const int c0 = tile_lo(ct, tileN), c1 = tile_hi(ct, tileN, N);
+    GemmArgs g = proto;
+    g.M = T; g.N = N; g.K = K;
+    g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+    g.A = dY; g.lda = ldy; g.a_trans = 0;
+    g.B = pw(m, W); g.ldb = ldw; g.b_trans = 1;
+    g.C = out; if (!g.ldc) g.ldc = N; g.c_dtype = out_dtype;
+    b.gemm_task(P, type, g, std::move(uses), 2.0 * m->TT * (c1 - c0) * K);
+  };
+  // dW tasks: grad[out tile, in tile] = dY^T X over all tokens
+  auto dw_gemm = [&](int type, const void* dY, const TGrid& gdY, int64_t ldy, int Nout, int tOut,
+                     const void* X, const TGrid& gX, int64_t ldx, int Nin, int tIn, const ParamInfo& W,
+                     int gidx) {
+    for (int ot = 0; ot < tiles_of(Nout, tOut); ++ot)
+      for (int it = 0; it < tiles_of(Nin, tIn); ++it) {
+        const int o0 = tile_lo(ot, tOut), o1 = tile_hi(ot, tOut, Nout);
+        const int i0 = tile_lo(it, tIn), i1 = tile_hi(it, tIn, Nin);
+        GemmArgs g = b.base();
+        g.M = Nout; g.N = Nin; g.K = T;
+        g.m0 = o0; g.mt = o1 - o0; g.n0 = i0; g.nt = i1 - i0;
+        g.A = dY; g.lda = ldy; g.a_trans = 1;
+        g.B = X; g.ldb = ldx; g.b_trans = 1;
+        g.C = pg(m, W); g.ldc = Nin; g.c_dtype = NNT_F32;
+        std::vector<TileUse> u;
+        box(u, gdY, ACC_R);
+        box(u, gX, ACC_R);
+        box(u, m->ggrad[gidx], ACC_W, ot, ot + 1, it, it + 1);
+        b.gemm_task(P, TT_GEMM_DW, g, std::move(u), 2.0 * (o1 - o0) * (i1 - i0) * T);
+      }
+  };
+  auto colsum_task = [&](const void* a, int a_dtype, const TGrid& ga, int N, const ParamInfo& bp, int gidx) {
+    Task t;
+    t.type = TT_COLSUM;
+    box(t.uses, ga, ACC_R);
+    box(t.uses, m->gcol_part, ACC_RW);
+    box(t.uses, m->ggrad[gidx], ACC_W);
+    t.bytes = (double)T * N * (a_dtype == NNT_BF16 ? 2 : 4);
+    float* out = pg(m, bp);
+    t.fn = [=](cudaStream_t s) {
+      return launch_colsum(a, a_dtype, T, N, N, m->col_part, out, 0, s);
+    };
+    P.add(std::move(t));
+  };
+  // LN backward per token tile + parameter-grad reduction
+  auto ln_bwd = [&](const float* dy, const TGrid& gdy, const float* xin, const TGrid& gxin, const float* mu,
+                    const float* rs, const TGrid& gst, const ParamInfo& gm, const ParamInfo& bt_,
+                    int gidx_g, int gidx_b, bool has_resid) {
+    for (int rt = 0; rt < m->n_tok; ++rt) {
+      Task t;
+      t.type = TT_LN_BWD;
+      box(t.uses, gdy, ACC_R, rt, rt + 1);
+      box(t.uses, gxin, ACC_R, rt, rt + 1);
+      box(t.uses, gst, ACC_R, rt, rt + 1);
+      box(t.uses, m->gdres, has_resid ? ACC_RW : ACC_W, rt, rt + 1);
+      box(t.uses, m->gdres_act, ACC_W, rt, rt + 1);
+      box(t.uses, m->gln_part, ACC_W, rt, rt + 1);
+      t.bytes = (double)m->TT * d * (4 * (has_resid ? 4 : 3) + as);
+      const int64_t r0 = (int64_t)rt * m->TT;
+      const float* gam = pm(m, gm);
+      t.fn = [=](cudaStream_t s) {
+        return launch_layernorm_bwd(dy + r0 * d, xin + r0 * d, mu + r0, rs + r0, gam,
+                                    has_resid ? m->dres + r0 * d : nullptr, m->dres + r0 * d,
+                                    (char*)m->dres_act + r0 * d * as,
+                                    m->ln_part_g + (int64_t)rt * lnp * d,
+                                    m->ln_part_b + (int64_t)rt * lnp * d, m->TT, d, act, s);
+      };
+      P.add(std::move(t));
+    }
+    Task t;
+    t.type = TT_LN_PARTS;
+    box(t.uses, m->gln_part, ACC_R);
+    box(t.uses, m->ggrad[gidx_g], ACC_W);
+    box(t.uses, m->ggrad[gidx_b], ACC_W);
+    t.bytes = 2.0 * m->n_tok * lnp * d * 4;
+    float* og = pg(m, gm);
+    float* ob = pg(m, bt_);
+    t.fn = [=](cudaStream_t s) {
+      NNT_TRY(launch_sum_parts(m->ln_part_g, (int64_t)m->n_tok * lnp, d, d, og, 0, s));
+      return launch_sum_parts(m->ln_part_b, (int64_t)m->n_tok * lnp, d, d, ob, 0, s);
+    };
+    P.add(std::move(t));
+  };
+  const int pidx_lnf = 2 + 12 * m->L;
+
+  // LM head backward: dy_f = dz wte (fp32), dwte = dz^T y
+  for (int rt = 0; rt < m->n_tok; ++rt)
+    for (int ct = 0; ct < m->nce; ++ct) {
+      const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+      GemmArgs g = b.base();
+      g.M = T; g.N = d; g.K = V;
+      g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
+      g.A = m->dz; g.lda = m->lddz; g.a_trans = 0;
+      g.B = pw(m, m->params[0]); g.ldb = d; g.b_trans = 1;
+      g.C = m->dtmp; g.ldc = d; g.c_dtype = NNT_F32;
+      std::vector<TileUse> u;
+      box(u, m->gdz, ACC_R, rt, rt + 1);
+      box(u, m->gdtmp, ACC_W, rt, rt + 1, ct, ct + 1);
+      b.gemm_task(P, TT_GEMM_LM_DX, g, std::move(u), 2.0 * m->TT * (c1 - c0) * V);
+    }
+  for (int vt = 0; vt < m->ncv; ++vt)
+    for (int ct = 0; ct < m->nce; ++ct) {
+      const int v0 = tile_lo(vt, m->tv), v1 = tile_hi(vt, m->tv, V);
+      const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+      GemmArgs g = b.base();
+      g.M = V; g.N = d; g.K = T;
+      g.m0 = v0; g.mt = v1 - v0; g.n0 = c0; g.nt = c1 - c0;
+      g.A = m->dz; g.lda = m->lddz; g.a_trans = 1;
+      g.B = m->y; g.ldb = d; g.b_trans = 1;
+      g.C = pg(m, m->params[0]); g.ldc = d; g.c_dtype = NNT_F32;
+      std::vector<TileUse> u;
+      box(u, m->gdz, ACC_R);
+      box(u, m->gy, ACC_R);
+      box(u, m->ggrad[0], ACC_W, vt, vt + 1, ct, ct + 1);
+      b.gemm_task(P, TT_GEMM_LM_DW, g, std::move(u), 2.0 * (v1 - v0) * (c1 - c0) * T);
+    }
+  // final LN backward (no residual input: dres starts here)
+  ln_bwd(m->dtmp, m->gdtmp, m->x[m->L], m->gx[m->L], m->muf, m->rf, m->gstatf, m->params[pidx_lnf],
+         m->params[pidx_lnf + 1], pidx_lnf, pidx_lnf + 1, false);
+
+  const size_t zq = (size_t)S * hd;
+  const int64_t BH = (int64_t)m->B * H;
+  for (int l = m->L - 1; l >= 0; --l) {
+    const int pi = 2 + 12 * l;
+    // MLP: du = (dres W2) * gelu'(u)
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->ncf; ++ct) {
+        GemmArgs proto = b.base();
+        proto.epi = EPI_GELU_BWD;
+        proto.aux = m->u[l];
+        proto.ld_aux = f;
+        std::vector<TileUse> u;
+        box(u, m->gdres_act, ACC_R, rt, rt + 1);
+        box(u, m->gu[l], ACC_R, rt, rt + 1, ct, ct + 1);
+        box(u, m->gdu, ACC_W, rt, rt + 1, ct, ct + 1);
+        dx_gemm(TT_GEMM_DX, m->dres_act, d, d, P_(m, l, PROJW), f, m->du, act, f, m->ti, rt, ct,
+                proto, std::move(u));
+      }
+    dw_gemm(TT_GEMM_DW, m->dres_act, m->gdres_act, d, d, m->te, m->g[l], m->gg[l], f, f, m->ti,
+            P_(m, l, PROJW), pi + PROJW);
+    colsum_task(m->dres, NNT_F32, m->gdres, d, P_(m, l, PROJB), pi + PROJB);
+    dw_gemm(TT_GEMM_DW, m->du, m->gdu, f, f, m->ti, m->h2[l], m->gh2[l], d, d, m->te, P_(m, l, FCW),
+            pi + FCW);
+    colsum_task(m->du, act, m->gdu, f, P_(m, l, FCB), pi + FCB);
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->nce; ++ct) {
+        std::vector<TileUse> u;
+        box(u, m->gdu, ACC_R, rt, rt + 1);
+        box(u, m->gdtmp, ACC_W, rt, rt + 1, ct, ct + 1);
+        dx_gemm(TT_GEMM_DX, m->du, f, f, P_(m, l, FCW), d, m->dtmp, NNT_F32, d, m->te, rt, ct,
+                b.base(), std::move(u));
+      }
+    ln_bwd(m->dtmp, m->gdtmp, m->xmid[l], m->gxmid[l], m->mu2[l], m->r2[l], m->gstat2[l],
+           P_(m, l, LN2G), P_(m, l, LN2B), pi + LN2G, pi + LN2B, true);
+    // attention output projection: dO (head-major), dWo, dbo
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->nce; ++ct) {
+        GemmArgs proto = b.base();
+        proto.out_mode = OUT_HEADSPLIT;
+        proto.hs_B = m->B; proto.hs_H = H; proto.hs_S = S; proto.hs_hd = hd; proto.hs_d = d;
+        proto.ldc = d;
+        const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+        int h0, h1;
+        b.head_tiles(c0, c1, h0, h1);
+        std::vector<TileUse> u;
+        box(u, m->gdres_act, ACC_R, rt, rt + 1);
+        box(u, m->gdOh, ACC_W, 0, 1, b.bt_of(rt), b.bt_of(rt) + 1, h0, h1, b.st_of(rt), b.st_of(rt) + 1);
+        dx_gemm(TT_GEMM_DX, m->dres_act, d, d, P_(m, l, OW), d, m->dOh, act, d, m->te, rt, ct, proto,
+                std::move(u));
+      }
+    dw_gemm(TT_GEMM_DW, m->dres_act, m->gdres_act, d, d, m->te, m->O[l], m->gO[l], d, d, m->te,
+            P_(m, l, OW), pi + OW);
+    colsum_task(m->dres, NNT_F32, m->gdres, d, P_(m, l, OB), pi + OB);
+    // attention backward per (batch tile, head tile)
+    const char* qkv_base = (const char*)m->qkvh[l];
+    for (int bt = 0; bt < m->n_bt; ++bt)
+      for (int ht = 0; ht < m->n_ht; ++ht) {
+        const int nz = m->tb * m->th;
+        ZMap zm{bt * m->tb, ht * m->th, m->th, H};
+        // dV = P^T dO per key tile
+        for (int kt = 0; kt < m->n_st; ++kt) {
+          const int k0 = kt * m->ts, nk = m->ts;
+          GemmArgs g = b.base();
+          g.M = S; g.N = hd; g.K = S; g.nbatch = nz; g.zm = zm;
+          g.m0 = k0; g.mt = nk; g.n0 = 0; g.nt = hd;
+          g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 1;
+          g.B = m->dOh; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
+          g.C = m->dqkv; g.ldc = 3 * d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
+          g.c_col_off = 2 * d; g.hs_hd = hd;
+          g.causal = CAUSAL_K_LOWER;
+          std::vector<TileUse> u;
+          box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1);
+          box(u, m->gdOh, ACC_R, 0, 1, bt, bt + 1, ht, ht + 1);
+          box(u, m->gdqkv, ACC_W, 2, 3, bt * m->n_st + kt, bt * m->n_st + kt + 1, ht, ht + 1);
+          const double pairs = (double)nk * S - causal_rows(k0, nk) + nk;  // sum_k (S - k)
+          b.gemm_task(P, TT_GEMM_ATTN_BWD, g, std::move(u), 2.0 * hd * pairs * nz);
+        }
+        // dP = dO V^T, dS = softmax_bwd(P, dP) (into P's buffer), dQ = dS K per query tile
+        for (int st = 0; st < m->n_st; ++st) {
+          const int q0 = st * m->ts, nq = m->ts;
+          {
+            GemmArgs g = b.base();
+            g.M = S; g.N = S; g.K = hd; g.nbatch = nz; g.zm = zm;
+            g.m0 = q0; g.mt = nq; g.n0 = 0; g.nt = std::min<int>(S, (int)round_up(q0 + nq, kCausalBlock));
+            g.A = m->dOh; g.lda = hd; g.a_zs = zq; g.a_trans = 0;
+            g.B = qkv_base + 2 * BH * zq * as; g.ldb = hd; g.b_zs = zq; g.b_trans = 0;
+            g.C = m->scores; g.ldc = S; g.c_zs = (int64_t)S * S; g.c_dtype = NNT_F32;
+            g.causal = CAUSAL_TILES;
+            std::vector<TileUse> u;
+            box(u, m->gdOh, ACC_R, 0, 1, bt, bt + 1, ht, ht + 1, st, st + 1);
+            box(u, m->gqkvh[l], ACC_R, 2, 3, bt, bt + 1, ht, ht + 1);
+            box(u, m->gscores, ACC_W, bt, bt + 1, ht, ht + 1, st, st + 1);
+            b.gemm_task(P, TT_GEMM_ATTN_BWD, g, std::move(u), 2.0 * hd * causal_rows(q0, nq) * nz);
+          }
+          {
+            Task t;
+            t.type = TT_SOFTMAX_BWD;
+            box(t.uses, m->gscores, ACC_R, bt, bt + 1, ht, ht + 1, st, st + 1);
+            box(t.uses, m->gP[l], ACC_RW, bt, bt + 1, ht, ht + 1, st, st + 1);
+            t.bytes = causal_rows(q0, nq) * nz * (4 + 2 * as);
+            void* Pl = m->P[l];
+            const float scale = 1.0f / sqrtf((float)hd);
+            t.fn = [=](cudaStream_t s) {
+              return launch_softmax_bwd(Pl, m->scores, Pl, S, zm, nz, q0, nq, scale, act, s);
+            };
+            P.add(std::move(t));
+          }
+          {
+            GemmArgs g = b.base();
+            g.M = S; g.N = hd; g.K = S; g.nbatch = nz; g.zm = zm;
+            g.m0 = q0; g.mt = nq; g.n0 = 0; g.nt = hd;
+            g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 0;
+            g.B = qkv_base + BH * zq * as; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
+            g.C = m->dqkv; g.ldc = 3 * d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
+            g.c_col_off = 0; g.hs_hd = hd;
+            g.causal = CAUSAL_K_UPPER;
+            std::vector<TileUse> u;
+            box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1, st, st + 1);
+            box(u, m->gqkvh[l], ACC_R, 1, 2, bt, bt + 1, ht, ht + 1);
+            box(u, m->gdqkv, ACC_W, 0, 1, bt * m->n_st + st, bt * m->n_st + st + 1, ht, ht + 1);
+            b.gemm_task(P, TT_GEMM_ATTN_BWD, g, std::move(u), 2.0 * hd * causal_rows(q0, nq) * nz);
+          }
+        }
+        // dK = dS^T Q per key tile
+        for (int kt = 0; kt < m->n_st; ++kt) {
+          const int k0 = kt * m->ts, nk = m->ts;
+          GemmArgs g = b.base();
+          g.M = S; g.N = hd; g.K = S; g.nbatch = nz; g.zm = zm;
+          g.m0 = k0; g.mt = nk; g.n0 = 0; g.nt = hd;
+          g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 1;
+          g.B = qkv_base; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
+          g.C = m->dqkv; g.ldc = 3 * d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
+          g.c_col_off = d; g.hs_hd = hd;
+          g.causal = CAUSAL_K_LOWER;
+          std::vector<TileUse> u;
+          box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1);
+          box(u, m->gqkvh[l], ACC_R, 0, 1, bt, bt + 1, ht, ht + 1);
+          box(u, m->gdqkv, ACC_W, 1, 2, bt * m->n_st + kt, bt * m->n_st + kt + 1, ht, ht + 1);
+          const double pairs = (double)nk * S - causal_rows(k0, nk) + nk;
+          b.gemm_task(P, TT_GEMM_ATTN_BWD, g, std::move(u), 2.0 * hd * pairs * nz);
+        }
+      }
+    // QKV projection backward
+    dw_gemm(TT_GEMM_DW, m->dqkv, m->gdqkv, 3 * d, 3 * d, m->te, m->h1[l], m->gh1[l], d, d, m->te,
+            P_(m, l, QKVW), pi + QKVW);
+    colsum_task(m->dqkv, act, m->gdqkv, 3 * d, P_(m, l, QKVB), pi + QKVB);
+    for (int rt = 0; rt < m->n_tok; ++rt)
+      for (int ct = 0; ct < m->nce; ++ct) {
+        std::vector<TileUse> u;
+        box(u, m->gdqkv, ACC_R, 0, 3, rt, rt + 1);
+        box(u, m->gdtmp, ACC_W, rt, rt + 1, ct, ct + 1);
+        dx_gemm(TT_GEMM_DX, m->dqkv, 3 * d, 3 * d, P_(m, l, QKVW), d, m->dtmp, NNT_F32, d, m->te, rt,
+                ct, b.base(), std::move(u));
+      }
+    ln_bwd(m->dtmp, m->gdtmp, m->x[l], m->gx[l], m->mu1[l], m->r1[l], m->gstat1[l], P_(m, l, LN1G),
+           P_(m, l, LN1B), pi + LN1G, pi + LN1B, true);
+  }
+  // embedding backward: token sort, wte scatter-add (after the LM-head dW), wpe sums
+  {
+    Task t;
+    t.type = TT_EMB_SORT;
+    box(t.uses, m->gtok, ACC_R);
+    box(t.uses, m->gkeys, ACC_W);
+    t.bytes = 6.0 * T;
+    t.fn = [m](cudaStream_t s) {
+      return launch_token_sort(m->tokens_dev, m->S + 1, m->B, m->S, m->sort_keys, s);
+    };
+    P.add(std::move(t));
+  }
+  {
+    Task t;
+    t.type = TT_EMB_SCATTER;
+    box(t.uses, m->gkeys, ACC_R);
+    box(t.uses, m->gdres, ACC_R);
+    box(t.uses, m->ggrad[0], ACC_RW);
+    t.bytes = (double)T * d * 12;
+    t.fn = [m](cudaStream_t s) {
+      return launch_embedding_scatter(m->sort_keys, m->T, m->dres, m->tm, m->S,
+                                      m->grad + m->params[0].off, m->d, m->V, s);
+    };
+    P.add(std::move(t));
+  }
+  for (int st = 0; st < m->n_st; ++st) {
+    Task t;
+    t.type = TT_WPE_GRAD;
+    for (int bt = 0; bt < m->n_bt; ++bt) box(t.uses, m->gdres, ACC_R, bt * m->n_st + st, bt * m->n_st + st + 1);
+    box(t.uses, m->ggrad[1], ACC_W, st, st + 1);
+    t.bytes = (double)T / m->n_st * d * 4 + (double)m->ts * d * 4;
+    const int s0 = st * m->ts;
+    t.fn = [m, s0](cudaStream_t s) {
+      return launch_wpe_grad(m->dres, m->tm, m->B, s0, m->ts, m->d, m->grad + m->params[1].off, 0, s);
+    };
+    P.add(std::move(t));
+  }
+}
+
+void build_optimizer(nnt_model* m) {
+  // one AdamW task per chunk of the flat parameter buffers (<= 256 Mi elements)
+  const int64_t chunk = 256ll << 20;
+  for (int64_t o = 0; o < m->n_flat; o += chunk) {
+    const int64_t n = std::min(chunk, m->n_flat - o);
+    Task t;
+    t.type = TT_ADAMW;
+    t.bytes = 30.0 * n;
+    t.fn = [m, o, n](cudaStream_t s) {
+      return launch_adamw_dev(m->master + o, m->grad + o, m->mom1 + o, m->mom2 + o, m->wbf + o, n,
+                              reinterpret_cast<const float*>(m->hyper_dev), s);
+    };
+    m->opt.add(std::move(t));
+  }
+}
+
+void make_grids(nnt_model* m) {
+  const int L = m->L;
+  for (int l = 0; l <= L; ++l) m->gx.push_back(new_grid(m, m->n_tok, m->nce));
+  for (int l = 0; l < L; ++l) {
+    m->gxmid.push_back(new_grid(m, m->n_tok, m->nce));
+    m->gh1.push_back(new_grid(m, m->n_tok, m->nce));
+    m->gstat1.push_back(new_grid(m, m->n_tok));
+    m->gqkvh.push_back(new_grid(m, 3, m->n_bt, m->n_ht, m->n_st));
+    m->gP.push_back(new_grid(m, m->n_bt, m->n_ht, m->n_st));
+    m->gO.push_back(new_grid(m, m->n_tok, m->nce));
+    m->gh2.push_back(new_grid(m, m->n_tok, m->nce));
+    m->gstat2.push_back(new_grid(m, m->n_tok));
+    m->gu.push_back(new_grid(m, m->n_tok, m->ncf));
+    m->gg.push_back(new_grid(m, m->n_tok, m->ncf));
+  }
+  m->gscores = new_grid(m, m->n_bt, m->n_ht, m->n_st);
+  m->gy = new_grid(m, m->n_tok, m->nce);
+  m->gstatf = new_grid(m, m->n_tok);
+  m->gz = new_grid(m, m->n_tok, m->ncv);
+  m->gdz = new_grid(m, m->n_tok, m->ncv);
+  m->grow_loss = new_grid(m, m->n_tok);
+  m->gloss = new_grid(m, 1);
+  m->gtok = new_grid(m, 1);
+  m->gdres = new_grid(m, m->n_tok, m->nce);
+  m->gdres_act = new_grid(m, m->n_tok, m->nce);
+  m->gdtmp = new_grid(m, m->n_tok, m->nce);
+  m->gdu = new_grid(m, m->n_tok, m->ncf);
+  m->gdOh = new_grid(m, 1, m->n_bt, m->n_ht, m->n_st);
+  m->gdqkv = new_grid(m, 3, m->n_tok, m->n_ht);
+  m->gln_part = new_grid(m, m->n_tok);
+  m->gcol_part = new_grid(m, 1);
+  m->gkeys = new_grid(m, 1);
+  // parameter gradients: weights tiled [out tile, in tile], vectors by their axis
+  for (const ParamInfo& p : m->params) {
+    auto axis_tile = [&](int64_t n) -> int {
+      if (n == m->d) return m->te;
+      if (n == 3 * (int64_t)m->d) return m->te;
+      if (n == m->f) return m->ti;
+      if (n == m->V) return m->tv;
+      if (n == m->S) return m->ts;
+      return (int)n;
+    };
+    int a = tiles_of((int)p.shape0, axis_tile(p.shape0));
+    int bcount = p.shape1 ? tiles_of((int)p.shape1, axis_tile(p.shape1)) : 1;
+    m->ggrad.push_back(new_grid(m, a, bcount));
+  }
+}
+
+nnt_status wait_event(nnt_model* m, cudaEvent_t ev) {
+  const uint32_t tmo = m->opts.timeout_ms ? m->opts.timeout_ms : 600000u;
+  auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return NNT_OK;
+    if (e != cudaErrorNotReady) {
+      set_thread_error("device work failed: %s", cudaGetErrorString(e));
+      return NNT_ERR_CUDA;
+    }
+    auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+    if (ms > tmo) {
+      set_thread_error("wait for the device timed out after %u ms", tmo);
+      return NNT_ERR_TIMEOUT;
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+nnt_status sync_model(nnt_model* m) {
+  NNT_CUDA_TRY(cudaEventRecord(m->done_event, m->ex.main_));
+  return wait_event(m, m->done_event);
+}
+
+nnt_status check_device_error(nnt_model* m) {
+  uint32_t code = 0;
+  NNT_TRY(read_and_clear_device_error(&code, m->ex.main_));
+  if (code & DEVERR_TOKEN_RANGE) {
+    set_thread_error("token id >= vocab (%d) in the batch", m->V);
+    return NNT_ERR_INVALID_ARG;
+  }
+  if (code) {
+    set_thread_error("device error word 0x%x", code);
+    return NNT_ERR_INTERNAL;
+  }
+  return NNT_OK;
+}
+
+void free_model(nnt_model* m) {
+  if (!m) return;
+  cudaDeviceSynchronize();
+  for (void* p : m->dev_allocs) cudaFree(p);
+  m->dev_allocs.clear();
+  if (m->loss_host) cudaFreeHost(m->loss_host);
+  if (m->done_event) cudaEventDestroy(m->done_event);
+  cudaStream_t own = m->ex.main_;
+  bool owned = m->opts.stream == nullptr;
+  m->ex.~Executor();
+  new (&m->ex) Executor();
+  if (owned && own) cudaStreamDestroy(own);
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
+                            const nnt_options* opts, nnt_model** out) {
+  if (!out) {
+    set_thread_error("out is NULL");
+    t_model_err = thread_error();
+    return NNT_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  nnt_status s = validate(cfg, tiles);
+  if (s != NNT_OK) return fail(nullptr, s);
+  nnt_model* m = new nnt_model();
+  m->cfg = *cfg;
+  nnt_tiles zt{};
+  m->tiles = tiles ? *tiles : zt;
+  nnt_options zo{};
+  m->opts = opts ? *opts : zo;
+  m->act = cfg->dtype;
+  m->act_size = m->act == NNT_BF16 ? 2 : 4;
+  m->L = cfg->n_layer; m->d = cfg->d_model; m->H = cfg->n_head; m->hd = m->d / m->H;
+  m->f = cfg->d_ff; m->V = cfg->vocab; m->S = cfg->n_ctx; m->B = cfg->batch; m->T = m->B * m->S;
+  m->tb = m->tiles.batch_tile ? m->tiles.batch_tile : m->B;
+  m->ts = m->tiles.seq_tile ? m->tiles.seq_tile : m->S;
+  m->te = m->tiles.embd_tile ? std::min(m->tiles.embd_tile, m->d) : m->d;
+  m->ti = m->tiles.inner_tile ? std::min(m->tiles.inner_tile, m->f) : m->f;
+  m->th = m->tiles.head_tile ? m->tiles.head_tile : m->H;
+  m->tv = m->tiles.vocab_tile ? std::min(m->tiles.vocab_tile, m->V) : m->V;
+  m->n_bt = m->B / m->tb; m->n_st = m->S / m->ts; m->n_ht = m->H / m->th;
+  m->n_tok = m->n_bt * m->n_st; m->TT = m->tb * m->ts;
+  m->nce = tiles_of(m->d, m->te); m->ncf = tiles_of(m->f, m->ti); m->ncv = tiles_of(m->V, m->tv);
+  m->tm = TokMap{m->S, m->tb, m->ts, m->n_st};
+  m->ldz = round_up(m->V, 4);
+  m->lddz = round_up(m->V, 8);
+  m->backend = m->opts.gemm_backend;
+  if (m->opts.n_streams <= 0) m->opts.n_streams = 2;
+  m->opts.n_streams = std::min(m->opts.n_streams, 8);
+
+  cudaStream_t main = (cudaStream_t)m->opts.stream;
+  if (!main) {
+    cudaError_t e = cudaStreamCreate(&main);
+    if (e != cudaSuccess) {
+      set_thread_error("cudaStreamCreate: %s", cudaGetErrorString(e));
+      delete m;
+      return fail(nullptr, NNT_ERR_CUDA);
+    }
+  }
+  s = m->ex.init(main, m->opts.n_streams, false, m->opts.trace != 0, TT_COUNT);
+  if (s == NNT_OK && cudaEventCreateWithFlags(&m->done_event, cudaEventDisableTiming) != cudaSuccess)
+    s = NNT_ERR_CUDA;
+  if (s == NNT_OK) s = alloc_all(m);
+  if (s == NNT_OK) s = init_params(m, main);
+  if (s == NNT_OK) {
+    make_grids(m);
+    build_forward(m);
+    build_backward(m);
+    build_optimizer(m);
+    m->fwd.finalize(m->opts.n_streams);
+    m->bwd.finalize(m->opts.n_streams);
+    m->opt.finalize(1);
+    s = sync_model(m);
+  }
+  if (s != NNT_OK) {
+    fail(nullptr, s);
+    free_model(m);
+    delete m;
+    return s;
+  }
+  *out = m;
+  return NNT_OK;
+}
+
+nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_device,
+                       float* loss_out) {
+  if (!m || !tokens) {
+    set_thread_error("NULL model or tokens");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  auto t0 = std::chrono::steady_clock::now();
+  const size_t tb = (size_t)m->B * (m->S + 1) * 2;
+  cudaStream_t st = m->ex.main_;
+  nnt_status s = NNT_OK;
+  if (cudaMemcpyAsync(m->tokens_dev, tokens, tb,
+                      tokens_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                      st) != cudaSuccess) {
+    set_thread_error("token copy failed: %s", cudaGetErrorString(cudaGetLastError()));
+    return fail(m, NNT_ERR_CUDA);
+  }
+  if (m->opts.trace) m->ex.reset_trace();
+  s = m->ex.run(m->fwd, m->opts.use_cuda_graph ? 0 : -1);
+  if (s != NNT_OK) return fail(m, s);
+  m->state = 1;
+  if (loss_out || m->opts.trace) {
+    if (cudaMemcpyAsync(m->loss_host, m->loss_dev, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return fail(m, NNT_ERR_CUDA);
+    s = check_device_error(m);
+    if (s != NNT_OK) {
+      m->state = 0;
+      return fail(m, s);
+    }
+    if (loss_out) *loss_out = *m->loss_host;
+    if (m->opts.trace) {
+      s = m->ex.collect_trace(m->fwd);
+      if (s != NNT_OK) return fail(m, s);
+    }
+    m->last_fwd_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  }
+  return NNT_OK;
+}
+
+nnt_status nnt_backward(nnt_model* m) {
+  if (!m) {
+    set_thread_error("NULL model");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  if (m->state != 1) {
+    set_thread_error("nnt_backward needs a preceding nnt_forward");
+    return fail(m, NNT_ERR_STATE);
+  }
+  auto t0 = std::chrono::steady_clock::now();
+  nnt_status s = m->ex.run(m->bwd, m->opts.use_cuda_graph ? 1 : -1);
+  if (s != NNT_OK) return fail(m, s);
+  m->state = 2;
+  if (m->opts.trace) {
+    s = sync_model(m);
+    if (s == NNT_OK) s = m->ex.collect_trace(m->bwd);
+    if (s != NNT_OK) return fail(m, s);
+    m->last_bwd_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  }
+  return NNT_OK;
+}
+
+nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp) {
+  if (!m || !hp) {
+    set_thread_error("NULL model or hyper-parameters");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  if (m->state != 2) {
+    set_thread_error("nnt_adamw_step needs a preceding nnt_backward");
+    return fail(m, NNT_ERR_STATE);
+  }
+  if (!(hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1) ||
+      !(hp->eps > 0) || !(hp->weight_decay >= 0)) {
+    set_thread_error("invalid AdamW hyper-parameters");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  auto t0 = std::chrono::steady_clock::now();
+  const int64_t t = m->step + 1;
+  AdamHyperDev& h = m->hyper_host;
+  h.lr = hp->lr; h.b1 = hp->beta1; h.b2 = hp->beta2; h.eps = hp->eps; h.wd = hp->weight_decay;
+  h.bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
+  h.bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
+  h.pad = 0;
+  if (cudaMemcpyAsync(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_) != cudaSuccess)
+    return fail(m, NNT_ERR_CUDA);
+  nnt_status s = m->ex.run(m->opt, m->opts.use_cuda_graph ? 2 : -1);
+  if (s != NNT_OK) return fail(m, s);
+  m->step = t;
+  m->state = 0;
+  if (m->opts.trace) {
+    s = sync_model(m);
+    if (s == NNT_OK) s = m->ex.collect_trace(m->opt);
+    if (s != NNT_OK) return fail(m, s);
+    m->last_opt_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  }
+  return NNT_OK;
+}
+
+void nnt_destroy(nnt_model* m) {
+  if (!m) return;
+  free_model(m);
+  delete m;
+}
+
+int32_t nnt_num_params(const nnt_model* m) { return m ? (int32_t)m->params.size() : -1; }
+
+nnt_status nnt_param_info(const nnt_model* m, int32_t i, const char** name, int64_t shape[2]) {
+  if (!m || i < 0 || i >= (int32_t)m->params.size()) {
+    set_thread_error("bad parameter index");
+    return NNT_ERR_INVALID_ARG;
+  }
+  if (name) *name = m->params[i].name.c_str();
+  if (shape) {
+    shape[0] = m->params[i].shape0;
+    shape[1] = m->params[i].shape1;
+  }
+  return NNT_OK;
+}
+
+static nnt_status copy_param(nnt_model* m, int32_t i, float* base, float* host, bool to_dev) {
+  if (!m || !host || i < 0 || i >= (int32_t)m->params.size()) {
+    set_thread_error("bad model, buffer or parameter index");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  const ParamInfo& p = m->params[i];
+  cudaStream_t st = m->ex.main_;
+  if (to_dev) {
+    if (cudaMemcpyAsync(base + p.off, host, p.n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return fail(m, NNT_ERR_CUDA);
+    if (base == m->master) {
+      nnt_status s = launch_cast_bf16(m->master + p.off, m->wbf + p.off, p.n, st);
+      if (s != NNT_OK) return fail(m, s);
+    }
+  } else {
+    if (cudaMemcpyAsync(host, base + p.off, p.n * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return fail(m, NNT_ERR_CUDA);
+  }
+  nnt_status s = sync_model(m);
+  return s == NNT_OK ? s : fail(m, s);
+}
+
+nnt_status nnt_get_param(nnt_model* m, int32_t i, float* host_buf) {
+  return copy_param(m, i, m ? m->master : nullptr, host_buf, false);
+}
+nnt_status nnt_set_param(nnt_model* m, int32_t i, const float* host_buf) {
+  return copy_param(m, i, m ? m->master : nullptr, const_cast<float*>(host_buf), true);
+}
+nnt_status nnt_get_grad(nnt_model* m, int32_t i, float* host_buf) {
+  return copy_param(m, i, m ? m->grad : nullptr, host_buf, false);
+}
+nnt_status nnt_get_adam_state(nnt_model* m, int32_t i, int32_t which, float* host_buf) {
+  if (which != 0 && which != 1) {
+    set_thread_error("which must be 0 (m) or 1 (v)");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  return copy_param(m, i, m ? (which ? m->mom2 : m->mom1) : nullptr, host_buf, false);
+}
+
+nnt_status nnt_get_logits(nnt_model* m, float* host_buf) {
+  if (!m || !host_buf) {
+    set_thread_error("NULL model or buffer");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  if (cudaMemcpy2DAsync(host_buf, (size_t)m->V * 4, m->z, (size_t)m->ldz * 4, (size_t)m->V * 4, m->T,
+                        cudaMemcpyDeviceToHost, m->ex.main_) != cudaSuccess)
+    return fail(m, NNT_ERR_CUDA);
+  nnt_status s = sync_model(m);
+  return s == NNT_OK ? s : fail(m, s);
+}
+
+nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out) {
+  if (!m || !out) {
+    set_thread_error("NULL model or stats");
+    return NNT_ERR_INVALID_ARG;
+  }
+  memset(out, 0, sizeof *out);
+  out->last_forward_ms = m->last_fwd_ms;
+  out->last_backward_ms = m->last_bwd_ms;
+  out->last_adamw_ms = m->last_opt_ms;
+  out->device_bytes = m->device_bytes;
+  out->host_pinned_bytes = m->host_bytes;
+  out->n_tasks_forward = (int64_t)m->fwd.size();
+  out->n_tasks_backward = (int64_t)m->bwd.size();
+  out->n_tasks_adamw = (int64_t)m->opt.size();
+  out->n_tiles = m->next_tile;
+  out->n_params = m->n_scalar;
+  out->n_streams = m->opts.n_streams;
+  return NNT_OK;
+}
+
+int32_t nnt_get_task_times(const nnt_model* m, int32_t max_types, const char** names,
+                           int64_t* launches, double* ms, double* flops, double* bytes) {
+  if (!m) return -1;
+  const int n = std::min<int>(max_types, TT_COUNT);
+  for (int i = 0; i < n; ++i) {
+    if (names) names[i] = kTaskNames[i];
+    if (launches) launches[i] = m->ex.type_launches_.empty() ? 0 : m->ex.type_launches_[i];
+    if (ms) ms[i] = m->ex.type_ms_.empty() ? 0 : m->ex.type_ms_[i];
+    if (flops) flops[i] = m->ex.type_flops_.empty() ? 0 : m->ex.type_flops_[i];
+    if (bytes) bytes[i] = m->ex.type_bytes_.empty() ? 0 : m->ex.type_bytes_[i];
+  }
+  return TT_COUNT;
+}
+
+const char* nnt_last_error(const nnt_model* m) {
+  if (m) return m->err.c_str();
+  return t_model_err.c_str();
+}
+
+}  // extern "C"
