@@ -1,0 +1,333 @@
+"""Benchmark: GPT2 training step (forward + backward + fused AdamW) tokens/s on one GB300.
+
+Default workload: the GPT2-small-shaped configuration of the NNTile README's
+GPT example ("Minimal working GPT example": 12 layers, d_model 768, 12 heads,
+d_ff 3072, vocab 50257, sequence 1024, minibatch 4; tiles seq 1024, embd 768,
+inner 3072, head 12), bf16 GEMM operands with fp32 master weights and AdamW
+states, synthetic uniform token ids and N(0, 0.02) weights.
+
+Prints one JSON line. ``value``: tokens/s over K timed steps with the tokens
+already on the device (CUDA events on the model's stream); ``e2e``: the same
+through the C ABI with the token windows copied in from pinned host memory and
+the loss read back every step. ``roofline``: the dominant kernel's achieved
+rate against MEASURED_PEAKS.json. ``cpu_baseline``: the CPU oracle on a
+bounded sample (one sequence) on the host cores.
+
+``--impl reference`` times the CPU oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GPT2 train tokens/s on 1 GB300; tile-kernel % of HBM/TC roofline"
+
+WORKLOADS = {
+    # name: (n_layer, d_model, n_head, d_ff, vocab, seq, batch, dtype, tiles)
+    "gpt2-small": (12, 768, 12, 3072, 50257, 1024, 4, "bf16",
+                   {"seq_tile": 1024, "embd_tile": 768, "inner_tile": 3072, "head_tile": 12,
+                    "batch_tile": 4}),
+    "tiny": (2, 64, 4, 256, 256, 32, 2, "fp32", {"seq_tile": 16, "embd_tile": 32}),
+    "wide-4": (4, 8192, 64, 32768, 50257, 1024, 8, "bf16",
+               {"seq_tile": 1024, "embd_tile": 2048, "inner_tile": 4096, "head_tile": 16}),
+}
+
+GEMM_TYPES = {"gemm_qkv", "gemm_qk", "gemm_pv", "gemm_attn_out", "gemm_fc_gelu", "gemm_mlp_proj",
+              "gemm_lm_head", "gemm_lm_dx", "gemm_lm_dw", "gemm_dx", "gemm_dw", "gemm_attn_bwd"}
+KERNEL_OF_TYPE = {t: "gemm_tc_kernel" for t in GEMM_TYPES}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(name, seed, batch=1):
+    """CPU oracle step on `batch` sequences of the workload; returns (tokens, seconds, cores)."""
+    import numpy as np
+
+    from oracle import gpt2 as O
+    from tile_task_transformer_gb300 import synth
+
+    L, d, H, f, V, S, _, _, _ = WORKLOADS[name]
+    cfg = O.GPT2Config(n_layer=L, d_model=d, n_head=H, d_ff=f, vocab=V, seq=S, batch=batch)
+    params = synth.gpt2_params(seed, L, d, f, V, S)
+    win = synth.token_windows(seed, batch, S, V)
+    t0 = time.perf_counter()
+    loss, grads, new_p, _, _ = O.train_step(cfg, params, win)
+    dt = time.perf_counter() - t0
+    assert np.isfinite(loss)
+    return batch * S, dt, os.cpu_count()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    name = args.workload
+    _, _, _, _, _, S, B, dtype, _ = WORKLOADS[name]
+    for _ in range(args.warmup):
+        oracle_sample(name, 1)
+    tot_tok, tot_t, cores = 0, 0.0, os.cpu_count()
+    for _ in range(args.steps):
+        tok, dt, cores = oracle_sample(name, 1)
+        tot_tok += tok
+        tot_t += dt
+    v = tot_tok / tot_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{name} (oracle sample: 1 sequence of {S} tokens per step)",
+                   "global_batch": 1, "seq_len": S, "parallelism": "none (CPU oracle)"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one {name} training step on 1 sequence x {S} tokens, fp64 numpy"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from tile_task_transformer_gb300 import nnt, synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    name = args.workload
+    L, d, H, f, V, S, B, dtype, tiles = WORKLOADS[name]
+    dt = nnt.BF16 if dtype == "bf16" else nnt.F32
+    stream = torch.cuda.Stream()
+    model = nnt.Model(L, d, H, f, V, S, B, dtype=dt, tiles=tiles, seed=1 + rank, stream=stream,
+                      n_streams=args.streams, use_cuda_graph=not args.no_graph)
+    st = model.stats()
+    T = B * S
+    win_host = synth.token_windows(1 + rank, B, S, V)
+    tok_dev = torch.as_tensor(win_host.view(np.int16)).to("cuda")
+    tok_pin = torch.as_tensor(win_host.view(np.int16)).pin_memory()
+    hp = dict(lr=3e-4, eps=1e-8, weight_decay=0.1)
+
+    def step(tokens, want_loss):
+        loss = model.forward(tokens, want_loss=want_loss)
+        model.backward()
+        model.adamw_step(**hp)
+        return loss
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up (also captures the CUDA graphs)
+    for _ in range(max(args.warmup, 1)):
+        step(tok_dev, False)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: tokens resident in HBM
+    clocks = ClockSampler()
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(tok_dev, False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tmax = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        ms = tmax.item()
+    value = world * T / (ms / 1000.0)
+
+    # ---- end to end through the C ABI: pinned host tokens in, loss out, every step
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    losses = []
+    for _ in range(args.steps):
+        losses.append(step(tok_pin, True))
+    torch.cuda.synchronize()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_value = world * T / e2e_s
+    assert all(np.isfinite(losses)), losses
+
+    # ---- per-task timing pass (CUDA events on each task's stream) for the roofline
+    model.set_trace(True)
+    for _ in range(2):
+        step(tok_dev, True)
+    times = model.task_times()
+    model.set_trace(False)
+    pk, pk_kind = peaks()
+    by_kernel = {}
+    for tname, rec in times.items():
+        if rec["launches"] == 0:
+            continue
+        k = KERNEL_OF_TYPE.get(tname, tname)
+        agg = by_kernel.setdefault(k, {"ms": 0.0, "launches": 0, "flops": 0.0, "bytes": 0.0})
+        agg["ms"] += rec["ms"]
+        agg["launches"] += rec["launches"]
+        agg["flops"] += rec["flops"]
+        agg["bytes"] += rec["bytes"]
+    total_ms = sum(a["ms"] for a in by_kernel.values())
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    a = by_kernel[dom]
+    if a["flops"] > 0:
+        achieved = a["flops"] / (a["ms"] / 1e3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "kernel": dom,
+                "peak_kind": f"{pk_kind} sustained bf16"}
+    else:
+        achieved = a["bytes"] / (a["ms"] / 1e3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "kernel": dom,
+                "peak_kind": f"{pk_kind} copy"}
+    kernel_table = {k: {"share": v["ms"] / total_ms, "launches": v["launches"],
+                        "ms_per_step": v["ms"] / 2,
+                        **({"tflops": v["flops"] / (v["ms"] / 1e3) / 1e12} if v["flops"] else {}),
+                        **({"gbs": v["bytes"] / (v["ms"] / 1e3) / 1e9} if v["bytes"] and not v["flops"] else {})}
+                    for k, v in sorted(by_kernel.items(), key=lambda kv: -kv[1]["ms"])}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only): one sequence of the workload
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, sec, cores = oracle_sample(name, 1 + rank)
+        cpu = {"value": tok / sec, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"one {name} training step on 1 sequence x {S} tokens (fp64 numpy, "
+                         f"{sec:.1f} s)"}
+
+    type_table = {k: {"ms_per_step": v["ms"] / 2, "launches_per_step": v["launches"] // 2,
+                      **({"tflops": v["flops"] / (v["ms"] / 1e3) / 1e12} if v["flops"] else {}),
+                      **({"gbs": v["bytes"] / (v["ms"] / 1e3) / 1e9} if v["bytes"] else {})}
+                  for k, v in sorted(times.items(), key=lambda kv: -kv[1]["ms"]) if v["launches"]}
+    n_kernels = st["kernels_forward"] + st["kernels_backward"] + st["kernels_adamw"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if dt == nnt.BF16 else "f32", "data": "synthetic",
+        "config": {"workload": f"{name}: L{L} d{d} H{H} ff{f} V{V} S{S} B{B}, tiles {tiles}",
+                   "global_batch": B * world, "seq_len": S,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "working set >> L2 (activations and weights are several GB per step)",
+                   "cuda_graph": not args.no_graph, "streams": args.streams},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(win_host.nbytes), "d2h_bytes_per_step": 4},
+        "gpu_launches": int(n_kernels * args.steps),
+        "roofline": roof,
+        "kernels": kernel_table,
+        "task_types": type_table,
+        "model_tflops": None,
+        "loss": float(losses[-1]),
+        "device_gib": st["device_bytes"] / 2 ** 30,
+    }
+    try:
+        from oracle import gpt2 as O
+        cfgo = O.GPT2Config(n_layer=L, d_model=d, n_head=H, d_ff=f, vocab=V, seq=S, batch=B)
+        line["model_tflops"] = world * O.step_flops(cfgo) / (ms / 1e3) / 1e12
+    except Exception:
+        pass
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line))
+    model.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="gpt2-small", choices=sorted(WORKLOADS))
+    ap.add_argument("--streams", type=int, default=2)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

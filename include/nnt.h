@@ -108,6 +108,7 @@ typedef struct {
   int64_t n_params;             /* scalar parameter count */
   int32_t n_streams;
   int32_t offload_active;
+  int64_t kernels_forward, kernels_backward, kernels_adamw; /* kernel launches per call */
 } nnt_stats;
 
 /* ---------------------------------------------------------------- model API */
@@ -173,6 +174,10 @@ nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out);
  * Returns the number of task types, or -1. */
 int32_t nnt_get_task_times(const nnt_model* m, int32_t max_types, const char** names,
                            int64_t* launches, double* ms, double* flops, double* bytes);
+
+/* Switch per-task CUDA-event timing on (1) or off (0) for the following calls
+ * (tracing runs the tasks without graph replay). */
+nnt_status nnt_set_trace(nnt_model* m, int32_t on);
 
 /* Last error message of this model (or of the calling thread when m is NULL). */
 const char* nnt_last_error(const nnt_model* m);

@@ -248,3 +248,47 @@ def test_gemm_cuda_cores_fp32(M, N, K, at, bt):
     ref = a.astype(np.float64) @ b.astype(np.float64)
     err = np.abs(n(C) - ref).max() / np.abs(ref).max()
     assert err < 1e-5
+
+
+def _bf16_round(a):
+    return torch.as_tensor(a).to(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 768), (300, 200, 1000), (64, 64, 16),
+                                   (1024, 2304, 768), (4096, 768, 3072), (200, 50257, 64)])
+@pytest.mark.parametrize("at,bt", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_gemm_tensor_cores_bf16(M, N, K, at, bt):
+    """tcgen05 GEMM vs fp64 products of the same bf16 inputs."""
+    if (at and M % 8) or (bt and N % 8) or (not at and K % 8) or (not bt and K % 8):
+        pytest.skip("leading dimension must be a multiple of 8 for TMA")
+    A = synth.normal_matrix(12, 1, (K, M) if at else (M, K), 1.0)
+    Bm = synth.normal_matrix(12, 2, (K, N) if bt else (N, K), 1.0)
+    At, Bt = t(A, torch.bfloat16), t(Bm, torch.bfloat16)
+    ldc = (N + 3) // 4 * 4
+    C = torch.full((M, ldc), float("nan"), device=DEV)
+    nnt.op_gemm(At, M if at else K, at, Bt, N if bt else K, bt, C, ldc, nnt.F32, M, N, K,
+                dtype=nnt.BF16, backend=0)
+    torch.cuda.synchronize()
+    assert nnt.read_device_error() == 0
+    a = _bf16_round(A)
+    b = _bf16_round(Bm)
+    ref = (a.T if at else a) @ (b if bt else b.T)
+    err = np.abs(n(C)[:, :N] - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
+
+
+def test_gemm_tensor_cores_bf16_out_and_accumulate():
+    M, N, K = 256, 384, 512
+    A = synth.normal_matrix(13, 1, (M, K), 1.0)
+    Bm = synth.normal_matrix(13, 2, (N, K), 1.0)
+    C0 = synth.normal_matrix(13, 3, (M, N), 1.0)
+    C = t(C0)
+    nnt.op_gemm(t(A, torch.bfloat16), K, 0, t(Bm, torch.bfloat16), K, 0, C, N, nnt.F32, M, N, K,
+                alpha=0.5, beta=1.0, dtype=nnt.BF16, backend=0)
+    Cb = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    nnt.op_gemm(t(A, torch.bfloat16), K, 0, t(Bm, torch.bfloat16), K, 0, Cb, N, nnt.BF16, M, N, K,
+                dtype=nnt.BF16, backend=0)
+    torch.cuda.synchronize()
+    ref = _bf16_round(A) @ _bf16_round(Bm).T
+    assert np.abs(n(C) - (C0 + 0.5 * ref)).max() / np.abs(ref).max() < 1e-5
+    close_bf16(n(Cb), ref)

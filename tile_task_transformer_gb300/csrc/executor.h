@@ -39,6 +39,7 @@ struct Task {
   std::function<nnt_status(cudaStream_t)> fn;
   double flops = 0, bytes = 0;
   int copy_engine = 0;  // 1: host<->device copy task, scheduled on the copy stream
+  int kernels = 1;      // kernel launches the task makes
   // schedule (finalize)
   int stream = 0;
   std::vector<int> waits;
@@ -55,6 +56,11 @@ class Program {
   const std::vector<Task>& tasks() const { return tasks_; }
   int n_edges() const { return n_edges_; }
   int n_streams_used() const { return n_streams_used_; }
+  int64_t kernels() const {
+    int64_t k = 0;
+    for (const Task& t : tasks_) k += t.kernels;
+    return k;
+  }
   const std::vector<std::vector<int>>& deps() const { return deps_; }
 
   std::vector<Task> tasks_;
@@ -77,6 +83,7 @@ class Executor {
   // totals (no-op unless tracing).
   nnt_status collect_trace(const Program& p);
   void reset_trace();
+  void set_trace(bool on) { trace_ = on; }
 
   cudaStream_t main_ = nullptr;
   std::vector<cudaStream_t> streams_;  // [0] = main, then side streams, then copy stream

@@ -16,11 +16,13 @@ template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
+  // tiles sit on absolute multiples of BM/BN (so no tile straddles a causal block)
   const int i = blockIdx.z;
-  const int m_start = g.m0 + blockIdx.y * BM;
-  const int n_start = g.n0 + blockIdx.x * BN;
-  const int m_end = min(g.m0 + g.mt, m_start + BM);
-  const int n_end = min(g.n0 + g.nt, n_start + BN);
+  const int m_box = (g.m0 / BM + (int)blockIdx.y) * BM;
+  const int n_box = (g.n0 / BN + (int)blockIdx.x) * BN;
+  const int m_start = max(g.m0, m_box), n_start = max(g.n0, n_box);
+  const int m_end = min(g.m0 + g.mt, m_box + BM);
+  const int n_end = min(g.n0 + g.nt, n_box + BN);
   if (!causal_tile_needed(g, m_start, m_end, n_start)) return;
   int k_lo, k_hi;
   causal_k_range(g, m_start, m_end, k_lo, k_hi);
@@ -36,16 +38,16 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
       const int e = tid + r * 256;
       int mm, kk;
       if (g.a_trans) { mm = e % BM; kk = e / BM; } else { mm = e / BK; kk = e % BK; }
-      const int m = m_start + mm, k = k0 + kk;
+      const int m = m_box + mm, k = k0 + kk;
       float v = 0.f;
-      if (m < m_end && k < k_hi)
+      if (m >= m_start && m < m_end && k < k_hi)
         v = ld_op(A, g.a_trans ? (int64_t)k * g.lda + m : (int64_t)m * g.lda + k);
       As[kk][mm] = v;
       int nn;
       if (g.b_trans) { nn = e % BN; kk = e / BN; } else { nn = e / BK; kk = e % BK; }
-      const int n = n_start + nn, k2 = k0 + kk;
+      const int n = n_box + nn, k2 = k0 + kk;
       float w = 0.f;
-      if (n < n_end && k2 < k_hi)
+      if (n >= n_start && n < n_end && k2 < k_hi)
         w = ld_op(B, g.b_trans ? (int64_t)k2 * g.ldb + n : (int64_t)n * g.ldb + k2);
       Bs[kk][nn] = w;
     }
@@ -69,15 +71,16 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int m = m_start + ty * 4 + r, n = n_start + tx * 4 + c;
-      if (m < m_end && n < n_end) epilogue_one(g, i, m, n, acc[r][c]);
+      const int m = m_box + ty * 4 + r, n = n_box + tx * 4 + c;
+      if (m >= m_start && m < m_end && n >= n_start && n < n_end) epilogue_one(g, i, m, n, acc[r][c]);
     }
 }
 }  // namespace
 
 nnt_status gemm_simt(const GemmArgs& g, cudaStream_t st) {
   if (g.mt <= 0 || g.nt <= 0 || g.nbatch <= 0) return NNT_OK;
-  dim3 grid((unsigned)ceil_div(g.nt, BN), (unsigned)ceil_div(g.mt, BM), (unsigned)g.nbatch);
+  dim3 grid((unsigned)((g.n0 + g.nt - 1) / BN - g.n0 / BN + 1),
+            (unsigned)((g.m0 + g.mt - 1) / BM - g.m0 / BM + 1), (unsigned)g.nbatch);
   NNT_CHECK_ARG(grid.y < 65536 && grid.z < 65536, "gemm: grid too large");
   if (g.op_dtype == NNT_BF16)
     gemm_simt_kernel<bf16><<<grid, 256, 0, st>>>(g);

@@ -1,6 +1,632 @@
-// placeholder, replaced by the tcgen05 kernel
+// Tensor-core tile GEMM for sm_103a: tcgen05.mma (kind::f16, bf16 in, fp32
+// accumulate in TMEM) fed by TMA, with the step's fused epilogues.
+//
+// The linear layers and the attention products QK^T, PV and their backward
+// products are the dense contractions of the step (review page "What carries
+// the argument": linear and attention tile tasks). One kernel covers all of
+// them: operands may be K-major or MN-major (weights [out, in] used as-is for
+// x W^T, dY W and dY^T X without transposes), batched over (sequence, head),
+// with the causal tile rules of gemm.cuh.
+//
+// Structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: 128x64 A box and BNx64 B box per k-block into a
+//               ring of shared-memory stages (128-byte swizzle), signalled by
+//               mbarrier transaction counts;
+//   warp 1      allocates 2*BN TMEM columns (two accumulators) and issues the
+//               MMAs (128 x BN x 16 each, four per k-block) from one thread;
+//               tcgen05.commit frees a stage / publishes an accumulator;
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time from their TMEM lane
+//               quarter, apply bias / residual / GELU / layout, store; the
+//               accumulator is handed back so the next tile's MMAs overlap.
+// Every mbarrier wait is bounded: on expiry the kernel sets the device error
+// word, stops issuing work, waits (bounded) for its own copies in flight,
+// frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "gemm.cuh"
+
 namespace nnt {
-bool gemm_tc_supported(const GemmArgs&) { return false; }
-nnt_status gemm_tc(const GemmArgs&, cudaStream_t) { return NNT_ERR_INVALID_ARG; }
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes: one swizzle row
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 5000000000ull;  // 5 s per wait, then give up
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase with the given parity; false when it ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 0) {
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+      __nanosleep(32);
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), A/B major (bit 15/16: 1 = MN-major), N>>3 at bit 17,
+// M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (>> 4), version 1 (bit 46), 128-byte swizzle (layout type 2 at bit 61).
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Output-tile space of one launch (host-computed).
+struct TileSpace {
+  int mt0, n_mt, nt0, n_nt;
+  int total;
+};
+
+struct TileCoord {
+  int i, m_box, m_start, m_end, n_box, n_start, n_end, kb_lo, kb_hi;
+  bool needed;
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord tile_at(const GemmArgs& g, const TileSpace& ts, int t) {
+  TileCoord c;
+  const int im = t % ts.n_mt;
+  const int rest = t / ts.n_mt;
+  const int in = rest % ts.n_nt;
+  c.i = rest / ts.n_nt;
+  c.m_box = (ts.mt0 + im) * BM;
+  c.m_start = max(g.m0, c.m_box);
+  c.m_end = min(g.m0 + g.mt, c.m_box + BM);
+  c.n_box = (ts.nt0 + in) * BN;
+  c.n_start = max(g.n0, c.n_box);
+  c.n_end = min(g.n0 + g.nt, c.n_box + BN);
+  c.needed = causal_tile_needed(g, c.m_start, c.m_end, c.n_start);
+  int k_lo, k_hi;
+  causal_k_range(g, c.m_start, c.m_end, k_lo, k_hi);
+  c.kb_lo = k_lo / BK;
+  c.kb_hi = (k_hi + BK - 1) / BK;
+  return c;
+}
+
+// Epilogue for 8 consecutive columns n..n+7 of row m (all inside the window).
+__device__ __forceinline__ void epi8(const GemmArgs& g, int i, int m, int n, const float* acc) {
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = g.alpha * acc[j];
+  const int64_t o = out_offset(g, i, m, n);
+  if (g.epi == EPI_STORE) {
+    if (g.bias) {
+      float4 b0 = *reinterpret_cast<const float4*>(g.bias + n);
+      float4 b1 = *reinterpret_cast<const float4*>(g.bias + n + 4);
+      v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
+      v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+    }
+    if (g.resid) {
+      const float* r = g.resid + (int64_t)m * g.ld_resid + n;
+      float4 r0 = *reinterpret_cast<const float4*>(r);
+      float4 r1 = *reinterpret_cast<const float4*>(r + 4);
+      v[0] += r0.x; v[1] += r0.y; v[2] += r0.z; v[3] += r0.w;
+      v[4] += r1.x; v[5] += r1.y; v[6] += r1.z; v[7] += r1.w;
+    }
+    if (g.beta) {
+      const float* c = static_cast<const float*>(g.C) + o;
+      float4 c0 = *reinterpret_cast<const float4*>(c);
+      float4 c1 = *reinterpret_cast<const float4*>(c + 4);
+      v[0] += c0.x; v[1] += c0.y; v[2] += c0.z; v[3] += c0.w;
+      v[4] += c1.x; v[5] += c1.y; v[6] += c1.z; v[7] += c1.w;
+    }
+  } else if (g.epi == EPI_GELU) {
+    if (g.bias) {
+      float4 b0 = *reinterpret_cast<const float4*>(g.bias + n);
+      float4 b1 = *reinterpret_cast<const float4*>(g.bias + n + 4);
+      v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
+      v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+    }
+    float* u = g.aux + (int64_t)m * g.ld_aux + n;
+    *reinterpret_cast<float4*>(u) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(u + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = gelu_fwd_dev(v[j]);
+  } else {
+    const float* u = g.aux + (int64_t)m * g.ld_aux + n;
+    float4 u0 = *reinterpret_cast<const float4*>(u);
+    float4 u1 = *reinterpret_cast<const float4*>(u + 4);
+    v[0] *= gelu_grad_dev(u0.x); v[1] *= gelu_grad_dev(u0.y);
+    v[2] *= gelu_grad_dev(u0.z); v[3] *= gelu_grad_dev(u0.w);
+    v[4] *= gelu_grad_dev(u1.x); v[5] *= gelu_grad_dev(u1.y);
+    v[6] *= gelu_grad_dev(u1.z); v[7] *= gelu_grad_dev(u1.w);
+  }
+  if (g.c_dtype == NNT_BF16) {
+    uint4 pk;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+    pk.x = *reinterpret_cast<uint32_t*>(&h0);
+    pk.y = *reinterpret_cast<uint32_t*>(&h1);
+    pk.z = *reinterpret_cast<uint32_t*>(&h2);
+    pk.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(static_cast<bf16*>(g.C) + o) = pk;
+  } else {
+    float* c = static_cast<float*>(g.C) + o;
+    *reinterpret_cast<float4*>(c) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs g, const TileSpace ts, uint32_t* err) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
+        const TileCoord c = tile_at<BN>(g, ts, t);
+        if (!c.needed) continue;
+        const int z = (int)g.zm.z(c.i);
+        for (int kb = c.kb_lo; kb < c.kb_hi; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1)) {
+            atomicOr(err, DEVERR_WAIT_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* sa = smem + s * C::STAGE;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          const int k = kb * BK;
+          if (A_MN) {
+            tma_load_3d(sa, &tmA, &full[s], c.m_box, k, z);
+            tma_load_3d(sa + 8192, &tmA, &full[s], c.m_box + 64, k, z);
+          } else {
+            tma_load_3d(sa, &tmA, &full[s], k, c.m_box, z);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 8192, &tmB, &full[s], c.n_box + 64 * j, k, z);
+          } else {
+            tma_load_3d(sb, &tmB, &full[s], k, c.n_box, z);
+          }
+          ++issued;
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // wait (bounded) until every copy issued into the ring has landed
+      int outstanding = issued < C::STAGES ? issued : C::STAGES;
+      int ss = s;
+      uint32_t pp = ph;
+      for (int j = 0; j < outstanding; ++j) {
+        if (--ss < 0) {
+          ss = C::STAGES - 1;
+          pp ^= 1;
+        }
+        if (!mbar_wait(&full[ss], pp)) atomicOr(err, DEVERR_WAIT_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
+        const TileCoord c = tile_at<BN>(g, ts, t);
+        if (!c.needed) continue;
+        if (!mbar_wait(&tempty[acc], aph ^ 1)) {
+          atomicOr(err, DEVERR_WAIT_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = c.kb_lo; kb < c.kb_hi; ++kb) {
+          if (!mbar_wait(&full[s], ph)) {
+            atomicOr(err, DEVERR_WAIT_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::STAGE);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? make_sdesc(sa + kk * 2048, 8192, 1024)
+                                     : make_sdesc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? make_sdesc(sb + kk * 2048, 8192, 1024)
+                                     : make_sdesc(sb + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb > c.kb_lo || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
+      const TileCoord c = tile_at<BN>(g, ts, t);
+      if (!c.needed) continue;
+      if (!mbar_wait(&tfull[acc], aph)) {
+        atomicOr(err, DEVERR_WAIT_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int m = c.m_box + row;
+      const bool row_ok = m >= c.m_start && m < c.m_end;
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        const int nb = c.n_box + ch * 32;
+        if (nb >= c.n_end) break;  // uniform across the warp
+        float v[32];
+        tmem_ld32(tbase + ch * 32, v);
+        if (!row_ok) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = nb + 8 * j;
+          if (n < c.n_start || n >= c.n_end) continue;
+          if (n + 8 <= c.n_end) {
+            epi8(g, c.i, m, n, v + 8 * j);
+          } else {
+            for (int e = 0; n + e < c.n_end; ++e) epilogue_one(g, c.i, m, n + e, v[8 * j + e]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Operand stored [Z][outer][ld] with `inner` contiguous elements per row.
+nnt_status make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t ld,
+                    int64_t zs, int64_t Z, int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_thread_error("cuTensorMapEncodeTiled is unavailable");
+    return NNT_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)Z};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)zs * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_thread_error("cuTensorMapEncodeTiled failed (%d): dims %lld x %lld x %lld, ld %lld, zs %lld",
+                     (int)r, (long long)inner, (long long)outer, (long long)Z, (long long)ld,
+                     (long long)zs);
+    return NNT_ERR_INVALID_ARG;
+  }
+  return NNT_OK;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+TileSpace tile_space(const GemmArgs& g, int BN) {
+  TileSpace t;
+  t.mt0 = g.m0 / BM;
+  t.n_mt = (g.m0 + g.mt - 1) / BM - t.mt0 + 1;
+  t.nt0 = g.n0 / BN;
+  t.n_nt = (g.n0 + g.nt - 1) / BN - t.nt0 + 1;
+  t.total = g.nbatch * t.n_mt * t.n_nt;
+  return t;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+nnt_status launch_tc(const GemmArgs& g, cudaStream_t st) {
+  using C = Cfg<BN>;
+  auto kern = gemm_tc_kernel<BN, A_MN, B_MN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (attr_err != cudaSuccess) {
+    set_thread_error("cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+    return NNT_ERR_CUDA;
+  }
+  const int64_t zmax = g.zm.z(g.nbatch - 1) + 1;
+  CUtensorMap ma, mb;
+  if (A_MN)
+    NNT_TRY(make_map(&ma, g.A, g.M, g.K, g.lda, g.a_zs > 0 ? g.a_zs : (int64_t)g.K * g.lda, zmax, 64, 64));
+  else
+    NNT_TRY(make_map(&ma, g.A, g.K, g.M, g.lda, g.a_zs > 0 ? g.a_zs : (int64_t)g.M * g.lda, zmax, 64, BM));
+  if (B_MN)
+    NNT_TRY(make_map(&mb, g.B, g.N, g.K, g.ldb, g.b_zs > 0 ? g.b_zs : (int64_t)g.K * g.ldb, zmax, 64, 64));
+  else
+    NNT_TRY(make_map(&mb, g.B, g.K, g.N, g.ldb, g.b_zs > 0 ? g.b_zs : (int64_t)g.N * g.ldb, zmax, 64, BN));
+  const TileSpace ts = tile_space(g, BN);
+  const int grid = std::min(ts.total, num_sms());
+  uint32_t* err = device_error_word();
+  if (!err) {
+    set_thread_error("device error word unavailable");
+    return NNT_ERR_CUDA;
+  }
+  gemm_tc_kernel<BN, A_MN, B_MN><<<grid, kThreads, C::SMEM, st>>>(ma, mb, g, ts, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_thread_error("gemm_tc launch: %s", cudaGetErrorString(e));
+    return NNT_ERR_CUDA;
+  }
+  return NNT_OK;
+}
+
+template <int BN>
+nnt_status launch_bn(const GemmArgs& g, cudaStream_t st) {
+  if (g.a_trans) {
+    if (g.b_trans) return launch_tc<BN, true, true>(g, st);
+    return launch_tc<BN, true, false>(g, st);
+  }
+  if (g.b_trans) return launch_tc<BN, false, true>(g, st);
+  return launch_tc<BN, false, false>(g, st);
+}
+
+// Tile width: the widest of 256/128/64 whose persistent schedule wastes at most
+// a little more than the narrower ones (tiles per CTA rounded up).
+int choose_bn(const GemmArgs& g) {
+  if (g.nt <= 64) return 64;
+  const int sms = num_sms();
+  double best = 0;
+  int best_bn = 64;
+  for (int bn : {256, 128, 64}) {
+    if (bn > 64 && g.nt <= bn / 2) continue;
+    const TileSpace t = tile_space(g, bn);
+    const double waves = std::ceil((double)t.total / sms);
+    const double eff = (double)t.total / (waves * sms) * (bn == 256 ? 1.0 : bn == 128 ? 0.93 : 0.8);
+    if (eff > best + 1e-9) {
+      best = eff;
+      best_bn = bn;
+    }
+  }
+  return best_bn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+bool gemm_tc_supported(const GemmArgs& g) {
+  if (g.op_dtype != NNT_BF16) return false;
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.mt <= 0 || g.nt <= 0 || g.nbatch <= 0) return false;
+  if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.C)) return false;
+  if (g.lda % 8 || g.ldb % 8) return false;
+  if (g.a_zs % 8 || g.b_zs % 8) return false;
+  if (g.m0 % 8 || g.n0 % 8) return false;
+  if (g.c_dtype == NNT_BF16 ? (g.ldc % 8) : (g.ldc % 4)) return false;
+  if (g.out_mode == OUT_PLAIN && g.nbatch > 1 && (g.c_dtype == NNT_BF16 ? g.c_zs % 8 : g.c_zs % 4)) return false;
+  if (g.out_mode != OUT_PLAIN && (g.hs_hd % 8 || g.c_col_off % 8)) return false;
+  if (g.bias && !aligned16(g.bias)) return false;
+  if (g.resid && (!aligned16(g.resid) || g.ld_resid % 4)) return false;
+  if (g.aux && (!aligned16(g.aux) || g.ld_aux % 4)) return false;
+  return true;
+}
+
+nnt_status gemm_tc(const GemmArgs& g, cudaStream_t st) {
+  if (!gemm_tc_supported(g)) {
+    set_thread_error("gemm_tc: unsupported shape/layout");
+    return NNT_ERR_INVALID_ARG;
+  }
+  switch (choose_bn(g)) {
+    case 256: return launch_bn<256>(g, st);
+    case 128: return launch_bn<128>(g, st);
+    default: return launch_bn<64>(g, st);
+  }
+}
+
 }  // namespace nnt

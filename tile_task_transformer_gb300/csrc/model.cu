@@ -677,6 +677,7 @@ void build_backward(nnt_model* m) {
   auto colsum_task = [&](const void* a, int a_dtype, const TGrid& ga, int N, const ParamInfo& bp, int gidx) {
     Task t;
     t.type = TT_COLSUM;
+    t.kernels = 2;
     box(t.uses, ga, ACC_R);
     box(t.uses, m->gcol_part, ACC_RW);
     box(t.uses, m->ggrad[gidx], ACC_W);
@@ -714,6 +715,7 @@ void build_backward(nnt_model* m) {
     }
     Task t;
     t.type = TT_LN_PARTS;
+    t.kernels = 2;
     box(t.uses, m->gln_part, ACC_R);
     box(t.uses, m->ggrad[gidx_g], ACC_W);
     box(t.uses, m->ggrad[gidx_b], ACC_W);
@@ -1167,7 +1169,6 @@ nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_d
     set_thread_error("token copy failed: %s", cudaGetErrorString(cudaGetLastError()));
     return fail(m, NNT_ERR_CUDA);
   }
-  if (m->opts.trace) m->ex.reset_trace();
   s = m->ex.run(m->fwd, m->opts.use_cuda_graph ? 0 : -1);
   if (s != NNT_OK) return fail(m, s);
   m->state = 1;
@@ -1336,6 +1337,9 @@ nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out) {
   out->n_tiles = m->next_tile;
   out->n_params = m->n_scalar;
   out->n_streams = m->opts.n_streams;
+  out->kernels_forward = m->fwd.kernels();
+  out->kernels_backward = m->bwd.kernels();
+  out->kernels_adamw = m->opt.kernels();
   return NNT_OK;
 }
 
@@ -1351,6 +1355,19 @@ int32_t nnt_get_task_times(const nnt_model* m, int32_t max_types, const char** n
     if (bytes) bytes[i] = m->ex.type_bytes_.empty() ? 0 : m->ex.type_bytes_[i];
   }
   return TT_COUNT;
+}
+
+nnt_status nnt_set_trace(nnt_model* m, int32_t on) {
+  if (!m) {
+    set_thread_error("NULL model");
+    return NNT_ERR_INVALID_ARG;
+  }
+  nnt_status s = sync_model(m);
+  if (s != NNT_OK) return fail(m, s);
+  m->opts.trace = on ? 1 : 0;
+  m->ex.set_trace(on != 0);
+  m->ex.reset_trace();
+  return NNT_OK;
 }
 
 const char* nnt_last_error(const nnt_model* m) {

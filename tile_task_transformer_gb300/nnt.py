@@ -60,7 +60,8 @@ class Stats(C.Structure):
                 ("d2h_bytes", C.c_uint64), ("n_tasks_forward", C.c_int64),
                 ("n_tasks_backward", C.c_int64), ("n_tasks_adamw", C.c_int64),
                 ("n_tiles", C.c_int64), ("n_params", C.c_int64), ("n_streams", C.c_int32),
-                ("offload_active", C.c_int32)]
+                ("offload_active", C.c_int32), ("kernels_forward", C.c_int64),
+                ("kernels_backward", C.c_int64), ("kernels_adamw", C.c_int64)]
 
 
 _P = C.c_void_p
@@ -84,6 +85,7 @@ _SIGS = {
     "nnt_get_task_times": (_I32, [_P, _I32, C.POINTER(C.c_char_p), C.POINTER(_I64),
                                   C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(C.c_double)]),
     "nnt_last_error": (C.c_char_p, [_P]),
+    "nnt_set_trace": (C.c_int, [_P, _I32]),
     "nnt_op_layernorm_fwd": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P]),
     "nnt_op_layernorm_bwd": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _P]),
     "nnt_op_softmax_causal_fwd": (C.c_int, [_P, _P, _I64, _I64, _I32, _P]),
@@ -156,7 +158,7 @@ class Model:
     """One GPT2 training step on tiled tensors (nnt_create_model ... nnt_destroy)."""
 
     def __init__(self, n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype=BF16,
-                 ln_eps=1e-5, tiles=None, seed=0, init_std=0.02, zero_bias=False, stream=None,
+                 ln_eps=1e-5, tiles=None, seed=0, init_std=0.0, zero_bias=False, stream=None,
                  n_streams=2, use_cuda_graph=False, timeout_ms=0, gemm_backend=0, trace=False,
                  allow_host_offload=False, hbm_budget_bytes=0):
         self.cfg = Config(n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype, ln_eps)
@@ -250,6 +252,9 @@ class Model:
         s = Stats()
         check(lib().nnt_get_stats(self.h, C.byref(s)), self.h)
         return {k: getattr(s, k) for k, _ in Stats._fields_}
+
+    def set_trace(self, on: bool):
+        check(lib().nnt_set_trace(self.h, int(on)), self.h)
 
     def task_times(self):
         n = 64
