@@ -86,6 +86,8 @@ typedef struct {
   uint32_t timeout_ms;         /* bound on every host wait (0 = 600000) */
   int32_t gemm_backend;        /* 0 = tensor cores (bf16) / CUDA cores (fp32); 1 = CUDA-core GEMM always */
   int32_t trace;               /* 1: time every task with CUDA events (nnt_get_task_times) */
+  int32_t gemm_min_task_cols;  /* consecutive output column tiles share one GEMM launch until it
+                                  is this wide (0 = 8192; negative = one launch per tile) */
 } nnt_options;
 
 /* AdamW hyper-parameters (README: --optimizer=fusedadamw, --optimizer-eps=1e-8,
@@ -175,8 +177,9 @@ nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out);
 int32_t nnt_get_task_times(const nnt_model* m, int32_t max_types, const char** names,
                            int64_t* launches, double* ms, double* flops, double* bytes);
 
-/* Switch per-task CUDA-event timing on (1) or off (0) for the following calls
- * (tracing runs the tasks without graph replay). */
+/* Switch per-task CUDA-event timing on (1) or off (0) for the following calls.
+ * While tracing, the tasks run in program order on one stream (in a separate
+ * captured graph when graphs are enabled), so each task's time is its own. */
 nnt_status nnt_set_trace(nnt_model* m, int32_t on);
 
 /* Last error message of this model (or of the calling thread when m is NULL). */

@@ -102,9 +102,10 @@ def test_tiny_fp32_step_matches_oracle():
     {"seq_tile": 16, "embd_tile": 48, "inner_tile": 96, "head_tile": 2, "vocab_tile": 80},
     {"batch_tile": 1, "seq_tile": 32, "embd_tile": 16, "head_tile": 1},
 ])
-def test_tiny_fp32_tile_invariance(tiles):
+@pytest.mark.parametrize("min_cols", [0, -1])
+def test_tiny_fp32_tile_invariance(tiles, min_cols):
     ref = run_step(TINY, nnt.F32, TINY_TILES)
-    got = run_step(TINY, nnt.F32, tiles)
+    got = run_step(TINY, nnt.F32, tiles, gemm_min_task_cols=min_cols)
     assert abs(got["loss"] - ref["loss"]) < 1e-5
     for n in ref["grads"]:
         assert relerr(got["grads"][n], ref["grads"][n].astype(np.float64)) < 1e-4, n
@@ -119,8 +120,11 @@ def test_tiny_fp32_streams_and_graphs(n_streams, graph):
     check_step(TINY, got, tol=1e-4)
 
 
-def test_tiny_bf16_step_matches_oracle():
-    got = run_step(TINY, nnt.BF16, TINY_TILES)
+@pytest.mark.parametrize("tiles,min_cols", [(TINY_TILES, 0), (TINY_TILES, -1),
+                                           ({"seq_tile": 8, "embd_tile": 48, "head_tile": 1,
+                                             "batch_tile": 1, "vocab_tile": 72}, -1)])
+def test_tiny_bf16_step_matches_oracle(tiles, min_cols):
+    got = run_step(TINY, nnt.BF16, tiles, gemm_min_task_cols=min_cols)
     check_step(TINY, got)
 
 

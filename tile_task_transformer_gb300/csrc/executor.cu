@@ -49,6 +49,7 @@ void Program::finalize(int n_streams) {
   for (const Task& t : tasks_) has_copy |= t.copy_engine != 0;
   const int ns = n_streams_ + (has_copy ? 1 : 0);
   const int copy_stream = n_streams_;
+  for (Task& t : tasks_) t.record = false;
   std::vector<int> last_on(ns, -1);
   std::vector<std::vector<int>> frontier(n, std::vector<int>(ns, -1));
   n_edges_ = 0;
@@ -158,7 +159,7 @@ nnt_status Executor::ensure_events(size_t n) {
   return NNT_OK;
 }
 
-nnt_status Executor::launch_all(Program& p, bool traced) {
+nnt_status Executor::launch_all(Program& p, bool traced, bool capturing) {
   NNT_TRY(ensure_events(p.size()));
   const int ns = (int)streams_.size();
   NNT_CUDA_TRY(cudaEventRecord(fork_join_[0], main_));
@@ -167,9 +168,14 @@ nnt_status Executor::launch_all(Program& p, bool traced) {
     Task& t = p.tasks_[i];
     cudaStream_t s = streams_[std::min(t.stream, ns - 1)];
     for (int w : t.waits) NNT_CUDA_TRY(cudaStreamWaitEvent(s, task_events_[w], 0));
-    if (traced) NNT_CUDA_TRY(cudaEventRecord(t0_[i], s));
+    // inside a capture, timing events become external event-record nodes
+    if (traced)
+      NNT_CUDA_TRY(capturing ? cudaEventRecordWithFlags(t0_[i], s, cudaEventRecordExternal)
+                             : cudaEventRecord(t0_[i], s));
     NNT_TRY(t.fn(s));
-    if (traced) NNT_CUDA_TRY(cudaEventRecord(t1_[i], s));
+    if (traced)
+      NNT_CUDA_TRY(capturing ? cudaEventRecordWithFlags(t1_[i], s, cudaEventRecordExternal)
+                             : cudaEventRecord(t1_[i], s));
     if (t.record) NNT_CUDA_TRY(cudaEventRecord(task_events_[i], s));
   }
   for (int s = 1; s < ns; ++s) {
@@ -180,12 +186,17 @@ nnt_status Executor::launch_all(Program& p, bool traced) {
 }
 
 nnt_status Executor::run(Program& p, int graph_slot) {
-  if (graph_slot < 0 || trace_) return launch_all(p, trace_);
+  if (graph_slot < 0) return launch_all(p, trace_, false);
+  // traced programs get their own graphs (with timing-event nodes) in slot + 4
+  if (trace_) {
+    NNT_TRY(ensure_events(p.size()));
+    graph_slot += 4;
+  }
   if ((size_t)graph_slot >= graphs_.size()) graphs_.resize(graph_slot + 1, nullptr);
   if (!graphs_[graph_slot]) {
     cudaGraph_t g = nullptr;
     NNT_CUDA_TRY(cudaStreamBeginCapture(main_, cudaStreamCaptureModeThreadLocal));
-    nnt_status st = launch_all(p, false);
+    nnt_status st = launch_all(p, trace_, true);
     cudaError_t e = cudaStreamEndCapture(main_, &g);
     if (st != NNT_OK) {
       if (g) cudaGraphDestroy(g);

@@ -84,6 +84,13 @@ class Executor {
   nnt_status collect_trace(const Program& p);
   void reset_trace();
   void set_trace(bool on) { trace_ = on; }
+  void drop_graphs() {
+    for (auto& g : graphs_)
+      if (g) {
+        cudaGraphExecDestroy(g);
+        g = nullptr;
+      }
+  }
 
   cudaStream_t main_ = nullptr;
   std::vector<cudaStream_t> streams_;  // [0] = main, then side streams, then copy stream
@@ -98,7 +105,7 @@ class Executor {
   std::vector<double> type_ms_, type_flops_, type_bytes_;
 
  private:
-  nnt_status launch_all(Program& p, bool traced);
+  nnt_status launch_all(Program& p, bool traced, bool capturing);
   nnt_status ensure_events(size_t n);
 };
 

@@ -24,6 +24,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <mutex>
 
 #include "gemm.cuh"
@@ -44,7 +47,9 @@ struct Cfg {
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+  // per epilogue warp: a 32x32 output chunk (4 KB) and a 32x32 fp32 GELU input chunk (4 KB)
+  static constexpr int STAGING_BYTES = 4 * 8192;
+  static constexpr int SMEM = STAGES * STAGE + STAGING_BYTES + BAR_BYTES + 1024;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -100,6 +105,39 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+// Bulk tensor stores from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, const void* src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -179,6 +217,8 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 struct TileSpace {
   int mt0, n_mt, nt0, n_nt;
   int total;
+  int c_mode;   // 0: direct stores; 1: TMA store, window map; 2: TMA head split; 3: TMA head merge
+  int aux_tma;  // 1: GELU input u written by TMA store (window map)
 };
 
 struct TileCoord {
@@ -186,13 +226,23 @@ struct TileCoord {
   bool needed;
 };
 
+// Tile order: batch item, then groups of kGroupM m-tiles; inside a group the m
+// index runs fastest. CTAs working at the same time then share a band of A rows
+// and a band of B rows, which stay in L2.
+constexpr int kGroupM = 16;
+
 template <int BN>
 __device__ __forceinline__ TileCoord tile_at(const GemmArgs& g, const TileSpace& ts, int t) {
   TileCoord c;
-  const int im = t % ts.n_mt;
-  const int rest = t / ts.n_mt;
-  const int in = rest % ts.n_nt;
-  c.i = rest / ts.n_nt;
+  const int per_batch = ts.n_mt * ts.n_nt;
+  c.i = t / per_batch;
+  const int r = t - c.i * per_batch;
+  const int grp = r / (kGroupM * ts.n_nt);
+  const int m_base = grp * kGroupM;
+  const int gs = min(kGroupM, ts.n_mt - m_base);
+  const int rr = r - grp * kGroupM * ts.n_nt;
+  const int im = m_base + rr % gs;
+  const int in = rr / gs;
   c.m_box = (ts.mt0 + im) * BM;
   c.m_start = max(g.m0, c.m_box);
   c.m_end = min(g.m0 + g.mt, c.m_box + BM);
@@ -207,80 +257,106 @@ __device__ __forceinline__ TileCoord tile_at(const GemmArgs& g, const TileSpace&
   return c;
 }
 
-// Epilogue for 8 consecutive columns n..n+7 of row m (all inside the window).
-__device__ __forceinline__ void epi8(const GemmArgs& g, int i, int m, int n, const float* acc) {
-  float v[8];
+// Elementwise epilogue of one 32-column chunk of row m held in registers
+// (columns nb..nb+31; `full`: all of them inside the window). Bias loads are
+// the same address across the warp (broadcast); residual / GELU-input loads
+// read each thread's own row segment.
+__device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool row_ok, int nb,
+                                          int n_lo, int n_hi, bool full, float* v, float* u_out) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = g.alpha * acc[j];
-  const int64_t o = out_offset(g, i, m, n);
+  for (int j = 0; j < 32; ++j) v[j] *= g.alpha;
+  if (g.bias) {
+    if (full) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(g.bias + nb) + k);
+        v[4 * k] += b.x; v[4 * k + 1] += b.y; v[4 * k + 2] += b.z; v[4 * k + 3] += b.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (nb + j >= n_lo && nb + j < n_hi) v[j] += g.bias[nb + j];
+    }
+  }
   if (g.epi == EPI_STORE) {
-    if (g.bias) {
-      float4 b0 = *reinterpret_cast<const float4*>(g.bias + n);
-      float4 b1 = *reinterpret_cast<const float4*>(g.bias + n + 4);
-      v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
-      v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+    const float* add = nullptr;
+    if (g.resid) add = g.resid + (int64_t)m * g.ld_resid;
+    if (add && row_ok) {
+      if (full) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 r = *(reinterpret_cast<const float4*>(add + nb) + k);
+          v[4 * k] += r.x; v[4 * k + 1] += r.y; v[4 * k + 2] += r.z; v[4 * k + 3] += r.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (nb + j >= n_lo && nb + j < n_hi) v[j] += add[nb + j];
+      }
     }
-    if (g.resid) {
-      const float* r = g.resid + (int64_t)m * g.ld_resid + n;
-      float4 r0 = *reinterpret_cast<const float4*>(r);
-      float4 r1 = *reinterpret_cast<const float4*>(r + 4);
-      v[0] += r0.x; v[1] += r0.y; v[2] += r0.z; v[3] += r0.w;
-      v[4] += r1.x; v[5] += r1.y; v[6] += r1.z; v[7] += r1.w;
-    }
-    if (g.beta) {
-      const float* c = static_cast<const float*>(g.C) + o;
-      float4 c0 = *reinterpret_cast<const float4*>(c);
-      float4 c1 = *reinterpret_cast<const float4*>(c + 4);
-      v[0] += c0.x; v[1] += c0.y; v[2] += c0.z; v[3] += c0.w;
-      v[4] += c1.x; v[5] += c1.y; v[6] += c1.z; v[7] += c1.w;
+    if (g.beta && row_ok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (nb + j >= n_lo && nb + j < n_hi) v[j] += static_cast<const float*>(g.C)[out_offset(g, i, m, nb + j)];
     }
   } else if (g.epi == EPI_GELU) {
-    if (g.bias) {
-      float4 b0 = *reinterpret_cast<const float4*>(g.bias + n);
-      float4 b1 = *reinterpret_cast<const float4*>(g.bias + n + 4);
-      v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
-      v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
-    }
-    float* u = g.aux + (int64_t)m * g.ld_aux + n;
-    *reinterpret_cast<float4*>(u) = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4*>(u + 4) = make_float4(v[4], v[5], v[6], v[7]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = gelu_fwd_dev(v[j]);
-  } else {
-    const float* u = g.aux + (int64_t)m * g.ld_aux + n;
-    float4 u0 = *reinterpret_cast<const float4*>(u);
-    float4 u1 = *reinterpret_cast<const float4*>(u + 4);
-    v[0] *= gelu_grad_dev(u0.x); v[1] *= gelu_grad_dev(u0.y);
-    v[2] *= gelu_grad_dev(u0.z); v[3] *= gelu_grad_dev(u0.w);
-    v[4] *= gelu_grad_dev(u1.x); v[5] *= gelu_grad_dev(u1.y);
-    v[6] *= gelu_grad_dev(u1.z); v[7] *= gelu_grad_dev(u1.w);
+    for (int j = 0; j < 32; ++j) {
+      u_out[j] = v[j];
+      v[j] = gelu_fwd_dev(v[j]);
+    }
+  } else if (row_ok) {  // EPI_GELU_BWD
+    const float* u = g.aux + (int64_t)m * g.ld_aux;
+    if (full) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 r = *(reinterpret_cast<const float4*>(u + nb) + k);
+        v[4 * k] *= gelu_grad_dev(r.x); v[4 * k + 1] *= gelu_grad_dev(r.y);
+        v[4 * k + 2] *= gelu_grad_dev(r.z); v[4 * k + 3] *= gelu_grad_dev(r.w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= gelu_grad_dev(u[nb + j]);
+    }
   }
-  if (g.c_dtype == NNT_BF16) {
+}
+
+// Row `lane` of a 32x32 chunk into shared memory in the TMA 128-byte (fp32) or
+// 64-byte (bf16) swizzled box layout: 16-byte piece k of row r goes to
+// position k ^ (r & 7) (fp32) or k ^ ((r >> 1) & 3) (bf16), so the eight lanes
+// of a quarter-warp hit different banks.
+__device__ __forceinline__ void stage_f32(uint8_t* st, int lane, const float* v) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    *reinterpret_cast<float4*>(st + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+        make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+__device__ __forceinline__ void stage_bf16(uint8_t* st, int lane, const float* v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
     uint4 pk;
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
-    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * k], v[8 * k + 1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * k + 2], v[8 * k + 3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * k + 4], v[8 * k + 5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * k + 6], v[8 * k + 7]);
     pk.x = *reinterpret_cast<uint32_t*>(&h0);
     pk.y = *reinterpret_cast<uint32_t*>(&h1);
     pk.z = *reinterpret_cast<uint32_t*>(&h2);
     pk.w = *reinterpret_cast<uint32_t*>(&h3);
-    *reinterpret_cast<uint4*>(static_cast<bf16*>(g.C) + o) = pk;
-  } else {
-    float* c = static_cast<float*>(g.C) + o;
-    *reinterpret_cast<float4*>(c) = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4*>(c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    *reinterpret_cast<uint4*>(st + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = pk;
   }
 }
 
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmU,
                    const GemmArgs g, const TileSpace ts, uint32_t* err) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::STAGING_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -416,7 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
     const int q = warp & 3;
-    const int row = q * 32 + lane;
+    // Staging: 8 KB per warp. GELU epilogues use it as output chunk + GELU input
+    // chunk (one store group in flight); the others ping-pong two 4 KB output
+    // buffers (two store groups in flight).
+    uint8_t* stage_base = smem + C::STAGES * C::STAGE + (warp - 2) * 8192;
+    const bool cbf = g.c_dtype == NNT_BF16;
+    const bool gelu = g.epi == EPI_GELU;
+    int buf = 0;
+    int issued = 0;  // bulk store groups of this warp so far
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
@@ -428,26 +511,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int m = c.m_box + row;
+      const int row0 = c.m_box + q * 32;
+      const int m = row0 + lane;
       const bool row_ok = m >= c.m_start && m < c.m_end;
+      const bool rows_full = row0 >= c.m_start && row0 + 32 <= c.m_end;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         const int nb = c.n_box + ch * 32;
         if (nb >= c.n_end) break;  // uniform across the warp
-        float v[32];
+        float v[32], u[32];
         tmem_ld32(tbase + ch * 32, v);
-        if (!row_ok) continue;
+        if (row0 >= c.m_end) continue;  // no row of this warp in the window (uniform)
+        const bool cols_full = nb >= c.n_start && nb + 32 <= c.n_end;
+        bool tma;
+        if (ts.c_mode == 1) tma = row0 >= c.m_start && nb >= c.n_start;
+        else tma = ts.c_mode > 1 && rows_full && cols_full;
+        if (tma && g.epi == EPI_GELU && !ts.aux_tma) tma = false;
+        epi_chunk(g, c.i, m, row_ok, nb, c.n_start, c.n_end, cols_full, v, u);
+        if (!tma) {
+          if (row_ok) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int n = nb + 8 * j;
-          if (n < c.n_start || n >= c.n_end) continue;
-          if (n + 8 <= c.n_end) {
-            epi8(g, c.i, m, n, v + 8 * j);
-          } else {
-            for (int e = 0; n + e < c.n_end; ++e) epilogue_one(g, c.i, m, n + e, v[8 * j + e]);
+            for (int j = 0; j < 32; ++j) {
+              const int n = nb + j;
+              if (n < c.n_start || n >= c.n_end) continue;
+              if (g.epi == EPI_GELU) g.aux[(int64_t)m * g.ld_aux + n] = u[j];
+              const int64_t o = out_offset(g, c.i, m, n);
+              if (cbf) static_cast<bf16*>(g.C)[o] = __float2bfloat16_rn(v[j]);
+              else static_cast<float*>(g.C)[o] = v[j];
+            }
           }
+          continue;
         }
+        uint8_t* stage_c = stage_base + (gelu ? 0 : buf * 4096);
+        uint8_t* stage_u = stage_base + 4096;
+        if (issued >= (gelu ? 1 : 2)) {
+          // the group that last used this buffer must have finished reading it
+          if (lane == 0) {
+            if (gelu) bulk_wait_read();
+            else bulk_wait_read1();
+          }
+          __syncwarp();
+        }
+        if (cbf) stage_bf16(stage_c, lane, v);
+        else stage_f32(stage_c, lane, v);
+        if (gelu) stage_f32(stage_u, lane, u);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (ts.c_mode == 1) {
+            tma_store_3d(&tmC, stage_c, nb - g.n0, row0 - g.m0, (int)g.zm.z(c.i));
+          } else if (ts.c_mode == 2) {
+            int b, sq;
+            g.tm.bs(row0, b, sq);
+            const int part = nb / g.hs_d, r = nb - part * g.hs_d;
+            const int h = r / g.hs_hd;
+            tma_store_5d(&tmC, stage_c, r - h * g.hs_hd, sq, h, b, part);
+          } else {
+            const int b = g.zm.b(c.i), h = g.zm.h(c.i);
+            tma_store_2d(&tmC, stage_c, (int)(g.c_col_off + (int64_t)h * g.hs_hd + nb),
+                         (int)g.tm.row(b, row0));
+          }
+          if (gelu) tma_store_2d(&tmU, stage_u, nb - g.n0, row0 - g.m0);
+          bulk_commit();
+        }
+        ++issued;
+        buf ^= 1;
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -456,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         aph ^= 1;
       }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -507,6 +638,78 @@ nnt_status make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t o
   return NNT_OK;
 }
 
+// General tiled map (rank 2..5) for the epilogue's bulk stores.
+nnt_status make_store_map(CUtensorMap* map, const void* base, bool bf, int rank, const cuuint64_t* dims,
+                          const cuuint64_t* stride_bytes) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_thread_error("cuTensorMapEncodeTiled is unavailable");
+    return NNT_ERR_CUDA;
+  }
+  cuuint32_t box[5] = {32, 32, 1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank,
+                  const_cast<void*>(base), dims, stride_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  bf ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_thread_error("cuTensorMapEncodeTiled (store map) failed (%d)", (int)r);
+    return NNT_ERR_INVALID_ARG;
+  }
+  return NNT_OK;
+}
+
+bool al16(int64_t bytes) { return (bytes & 15) == 0; }
+
+// Epilogue store maps and mode for one launch (see TileSpace::c_mode).
+nnt_status store_maps(const GemmArgs& g, int64_t zmax, CUtensorMap* mc, CUtensorMap* mu, int& c_mode,
+                      int& aux_tma) {
+  memset(mc, 0, sizeof *mc);
+  memset(mu, 0, sizeof *mu);
+  c_mode = 0;
+  aux_tma = 0;
+  const bool bf = g.c_dtype == NNT_BF16;
+  const int64_t es = bf ? 2 : 4;
+  const char* C = static_cast<const char*>(g.C);
+  if (g.out_mode == OUT_PLAIN) {
+    const char* base = C + ((int64_t)g.m0 * g.ldc + g.n0) * es;
+    const int64_t zs = g.c_zs > 0 ? g.c_zs : (int64_t)g.M * g.ldc;
+    if (al16((int64_t)(uintptr_t)base) && al16(g.ldc * es) && al16(zs * es)) {
+      cuuint64_t dims[3] = {(cuuint64_t)g.nt, (cuuint64_t)g.mt, (cuuint64_t)zmax};
+      cuuint64_t str[2] = {(cuuint64_t)(g.ldc * es), (cuuint64_t)(zs * es)};
+      NNT_TRY(make_store_map(mc, base, bf, 3, dims, str));
+      c_mode = 1;
+    }
+  } else if (g.hs_hd % 32 == 0 && g.tm.ts % 32 == 0 && al16((int64_t)(uintptr_t)C)) {
+    if (g.out_mode == OUT_HEADSPLIT) {
+      const int64_t hd = g.hs_hd, S = g.hs_S, H = g.hs_H, B = g.hs_B;
+      cuuint64_t dims[5] = {(cuuint64_t)hd, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B,
+                            (cuuint64_t)(g.N / g.hs_d)};
+      cuuint64_t str[4] = {(cuuint64_t)(hd * es), (cuuint64_t)(S * hd * es), (cuuint64_t)(H * S * hd * es),
+                           (cuuint64_t)(B * H * S * hd * es)};
+      if (g.hs_d % 32 == 0 && al16(hd * es)) {
+        NNT_TRY(make_store_map(mc, C, bf, 5, dims, str));
+        c_mode = 2;
+      }
+    } else if (al16(g.ldc * es) && g.c_col_off % 8 == 0) {
+      cuuint64_t dims[2] = {(cuuint64_t)g.ldc, (cuuint64_t)((int64_t)g.hs_B * g.hs_S)};
+      cuuint64_t str[1] = {(cuuint64_t)(g.ldc * es)};
+      NNT_TRY(make_store_map(mc, C, bf, 2, dims, str));
+      c_mode = 3;
+    }
+  }
+  if (g.epi == EPI_GELU && c_mode == 1) {
+    const char* base = reinterpret_cast<const char*>(g.aux) + ((int64_t)g.m0 * g.ld_aux + g.n0) * 4;
+    if (al16((int64_t)(uintptr_t)base) && al16(g.ld_aux * 4)) {
+      cuuint64_t dims[2] = {(cuuint64_t)g.nt, (cuuint64_t)g.mt};
+      cuuint64_t str[1] = {(cuuint64_t)(g.ld_aux * 4)};
+      NNT_TRY(make_store_map(mu, base, false, 2, dims, str));
+      aux_tma = 1;
+    }
+  }
+  return NNT_OK;
+}
+
 int num_sms() {
   static int n = 0;
   if (!n) {
@@ -525,6 +728,8 @@ TileSpace tile_space(const GemmArgs& g, int BN) {
   t.nt0 = g.n0 / BN;
   t.n_nt = (g.n0 + g.nt - 1) / BN - t.nt0 + 1;
   t.total = g.nbatch * t.n_mt * t.n_nt;
+  t.c_mode = 0;
+  t.aux_tma = 0;
   return t;
 }
 
@@ -551,14 +756,16 @@ nnt_status launch_tc(const GemmArgs& g, cudaStream_t st) {
     NNT_TRY(make_map(&mb, g.B, g.N, g.K, g.ldb, g.b_zs > 0 ? g.b_zs : (int64_t)g.K * g.ldb, zmax, 64, 64));
   else
     NNT_TRY(make_map(&mb, g.B, g.K, g.N, g.ldb, g.b_zs > 0 ? g.b_zs : (int64_t)g.N * g.ldb, zmax, 64, BN));
-  const TileSpace ts = tile_space(g, BN);
+  TileSpace ts = tile_space(g, BN);
+  CUtensorMap mc, mu;
+  NNT_TRY(store_maps(g, zmax, &mc, &mu, ts.c_mode, ts.aux_tma));
   const int grid = std::min(ts.total, num_sms());
   uint32_t* err = device_error_word();
   if (!err) {
     set_thread_error("device error word unavailable");
     return NNT_ERR_CUDA;
   }
-  gemm_tc_kernel<BN, A_MN, B_MN><<<grid, kThreads, C::SMEM, st>>>(ma, mb, g, ts, err);
+  gemm_tc_kernel<BN, A_MN, B_MN><<<grid, kThreads, C::SMEM, st>>>(ma, mb, mc, mu, g, ts, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_thread_error("gemm_tc launch: %s", cudaGetErrorString(e));
@@ -579,7 +786,20 @@ nnt_status launch_bn(const GemmArgs& g, cudaStream_t st) {
 
 // Tile width: the widest of 256/128/64 whose persistent schedule wastes at most
 // a little more than the narrower ones (tiles per CTA rounded up).
+// Relative tensor-pipe efficiency of a 128 x BN tile (smem operand traffic per
+// MMA grows as BN shrinks), measured on GB300 for K >= 768.
+int bn_override() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("NNT_GEMM_BN");
+    v = e ? atoi(e) : 0;
+    if (v != 64 && v != 128 && v != 256) v = 0;
+  }
+  return v;
+}
+
 int choose_bn(const GemmArgs& g) {
+  if (bn_override()) return bn_override();
   if (g.nt <= 64) return 64;
   const int sms = num_sms();
   double best = 0;
@@ -588,7 +808,7 @@ int choose_bn(const GemmArgs& g) {
     if (bn > 64 && g.nt <= bn / 2) continue;
     const TileSpace t = tile_space(g, bn);
     const double waves = std::ceil((double)t.total / sms);
-    const double eff = (double)t.total / (waves * sms) * (bn == 256 ? 1.0 : bn == 128 ? 0.93 : 0.8);
+    const double eff = (double)t.total / (waves * sms) * (bn == 256 ? 1.0 : bn == 128 ? 0.8 : 0.35);
     if (eff > best + 1e-9) {
       best = eff;
       best_bn = bn;

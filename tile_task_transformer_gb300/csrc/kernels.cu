@@ -310,195 +310,260 @@ nnt_status launch_layernorm_fwd(const float* x, const float* g, const float* b, 
   return launch_check("layernorm_fwd");
 }
 
-static int ln_bwd_grid(int64_t rows, int cols) {
-  const int tpr = row_tpr(cols);
-  const int rpc = std::max(256, tpr) / tpr;
-  return (int)std::min<int64_t>(ceil_div(rows, rpc), 256);
-}
-int ln_bwd_nparts(int64_t rows, int cols) { return ln_bwd_grid(rows, cols); }
-
-// dx = rstd*(gdy - mean(gdy) - xhat*mean(gdy*xhat)) (+ resid), gdy = g*dy.
-// Each CTA walks rows with a grid stride, keeps per-column sums of dy*xhat and
-// dy for the columns its threads own, combines its row groups in shared memory
-// and writes one partial row per CTA.
+// dx = rstd*(gdy - mean(gdy) - xhat*mean(gdy*xhat)) (+ resid), gdy = g*dy; the
+// parameter gradients come from ln_bwd_colsums_kernel.
 template <int TPR, int MAXV, typename T>
 __global__ void ln_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
                               const float* __restrict__ mean, const float* __restrict__ rstd,
-                              const float* __restrict__ g, const float* resid,
-                              float* dx, T* __restrict__ dx_act,
-                              float* __restrict__ part_g, float* __restrict__ part_b, int64_t rows,
-                              int cols) {
+                              const float* __restrict__ g, const float* resid, float* dx,
+                              T* __restrict__ dx_act, int64_t rows, int cols) {
   __shared__ float red[32];
-  extern __shared__ float comb[];  // [rpc][cols] x 2 when rpc > 1
   const int rpc = blockDim.x / TPR;
-  const int grp = threadIdx.x / TPR;
   const int lane = threadIdx.x % TPR;
+  const int64_t row = (int64_t)blockIdx.x * rpc + threadIdx.x / TPR;
+  const bool active = row < rows;
+  const int64_t r = active ? row : 0;
   const int nv = cols >> 2;
-  float4 pg[MAXV], pb[MAXV], gam[MAXV];
+  const float mu = mean[r], rs = rstd[r];
+  float4 xh[MAXV], gd[MAXV];
+  float s1 = 0.f, s2 = 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
-    pg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    pb[i] = pg[i];
     const int c = lane + i * TPR;
-    gam[i] = (c < nv) ? load4(g + 4 * c) : pg[i];
+    if (active && c < nv) {
+      const float4 dv = load4(dy + r * cols + 4 * c);
+      const float4 xv = load4(x + r * cols + 4 * c);
+      const float4 gm = load4(g + 4 * c);
+      xh[i] = make_float4((xv.x - mu) * rs, (xv.y - mu) * rs, (xv.z - mu) * rs, (xv.w - mu) * rs);
+      gd[i] = make_float4(gm.x * dv.x, gm.y * dv.y, gm.z * dv.z, gm.w * dv.w);
+      s1 += (gd[i].x + gd[i].y) + (gd[i].z + gd[i].w);
+      s2 += (gd[i].x * xh[i].x + gd[i].y * xh[i].y) + (gd[i].z * xh[i].z + gd[i].w * xh[i].w);
+    } else {
+      xh[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      gd[i] = xh[i];
+    }
   }
   const float inv_n = 1.0f / (float)cols;
-  for (int64_t row0 = (int64_t)blockIdx.x * rpc; row0 < rows; row0 += (int64_t)gridDim.x * rpc) {
-    const int64_t row = row0 + grp;
-    const bool active = row < rows;
-    const int64_t r = active ? row : 0;
-    const float mu = mean[r], rs = rstd[r];
-    float4 xh[MAXV], gd[MAXV];
-    float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int c = lane + i * TPR;
-      if (active && c < nv) {
-        float4 dv = load4(dy + r * cols + 4 * c);
-        float4 xv = load4(x + r * cols + 4 * c);
-        xh[i] = make_float4((xv.x - mu) * rs, (xv.y - mu) * rs, (xv.z - mu) * rs, (xv.w - mu) * rs);
-        gd[i] = make_float4(gam[i].x * dv.x, gam[i].y * dv.y, gam[i].z * dv.z, gam[i].w * dv.w);
-        s1 += (gd[i].x + gd[i].y) + (gd[i].z + gd[i].w);
-        s2 += (gd[i].x * xh[i].x + gd[i].y * xh[i].y) + (gd[i].z * xh[i].z + gd[i].w * xh[i].w);
-        pg[i].x += dv.x * xh[i].x;
-        pg[i].y += dv.y * xh[i].y;
-        pg[i].z += dv.z * xh[i].z;
-        pg[i].w += dv.w * xh[i].w;
-        pb[i].x += dv.x;
-        pb[i].y += dv.y;
-        pb[i].z += dv.z;
-        pb[i].w += dv.w;
-      } else {
-        xh[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        gd[i] = xh[i];
-      }
-    }
-    s1 = group_sum<TPR>(s1, red) * inv_n;
-    s2 = group_sum<TPR>(s2, red) * inv_n;
-    if (active) {
-#pragma unroll
-      for (int i = 0; i < MAXV; ++i) {
-        const int c = lane + i * TPR;
-        if (c < nv) {
-          float4 o;
-          o.x = rs * (gd[i].x - s1 - xh[i].x * s2);
-          o.y = rs * (gd[i].y - s1 - xh[i].y * s2);
-          o.z = rs * (gd[i].z - s1 - xh[i].z * s2);
-          o.w = rs * (gd[i].w - s1 - xh[i].w * s2);
-          if (resid) {
-            float4 q = load4(resid + r * cols + 4 * c);
-            o.x += q.x;
-            o.y += q.y;
-            o.z += q.z;
-            o.w += q.w;
-          }
-          store4(dx + r * cols + 4 * c, o);
-          if (dx_act) store4(dx_act + r * cols + 4 * c, o);
-        }
-      }
-    }
-  }
-  if (!part_g) return;
-  if (rpc == 1) {
-#pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int c = lane + i * TPR;
-      if (c < nv) {
-        store4(part_g + (int64_t)blockIdx.x * cols + 4 * c, pg[i]);
-        store4(part_b + (int64_t)blockIdx.x * cols + 4 * c, pb[i]);
-      }
-    }
-    return;
-  }
-  float* cg = comb;
-  float* cb = comb + rpc * cols;
+  s1 = group_sum<TPR>(s1, red) * inv_n;
+  s2 = group_sum<TPR>(s2, red) * inv_n;
+  if (!active) return;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int c = lane + i * TPR;
     if (c < nv) {
-      store4(cg + grp * cols + 4 * c, pg[i]);
-      store4(cb + grp * cols + 4 * c, pb[i]);
+      float4 o;
+      o.x = rs * (gd[i].x - s1 - xh[i].x * s2);
+      o.y = rs * (gd[i].y - s1 - xh[i].y * s2);
+      o.z = rs * (gd[i].z - s1 - xh[i].z * s2);
+      o.w = rs * (gd[i].w - s1 - xh[i].w * s2);
+      if (resid) {
+        const float4 q = load4(resid + r * cols + 4 * c);
+        o.x += q.x;
+        o.y += q.y;
+        o.z += q.z;
+        o.w += q.w;
+      }
+      store4(dx + r * cols + 4 * c, o);
+      if (dx_act) store4(dx_act + r * cols + 4 * c, o);
     }
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
-    float a = 0.f, bsum = 0.f;
-    for (int j = 0; j < rpc; ++j) {
-      a += cg[j * cols + c];
-      bsum += cb[j * cols + c];
-    }
-    part_g[(int64_t)blockIdx.x * cols + c] = a;
-    part_b[(int64_t)blockIdx.x * cols + c] = bsum;
   }
 }
 
 nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* mean,
                                 const float* rstd, const float* g, const float* resid, float* dx,
-                                void* dx_act, float* part_g, float* part_b, int64_t rows, int cols,
-                                int act_dtype, cudaStream_t st) {
+                                void* dx_act, int64_t rows, int cols, int act_dtype,
+                                cudaStream_t st) {
   NNT_CHECK_ARG(cols % 4 == 0 && cols > 0 && cols <= 32768,
                 "layernorm bwd: cols must be a multiple of 4 in [4, 32768] (got %d)", cols);
   if (rows == 0) return NNT_OK;
   const int tpr = row_tpr(cols);
   const int block = std::max(256, tpr);
-  const int rpc = block / tpr;
-  const int grid = ln_bwd_grid(rows, cols);
-  const size_t smem = (rpc > 1 && part_g) ? (size_t)2 * rpc * cols * sizeof(float) : 0;
+  const int64_t grid = ceil_div(rows, block / tpr);
   NNT_TPR_DISPATCH(tpr, {
-    if (act_dtype == NNT_BF16) {
-      auto k = ln_bwd_kernel<TPR, 8, bf16>;
-      if (smem > 48 * 1024) NNT_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-      k<<<grid, block, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, part_g, part_b, rows, cols);
-    } else {
-      auto k = ln_bwd_kernel<TPR, 8, float>;
-      if (smem > 48 * 1024) NNT_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-      k<<<grid, block, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, part_g, part_b, rows, cols);
-    }
+    if (act_dtype == NNT_BF16)
+      ln_bwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols);
+    else
+      ln_bwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols);
   });
   return launch_check("layernorm_bwd");
 }
 
-// out[c] (+)= sum_p part[p*ld + c], p ascending.
+// Column sums of the layer-norm backward over a chunk of rows: sum dy*xhat
+// (gain gradient), sum dy (shift gradient) and, when `out` is given, sum out
+// (the bias gradient of the linear layer whose output gradient `out` is).
+// CTA (strip of 128 columns, row chunk): each lane owns 4 columns (16-byte
+// loads), warp w takes rows w, w+8, ...; the 8 warp sums are added in warp
+// order. part: [nchunks][3][cols].
+__global__ void ln_bwd_colsums_kernel(const float* __restrict__ dy, const float* __restrict__ x,
+                                      const float* __restrict__ mean,
+                                      const float* __restrict__ rstd, const float* __restrict__ out,
+                                      int64_t rows, int cols, int64_t rows_per_chunk,
+                                      float* __restrict__ part) {
+  __shared__ float4 red[3][8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = (blockIdx.x * 32 + lane) * 4;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_chunk;
+  const int64_t r1 = r0 + rows_per_chunk < rows ? r0 + rows_per_chunk : rows;
+  float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), sb = sg, so = sg;
+  if (c < cols) {
+#pragma unroll 2
+    for (int64_t r = r0 + w; r < r1; r += 8) {
+      const float4 d = load4(dy + r * cols + c);
+      const float4 xv = load4(x + r * cols + c);
+      const float mu = mean[r], rs = rstd[r];
+      sg.x += d.x * ((xv.x - mu) * rs);
+      sg.y += d.y * ((xv.y - mu) * rs);
+      sg.z += d.z * ((xv.z - mu) * rs);
+      sg.w += d.w * ((xv.w - mu) * rs);
+      sb.x += d.x; sb.y += d.y; sb.z += d.z; sb.w += d.w;
+      if (out) {
+        const float4 o = load4(out + r * cols + c);
+        so.x += o.x; so.y += o.y; so.z += o.z; so.w += o.w;
+      }
+    }
+  }
+  red[0][w][lane] = sg;
+  red[1][w][lane] = sb;
+  red[2][w][lane] = so;
+  __syncthreads();
+  if (w < 3 && c < cols) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = red[w][i][lane];
+      t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+    }
+    store4(part + ((int64_t)blockIdx.y * 3 + w) * cols + c, t);
+  }
+}
+
+int64_t ln_colsum_chunks(int64_t rows) { return std::min<int64_t>(128, std::max<int64_t>(1, ceil_div(rows, 32))); }
+
+nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* mean,
+                                 const float* rstd, const float* out, int64_t rows, int cols,
+                                 float* part, float* dg, float* db, float* dbias, cudaStream_t st) {
+  NNT_CHECK_ARG(cols % 4 == 0, "layernorm colsums: cols must be a multiple of 4");
+  const int64_t nch = ln_colsum_chunks(rows);
+  const int64_t rpc = ceil_div(rows, nch);
+  dim3 grid((unsigned)ceil_div(cols, 128), (unsigned)nch);
+  ln_bwd_colsums_kernel<<<grid, 256, 0, st>>>(dy, x, mean, rstd, out, rows, cols, rpc, part);
+  NNT_TRY(launch_check("ln_bwd_colsums"));
+  return launch_sum_parts3(part, nch, cols, dg, db, out ? dbias : nullptr, st);
+}
+
+// out[c] (+)= sum_p part[p*ld + c]. A CTA owns 32 columns; its 8 warps take
+// every 8th partial row (lane = column, so each row read is one coalesced
+// 128-byte segment) and the 8 warp sums are added in warp order: a fixed
+// summation order, independent of scheduling.
 __global__ void sum_parts_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
                                  int64_t ld, float* __restrict__ out, int accumulate) {
-  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = blockIdx.x * 32ll + lane;
   float s = 0.f;
-  for (int64_t p = 0; p < nparts; ++p) s += part[p * ld + c];
-  out[c] = accumulate ? out[c] + s : s;
+  if (c < cols) {
+    int64_t p = w;
+    for (; p + 24 < nparts; p += 32) {
+      const float a0 = part[p * ld + c], a1 = part[(p + 8) * ld + c];
+      const float a2 = part[(p + 16) * ld + c], a3 = part[(p + 24) * ld + c];
+      s += a0;
+      s += a1;
+      s += a2;
+      s += a3;
+    }
+    for (; p < nparts; p += 8) s += part[p * ld + c];
+  }
+  red[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && c < cols) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][lane];
+    out[c] = accumulate ? out[c] + t : t;
+  }
+}
+
+__global__ void sum_parts3_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
+                                  float* o0, float* o1, float* o2) {
+  float* outs[3] = {o0, o1, o2};
+  float* out = outs[blockIdx.y];
+  if (!out) return;
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = blockIdx.x * 32ll + lane;
+  const int64_t ld = 3 * cols;
+  const float* p0 = part + blockIdx.y * cols;
+  float s = 0.f;
+  if (c < cols)
+    for (int64_t p = w; p < nparts; p += 8) s += p0[p * ld + c];
+  red[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && c < cols) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][lane];
+    out[c] = t;
+  }
+}
+
+nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, float* o0, float* o1,
+                             float* o2, cudaStream_t st) {
+  if (cols == 0) return NNT_OK;
+  dim3 grid((unsigned)ceil_div(cols, 32), 3);
+  sum_parts3_kernel<<<grid, 256, 0, st>>>(part, nparts, cols, o0, o1, o2);
+  return launch_check("sum_parts3");
 }
 
 nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,
                             float* out, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
-  sum_parts_kernel<<<(unsigned)ceil_div(cols, 256), 256, 0, st>>>(part, nparts, cols, ld, out,
-                                                                   accumulate);
+  sum_parts_kernel<<<(unsigned)ceil_div(cols, 32), 256, 0, st>>>(part, nparts, cols, ld, out,
+                                                                  accumulate);
   return launch_check("sum_parts");
 }
 
-// Column sums in two fixed-order stages: CTA (cb, rb) sums rows
-// [rb*kColRows, +kColRows) of columns [cb*256, +256) into part[rb][c].
+// Column sums in two fixed-order stages: CTA (strip of 128 columns, chunk of
+// kColRows rows) adds its rows with 4 columns per lane and 8 warps in warp
+// order into part[chunk][c]; launch_sum_parts adds the chunks.
 static constexpr int kColRows = 64;
 int64_t colsum_nparts(int64_t rows) { return ceil_div(rows, kColRows); }
 
 template <typename T>
 __global__ void colsum_part_kernel(const T* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
                                    float* __restrict__ part) {
-  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+  __shared__ float4 red[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = ((int64_t)blockIdx.x * 32 + lane) * 4;
   const int64_t r0 = (int64_t)blockIdx.y * kColRows;
   const int64_t r1 = r0 + kColRows < rows ? r0 + kColRows : rows;
-  float s = 0.f;
-  for (int64_t r = r0; r < r1; ++r) s += to_f(a[r * ld + c]);
-  part[(int64_t)blockIdx.y * cols + c] = s;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c < cols) {
+#pragma unroll 4
+    for (int64_t r = r0 + w; r < r1; r += 8) {
+      const float4 v = load4(a + r * ld + c);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+  }
+  red[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && c < cols) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = red[i][lane];
+      t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+    }
+    store4(part + (int64_t)blockIdx.y * cols + c, t);
+  }
 }
 
 nnt_status launch_colsum(const void* a, int a_dtype, int64_t rows, int64_t cols, int64_t ld,
                          float* part, float* out, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
+  NNT_CHECK_ARG(cols % 4 == 0 && ld % 4 == 0, "colsum: cols and ld must be multiples of 4");
   const int64_t np = colsum_nparts(rows);
   NNT_CHECK_ARG(np < 65536, "colsum: too many rows");
-  dim3 grid((unsigned)ceil_div(cols, 256), (unsigned)np);
+  dim3 grid((unsigned)ceil_div(cols, 128), (unsigned)np);
   if (a_dtype == NNT_BF16)
     colsum_part_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)a, rows, cols, ld, part);
   else
@@ -618,15 +683,17 @@ __global__ void softmax_bwd_kernel(const T* __restrict__ p, const float* __restr
   }
 }
 
+// Threads per row such that a row needs at most 4 float4 per thread: fewer
+// registers, so more rows (and more loads) are in flight per SM.
 static int softmax_tpr(int64_t S) {
   int tpr = 32;
-  while ((int64_t)tpr * 8 * 4 < S && tpr < 1024) tpr <<= 1;
+  while ((int64_t)tpr * 4 * 4 < S && tpr < 1024) tpr <<= 1;
   return tpr;
 }
 
 nnt_status launch_softmax_fwd(const float* s, void* p, int64_t S, ZMap zm, int nz, int q0, int nq,
                               int act_dtype, cudaStream_t st) {
-  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 32768, "softmax: seq must be a multiple of 4 <= 32768");
+  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 16384, "softmax: seq must be a multiple of 4 <= 16384");
   const int64_t rows = (int64_t)nz * nq;
   if (rows == 0) return NNT_OK;
   const int tpr = softmax_tpr(S);
@@ -634,16 +701,16 @@ nnt_status launch_softmax_fwd(const float* s, void* p, int64_t S, ZMap zm, int n
   const int64_t grid = ceil_div(rows, block / tpr);
   NNT_TPR_DISPATCH(tpr, {
     if (act_dtype == NNT_BF16)
-      softmax_fwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>(s, (bf16*)p, S, zm, nz, q0, nq);
+      softmax_fwd_kernel<TPR, 4, bf16><<<grid, block, 0, st>>>(s, (bf16*)p, S, zm, nz, q0, nq);
     else
-      softmax_fwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>(s, (float*)p, S, zm, nz, q0, nq);
+      softmax_fwd_kernel<TPR, 4, float><<<grid, block, 0, st>>>(s, (float*)p, S, zm, nz, q0, nq);
   });
   return launch_check("softmax_fwd");
 }
 
 nnt_status launch_softmax_bwd(const void* p, const float* dp, void* ds, int64_t S, ZMap zm, int nz,
                               int q0, int nq, float scale, int act_dtype, cudaStream_t st) {
-  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 32768, "softmax bwd: seq must be a multiple of 4 <= 32768");
+  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 16384, "softmax bwd: seq must be a multiple of 4 <= 16384");
   const int64_t rows = (int64_t)nz * nq;
   if (rows == 0) return NNT_OK;
   const int tpr = softmax_tpr(S);
@@ -651,9 +718,9 @@ nnt_status launch_softmax_bwd(const void* p, const float* dp, void* ds, int64_t 
   const int64_t grid = ceil_div(rows, block / tpr);
   NNT_TPR_DISPATCH(tpr, {
     if (act_dtype == NNT_BF16)
-      softmax_bwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>((const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
+      softmax_bwd_kernel<TPR, 4, bf16><<<grid, block, 0, st>>>((const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
     else
-      softmax_bwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>((const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
+      softmax_bwd_kernel<TPR, 4, float><<<grid, block, 0, st>>>((const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
   });
   return launch_check("softmax_bwd");
 }
@@ -720,17 +787,18 @@ nnt_status launch_gelu_bwd(const void* dg, const float* u, void* du, int64_t n, 
 // cross-entropy (mean over tokens) + dlogits
 // =====================================================================
 
-// One CTA per row: pass 1 keeps a running (max, sum of exp) per thread and
-// merges them across the CTA; pass 2 re-reads the row (from L2) and writes
-// dz = (exp(z - lse) - onehot) * inv_rows, zero in the padding columns.
+// Each CTA takes rows in turn: pass 1 keeps a running (max, sum of exp) per
+// thread and merges them across the CTA; pass 2 re-reads the row (from L2) and
+// writes dz = (exp(z - lse) - onehot) * inv_rows, zero in the padding columns.
 template <typename T>
 __global__ void __launch_bounds__(512) cross_entropy_kernel(
-    const float* __restrict__ z, int64_t ldz, int64_t r0, int64_t cols,
+    const float* __restrict__ z, int64_t ldz, int64_t r0, int64_t nrows, int64_t cols,
     const uint16_t* __restrict__ tok_ids, TokMap tm, const uint16_t* __restrict__ tgt,
     int64_t tgt_stride, T* __restrict__ dz, int64_t lddz, float* __restrict__ row_loss,
     float inv_rows) {
   __shared__ float red_m[32], red_s[32];
-  const int64_t r = r0 + blockIdx.x;
+  for (int64_t rr = blockIdx.x; rr < nrows; rr += gridDim.x) {
+  const int64_t r = r0 + rr;
   const float* zr = z + r * ldz;
   const int64_t n4 = cols >> 2;  // full float4s
   float m = -INFINITY, s = 0.f;
@@ -808,6 +876,8 @@ __global__ void __launch_bounds__(512) cross_entropy_kernel(
     if (c < cols) o = (exp2f(zr[c] * kLog2e - ls) - (c == y ? 1.f : 0.f)) * inv_rows;
     dr[c] = from_f<T>(o);
   }
+  __syncthreads();  // red_m / red_s are reused by the next row
+  }
 }
 
 nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t nrows,
@@ -817,12 +887,14 @@ nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t
   NNT_CHECK_ARG(ldz % 4 == 0 && lddz % 4 == 0 && ldz >= cols && lddz >= cols,
                 "cross entropy: leading dimensions must be multiples of 4 and >= cols");
   if (nrows == 0) return NNT_OK;
+  // two CTAs per SM walk the rows, so the rows being re-read (pass 2) stay in L2
+  const unsigned grid = (unsigned)std::min<int64_t>(nrows, 2 * 152);
   if (act_dtype == NNT_BF16)
-    cross_entropy_kernel<bf16><<<(unsigned)nrows, 512, 0, st>>>(
-        z, ldz, r0, cols, tok_ids, tm, tgt, tgt_stride, (bf16*)dz, lddz, row_loss, inv_rows);
+    cross_entropy_kernel<bf16><<<grid, 512, 0, st>>>(
+        z, ldz, r0, nrows, cols, tok_ids, tm, tgt, tgt_stride, (bf16*)dz, lddz, row_loss, inv_rows);
   else
-    cross_entropy_kernel<float><<<(unsigned)nrows, 512, 0, st>>>(
-        z, ldz, r0, cols, tok_ids, tm, tgt, tgt_stride, (float*)dz, lddz, row_loss, inv_rows);
+    cross_entropy_kernel<float><<<grid, 512, 0, st>>>(
+        z, ldz, r0, nrows, cols, tok_ids, tm, tgt, tgt_stride, (float*)dz, lddz, row_loss, inv_rows);
   return launch_check("cross_entropy");
 }
 

@@ -27,12 +27,18 @@ nnt_status launch_wpe_grad(const float* dx, TokMap tm, int B, int s0, int ns, in
 nnt_status launch_layernorm_fwd(const float* x, const float* g, const float* b, void* y,
                                 float* mean, float* rstd, int64_t rows, int cols, float eps,
                                 int act_dtype, cudaStream_t st);
-// partials: [ln_bwd_nparts(rows, cols)][cols] for dg and for db (may be NULL)
-int ln_bwd_nparts(int64_t rows, int cols);
 nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* mean,
                                 const float* rstd, const float* g, const float* resid, float* dx,
-                                void* dx_act, float* part_g, float* part_b, int64_t rows, int cols,
-                                int act_dtype, cudaStream_t st);
+                                void* dx_act, int64_t rows, int cols, int act_dtype,
+                                cudaStream_t st);
+// dg = sum_rows dy*xhat, db = sum_rows dy and (out != NULL) dbias = sum_rows out,
+// in a fixed order; part: scratch of ln_colsum_chunks(rows) * 3 * cols floats
+int64_t ln_colsum_chunks(int64_t rows);
+nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* mean,
+                                 const float* rstd, const float* out, int64_t rows, int cols,
+                                 float* part, float* dg, float* db, float* dbias, cudaStream_t st);
+nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, float* o0, float* o1,
+                             float* o2, cudaStream_t st);
 
 // out[c] (=|+=) sum over p of part[p][c], p in increasing order
 nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,

@@ -80,6 +80,7 @@ struct nnt_model {
   TokMap tm;
   int64_t ldz, lddz;
   int backend = 0;
+  int gemm_min_cols = 2048;
   std::string err;
 
   // memory
@@ -320,9 +321,7 @@ nnt_status alloc_all(nnt_model* m) {
   NNT_TRY(dalloc(m, m->du, (size_t)T * f * as));
   NNT_TRY(dalloc(m, m->dOh, Td * as));
   NNT_TRY(dalloc(m, m->dqkv, 3 * Td * as));
-  const int lnp = ln_bwd_nparts(m->TT, d);
-  NNT_TRY(dalloc(m, m->ln_part_g, (size_t)m->n_tok * lnp * d * 4));
-  NNT_TRY(dalloc(m, m->ln_part_b, (size_t)m->n_tok * lnp * d * 4));
+  NNT_TRY(dalloc(m, m->ln_part_g, (size_t)ln_colsum_chunks(T) * 3 * d * 4));
   const int64_t maxcols = std::max<int64_t>(3 * d, f);
   NNT_TRY(dalloc(m, m->col_part, (size_t)colsum_nparts(T) * maxcols * 4));
   NNT_TRY(dalloc(m, m->sort_keys, (size_t)T * 4));
@@ -390,6 +389,23 @@ struct Builder {
     c0 = part * m->d + tile_lo(c, m->te);
     c1 = part * m->d + tile_hi(c, m->te, m->d);
   }
+  // Consecutive column tiles [t0, t1) merged into one GEMM launch until the
+  // launch is at least gemm_min_cols wide; tiles stay the dependency unit.
+  template <class Lo, class Hi>
+  std::vector<std::pair<int, int>> groups(int n, Lo lo, Hi hi) const {
+    std::vector<std::pair<int, int>> out;
+    int t0 = 0;
+    while (t0 < n) {
+      int t1 = t0 + 1;
+      while (t1 < n && hi(t1 - 1) - lo(t0) < m->gemm_min_cols) ++t1;
+      out.push_back({t0, t1});
+      t0 = t1;
+    }
+    return out;
+  }
+  std::vector<std::pair<int, int>> col_groups(int n, int tile, int N) const {
+    return groups(n, [=](int t) { return tile_lo(t, tile); }, [=](int t) { return tile_hi(t, tile, N); });
+  }
   // head-tile range overlapped by columns [c0, c1) of one part (c relative to part)
   void head_tiles(int c0, int c1, int& h0, int& h1) const {
     const int hl = c0 / m->hd, hh = (c1 + m->hd - 1) / m->hd;
@@ -447,25 +463,28 @@ void build_forward(nnt_model* m) {
       ln_fwd_task(TT_LN_FWD, &m->x[l], m->gx[l], &P_(m, l, LN1G), &P_(m, l, LN1B), &m->h1[l],
                   m->gh1[l], &m->mu1[l], &m->r1[l], m->gstat1[l], rt);
     // QKV projection, epilogue writes head-major q/k/v
+    auto qlo = [&](int ct) { int a, c; b.qkv_cols(ct, a, c); return a; };
+    auto qhi = [&](int ct) { int a, c; b.qkv_cols(ct, a, c); return c; };
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < 3 * m->nce; ++ct) {
-        int c0, c1;
-        b.qkv_cols(ct, c0, c1);
+      for (auto [t0, t1] : b.groups(3 * m->nce, qlo, qhi)) {
+        const int c0 = qlo(t0), c1 = qhi(t1 - 1);
         GemmArgs g = b.base();
         g.M = T; g.N = 3 * d; g.K = d;
         g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
         g.A = m->h1[l]; g.lda = d; g.a_trans = 0;
         g.B = pw(m, P_(m, l, QKVW)); g.ldb = d; g.b_trans = 0;
         g.C = m->qkvh[l]; g.c_dtype = act; g.out_mode = OUT_HEADSPLIT;
-        g.hs_B = m->B; g.hs_H = H; g.hs_S = S; g.hs_hd = hd; g.hs_d = d;
+        g.hs_B = m->B; g.hs_H = H; g.hs_S = S; g.hs_hd = hd; g.hs_B = m->B; g.hs_S = S; g.hs_H = H; g.hs_d = d;
         g.bias = pm(m, P_(m, l, QKVB));
         std::vector<TileUse> u;
         box(u, m->gh1[l], ACC_R, rt, rt + 1);
-        const int part = ct / m->nce;
-        int h0, h1;
-        b.head_tiles(c0 - part * d, c1 - part * d, h0, h1);
-        box(u, m->gqkvh[l], ACC_W, part, part + 1, b.bt_of(rt), b.bt_of(rt) + 1, h0, h1,
-            b.st_of(rt), b.st_of(rt) + 1);
+        for (int ct = t0; ct < t1; ++ct) {
+          const int part = ct / m->nce;
+          int h0, h1;
+          b.head_tiles(qlo(ct) - part * d, qhi(ct) - part * d, h0, h1);
+          box(u, m->gqkvh[l], ACC_W, part, part + 1, b.bt_of(rt), b.bt_of(rt) + 1, h0, h1,
+              b.st_of(rt), b.st_of(rt) + 1);
+        }
         b.gemm_task(P, TT_GEMM_QKV, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
       }
     // attention per (batch tile, head tile, query tile)
@@ -513,7 +532,7 @@ void build_forward(nnt_model* m) {
             g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 0;
             g.B = qkv_base + 2 * BH * zq * as; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
             g.C = m->O[l]; g.ldc = d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
-            g.hs_hd = hd;
+            g.hs_hd = hd; g.hs_B = m->B; g.hs_S = S; g.hs_H = H;
             g.causal = CAUSAL_K_UPPER;
             std::vector<TileUse> u;
             box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1, st, st + 1);
@@ -524,8 +543,8 @@ void build_forward(nnt_model* m) {
         }
     // attention output projection + residual: xmid = x + O Wo^T + bo
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->nce; ++ct) {
-        const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+      for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
+        const int c0 = tile_lo(t0, m->te), c1 = tile_hi(t1 - 1, m->te, d);
         GemmArgs g = b.base();
         g.M = T; g.N = d; g.K = d;
         g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
@@ -536,8 +555,8 @@ void build_forward(nnt_model* m) {
         g.resid = m->x[l]; g.ld_resid = d;
         std::vector<TileUse> u;
         box(u, m->gO[l], ACC_R, rt, rt + 1);
-        box(u, m->gx[l], ACC_R, rt, rt + 1, ct, ct + 1);
-        box(u, m->gxmid[l], ACC_W, rt, rt + 1, ct, ct + 1);
+        box(u, m->gx[l], ACC_R, rt, rt + 1, t0, t1);
+        box(u, m->gxmid[l], ACC_W, rt, rt + 1, t0, t1);
         b.gemm_task(P, TT_GEMM_ATTN_O, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
       }
     // LN2
@@ -546,8 +565,8 @@ void build_forward(nnt_model* m) {
                   m->gh2[l], &m->mu2[l], &m->r2[l], m->gstat2[l], rt);
     // FC + GELU: u = h2 W1^T + b1 (kept, fp32), g = gelu(u)
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->ncf; ++ct) {
-        const int c0 = tile_lo(ct, m->ti), c1 = tile_hi(ct, m->ti, f);
+      for (auto [t0, t1] : b.col_groups(m->ncf, m->ti, f)) {
+        const int c0 = tile_lo(t0, m->ti), c1 = tile_hi(t1 - 1, m->ti, f);
         GemmArgs g = b.base();
         g.M = T; g.N = f; g.K = d;
         g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
@@ -558,14 +577,14 @@ void build_forward(nnt_model* m) {
         g.epi = EPI_GELU; g.aux = m->u[l]; g.ld_aux = f;
         std::vector<TileUse> u;
         box(u, m->gh2[l], ACC_R, rt, rt + 1);
-        box(u, m->gu[l], ACC_W, rt, rt + 1, ct, ct + 1);
-        box(u, m->gg[l], ACC_W, rt, rt + 1, ct, ct + 1);
+        box(u, m->gu[l], ACC_W, rt, rt + 1, t0, t1);
+        box(u, m->gg[l], ACC_W, rt, rt + 1, t0, t1);
         b.gemm_task(P, TT_GEMM_FC, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
       }
     // MLP projection + residual: x[l+1] = xmid + g W2^T + b2
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->nce; ++ct) {
-        const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+      for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
+        const int c0 = tile_lo(t0, m->te), c1 = tile_hi(t1 - 1, m->te, d);
         GemmArgs g = b.base();
         g.M = T; g.N = d; g.K = f;
         g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
@@ -576,8 +595,8 @@ void build_forward(nnt_model* m) {
         g.resid = m->xmid[l]; g.ld_resid = d;
         std::vector<TileUse> u;
         box(u, m->gg[l], ACC_R, rt, rt + 1);
-        box(u, m->gxmid[l], ACC_R, rt, rt + 1, ct, ct + 1);
-        box(u, m->gx[l + 1], ACC_W, rt, rt + 1, ct, ct + 1);
+        box(u, m->gxmid[l], ACC_R, rt, rt + 1, t0, t1);
+        box(u, m->gx[l + 1], ACC_W, rt, rt + 1, t0, t1);
         b.gemm_task(P, TT_GEMM_MLP_PROJ, g, std::move(u), 2.0 * m->TT * (c1 - c0) * f);
       }
   }
@@ -589,8 +608,8 @@ void build_forward(nnt_model* m) {
                 m->gstatf, rt);
   // tied LM head: z = y wte^T (fp32 logits)
   for (int rt = 0; rt < m->n_tok; ++rt)
-    for (int vt = 0; vt < m->ncv; ++vt) {
-      const int c0 = tile_lo(vt, m->tv), c1 = tile_hi(vt, m->tv, V);
+    for (auto [t0, t1] : b.col_groups(m->ncv, m->tv, V)) {
+      const int c0 = tile_lo(t0, m->tv), c1 = tile_hi(t1 - 1, m->tv, V);
       GemmArgs g = b.base();
       g.M = T; g.N = V; g.K = d;
       g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
@@ -599,7 +618,7 @@ void build_forward(nnt_model* m) {
       g.C = m->z; g.ldc = m->ldz; g.c_dtype = NNT_F32;
       std::vector<TileUse> u;
       box(u, m->gy, ACC_R, rt, rt + 1);
-      box(u, m->gz, ACC_W, rt, rt + 1, vt, vt + 1);
+      box(u, m->gz, ACC_W, rt, rt + 1, t0, t1);
       b.gemm_task(P, TT_GEMM_LM_HEAD, g, std::move(u), 2.0 * m->TT * (c1 - c0) * d);
     }
   // cross-entropy + dlogits per token tile (over every vocab tile)
@@ -637,14 +656,13 @@ void build_backward(nnt_model* m) {
   const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
   const size_t as = m->act_size;
   const int act = m->act;
-  const int lnp = ln_bwd_nparts(m->TT, d);
 
   // dX tasks: out[rows rt, cols ct] = dY[rt] * W  (W [out, in], K = out); the
   // caller lists the tiles read and written.
   auto dx_gemm = [&](int type, const void* dY, int64_t ldy, int K, const ParamInfo& W, int64_t ldw,
-                     void* out, int out_dtype, int N, int tileN, int rt, int ct, GemmArgs proto,
-                     std::vector<TileUse> uses) {
-    const int c0 = tile_lo(ct, tileN), c1 = tile_hi(ct, tileN, N);
+                     void* out, int out_dtype, int N, int tileN, int rt, int t0, int t1,
+                     GemmArgs proto, std::vector<TileUse> uses) {
+    const int c0 = tile_lo(t0, tileN), c1 = tile_hi(t1 - 1, tileN, N);
     GemmArgs g = proto;
     g.M = T; g.N = N; g.K = K;
     g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
@@ -657,10 +675,10 @@ void build_backward(nnt_model* m) {
   auto dw_gemm = [&](int type, const void* dY, const TGrid& gdY, int64_t ldy, int Nout, int tOut,
                      const void* X, const TGrid& gX, int64_t ldx, int Nin, int tIn, const ParamInfo& W,
                      int gidx) {
-    for (int ot = 0; ot < tiles_of(Nout, tOut); ++ot)
-      for (int it = 0; it < tiles_of(Nin, tIn); ++it) {
-        const int o0 = tile_lo(ot, tOut), o1 = tile_hi(ot, tOut, Nout);
-        const int i0 = tile_lo(it, tIn), i1 = tile_hi(it, tIn, Nin);
+    for (auto [ot0, ot1] : b.col_groups(tiles_of(Nout, tOut), tOut, Nout))
+      for (auto [it0, it1] : b.col_groups(tiles_of(Nin, tIn), tIn, Nin)) {
+        const int o0 = tile_lo(ot0, tOut), o1 = tile_hi(ot1 - 1, tOut, Nout);
+        const int i0 = tile_lo(it0, tIn), i1 = tile_hi(it1 - 1, tIn, Nin);
         GemmArgs g = b.base();
         g.M = Nout; g.N = Nin; g.K = T;
         g.m0 = o0; g.mt = o1 - o0; g.n0 = i0; g.nt = i1 - i0;
@@ -670,7 +688,7 @@ void build_backward(nnt_model* m) {
         std::vector<TileUse> u;
         box(u, gdY, ACC_R);
         box(u, gX, ACC_R);
-        box(u, m->ggrad[gidx], ACC_W, ot, ot + 1, it, it + 1);
+        box(u, m->ggrad[gidx], ACC_W, ot0, ot1, it0, it1);
         b.gemm_task(P, TT_GEMM_DW, g, std::move(u), 2.0 * (o1 - o0) * (i1 - i0) * T);
       }
   };
@@ -688,10 +706,12 @@ void build_backward(nnt_model* m) {
     };
     P.add(std::move(t));
   };
-  // LN backward per token tile + parameter-grad reduction
+  // LN backward per token tile, then one column reduction over all tokens for
+  // the gain/shift gradients and (bias_idx >= 0) the gradient of the bias whose
+  // output gradient is the new residual gradient.
   auto ln_bwd = [&](const float* dy, const TGrid& gdy, const float* xin, const TGrid& gxin, const float* mu,
                     const float* rs, const TGrid& gst, const ParamInfo& gm, const ParamInfo& bt_,
-                    int gidx_g, int gidx_b, bool has_resid) {
+                    int gidx_g, int gidx_b, bool has_resid, int bias_idx) {
     for (int rt = 0; rt < m->n_tok; ++rt) {
       Task t;
       t.type = TT_LN_BWD;
@@ -700,31 +720,34 @@ void build_backward(nnt_model* m) {
       box(t.uses, gst, ACC_R, rt, rt + 1);
       box(t.uses, m->gdres, has_resid ? ACC_RW : ACC_W, rt, rt + 1);
       box(t.uses, m->gdres_act, ACC_W, rt, rt + 1);
-      box(t.uses, m->gln_part, ACC_W, rt, rt + 1);
       t.bytes = (double)m->TT * d * (4 * (has_resid ? 4 : 3) + as);
       const int64_t r0 = (int64_t)rt * m->TT;
       const float* gam = pm(m, gm);
       t.fn = [=](cudaStream_t s) {
         return launch_layernorm_bwd(dy + r0 * d, xin + r0 * d, mu + r0, rs + r0, gam,
                                     has_resid ? m->dres + r0 * d : nullptr, m->dres + r0 * d,
-                                    (char*)m->dres_act + r0 * d * as,
-                                    m->ln_part_g + (int64_t)rt * lnp * d,
-                                    m->ln_part_b + (int64_t)rt * lnp * d, m->TT, d, act, s);
+                                    (char*)m->dres_act + r0 * d * as, m->TT, d, act, s);
       };
       P.add(std::move(t));
     }
     Task t;
     t.type = TT_LN_PARTS;
     t.kernels = 2;
-    box(t.uses, m->gln_part, ACC_R);
+    box(t.uses, gdy, ACC_R);
+    box(t.uses, gxin, ACC_R);
+    box(t.uses, gst, ACC_R);
+    box(t.uses, m->gdres, ACC_R);
+    box(t.uses, m->gln_part, ACC_RW);
     box(t.uses, m->ggrad[gidx_g], ACC_W);
     box(t.uses, m->ggrad[gidx_b], ACC_W);
-    t.bytes = 2.0 * m->n_tok * lnp * d * 4;
+    if (bias_idx >= 0) box(t.uses, m->ggrad[bias_idx], ACC_W);
+    t.bytes = (double)T * d * 4 * (bias_idx >= 0 ? 3 : 2);
     float* og = pg(m, gm);
     float* ob = pg(m, bt_);
+    float* obias = bias_idx >= 0 ? pg(m, m->params[bias_idx]) : nullptr;
     t.fn = [=](cudaStream_t s) {
-      NNT_TRY(launch_sum_parts(m->ln_part_g, (int64_t)m->n_tok * lnp, d, d, og, 0, s));
-      return launch_sum_parts(m->ln_part_b, (int64_t)m->n_tok * lnp, d, d, ob, 0, s);
+      return launch_ln_bwd_colsums(dy, xin, mu, rs, obias ? m->dres : nullptr, T, d, m->ln_part_g, og,
+                                   ob, obias, s);
     };
     P.add(std::move(t));
   };
@@ -732,8 +755,8 @@ void build_backward(nnt_model* m) {
 
   // LM head backward: dy_f = dz wte (fp32), dwte = dz^T y
   for (int rt = 0; rt < m->n_tok; ++rt)
-    for (int ct = 0; ct < m->nce; ++ct) {
-      const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+    for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
+      const int c0 = tile_lo(t0, m->te), c1 = tile_hi(t1 - 1, m->te, d);
       GemmArgs g = b.base();
       g.M = T; g.N = d; g.K = V;
       g.m0 = b.row0(rt); g.mt = m->TT; g.n0 = c0; g.nt = c1 - c0;
@@ -742,13 +765,13 @@ void build_backward(nnt_model* m) {
       g.C = m->dtmp; g.ldc = d; g.c_dtype = NNT_F32;
       std::vector<TileUse> u;
       box(u, m->gdz, ACC_R, rt, rt + 1);
-      box(u, m->gdtmp, ACC_W, rt, rt + 1, ct, ct + 1);
+      box(u, m->gdtmp, ACC_W, rt, rt + 1, t0, t1);
       b.gemm_task(P, TT_GEMM_LM_DX, g, std::move(u), 2.0 * m->TT * (c1 - c0) * V);
     }
   for (int vt = 0; vt < m->ncv; ++vt)
-    for (int ct = 0; ct < m->nce; ++ct) {
+    for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
       const int v0 = tile_lo(vt, m->tv), v1 = tile_hi(vt, m->tv, V);
-      const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+      const int c0 = tile_lo(t0, m->te), c1 = tile_hi(t1 - 1, m->te, d);
       GemmArgs g = b.base();
       g.M = V; g.N = d; g.K = T;
       g.m0 = v0; g.mt = v1 - v0; g.n0 = c0; g.nt = c1 - c0;
@@ -758,12 +781,13 @@ void build_backward(nnt_model* m) {
       std::vector<TileUse> u;
       box(u, m->gdz, ACC_R);
       box(u, m->gy, ACC_R);
-      box(u, m->ggrad[0], ACC_W, vt, vt + 1, ct, ct + 1);
+      box(u, m->ggrad[0], ACC_W, vt, vt + 1, t0, t1);
       b.gemm_task(P, TT_GEMM_LM_DW, g, std::move(u), 2.0 * (v1 - v0) * (c1 - c0) * T);
     }
   // final LN backward (no residual input: dres starts here)
   ln_bwd(m->dtmp, m->gdtmp, m->x[m->L], m->gx[m->L], m->muf, m->rf, m->gstatf, m->params[pidx_lnf],
-         m->params[pidx_lnf + 1], pidx_lnf, pidx_lnf + 1, false);
+         m->params[pidx_lnf + 1], pidx_lnf, pidx_lnf + 1, false,
+         m->L > 0 ? 2 + 12 * (m->L - 1) + PROJB : -1);
 
   const size_t zq = (size_t)S * hd;
   const int64_t BH = (int64_t)m->B * H;
@@ -771,53 +795,51 @@ void build_backward(nnt_model* m) {
     const int pi = 2 + 12 * l;
     // MLP: du = (dres W2) * gelu'(u)
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->ncf; ++ct) {
+      for (auto [t0, t1] : b.col_groups(m->ncf, m->ti, f)) {
         GemmArgs proto = b.base();
         proto.epi = EPI_GELU_BWD;
         proto.aux = m->u[l];
         proto.ld_aux = f;
         std::vector<TileUse> u;
         box(u, m->gdres_act, ACC_R, rt, rt + 1);
-        box(u, m->gu[l], ACC_R, rt, rt + 1, ct, ct + 1);
-        box(u, m->gdu, ACC_W, rt, rt + 1, ct, ct + 1);
-        dx_gemm(TT_GEMM_DX, m->dres_act, d, d, P_(m, l, PROJW), f, m->du, act, f, m->ti, rt, ct,
+        box(u, m->gu[l], ACC_R, rt, rt + 1, t0, t1);
+        box(u, m->gdu, ACC_W, rt, rt + 1, t0, t1);
+        dx_gemm(TT_GEMM_DX, m->dres_act, d, d, P_(m, l, PROJW), f, m->du, act, f, m->ti, rt, t0, t1,
                 proto, std::move(u));
       }
     dw_gemm(TT_GEMM_DW, m->dres_act, m->gdres_act, d, d, m->te, m->g[l], m->gg[l], f, f, m->ti,
             P_(m, l, PROJW), pi + PROJW);
-    colsum_task(m->dres, NNT_F32, m->gdres, d, P_(m, l, PROJB), pi + PROJB);
     dw_gemm(TT_GEMM_DW, m->du, m->gdu, f, f, m->ti, m->h2[l], m->gh2[l], d, d, m->te, P_(m, l, FCW),
             pi + FCW);
     colsum_task(m->du, act, m->gdu, f, P_(m, l, FCB), pi + FCB);
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->nce; ++ct) {
+      for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
         std::vector<TileUse> u;
         box(u, m->gdu, ACC_R, rt, rt + 1);
-        box(u, m->gdtmp, ACC_W, rt, rt + 1, ct, ct + 1);
-        dx_gemm(TT_GEMM_DX, m->du, f, f, P_(m, l, FCW), d, m->dtmp, NNT_F32, d, m->te, rt, ct,
+        box(u, m->gdtmp, ACC_W, rt, rt + 1, t0, t1);
+        dx_gemm(TT_GEMM_DX, m->du, f, f, P_(m, l, FCW), d, m->dtmp, NNT_F32, d, m->te, rt, t0, t1,
                 b.base(), std::move(u));
       }
     ln_bwd(m->dtmp, m->gdtmp, m->xmid[l], m->gxmid[l], m->mu2[l], m->r2[l], m->gstat2[l],
-           P_(m, l, LN2G), P_(m, l, LN2B), pi + LN2G, pi + LN2B, true);
+           P_(m, l, LN2G), P_(m, l, LN2B), pi + LN2G, pi + LN2B, true, pi + OB);
     // attention output projection: dO (head-major), dWo, dbo
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->nce; ++ct) {
+      for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
         GemmArgs proto = b.base();
         proto.out_mode = OUT_HEADSPLIT;
         proto.hs_B = m->B; proto.hs_H = H; proto.hs_S = S; proto.hs_hd = hd; proto.hs_d = d;
         proto.ldc = d;
-        const int c0 = tile_lo(ct, m->te), c1 = tile_hi(ct, m->te, d);
+        const int c0 = tile_lo(t0, m->te), c1 = tile_hi(t1 - 1, m->te, d);
         int h0, h1;
         b.head_tiles(c0, c1, h0, h1);
         std::vector<TileUse> u;
         box(u, m->gdres_act, ACC_R, rt, rt + 1);
         box(u, m->gdOh, ACC_W, 0, 1, b.bt_of(rt), b.bt_of(rt) + 1, h0, h1, b.st_of(rt), b.st_of(rt) + 1);
-        dx_gemm(TT_GEMM_DX, m->dres_act, d, d, P_(m, l, OW), d, m->dOh, act, d, m->te, rt, ct, proto,
-                std::move(u));
+        dx_gemm(TT_GEMM_DX, m->dres_act, d, d, P_(m, l, OW), d, m->dOh, act, d, m->te, rt, t0, t1,
+                proto, std::move(u));
       }
     dw_gemm(TT_GEMM_DW, m->dres_act, m->gdres_act, d, d, m->te, m->O[l], m->gO[l], d, d, m->te,
             P_(m, l, OW), pi + OW);
-    colsum_task(m->dres, NNT_F32, m->gdres, d, P_(m, l, OB), pi + OB);
     // attention backward per (batch tile, head tile)
     const char* qkv_base = (const char*)m->qkvh[l];
     for (int bt = 0; bt < m->n_bt; ++bt)
@@ -833,7 +855,7 @@ void build_backward(nnt_model* m) {
           g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 1;
           g.B = m->dOh; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
           g.C = m->dqkv; g.ldc = 3 * d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
-          g.c_col_off = 2 * d; g.hs_hd = hd;
+          g.c_col_off = 2 * d; g.hs_hd = hd; g.hs_B = m->B; g.hs_S = S; g.hs_H = H;
           g.causal = CAUSAL_K_LOWER;
           std::vector<TileUse> u;
           box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1);
@@ -879,7 +901,7 @@ void build_backward(nnt_model* m) {
             g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 0;
             g.B = qkv_base + BH * zq * as; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
             g.C = m->dqkv; g.ldc = 3 * d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
-            g.c_col_off = 0; g.hs_hd = hd;
+            g.c_col_off = 0; g.hs_hd = hd; g.hs_B = m->B; g.hs_S = S; g.hs_H = H;
             g.causal = CAUSAL_K_UPPER;
             std::vector<TileUse> u;
             box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1, st, st + 1);
@@ -897,7 +919,7 @@ void build_backward(nnt_model* m) {
           g.A = m->P[l]; g.lda = S; g.a_zs = (int64_t)S * S; g.a_trans = 1;
           g.B = qkv_base; g.ldb = hd; g.b_zs = zq; g.b_trans = 1;
           g.C = m->dqkv; g.ldc = 3 * d; g.c_dtype = act; g.out_mode = OUT_HEADMERGE;
-          g.c_col_off = d; g.hs_hd = hd;
+          g.c_col_off = d; g.hs_hd = hd; g.hs_B = m->B; g.hs_S = S; g.hs_H = H;
           g.causal = CAUSAL_K_LOWER;
           std::vector<TileUse> u;
           box(u, m->gP[l], ACC_R, bt, bt + 1, ht, ht + 1);
@@ -912,15 +934,15 @@ void build_backward(nnt_model* m) {
             P_(m, l, QKVW), pi + QKVW);
     colsum_task(m->dqkv, act, m->gdqkv, 3 * d, P_(m, l, QKVB), pi + QKVB);
     for (int rt = 0; rt < m->n_tok; ++rt)
-      for (int ct = 0; ct < m->nce; ++ct) {
+      for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
         std::vector<TileUse> u;
         box(u, m->gdqkv, ACC_R, 0, 3, rt, rt + 1);
-        box(u, m->gdtmp, ACC_W, rt, rt + 1, ct, ct + 1);
+        box(u, m->gdtmp, ACC_W, rt, rt + 1, t0, t1);
         dx_gemm(TT_GEMM_DX, m->dqkv, 3 * d, 3 * d, P_(m, l, QKVW), d, m->dtmp, NNT_F32, d, m->te, rt,
-                ct, b.base(), std::move(u));
+                t0, t1, b.base(), std::move(u));
       }
     ln_bwd(m->dtmp, m->gdtmp, m->x[l], m->gx[l], m->mu1[l], m->r1[l], m->gstat1[l], P_(m, l, LN1G),
-           P_(m, l, LN1B), pi + LN1G, pi + LN1B, true);
+           P_(m, l, LN1B), pi + LN1G, pi + LN1B, true, l > 0 ? pi - 12 + PROJB : -1);
   }
   // embedding backward: token sort, wte scatter-add (after the LM-head dW), wpe sums
   {
@@ -1116,6 +1138,7 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
   m->ldz = round_up(m->V, 4);
   m->lddz = round_up(m->V, 8);
   m->backend = m->opts.gemm_backend;
+  m->gemm_min_cols = m->opts.gemm_min_task_cols == 0 ? 8192 : std::max(0, m->opts.gemm_min_task_cols);
   if (m->opts.n_streams <= 0) m->opts.n_streams = 2;
   m->opts.n_streams = std::min(m->opts.n_streams, 8);
 
@@ -1367,6 +1390,11 @@ nnt_status nnt_set_trace(nnt_model* m, int32_t on) {
   m->opts.trace = on ? 1 : 0;
   m->ex.set_trace(on != 0);
   m->ex.reset_trace();
+  // traced runs are serialised on one stream, so each task's time is its own
+  const int ns = on ? 1 : m->opts.n_streams;
+  m->fwd.finalize(ns);
+  m->bwd.finalize(ns);
+  m->ex.drop_graphs();
   return NNT_OK;
 }
 

@@ -70,24 +70,18 @@ nnt_status nnt_op_layernorm_bwd(const float* dy_dev, const float* x_dev, const f
   NNT_CHECK_ARG((dg_dev == nullptr) == (db_dev == nullptr), "dg and db must both be given or both NULL");
   NNT_CHECK_ARG(rows >= 0 && cols > 0 && cols <= 32768 && dtype_ok(dtype), "bad size or dtype");
   cudaStream_t st = (cudaStream_t)stream;
-  float *pgp = nullptr, *pbp = nullptr;
-  const int np = ln_bwd_nparts(rows, (int)cols);
-  if (dg_dev && rows > 0) {
-    void* s = nullptr;
-    NNT_TRY(scratch((size_t)2 * np * cols * 4, &s));
-    pgp = (float*)s;
-    pbp = pgp + (size_t)np * cols;
-  }
   NNT_TRY(launch_layernorm_bwd(dy_dev, x_dev, mean_dev, rstd_dev, g_dev, resid_dev, dx_dev,
-                               dx_act_dev, pgp, pbp, rows, (int)cols, dtype, st));
+                               dx_act_dev, rows, (int)cols, dtype, st));
   if (dg_dev) {
     if (rows == 0) {
       NNT_CUDA_TRY(cudaMemsetAsync(dg_dev, 0, cols * 4, st));
       NNT_CUDA_TRY(cudaMemsetAsync(db_dev, 0, cols * 4, st));
       return NNT_OK;
     }
-    NNT_TRY(launch_sum_parts(pgp, np, cols, cols, dg_dev, 0, st));
-    NNT_TRY(launch_sum_parts(pbp, np, cols, cols, db_dev, 0, st));
+    void* part = nullptr;
+    NNT_TRY(scratch((size_t)ln_colsum_chunks(rows) * 3 * cols * 4, &part));
+    NNT_TRY(launch_ln_bwd_colsums(dy_dev, x_dev, mean_dev, rstd_dev, nullptr, rows, (int)cols,
+                                  (float*)part, dg_dev, db_dev, nullptr, st));
   }
   return NNT_OK;
 }

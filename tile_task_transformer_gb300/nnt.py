@@ -45,7 +45,8 @@ class Options(C.Structure):
                 ("allow_host_offload", C.c_int32), ("init_seed", C.c_uint64),
                 ("init_std", C.c_float), ("init_zero_bias", C.c_int32), ("n_streams", C.c_int32),
                 ("use_cuda_graph", C.c_int32), ("timeout_ms", C.c_uint32),
-                ("gemm_backend", C.c_int32), ("trace", C.c_int32)]
+                ("gemm_backend", C.c_int32), ("trace", C.c_int32),
+                ("gemm_min_task_cols", C.c_int32)]
 
 
 class AdamW(C.Structure):
@@ -160,14 +161,14 @@ class Model:
     def __init__(self, n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype=BF16,
                  ln_eps=1e-5, tiles=None, seed=0, init_std=0.0, zero_bias=False, stream=None,
                  n_streams=2, use_cuda_graph=False, timeout_ms=0, gemm_backend=0, trace=False,
-                 allow_host_offload=False, hbm_budget_bytes=0):
+                 allow_host_offload=False, hbm_budget_bytes=0, gemm_min_task_cols=0):
         self.cfg = Config(n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype, ln_eps)
         t = tiles or {}
         self.tiles = Tiles(t.get("batch_tile", 0), t.get("seq_tile", 0), t.get("embd_tile", 0),
                            t.get("inner_tile", 0), t.get("head_tile", 0), t.get("vocab_tile", 0))
         self.opts = Options(_stream(stream), hbm_budget_bytes, int(allow_host_offload), seed,
                             init_std, int(zero_bias), n_streams, int(use_cuda_graph), timeout_ms,
-                            gemm_backend, int(trace))
+                            gemm_backend, int(trace), gemm_min_task_cols)
         h = C.c_void_p()
         check(lib().nnt_create_model(C.byref(self.cfg), C.byref(self.tiles), C.byref(self.opts),
                                      C.byref(h)))
