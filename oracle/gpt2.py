@@ -32,6 +32,12 @@ Readings where the pages are silent (each also listed in the design notes):
 
 Arithmetic runs in ``dtype`` (float64 by default). Weight matrices are stored
 ``[out, in]``; a linear layer is ``y = x W^T + b``.
+
+Precision model (optional): ``forward(..., gemm_operands="bf16")`` rounds both
+operands of every matrix product to bfloat16 (round to nearest, ties to even)
+before multiplying in ``dtype`` -- the "bf16 in, fp32 accumulate" precision of
+the tensor-core path -- so that the effect of that rounding on the loss can be
+told apart from arithmetic errors.
 """
 from __future__ import annotations
 
@@ -85,6 +91,19 @@ def param_order(cfg: GPT2Config):
 # --------------------------------------------------------------------------
 # single operations
 # --------------------------------------------------------------------------
+
+def round_bf16(a):
+    """Round to the nearest bfloat16 (ties to even), returned as float32.
+
+    bfloat16 keeps the top 16 bits of an IEEE float32: add 0x7FFF plus the
+    lowest kept bit, then clear the low 16 bits. NaN stays NaN.
+    """
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    out = r.astype(np.uint32).view(np.float32)
+    return np.where(np.isnan(f), f, out)
+
 
 def embedding_forward(ids, wte, wpe):
     """x[b, s, :] = wte[ids[b, s], :] + wpe[s, :] (one add, in the arrays' dtype)."""
@@ -262,8 +281,14 @@ def _cast(params, dtype):
     return {k: np.asarray(v, dtype=dtype) for k, v in params.items()}
 
 
-def forward(cfg: GPT2Config, params, windows, dtype=np.float64, keep=True):
-    """Forward pass; returns ``(loss, cache)``. ``windows`` is ``[B, S+1]``."""
+def forward(cfg: GPT2Config, params, windows, dtype=np.float64, keep=True, gemm_operands=None):
+    """Forward pass; returns ``(loss, cache)``. ``windows`` is ``[B, S+1]``.
+
+    ``gemm_operands="bf16"`` applies the bfloat16 precision model (module doc)
+    to every matrix product; the cache is then meant for the loss only.
+    """
+    if gemm_operands == "bf16":
+        return _forward_bf16_operands(cfg, params, windows, dtype)
     p = _cast(params, dtype)
     ids = windows[:, :cfg.seq].astype(np.int64)
     tgt = windows[:, 1:cfg.seq + 1].astype(np.int64)
@@ -293,6 +318,101 @@ def forward(cfg: GPT2Config, params, windows, dtype=np.float64, keep=True):
     cache["z"] = z
     cache["dz"] = dz
     return loss, cache
+
+
+def _forward_bf16_operands(cfg: GPT2Config, params, windows, dtype, r=None):
+    """The forward of :func:`forward` with both operands of each matrix product
+    (activations and weights, including Q, K, V and the probabilities) rounded
+    by ``r`` (bfloat16 by default) first; everything else as in
+    :func:`forward`. The cache feeds :func:`backward_bf16_operands`."""
+    p = _cast(params, dtype)
+    if r is None:
+        r = lambda a: round_bf16(a).astype(dtype)  # noqa: E731
+    ids = windows[:, :cfg.seq].astype(np.int64)
+    tgt = windows[:, 1:cfg.seq + 1].astype(np.int64)
+    B, S, d, H = cfg.batch, cfg.seq, cfg.d_model, cfg.n_head
+    c = {"ids": ids, "layers": []}
+    x = embedding_forward(ids, p["wte"], p["wpe"])
+    for l in range(cfg.n_layer):
+        q = f"h{l}."
+        L = {"x_in": x}
+        h1, L["mu1"], L["r1"] = layernorm_forward(x, p[q + "ln1.g"], p[q + "ln1.b"], cfg.ln_eps)
+        L["h1"] = r(h1)
+        qkv = linear_forward(L["h1"], r(p[q + "qkv.w"]), p[q + "qkv.b"])
+        L["q"] = split_heads(r(qkv[..., :d]), H)
+        L["k"] = split_heads(r(qkv[..., d:2 * d]), H)
+        L["v"] = split_heads(r(qkv[..., 2 * d:]), H)
+        P = causal_softmax_forward((L["q"] @ L["k"].transpose(0, 1, 3, 2)) * (1.0 / math.sqrt(d // H)))
+        L["P"] = r(P)
+        L["o"] = r(merge_heads(L["P"] @ L["v"]))
+        x = x + linear_forward(L["o"], r(p[q + "o.w"]), p[q + "o.b"])
+        L["x_mid"] = x
+        h2, L["mu2"], L["r2"] = layernorm_forward(x, p[q + "ln2.g"], p[q + "ln2.b"], cfg.ln_eps)
+        L["h2"] = r(h2)
+        L["u"] = linear_forward(L["h2"], r(p[q + "fc.w"]), p[q + "fc.b"])
+        L["g"] = r(gelu_forward(L["u"]))
+        x = x + linear_forward(L["g"], r(p[q + "proj.w"]), p[q + "proj.b"])
+        c["layers"].append(L)
+    c["x_L"] = x
+    y, c["muf"], c["rf"] = layernorm_forward(x, p["ln_f.g"], p["ln_f.b"], cfg.ln_eps)
+    c["y"] = r(y)
+    z = linear_forward(c["y"].reshape(B * S, d), r(p["wte"]))
+    loss, dz = cross_entropy_forward_backward(z, tgt.reshape(-1))
+    c["z"] = z
+    c["dz"] = dz
+    return loss, c
+
+
+def backward_bf16_operands(cfg: GPT2Config, params, cache, dtype=np.float64, r=None):
+    """Gradients under the bfloat16 precision model: the backward of
+    :func:`backward`, with every matrix-product operand rounded by ``r``
+    (bfloat16 by default), and the gradients that the tensor-core path keeps
+    only as matrix-product operands (the logits, GELU-input and attention-score
+    gradients, the head outputs' and the fused projection's gradients) rounded
+    where they are formed. Needs the cache of ``forward(..., gemm_operands="bf16")``."""
+    p = _cast(params, dtype)
+    if r is None:
+        r = lambda a: round_bf16(a).astype(dtype)  # noqa: E731
+    B, S, d, H = cfg.batch, cfg.seq, cfg.d_model, cfg.n_head
+    scale = 1.0 / math.sqrt(d // H)
+    grads = {}
+    dz = r(cache["dz"])
+    dwte = dz.T @ cache["y"].reshape(B * S, d)
+    dy = (dz @ r(p["wte"])).reshape(B, S, d)
+    dx, grads["ln_f.g"], grads["ln_f.b"] = layernorm_backward(
+        dy, cache["x_L"], cache["muf"], cache["rf"], p["ln_f.g"])
+    for l in reversed(range(cfg.n_layer)):
+        q = f"h{l}."
+        c = cache["layers"][l]
+        dxa = r(dx)
+        grads[q + "proj.w"] = dxa.reshape(B * S, d).T @ c["g"].reshape(B * S, -1)
+        grads[q + "proj.b"] = dx.sum(axis=(0, 1))
+        du = r(gelu_backward(dxa @ r(p[q + "proj.w"]), c["u"]))
+        grads[q + "fc.w"] = du.reshape(B * S, -1).T @ c["h2"].reshape(B * S, d)
+        grads[q + "fc.b"] = du.sum(axis=(0, 1))
+        dh2 = du @ r(p[q + "fc.w"])
+        dln, grads[q + "ln2.g"], grads[q + "ln2.b"] = layernorm_backward(
+            dh2, c["x_mid"], c["mu2"], c["r2"], p[q + "ln2.g"])
+        dx = dx + dln
+        dxa = r(dx)
+        grads[q + "o.w"] = dxa.reshape(B * S, d).T @ c["o"].reshape(B * S, d)
+        grads[q + "o.b"] = dx.sum(axis=(0, 1))
+        dO = split_heads(r(dxa @ r(p[q + "o.w"])), H)
+        dv = r(c["P"].transpose(0, 1, 3, 2) @ dO)
+        dP = dO @ c["v"].transpose(0, 1, 3, 2)
+        dS = r(causal_softmax_backward(dP, c["P"]) * scale)
+        dq = r(dS @ c["k"])
+        dk = r(dS.transpose(0, 1, 3, 2) @ c["q"])
+        dqkv = np.concatenate([merge_heads(dq), merge_heads(dk), merge_heads(dv)], axis=-1)
+        grads[q + "qkv.w"] = dqkv.reshape(B * S, -1).T @ c["h1"].reshape(B * S, d)
+        grads[q + "qkv.b"] = dqkv.sum(axis=(0, 1))
+        dh1 = dqkv @ r(p[q + "qkv.w"])
+        dln, grads[q + "ln1.g"], grads[q + "ln1.b"] = layernorm_backward(
+            dh1, c["x_in"], c["mu1"], c["r1"], p[q + "ln1.g"])
+        dx = dx + dln
+    dwpe = np.zeros_like(p["wpe"])
+    grads["wte"], grads["wpe"] = embedding_backward(dx, cache["ids"], dwte, dwpe)
+    return grads
 
 
 def backward(cfg: GPT2Config, params, cache, dtype=np.float64):

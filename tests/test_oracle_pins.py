@@ -360,3 +360,56 @@ def test_step_flops_counts_by_hand():
     # dense per token: 2*(2*6 + 2*2 + 2*2*4) = 64 ; lm head 2*2*3 = 12 ; T = 2
     # attention: 2 products * 2*hd*S(S+1)/2 = 2*2*2*3 = 24
     assert O.step_flops(cfg) == 3.0 * (2 * (64 + 12) + 24)
+
+
+def test_round_bf16_exact_cases_and_library_agreement():
+    one = 1.0
+    cases = {
+        one: one,
+        one + 2.0 ** -8: one,                          # tie, even neighbour is 1
+        one + 2.0 ** -7 + 2.0 ** -8: one + 2.0 ** -6,  # tie, rounds up to the even neighbour
+        one + 2.0 ** -9: one,                           # below half an ulp
+        one + 2.0 ** -8 + 2.0 ** -12: one + 2.0 ** -7,  # above half an ulp
+        -3.0: -3.0,
+        0.0: 0.0,
+    }
+    for a, want in cases.items():
+        assert O.round_bf16(np.array([a]))[0] == np.float32(want), a
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(15).standard_normal(100000).astype(np.float32) * 10.0 ** \
+        np.random.default_rng(16).integers(-20, 20, 100000)
+    lib = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(O.round_bf16(x), lib)
+
+
+def test_bf16_operand_model_reduces_to_forward_without_rounding_when_exact():
+    """With all GEMM operands already bf16-representable the precision model
+    changes nothing but the rounding of activations between products; on a
+    tiny model the two forwards agree to the bf16 scale."""
+    cfg = O.GPT2Config(n_layer=1, d_model=8, n_head=2, d_ff=16, vocab=11, seq=5, batch=2)
+    p = {k: O.round_bf16(v) for k, v in _rand_params(cfg, 40).items()}
+    win = _windows(cfg, 41)
+    l_ref, _ = O.forward(cfg, p, win)
+    l_bf, _ = O.forward(cfg, p, win, gemm_operands="bf16")
+    assert abs(l_ref - l_bf) < 2e-2 and l_ref != l_bf
+
+
+def test_bf16_precision_model_reduces_to_exact_step_with_identity_rounding():
+    """With the rounding replaced by the identity, the precision-model forward
+    and backward are term for term the plain ones."""
+    cfg = O.GPT2Config(n_layer=2, d_model=8, n_head=2, d_ff=16, vocab=11, seq=5, batch=2)
+    p = _rand_params(cfg, 42)
+    win = _windows(cfg, 43)
+    ident = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    l0, c0 = O.forward(cfg, p, win)
+    g0 = O.backward(cfg, p, c0)
+    l1, c1 = O._forward_bf16_operands(cfg, p, win, np.float64, r=ident)
+    g1 = O.backward_bf16_operands(cfg, p, c1, np.float64, r=ident)
+    assert abs(l0 - l1) < 1e-13
+    for k in g0:
+        np.testing.assert_allclose(g1[k], g0[k], rtol=1e-10, atol=1e-14, err_msg=k)
+    # and with bfloat16 rounding the gradients stay close to the exact ones
+    lb, cb = O.forward(cfg, p, win, gemm_operands="bf16")
+    gb = O.backward_bf16_operands(cfg, p, cb)
+    for k in g0:
+        assert np.abs(gb[k] - g0[k]).max() <= 3e-2 * np.abs(g0[k]).max() + 1e-12, k

@@ -1336,9 +1336,18 @@ nnt_status nnt_get_logits(nnt_model* m, float* host_buf) {
     set_thread_error("NULL model or buffer");
     return fail(m, NNT_ERR_INVALID_ARG);
   }
-  if (cudaMemcpy2DAsync(host_buf, (size_t)m->V * 4, m->z, (size_t)m->ldz * 4, (size_t)m->V * 4, m->T,
-                        cudaMemcpyDeviceToHost, m->ex.main_) != cudaSuccess)
-    return fail(m, NNT_ERR_CUDA);
+  // storage rows are tile-major; copy each run of seq_tile positions of one
+  // sequence to its (b, s) place
+  for (int bt = 0; bt < m->n_bt; ++bt)
+    for (int st = 0; st < m->n_st; ++st)
+      for (int bl = 0; bl < m->tb; ++bl) {
+        const int b = bt * m->tb + bl, s0 = st * m->ts;
+        const int64_t src_row = m->tm.row(b, s0);
+        if (cudaMemcpy2DAsync(host_buf + ((int64_t)b * m->S + s0) * m->V, (size_t)m->V * 4,
+                              m->z + src_row * m->ldz, (size_t)m->ldz * 4, (size_t)m->V * 4, m->ts,
+                              cudaMemcpyDeviceToHost, m->ex.main_) != cudaSuccess)
+          return fail(m, NNT_ERR_CUDA);
+      }
   nnt_status s = sync_model(m);
   return s == NNT_OK ? s : fail(m, s);
 }

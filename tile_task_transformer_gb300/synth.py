@@ -58,16 +58,38 @@ def uniform01(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     return ((b >> np.uint64(11)).astype(np.float64) + 0.5) * (2.0 ** -53)
 
 
-def normal_f32(seed: int, stream: int, count: int, std: float) -> np.ndarray:
-    """``count`` N(0, std^2) values rounded to fp32 (Box-Muller, see module doc)."""
-    npairs = (count + 1) // 2
-    u = uniform01(seed, stream, 0, 2 * npairs).reshape(npairs, 2)
+def _normal_pairs(seed, stream, p0, n, count, std, out):
+    u = uniform01(seed, stream, 2 * p0, 2 * n).reshape(n, 2)
     r = np.sqrt(-2.0 * np.log(u[:, 0]))
     t = 2.0 * np.pi * u[:, 1]
-    z = np.empty((npairs, 2), dtype=np.float64)
+    z = np.empty((n, 2), dtype=np.float64)
     z[:, 0] = r * np.cos(t)
     z[:, 1] = r * np.sin(t)
-    return (z.reshape(-1)[:count] * std).astype(np.float32)
+    z = z.reshape(-1)
+    e = min(2 * (p0 + n), count)
+    out[2 * p0:e] = (z[: e - 2 * p0] * std).astype(np.float32)
+
+
+def normal_f32(seed: int, stream: int, count: int, std: float) -> np.ndarray:
+    """``count`` N(0, std^2) values rounded to fp32 (Box-Muller, see module doc).
+
+    Large requests are generated in chunks on a thread pool (numpy releases the
+    interpreter lock in its element-wise loops); the values do not depend on it.
+    """
+    out = np.empty(count, dtype=np.float32)
+    chunk = 1 << 22  # pairs per chunk, to bound temporary memory
+    npairs = (count + 1) // 2
+    starts = list(range(0, npairs, chunk))
+    if len(starts) <= 1:
+        for p0 in starts:
+            _normal_pairs(seed, stream, p0, min(chunk, npairs - p0), count, std, out)
+        return out
+    import concurrent.futures as cf
+    import os
+    with cf.ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 4)) as ex:
+        list(ex.map(lambda p0: _normal_pairs(seed, stream, p0, min(chunk, npairs - p0), count, std, out),
+                    starts))
+    return out
 
 
 def token_windows(seed: int, batch: int, seq: int, vocab: int) -> np.ndarray:
