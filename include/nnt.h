@@ -165,7 +165,7 @@ nnt_status nnt_set_param(nnt_model* m, int32_t i, const float* host_buf);
 nnt_status nnt_get_grad(nnt_model* m, int32_t i, float* host_buf);
 nnt_status nnt_get_adam_state(nnt_model* m, int32_t i, int32_t which, float* host_buf);
 
-/* Copy the logits of the last forward (fp32 [batch*n_ctx, vocab]) to host. */
+/* Copy the logits of the last forward to host: fp32 [batch][n_ctx][vocab]. */
 nnt_status nnt_get_logits(nnt_model* m, float* host_buf);
 
 nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out);
@@ -262,6 +262,26 @@ nnt_status nnt_op_embedding_fwd(const uint16_t* ids_dev, int64_t ids_stride, con
 nnt_status nnt_op_embedding_bwd(const uint16_t* ids_dev, int64_t ids_stride, const float* dx_dev,
                                 float* dwte_dev, float* dwpe_dev, int64_t batch, int64_t seq,
                                 int64_t d, int64_t vocab, void* stream);
+
+/* Same as nnt_op_embedding_bwd (same results, bit for bit), but it allocates
+ * nothing. It is meant for callers that cannot allocate device memory while
+ * they run: code enqueuing work inside a CUDA stream capture (cudaMalloc is not
+ * capturable), hosts that own all device memory through their own allocator or
+ * a fixed budget, and loops that cannot afford an allocation's implicit
+ * synchronisation. The NNTile pages have no counterpart of this call; it only
+ * changes where the scratch lives.
+ * Scratch: one fixed array of 16384 uint32 sort keys (64 KiB) compiled into
+ * the library, present on every device that loads it until the process exits;
+ * so batch*seq must be <= 16384 (INVALID_ARG otherwise, before any work).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call uses the same array: calls whose GPU
+ * work overlaps (different streams, no ordering between them) race and give
+ * wrong results. Calls never free or allocate anything. */
+nnt_status nnt_op_embedding_bwd_noalloc(const uint16_t* ids_dev, int64_t ids_stride,
+                                        const float* dx_dev, float* dwte_dev, float* dwpe_dev,
+                                        int64_t batch, int64_t seq, int64_t d, int64_t vocab,
+                                        void* stream);
 
 /* Tile GEMM C = alpha * op(A) op(B) (+ beta * C): op(A) is [M, K], op(B) is
  * [K, N]. a_trans = 0: A stored [M][lda] (K contiguous); 1: A stored [K][lda]

@@ -97,6 +97,7 @@ _SIGS = {
     "nnt_op_adamw": (C.c_int, [_P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _F, _F, _P]),
     "nnt_op_embedding_fwd": (C.c_int, [_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "nnt_op_embedding_bwd": (C.c_int, [_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "nnt_op_embedding_bwd_noalloc": (C.c_int, [_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "nnt_op_gemm": (C.c_int, [_P, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32, _I64, _I64, _I64, _F,
                               _F, _I32, _I32, _P]),
     "nnt_op_read_error": (C.c_int, [C.POINTER(C.c_uint32), _P]),
@@ -316,6 +317,12 @@ def op_embedding_fwd(ids, ids_stride, wte, wpe, x, batch, seq, d, vocab, stream=
 def op_embedding_bwd(ids, ids_stride, dx, dwte, dwpe, batch, seq, d, vocab, stream=None):
     check(lib().nnt_op_embedding_bwd(_ptr(ids), ids_stride, _ptr(dx), _ptr(dwte), _ptr(dwpe), batch,
                                      seq, d, vocab, _stream(stream)))
+
+
+def op_embedding_bwd_noalloc(ids, ids_stride, dx, dwte, dwpe, batch, seq, d, vocab, stream=None):
+    """nnt_op_embedding_bwd without any device allocation (fixed 16384-token scratch)."""
+    check(lib().nnt_op_embedding_bwd_noalloc(_ptr(ids), ids_stride, _ptr(dx), _ptr(dwte), _ptr(dwpe),
+                                             batch, seq, d, vocab, _stream(stream)))
 
 
 def op_gemm(a, lda, a_trans, b, ldb, b_trans, c, ldc, c_dtype, M, N, K, alpha=1.0, beta=0.0,
