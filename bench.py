@@ -53,6 +53,24 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def gemm_traffic(workload):
+    """DRAM bytes (read + write) per GEMM launch from the committed ncu summary,
+    or None when that summary was taken on another workload or on a different
+    version of the kernel source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", f"gemm_tc_traffic_{workload.replace('-', '_')}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    csrc = os.path.join(ROOT, "tile_task_transformer_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "gemm.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return d["bytes_per_launch"] if h.hexdigest() == d.get("source_sha256") else None
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
 
@@ -67,7 +85,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
@@ -249,8 +267,9 @@ def run_gpu(args):
         achieved = a["flops"] / (a["ms"] / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "kernel": dom,
-                "peak_kind": f"{pk_kind} sustained bf16"}
+                "frac": achieved / peak, "traffic": gemm_traffic(name), "kernel": dom,
+                "peak_kind": f"{pk_kind} sustained bf16",
+                "launches_per_step": a["launches"] // 2}
     else:
         achieved = a["bytes"] / (a["ms"] / 1e3) / 1e9
         peak = pk["hbm_gbs"]
@@ -311,6 +330,149 @@ def run_gpu(args):
     return 0
 
 
+# --------------------------------------------------------------------------
+# tile-kernel sweep: the step's tile kernels alone on synthetic tiles
+# --------------------------------------------------------------------------
+
+SWEEP_ROWS = (256, 1024, 4096, 8192)
+SWEEP_COLS = (768, 3072, 16384, 65536)
+SWEEP_GEMM = (1024, 2048, 4096, 8192)
+
+
+def run_sweep(args):
+    """One JSON line per (kernel, shape): time per call (CUDA events, median of
+    `--steps` calls after `--warmup`), algorithmic bytes or flops, and the
+    fraction of the measured HBM copy / dense bf16 peak. Inputs N(0, 1), logits
+    N(0, 3). Memory-bound inputs are at least 256 MiB where the shape allows,
+    else the buffers are cycled to exceed L2."""
+    import numpy as np
+    import torch
+
+    from tile_task_transformer_gb300 import nnt
+
+    pk, pk_kind = peaks()
+    torch.manual_seed(4)
+    dev = "cuda"
+    kernels = args.sweep_kernel.split(",") if args.sweep_kernel else [
+        "layernorm_fwd", "layernorm_bwd", "softmax_fwd", "softmax_bwd", "gelu_fwd", "gelu_bwd",
+        "cross_entropy", "adamw", "gemm"]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timeit(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def emit(kernel, shape, dtype, ms, nbytes=None, flops=None):
+        line = {"sweep": kernel, "shape": shape, "dtype": dtype, "ms": ms}
+        if flops:
+            tf = flops / (ms / 1e3) / 1e12
+            line.update(tflops=tf, frac=tf / pk["bf16_tflops"], peak=f"{pk_kind} burst bf16")
+        else:
+            gbs = nbytes / (ms / 1e3) / 1e9
+            line.update(gbs=gbs, frac=gbs / pk["hbm_gbs"], peak=f"{pk_kind} HBM copy")
+        print(json.dumps(line), flush=True)
+
+    rows_list = [int(x) for x in args.sweep_rows.split(",")] if args.sweep_rows else SWEEP_ROWS
+    cols_list = [int(x) for x in args.sweep_cols.split(",")] if args.sweep_cols else SWEEP_COLS
+    for dt_name, dt, tdt, es in (("f32", nnt.F32, torch.float32, 4), ("bf16", nnt.BF16, torch.bfloat16, 2)):
+        if args.sweep_dtype and dt_name != args.sweep_dtype:
+            continue
+        for R in rows_list:
+            for Cc in cols_list:
+                if "layernorm_fwd" in kernels or "layernorm_bwd" in kernels:
+                    if Cc <= 32768:
+                        x = torch.randn(R, Cc, device=dev)
+                        g = torch.randn(Cc, device=dev)
+                        b = torch.randn(Cc, device=dev)
+                        y = torch.empty(R, Cc, device=dev, dtype=tdt)
+                        mu = torch.empty(R, device=dev)
+                        rs = torch.empty(R, device=dev)
+                        if "layernorm_fwd" in kernels:
+                            ms = timeit(lambda: nnt.op_layernorm_fwd(x, g, b, y, mu, rs, R, Cc, 1e-5, dt))
+                            emit("layernorm_fwd", [R, Cc], dt_name, ms, nbytes=R * Cc * (4 + es) + 8 * R)
+                        if "layernorm_bwd" in kernels:
+                            dy = torch.randn(R, Cc, device=dev)
+                            dx = torch.empty(R, Cc, device=dev)
+                            dxa = torch.empty(R, Cc, device=dev, dtype=tdt)
+                            dg = torch.empty(Cc, device=dev)
+                            db = torch.empty(Cc, device=dev)
+                            ms = timeit(lambda: nnt.op_layernorm_bwd(dy, x, mu, rs, g, None, dx, dxa, dg, db,
+                                                                     R, Cc, dt))
+                            # dx pass (read dy, x; write dx, copy) + gain/shift column pass (read dy, x)
+                            emit("layernorm_bwd", [R, Cc], dt_name, ms, nbytes=R * Cc * (8 + 4 + es + 8))
+                        del x, y
+                if ("gelu_fwd" in kernels or "gelu_bwd" in kernels):
+                    n = R * Cc
+                    u = torch.randn(n, device=dev)
+                    gg = torch.empty(n, device=dev, dtype=tdt)
+                    if "gelu_fwd" in kernels:
+                        ms = timeit(lambda: nnt.op_gelu_fwd(u, gg, n, dt))
+                        emit("gelu_fwd", [R, Cc], dt_name, ms, nbytes=n * (4 + es))
+                    if "gelu_bwd" in kernels:
+                        du = torch.empty(n, device=dev, dtype=tdt)
+                        ms = timeit(lambda: nnt.op_gelu_bwd(gg, u, du, n, dt))
+                        emit("gelu_bwd", [R, Cc], dt_name, ms, nbytes=n * (es + 4 + es))
+                        del du
+                    del u, gg
+                if "cross_entropy" in kernels and Cc >= 3072:
+                    ldz = (Cc + 3) // 4 * 4
+                    lddz = (Cc + 7) // 8 * 8
+                    z = torch.randn(R, ldz, device=dev) * 3
+                    tg = torch.randint(0, Cc, (R,), device=dev, dtype=torch.int32).to(torch.int16)  # uint16 bits
+                    dz = torch.empty(R, lddz, device=dev, dtype=tdt)
+                    rl = torch.empty(R, device=dev)
+                    loss = torch.empty(1, device=dev)
+                    ms = timeit(lambda: nnt.op_cross_entropy(z, R, Cc, ldz, tg, 1, dz, lddz, rl, loss, dt))
+                    emit("cross_entropy", [R, Cc], dt_name, ms, nbytes=R * Cc * (4 + es) + 2 * R)
+                    del z, dz
+        # causal softmax on [nmat, S, S] score tiles
+        for S in (1024, 2048, 4096):
+            if not ("softmax_fwd" in kernels or "softmax_bwd" in kernels):
+                break
+            nmat = max(1, (512 << 20) // (S * S * 4))
+            s_ = torch.randn(nmat, S, S, device=dev)
+            p_ = torch.empty(nmat, S, S, device=dev, dtype=tdt)
+            causal = nmat * S * (S + 1) / 2
+            if "softmax_fwd" in kernels:
+                ms = timeit(lambda: nnt.op_softmax_causal_fwd(s_, p_, nmat, S, dt))
+                emit("softmax_fwd", [nmat, S, S], dt_name, ms, nbytes=causal * (4 + es))
+            if "softmax_bwd" in kernels:
+                nnt.op_softmax_causal_fwd(s_, p_, nmat, S, dt)
+                ds = torch.empty_like(p_)
+                ms = timeit(lambda: nnt.op_softmax_causal_bwd(p_, s_, ds, nmat, S, 0.125, dt))
+                emit("softmax_bwd", [nmat, S, S], dt_name, ms, nbytes=causal * (es + 4 + es))
+                del ds
+            del s_, p_
+    if "adamw" in kernels:
+        for n in (1 << 24, 1 << 26, 1 << 28):
+            w, g_, m_, v_ = (torch.randn(n, device=dev) for _ in range(4))
+            v_.abs_()
+            wb = torch.empty(n, device=dev, dtype=torch.bfloat16)
+            ms = timeit(lambda: nnt.op_adamw(w, g_, m_, v_, wb, n, 3e-4, 0.9, 0.999, 1e-8, 0.1, 0.1, 0.001))
+            emit("adamw", [n], "f32", ms, nbytes=30 * n)
+            del w, g_, m_, v_, wb
+    if "gemm" in kernels:
+        sizes = [int(x) for x in args.sweep_gemm.split(",")] if args.sweep_gemm else SWEEP_GEMM
+        for N in sizes:
+            A = torch.randn(N, N, device=dev).to(torch.bfloat16)
+            B = torch.randn(N, N, device=dev).to(torch.bfloat16)
+            Cm = torch.empty(N, N, device=dev, dtype=torch.bfloat16)
+            ms = timeit(lambda: nnt.op_gemm(A, N, 0, B, N, 0, Cm, N, nnt.BF16, N, N, N, dtype=nnt.BF16))
+            emit("gemm", [N, N, N], "bf16", ms, flops=2.0 * N ** 3)
+            del A, B, Cm
+    print(json.dumps({"sweep_device_error": nnt.read_device_error()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -321,11 +483,19 @@ def main():
     ap.add_argument("--streams", type=int, default=2)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="tile-kernel sweep instead of the step")
+    ap.add_argument("--sweep-kernel", default="", help="comma list (default: all)")
+    ap.add_argument("--sweep-dtype", default="", choices=["", "f32", "bf16"])
+    ap.add_argument("--sweep-rows", default="")
+    ap.add_argument("--sweep-cols", default="")
+    ap.add_argument("--sweep-gemm", default="", help="comma list of M=N=K")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_gpu(args)
 
 
