@@ -37,6 +37,9 @@ WORKLOADS = {
     "tiny": (2, 64, 4, 256, 256, 32, 2, "fp32", {"seq_tile": 16, "embd_tile": 32}),
     "wide-4": (4, 8192, 64, 32768, 50257, 1024, 8, "bf16",
                {"seq_tile": 1024, "embd_tile": 2048, "inner_tile": 4096, "head_tile": 16}),
+    # 26.6B parameters: AdamW moments partly in pinned host memory, fused backward + AdamW
+    "wide-8": (8, 16384, 128, 65536, 50257, 1024, 4, "bf16",
+               {"seq_tile": 1024, "embd_tile": 2048, "inner_tile": 4096, "head_tile": 16}),
 }
 
 GEMM_TYPES = {"gemm_qkv", "gemm_qk", "gemm_pv", "gemm_attn_out", "gemm_fc_gelu", "gemm_mlp_proj",
@@ -183,9 +186,13 @@ def run_gpu(args):
     L, d, H, f, V, S, B, dtype, tiles = WORKLOADS[name]
     dt = nnt.BF16 if dtype == "bf16" else nnt.F32
     stream = torch.cuda.Stream()
+    t_create = time.perf_counter()
     model = nnt.Model(L, d, H, f, V, S, B, dtype=dt, tiles=tiles, seed=1 + rank, stream=stream,
-                      n_streams=args.streams, use_cuda_graph=not args.no_graph)
+                      n_streams=args.streams, use_cuda_graph=not args.no_graph,
+                      allow_host_offload=True)
+    t_create = time.perf_counter() - t_create
     st = model.stats()
+    fused = args.fused or st["offload_active"] == 1
     T = B * S
     win_host = synth.token_windows(1 + rank, B, S, V)
     tok_dev = torch.as_tensor(win_host.view(np.int16)).to("cuda")
@@ -194,8 +201,11 @@ def run_gpu(args):
 
     def step(tokens, want_loss):
         loss = model.forward(tokens, want_loss=want_loss)
-        model.backward()
-        model.adamw_step(**hp)
+        if fused:
+            model.backward_adamw(**hp)
+        else:
+            model.backward()
+            model.adamw_step(**hp)
         return loss
 
     def barrier():
@@ -304,7 +314,11 @@ def run_gpu(args):
                    "global_batch": B * world, "seq_len": S,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "working set >> L2 (activations and weights are several GB per step)",
-                   "cuda_graph": not args.no_graph, "streams": args.streams},
+                   "cuda_graph": not args.no_graph, "streams": args.streams,
+                   "fused_backward_adamw": fused,
+                   "host_offload": {"active": bool(st["offload_active"]),
+                                    "pinned_gib": st["host_pinned_bytes"] / 2 ** 30,
+                                    "h2d_gib_per_step": None, "d2h_gib_per_step": None}},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(win_host.nbytes), "d2h_bytes_per_step": 4},
@@ -315,7 +329,13 @@ def run_gpu(args):
         "model_tflops": None,
         "loss": float(losses[-1]),
         "device_gib": st["device_bytes"] / 2 ** 30,
+        "create_s": t_create,
     }
+    if st["offload_active"]:
+        st2 = model.stats()
+        nsteps = max(args.warmup, 1) + 2 * args.steps + 2
+        line["config"]["host_offload"]["h2d_gib_per_step"] = st2["h2d_bytes"] / nsteps / 2 ** 30
+        line["config"]["host_offload"]["d2h_gib_per_step"] = st2["d2h_bytes"] / nsteps / 2 ** 30
     try:
         from oracle import gpt2 as O
         cfgo = O.GPT2Config(n_layer=L, d_model=d, n_head=H, d_ff=f, vocab=V, seq=S, batch=B)
@@ -482,6 +502,7 @@ def main():
     ap.add_argument("--workload", default="gpt2-small", choices=sorted(WORKLOADS))
     ap.add_argument("--streams", type=int, default=2)
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--fused", action="store_true", help="backward with AdamW fused in")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="tile-kernel sweep instead of the step")
     ap.add_argument("--sweep-kernel", default="", help="comma list (default: all)")

@@ -104,7 +104,7 @@ typedef struct {
   double last_forward_ms, last_backward_ms, last_adamw_ms; /* host wall time of the last calls */
   uint64_t device_bytes;        /* bytes allocated on the device by this model */
   uint64_t host_pinned_bytes;   /* bytes in pinned host RAM (offloaded tiles) */
-  uint64_t h2d_bytes, d2h_bytes;/* cumulative tile traffic of the offload manager */
+  uint64_t h2d_bytes, d2h_bytes;/* cumulative host<->device moment traffic of offloaded chunks */
   int64_t n_tasks_forward, n_tasks_backward, n_tasks_adamw;
   int64_t n_tiles;
   int64_t n_params;             /* scalar parameter count */
@@ -135,13 +135,26 @@ nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_d
                        float* loss_out);
 
 /* Backward pass of the last forward: fp32 gradients of every parameter
- * (overwritten, not accumulated). STATE error if no forward preceded it. */
+ * (overwritten, not accumulated). STATE error if no forward preceded it, or if
+ * the model offloads AdamW moments (use nnt_backward_adamw). */
 nnt_status nnt_backward(nnt_model* m);
 
 /* One fused AdamW update of every parameter tile from the current gradients;
  * the step counter starts at 1 and grows by one per call. STATE error if no
  * backward preceded it since the last update. */
 nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp);
+
+/* Backward pass fused with AdamW: each parameter chunk is updated as soon as
+ * its gradient is final and every task of this pass that reads its old value
+ * has been issued, so AdamW overlaps the rest of the backward (the update is
+ * the same as nnt_backward + nnt_adamw_step). Required for models whose AdamW
+ * moments are offloaded to pinned host memory (nnt_options.allow_host_offload
+ * when the state does not fit the device budget): there, gradients of the
+ * layer matrices only pass through a small ring of device slots and cannot be
+ * read back, and the AdamW kernel updates the moments of host-resident chunks
+ * in place in pinned, device-mapped host memory (over NVLink-C2C on GB300).
+ * Same STATE/INVALID_ARG rules as nnt_backward / nnt_adamw_step. */
+nnt_status nnt_backward_adamw(nnt_model* m, const nnt_adamw* hp);
 
 /* Free everything the model owns. NULL-safe; always succeeds. */
 void nnt_destroy(nnt_model* m);

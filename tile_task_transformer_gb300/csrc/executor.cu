@@ -59,6 +59,8 @@ void Program::finalize(int n_streams) {
     int s;
     if (t.copy_engine) {
       s = copy_stream;
+    } else if (t.stream_hint >= 0) {
+      s = std::min(t.stream_hint, n_streams_ - 1);
     } else {
       // continue the stream whose latest task is one of our dependencies
       s = -1;

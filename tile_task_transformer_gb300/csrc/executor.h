@@ -40,6 +40,7 @@ struct Task {
   double flops = 0, bytes = 0;
   int copy_engine = 0;  // 1: host<->device copy task, scheduled on the copy stream
   int kernels = 1;      // kernel launches the task makes
+  int stream_hint = -1; // >= 0: run on this compute stream (side work kept off the main chain)
   // schedule (finalize)
   int stream = 0;
   std::vector<int> waits;

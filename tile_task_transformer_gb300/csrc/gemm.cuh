@@ -48,6 +48,7 @@ struct GemmArgs {
   TokMap tm{1, 1, 1, 1};
   int hs_B = 1, hs_H = 1, hs_S = 1, hs_hd = 1, hs_d = 1;  // head split/merge geometry
   int64_t c_col_off = 0;                                   // OUT_HEADMERGE column offset
+  int64_t c_row0 = 0;  // OUT_PLAIN: row m is stored at (m - c_row0) * ldc (C holds rows from c_row0)
   float alpha = 1.f;
   int beta = 0;
   int epi = EPI_STORE;
@@ -71,7 +72,7 @@ __device__ __forceinline__ float gelu_grad_dev(float u) {
 
 // Element offset of output (i, m, n) in C.
 __device__ __forceinline__ int64_t out_offset(const GemmArgs& g, int i, int m, int n) {
-  if (g.out_mode == OUT_PLAIN) return g.zm.z(i) * g.c_zs + (int64_t)m * g.ldc + n;
+  if (g.out_mode == OUT_PLAIN) return g.zm.z(i) * g.c_zs + (int64_t)(m - g.c_row0) * g.ldc + n;
   if (g.out_mode == OUT_HEADSPLIT) {
     int b, s;
     g.tm.bs(m, b, s);

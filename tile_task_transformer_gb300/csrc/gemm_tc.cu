@@ -672,7 +672,7 @@ nnt_status store_maps(const GemmArgs& g, int64_t zmax, CUtensorMap* mc, CUtensor
   const int64_t es = bf ? 2 : 4;
   const char* C = static_cast<const char*>(g.C);
   if (g.out_mode == OUT_PLAIN) {
-    const char* base = C + ((int64_t)g.m0 * g.ldc + g.n0) * es;
+    const char* base = C + ((int64_t)(g.m0 - g.c_row0) * g.ldc + g.n0) * es;
     const int64_t zs = g.c_zs > 0 ? g.c_zs : (int64_t)g.M * g.ldc;
     if (al16((int64_t)(uintptr_t)base) && al16(g.ldc * es) && al16(zs * es)) {
       cuuint64_t dims[3] = {(cuuint64_t)g.nt, (cuuint64_t)g.mt, (cuuint64_t)zmax};

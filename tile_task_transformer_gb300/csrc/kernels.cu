@@ -933,6 +933,10 @@ __device__ __forceinline__ void adamw_one(float& w, float g, float& m, float& v,
 
 // hyper (optional, device): lr, beta1, beta2, eps, wd, bc1, bc2 -- overrides the
 // by-value arguments so a captured graph can be replayed with new values.
+// UNROLL float4 groups per thread per iteration: all their loads are issued
+// before any math, which keeps enough bytes in flight when m and v sit behind
+// the slower host link.
+template <int UNROLL>
 __global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
                              float* __restrict__ m, float* __restrict__ v, bf16* __restrict__ wb,
                              int64_t n, float lr, float b1, float b2, float eps, float wd,
@@ -942,18 +946,33 @@ __global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
     bc1 = hyper[5]; bc2 = hyper[6];
   }
   const int64_t n4 = n >> 2;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    float4 W = load4_stream(w + 4 * i), G = load4_stream(g + 4 * i);
-    float4 M = load4_stream(m + 4 * i), V = load4_stream(v + 4 * i);
-    adamw_one(W.x, G.x, M.x, V.x, lr, b1, b2, eps, wd, bc1, bc2);
-    adamw_one(W.y, G.y, M.y, V.y, lr, b1, b2, eps, wd, bc1, bc2);
-    adamw_one(W.z, G.z, M.z, V.z, lr, b1, b2, eps, wd, bc1, bc2);
-    adamw_one(W.w, G.w, M.w, V.w, lr, b1, b2, eps, wd, bc1, bc2);
-    store4_stream(w + 4 * i, W);
-    store4_stream(m + 4 * i, M);
-    store4_stream(v + 4 * i, V);
-    if (wb) store4(wb + 4 * i, W);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < n4; i0 += stride * UNROLL) {
+    float4 W[UNROLL], G[UNROLL], M[UNROLL], V[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n4) {
+        W[u] = load4_stream(w + 4 * i);
+        G[u] = load4_stream(g + 4 * i);
+        M[u] = load4_stream(m + 4 * i);
+        V[u] = load4_stream(v + 4 * i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n4) {
+        adamw_one(W[u].x, G[u].x, M[u].x, V[u].x, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].y, G[u].y, M[u].y, V[u].y, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].z, G[u].z, M[u].z, V[u].z, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].w, G[u].w, M[u].w, V[u].w, lr, b1, b2, eps, wd, bc1, bc2);
+        store4_stream(w + 4 * i, W[u]);
+        store4_stream(m + 4 * i, M[u]);
+        store4_stream(v + 4 * i, V[u]);
+        if (wb) store4(wb + 4 * i, W[u]);
+      }
+    }
   }
   // tail
   const int64_t t = 4 * n4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
@@ -975,15 +994,20 @@ nnt_status launch_adamw(float* w, const float* g, float* m, float* v, bf16* w_bf
                     ((uintptr_t)w_bf16) % 8 == 0,
                 "adamw: buffers must be 16-byte aligned (bf16 copy 8-byte)");
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
-  adamw_kernel<<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, lr, b1, b2, eps, wd, bc1, bc2, nullptr);
+  adamw_kernel<1><<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, lr, b1, b2, eps, wd, bc1, bc2, nullptr);
   return launch_check("adamw");
 }
 
 nnt_status launch_adamw_dev(float* w, const float* g, float* m, float* v, bf16* w_bf16, int64_t n,
-                            const float* hyper_dev, cudaStream_t st) {
+                            const float* hyper_dev, cudaStream_t st, int max_ctas) {
   if (n == 0) return NNT_OK;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
-  adamw_kernel<<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
+  if (max_ctas > 0) {
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256 * 4), max_ctas));
+    adamw_kernel<4><<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
+  } else {
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
+    adamw_kernel<1><<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
+  }
   return launch_check("adamw");
 }
 

@@ -76,8 +76,10 @@ nnt_status launch_adamw(float* w, const float* g, float* m, float* v, bf16* w_bf
 
 // same, hyper-parameters read on the device from hyper_dev[0..6] =
 // (lr, beta1, beta2, eps, weight_decay, 1-beta1^t, 1-beta2^t)
+// max_ctas > 0 caps the grid (moments in host memory: a few CTAs keep NVLink-C2C
+// busy without taking SMs from concurrent tasks)
 nnt_status launch_adamw_dev(float* w, const float* g, float* m, float* v, bf16* w_bf16, int64_t n,
-                            const float* hyper_dev, cudaStream_t st);
+                            const float* hyper_dev, cudaStream_t st, int max_ctas = 0);
 
 // ---- init / casts
 // std in double: the default 0.02 is the double 0.02, as in the host generator

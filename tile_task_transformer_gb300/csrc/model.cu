@@ -37,20 +37,21 @@ enum TaskType : int {
   TT_GEMM_FC, TT_GEMM_MLP_PROJ, TT_GEMM_LM_HEAD, TT_XENT, TT_LOSS,
   TT_GEMM_LM_DX, TT_GEMM_LM_DW, TT_LN_BWD, TT_LN_PARTS, TT_GEMM_DX, TT_GEMM_DW, TT_COLSUM,
   TT_GEMM_ATTN_BWD, TT_SOFTMAX_BWD, TT_EMB_SORT, TT_EMB_SCATTER, TT_WPE_GRAD, TT_ADAMW,
-  TT_COUNT
+  TT_ADAMW_HOST, TT_COUNT
 };
 const char* kTaskNames[TT_COUNT] = {
     "embedding_fwd", "layernorm_fwd", "gemm_qkv", "gemm_qk", "softmax_fwd", "gemm_pv",
     "gemm_attn_out", "gemm_fc_gelu", "gemm_mlp_proj", "gemm_lm_head", "cross_entropy",
     "mean_loss", "gemm_lm_dx", "gemm_lm_dw", "layernorm_bwd", "layernorm_param_grads",
     "gemm_dx", "gemm_dw", "bias_grads", "gemm_attn_bwd", "softmax_bwd", "token_sort",
-    "embedding_scatter", "wpe_grad", "adamw"};
+    "embedding_scatter", "wpe_grad", "adamw", "adamw_host_moments"};
 
 
 struct ParamInfo {
   std::string name;
   int64_t shape0, shape1;  // shape1 = 0 for vectors
   int64_t off, n;
+  int64_t goff = -1;  // gradient offset in the gradient buffer (-1: streamed through the ring)
   int kind;  // 0 weight (normal), 1 bias (normal or 0), 2 ln gain (1), 3 ln bias (0)
 };
 
@@ -58,6 +59,19 @@ struct ParamInfo {
 struct TGrid {
   int64_t base = 0;
   int g[4] = {1, 1, 1, 1};
+};
+
+// A contiguous run of rows of one parameter that AdamW updates as one task.
+struct Chunk {
+  int param = 0;
+  int64_t r0 = 0, r1 = 1;  // rows (a vector is one row)
+  int64_t e0 = 0, n = 0;   // element offset inside the parameter and count
+  int t0 = 0, t1 = 1;      // rows of the parameter's gradient tile grid it covers
+  bool ring = false;       // gradient streamed through a ring slot
+  int slot = -1;           // ring slot, or staging slot for host-resident moments
+  int64_t goff = -1;       // offset of the gradient in the gradient buffer
+  bool host = false;       // AdamW moments in pinned host memory
+  int64_t mv_off = -1;     // offset in the device or host moment pool
 };
 
 struct AdamHyperDev {
@@ -124,7 +138,21 @@ struct nnt_model {
   std::vector<TGrid> gparam, ggrad;
   int64_t next_tile = 0;
 
-  Program fwd, bwd, opt;
+  // fused backward + AdamW and host offload of AdamW moments
+  bool offload = false;                 // some moments live in pinned host memory
+  std::vector<Chunk> chunks;
+  std::vector<std::vector<int>> chunks_of;  // parameter -> its chunks, in row order
+  float *host_m = nullptr, *host_v = nullptr;          // pinned host pools (host addresses)
+  float *host_m_dev = nullptr, *host_v_dev = nullptr;  // the same pools as device addresses
+  int64_t n_host_mv = 0, n_dev_mv = 0, n_grad = 0;
+  float* ring = nullptr;                 // gradient ring slots [n_ring][ring_elems]
+  int n_ring = 0;
+  int64_t ring_elems = 0;
+  std::vector<TGrid> gpchunk;            // per parameter: one tile per chunk
+  TGrid gring;
+  uint64_t h2d_bytes = 0, d2h_bytes = 0;
+
+  Program fwd, bwd, bwdf, opt;
   Executor ex;
   cudaEvent_t done_event = nullptr;
   int state = 0;  // 0: created, 1: forward done, 2: backward done
@@ -229,6 +257,166 @@ nnt_status validate(const nnt_gpt2_config* c, const nnt_tiles* t) {
   return NNT_OK;
 }
 
+int axis_tile(const nnt_model* m, int64_t n) {
+  if (n == m->d) return m->te;
+  if (n == 3 * (int64_t)m->d) return m->te;
+  if (n == m->f) return m->ti;
+  if (n == m->V) return m->tv;
+  if (n == m->S) return m->ts;
+  return (int)n;
+}
+
+// Parameters whose gradients are streamed through the ring when offloading:
+// the four weight matrices of every layer.
+bool ring_param(const nnt_model* m, int i) { return i >= 2 && i < 2 + 12 * m->L && m->params[i].kind == 0; }
+
+// AdamW chunks: vectors whole; matrices in runs of whole out-tiles of at most
+// 2^27 elements (512 MiB of fp32), so a chunk is a contiguous row block.
+void plan_chunks(nnt_model* m) {
+  m->chunks.clear();
+  m->chunks_of.assign(m->params.size(), {});
+  for (int i = 0; i < (int)m->params.size(); ++i) {
+    const ParamInfo& p = m->params[i];
+    if (p.shape1 == 0) {
+      Chunk c;
+      c.param = i;
+      c.r0 = 0;
+      c.r1 = 1;
+      c.e0 = 0;
+      c.n = p.n;
+      c.t0 = 0;
+      c.t1 = tiles_of((int)p.shape0, axis_tile(m, p.shape0));
+      m->chunks_of[i].push_back((int)m->chunks.size());
+      m->chunks.push_back(c);
+      continue;
+    }
+    const int64_t rows = p.shape0, cols = p.shape1;
+    const int64_t tr = axis_tile(m, rows);
+    const int64_t per = tr * std::max<int64_t>(1, (1ll << 27) / (tr * cols));
+    for (int64_t r0 = 0; r0 < rows; r0 += per) {
+      Chunk c;
+      c.param = i;
+      c.r0 = r0;
+      c.r1 = std::min(rows, r0 + per);
+      c.e0 = r0 * cols;
+      c.n = (c.r1 - c.r0) * cols;
+      c.t0 = (int)(r0 / tr);
+      c.t1 = (int)ceil_div(c.r1, tr);
+      m->chunks_of[i].push_back((int)m->chunks.size());
+      m->chunks.push_back(c);
+    }
+  }
+}
+
+// Gradients, AdamW moments and (when offloading) the ring and staging slots.
+// Everything fits in `budget` device bytes: flat gradient and moment buffers
+// with the master layout. Otherwise, with host offload allowed: gradients of the
+// layer matrices go through a ring of slots (the fused backward updates each
+// chunk as soon as its gradient is final), the other gradients keep a device
+// buffer, and the moments of as many chunks as fit stay on the device while the
+// rest live in pinned, device-mapped host memory that the AdamW kernel reads
+// and writes directly.
+nnt_status alloc_param_state(nnt_model* m, uint64_t budget) {
+  plan_chunks(m);
+  const uint64_t flat_state = (uint64_t)m->n_flat * 12;
+  if (m->device_bytes + flat_state <= budget || !m->opts.allow_host_offload) {
+    m->offload = false;
+    const size_t pf = (size_t)m->n_flat * 4;
+    NNT_TRY(dalloc(m, m->grad, pf));
+    NNT_TRY(dalloc(m, m->mom1, pf));
+    NNT_TRY(dalloc(m, m->mom2, pf));
+    NNT_CUDA_TRY(cudaMemset(m->grad, 0, pf));
+    NNT_CUDA_TRY(cudaMemset(m->mom1, 0, pf));
+    NNT_CUDA_TRY(cudaMemset(m->mom2, 0, pf));
+    m->n_grad = m->n_dev_mv = m->n_flat;
+    for (ParamInfo& p : m->params) p.goff = p.off;
+    for (Chunk& c : m->chunks) {
+      const int64_t off = m->params[c.param].off + c.e0;
+      c.goff = off;
+      c.mv_off = off;
+    }
+    return NNT_OK;
+  }
+  m->offload = true;
+  int64_t max_ring = 0, n_grad = 0;
+  for (int i = 0; i < (int)m->params.size(); ++i) {
+    ParamInfo& p = m->params[i];
+    if (ring_param(m, i)) {
+      p.goff = -1;
+      continue;
+    }
+    p.goff = n_grad;  // contiguous per parameter (the LM head and scatter see [V, d])
+    n_grad += round_up(p.n, 64);
+  }
+  for (Chunk& c : m->chunks) {
+    c.ring = ring_param(m, c.param);
+    if (c.ring) max_ring = std::max(max_ring, c.n);
+    else c.goff = m->params[c.param].goff + c.e0;
+  }
+  m->n_grad = n_grad;
+  NNT_TRY(dalloc(m, m->grad, (size_t)std::max<int64_t>(n_grad, 64) * 4));
+  NNT_CUDA_TRY(cudaMemset(m->grad, 0, (size_t)n_grad * 4));
+  m->n_ring = max_ring ? 4 : 0;
+  m->ring_elems = round_up(max_ring, 64);
+  if (m->n_ring) NNT_TRY(dalloc(m, m->ring, (size_t)m->n_ring * m->ring_elems * 4));
+  int r = 0;
+  for (Chunk& c : m->chunks)
+    if (c.ring) c.slot = r++ % m->n_ring;
+  // moments: small chunks first on the device, then large ones while they fit
+  std::vector<int> order(m->chunks.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return m->chunks[a].n < m->chunks[b].n; });
+  const uint64_t used = m->device_bytes;
+  uint64_t room = budget > used ? budget - used : 0;
+  int64_t dev_mv = 0, host_mv = 0;
+  for (int i : order) {
+    Chunk& c = m->chunks[i];
+    const uint64_t need = (uint64_t)round_up(c.n, 64) * 8;
+    if (need <= room) {
+      c.host = false;
+      c.mv_off = dev_mv;
+      dev_mv += round_up(c.n, 64);
+      room -= need;
+    } else {
+      c.host = true;
+      c.mv_off = host_mv;
+      host_mv += round_up(c.n, 64);
+    }
+  }
+  m->n_dev_mv = dev_mv;
+  m->n_host_mv = host_mv;
+  NNT_TRY(dalloc(m, m->mom1, (size_t)std::max<int64_t>(dev_mv, 64) * 4));
+  NNT_TRY(dalloc(m, m->mom2, (size_t)std::max<int64_t>(dev_mv, 64) * 4));
+  NNT_CUDA_TRY(cudaMemset(m->mom1, 0, (size_t)dev_mv * 4));
+  NNT_CUDA_TRY(cudaMemset(m->mom2, 0, (size_t)dev_mv * 4));
+  if (host_mv) {
+    void* hm = nullptr;
+    void* hv = nullptr;
+    const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
+    if (cudaHostAlloc(&hm, (size_t)host_mv * 4, fl) != cudaSuccess ||
+        cudaHostAlloc(&hv, (size_t)host_mv * 4, fl) != cudaSuccess) {
+      cudaGetLastError();
+      if (hm) cudaFreeHost(hm);
+      set_thread_error("pinned host allocation of 2 x %lld bytes for AdamW moments failed",
+                       (long long)host_mv * 4);
+      return NNT_ERR_OOM;
+    }
+    m->host_m = (float*)hm;
+    m->host_v = (float*)hv;
+    m->host_bytes += (uint64_t)host_mv * 8;
+    memset(m->host_m, 0, (size_t)host_mv * 4);
+    memset(m->host_v, 0, (size_t)host_mv * 4);
+    void* dm = nullptr;
+    void* dv = nullptr;
+    NNT_CUDA_TRY(cudaHostGetDevicePointer(&dm, m->host_m, 0));
+    NNT_CUDA_TRY(cudaHostGetDevicePointer(&dv, m->host_v, 0));
+    m->host_m_dev = (float*)dm;
+    m->host_v_dev = (float*)dv;
+  }
+  return NNT_OK;
+}
+
 nnt_status alloc_all(nnt_model* m) {
   const int L = m->L, d = m->d, f = m->f, T = m->T, H = m->H, S = m->S, B = m->B;
   const size_t as = m->act_size;
@@ -264,17 +452,13 @@ nnt_status alloc_all(nnt_model* m) {
   }
   add_param("ln_f.g", d, 0, 2);
   add_param("ln_f.b", d, 0, 3);
+  size_t free_b = 0, total_b = 0;
+  NNT_CUDA_TRY(cudaMemGetInfo(&free_b, &total_b));
   const size_t pf = (size_t)m->n_flat * 4;
   NNT_TRY(dalloc(m, m->master, pf));
-  NNT_TRY(dalloc(m, m->grad, pf));
-  NNT_TRY(dalloc(m, m->mom1, pf));
-  NNT_TRY(dalloc(m, m->mom2, pf));
   NNT_TRY(dalloc(m, m->wbf, (size_t)m->n_flat * 2));
   NNT_TRY(dalloc(m, m->hyper_dev, sizeof(AdamHyperDev)));
   NNT_CUDA_TRY(cudaMemset(m->master, 0, pf));
-  NNT_CUDA_TRY(cudaMemset(m->grad, 0, pf));
-  NNT_CUDA_TRY(cudaMemset(m->mom1, 0, pf));
-  NNT_CUDA_TRY(cudaMemset(m->mom2, 0, pf));
   NNT_CUDA_TRY(cudaMemset(m->wbf, 0, (size_t)m->n_flat * 2));
 
   NNT_TRY(dalloc(m, m->tokens_dev, (size_t)B * (S + 1) * 2));
@@ -332,7 +516,11 @@ nnt_status alloc_all(nnt_model* m) {
   NNT_CUDA_TRY(cudaMallocHost(&lh, 64));
   m->loss_host = (float*)lh;
   m->host_bytes += 64;
-  return NNT_OK;
+  // gradients and AdamW moments last, once everything else is placed
+  const uint64_t budget = m->opts.hbm_budget_bytes
+                              ? m->opts.hbm_budget_bytes
+                              : (free_b > (2ull << 30) ? free_b - (2ull << 30) : 0);
+  return alloc_param_state(m, budget);
 }
 
 nnt_status init_params(nnt_model* m, cudaStream_t st) {
@@ -355,7 +543,7 @@ enum { LN1G = 0, LN1B, QKVW, QKVB, OW, OB, LN2G, LN2B, FCW, FCB, PROJW, PROJB };
 
 // pointer helpers
 float* pm(nnt_model* m, const ParamInfo& p) { return m->master + p.off; }
-float* pg(nnt_model* m, const ParamInfo& p) { return m->grad + p.off; }
+float* pg(nnt_model* m, const ParamInfo& p) { return m->grad + p.goff; }
 const void* pw(nnt_model* m, const ParamInfo& p) {  // GEMM operand copy of a weight
   if (m->act == NNT_BF16) return m->wbf + p.off;
   return m->master + p.off;
@@ -650,12 +838,53 @@ void build_forward(nnt_model* m) {
 }
 
 // -------------------------------------------------------------- backward
-void build_backward(nnt_model* m) {
+// Backward program. fused: each parameter chunk gets its AdamW task as soon as
+// its gradient is final and every task that reads the old weights has been
+// issued (weight reads are declared, so the executor orders the update after
+// them); moments in pinned host memory are updated in place over NVLink-C2C.
+void build_backward(nnt_model* m, Program& P, bool fused) {
   Builder b{m};
-  Program& P = m->bwd;
   const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
   const size_t as = m->act_size;
   const int act = m->act;
+
+  auto grad_ptr = [m](const Chunk& c) -> float* {
+    if (c.ring) return m->ring + (int64_t)c.slot * m->ring_elems;
+    return m->grad + c.goff;
+  };
+  auto adam_chunk = [&](int ci) {
+    if (!fused) return;
+    const Chunk c = m->chunks[ci];
+    const ParamInfo& p = m->params[c.param];
+    const int k = ci - m->chunks_of[c.param][0];
+    float* gptr = grad_ptr(c);
+    // host-resident moments are read and written in place over NVLink-C2C
+    // (pinned, device-mapped memory); device-resident ones from the pool
+    float* mptr = c.host ? m->host_m_dev + c.mv_off : m->mom1 + c.mv_off;
+    float* vptr = c.host ? m->host_v_dev + c.mv_off : m->mom2 + c.mv_off;
+    const int64_t n = c.n;
+    Task t;
+    t.type = TT_ADAMW;
+    t.bytes = 30.0 * n;
+    box(t.uses, m->gpchunk[c.param], ACC_RW, k, k + 1);
+    box(t.uses, m->ggrad[c.param], ACC_R, c.t0, c.t1);
+    if (c.ring) box(t.uses, m->gring, ACC_R, c.slot, c.slot + 1);
+    float* w = m->master + p.off + c.e0;
+    bf16* wb = m->wbf + p.off + c.e0;
+    const float* hyper = reinterpret_cast<const float*>(m->hyper_dev);
+    const bool host = c.host;
+    t.fn = [=](cudaStream_t s) {
+      return launch_adamw_dev(w, gptr, mptr, vptr, wb, n, hyper, s, host ? 152 : 0);
+    };
+    if (host) t.type = TT_ADAMW_HOST;
+    // updates run on the last stream, next to the GEMM chain on the others
+    t.stream_hint = m->opts.n_streams - 1;
+    P.add(std::move(t));
+  };
+  auto adam_param = [&](int pi) {
+    for (int ci : m->chunks_of[pi]) adam_chunk(ci);
+  };
+  auto param_index = [m](const ParamInfo& p) { return (int)(&p - m->params.data()); };
 
   // dX tasks: out[rows rt, cols ct] = dY[rt] * W  (W [out, in], K = out); the
   // caller lists the tiles read and written.
@@ -669,12 +898,32 @@ void build_backward(nnt_model* m) {
     g.A = dY; g.lda = ldy; g.a_trans = 0;
     g.B = pw(m, W); g.ldb = ldw; g.b_trans = 1;
     g.C = out; if (!g.ldc) g.ldc = N; g.c_dtype = out_dtype;
+    box(uses, m->gpchunk[param_index(W)], ACC_R);  // reads the weight (before its update)
     b.gemm_task(P, type, g, std::move(uses), 2.0 * m->TT * (c1 - c0) * K);
   };
   // dW tasks: grad[out tile, in tile] = dY^T X over all tokens
   auto dw_gemm = [&](int type, const void* dY, const TGrid& gdY, int64_t ldy, int Nout, int tOut,
                      const void* X, const TGrid& gX, int64_t ldx, int Nin, int tIn, const ParamInfo& W,
                      int gidx) {
+    if (fused) {  // one GEMM per AdamW chunk (whole rows), then its update
+      for (int ci : m->chunks_of[gidx]) {
+        const Chunk c = m->chunks[ci];
+        GemmArgs g = b.base();
+        g.M = Nout; g.N = Nin; g.K = T;
+        g.m0 = (int)c.r0; g.mt = (int)(c.r1 - c.r0); g.n0 = 0; g.nt = Nin;
+        g.A = dY; g.lda = ldy; g.a_trans = 1;
+        g.B = X; g.ldb = ldx; g.b_trans = 1;
+        g.C = grad_ptr(c); g.c_row0 = c.r0; g.ldc = Nin; g.c_dtype = NNT_F32;
+        std::vector<TileUse> u;
+        box(u, gdY, ACC_R);
+        box(u, gX, ACC_R);
+        box(u, m->ggrad[gidx], ACC_W, c.t0, c.t1);
+        if (c.ring) box(u, m->gring, ACC_W, c.slot, c.slot + 1);
+        b.gemm_task(P, TT_GEMM_DW, g, std::move(u), 2.0 * (c.r1 - c.r0) * Nin * T);
+        adam_chunk(ci);
+      }
+      return;
+    }
     for (auto [ot0, ot1] : b.col_groups(tiles_of(Nout, tOut), tOut, Nout))
       for (auto [it0, it1] : b.col_groups(tiles_of(Nin, tIn), tIn, Nin)) {
         const int o0 = tile_lo(ot0, tOut), o1 = tile_hi(ot1 - 1, tOut, Nout);
@@ -705,6 +954,7 @@ void build_backward(nnt_model* m) {
       return launch_colsum(a, a_dtype, T, N, N, m->col_part, out, 0, s);
     };
     P.add(std::move(t));
+    adam_param(gidx);
   };
   // LN backward per token tile, then one column reduction over all tokens for
   // the gain/shift gradients and (bias_idx >= 0) the gradient of the bias whose
@@ -720,6 +970,7 @@ void build_backward(nnt_model* m) {
       box(t.uses, gst, ACC_R, rt, rt + 1);
       box(t.uses, m->gdres, has_resid ? ACC_RW : ACC_W, rt, rt + 1);
       box(t.uses, m->gdres_act, ACC_W, rt, rt + 1);
+      box(t.uses, m->gpchunk[gidx_g], ACC_R);  // reads the gain (before its update)
       t.bytes = (double)m->TT * d * (4 * (has_resid ? 4 : 3) + as);
       const int64_t r0 = (int64_t)rt * m->TT;
       const float* gam = pm(m, gm);
@@ -750,6 +1001,9 @@ void build_backward(nnt_model* m) {
                                    ob, obias, s);
     };
     P.add(std::move(t));
+    adam_param(gidx_g);
+    adam_param(gidx_b);
+    if (bias_idx >= 0) adam_param(bias_idx);
   };
   const int pidx_lnf = 2 + 12 * m->L;
 
@@ -766,6 +1020,7 @@ void build_backward(nnt_model* m) {
       std::vector<TileUse> u;
       box(u, m->gdz, ACC_R, rt, rt + 1);
       box(u, m->gdtmp, ACC_W, rt, rt + 1, t0, t1);
+      box(u, m->gpchunk[0], ACC_R);  // reads wte (before its update)
       b.gemm_task(P, TT_GEMM_LM_DX, g, std::move(u), 2.0 * m->TT * (c1 - c0) * V);
     }
   for (int vt = 0; vt < m->ncv; ++vt)
@@ -809,9 +1064,7 @@ void build_backward(nnt_model* m) {
       }
     dw_gemm(TT_GEMM_DW, m->dres_act, m->gdres_act, d, d, m->te, m->g[l], m->gg[l], f, f, m->ti,
             P_(m, l, PROJW), pi + PROJW);
-    dw_gemm(TT_GEMM_DW, m->du, m->gdu, f, f, m->ti, m->h2[l], m->gh2[l], d, d, m->te, P_(m, l, FCW),
-            pi + FCW);
-    colsum_task(m->du, act, m->gdu, f, P_(m, l, FCB), pi + FCB);
+    // dX before dW for each weight, so a fused update follows every read of it
     for (int rt = 0; rt < m->n_tok; ++rt)
       for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
         std::vector<TileUse> u;
@@ -820,6 +1073,9 @@ void build_backward(nnt_model* m) {
         dx_gemm(TT_GEMM_DX, m->du, f, f, P_(m, l, FCW), d, m->dtmp, NNT_F32, d, m->te, rt, t0, t1,
                 b.base(), std::move(u));
       }
+    dw_gemm(TT_GEMM_DW, m->du, m->gdu, f, f, m->ti, m->h2[l], m->gh2[l], d, d, m->te, P_(m, l, FCW),
+            pi + FCW);
+    colsum_task(m->du, act, m->gdu, f, P_(m, l, FCB), pi + FCB);
     ln_bwd(m->dtmp, m->gdtmp, m->xmid[l], m->gxmid[l], m->mu2[l], m->r2[l], m->gstat2[l],
            P_(m, l, LN2G), P_(m, l, LN2B), pi + LN2G, pi + LN2B, true, pi + OB);
     // attention output projection: dO (head-major), dWo, dbo
@@ -929,10 +1185,7 @@ void build_backward(nnt_model* m) {
           b.gemm_task(P, TT_GEMM_ATTN_BWD, g, std::move(u), 2.0 * hd * pairs * nz);
         }
       }
-    // QKV projection backward
-    dw_gemm(TT_GEMM_DW, m->dqkv, m->gdqkv, 3 * d, 3 * d, m->te, m->h1[l], m->gh1[l], d, d, m->te,
-            P_(m, l, QKVW), pi + QKVW);
-    colsum_task(m->dqkv, act, m->gdqkv, 3 * d, P_(m, l, QKVB), pi + QKVB);
+    // QKV projection backward (dX first, then dW and its update)
     for (int rt = 0; rt < m->n_tok; ++rt)
       for (auto [t0, t1] : b.col_groups(m->nce, m->te, d)) {
         std::vector<TileUse> u;
@@ -941,6 +1194,9 @@ void build_backward(nnt_model* m) {
         dx_gemm(TT_GEMM_DX, m->dqkv, 3 * d, 3 * d, P_(m, l, QKVW), d, m->dtmp, NNT_F32, d, m->te, rt,
                 t0, t1, b.base(), std::move(u));
       }
+    dw_gemm(TT_GEMM_DW, m->dqkv, m->gdqkv, 3 * d, 3 * d, m->te, m->h1[l], m->gh1[l], d, d, m->te,
+            P_(m, l, QKVW), pi + QKVW);
+    colsum_task(m->dqkv, act, m->gdqkv, 3 * d, P_(m, l, QKVB), pi + QKVB);
     ln_bwd(m->dtmp, m->gdtmp, m->x[l], m->gx[l], m->mu1[l], m->r1[l], m->gstat1[l], P_(m, l, LN1G),
            P_(m, l, LN1B), pi + LN1G, pi + LN1B, true, l > 0 ? pi - 12 + PROJB : -1);
   }
@@ -965,9 +1221,10 @@ void build_backward(nnt_model* m) {
     t.bytes = (double)T * d * 12;
     t.fn = [m](cudaStream_t s) {
       return launch_embedding_scatter(m->sort_keys, m->T, m->dres, m->tm, m->S,
-                                      m->grad + m->params[0].off, m->d, m->V, s);
+                                      pg(m, m->params[0]), m->d, m->V, s);
     };
     P.add(std::move(t));
+    adam_param(0);
   }
   for (int st = 0; st < m->n_st; ++st) {
     Task t;
@@ -977,14 +1234,16 @@ void build_backward(nnt_model* m) {
     t.bytes = (double)T / m->n_st * d * 4 + (double)m->ts * d * 4;
     const int s0 = st * m->ts;
     t.fn = [m, s0](cudaStream_t s) {
-      return launch_wpe_grad(m->dres, m->tm, m->B, s0, m->ts, m->d, m->grad + m->params[1].off, 0, s);
+      return launch_wpe_grad(m->dres, m->tm, m->B, s0, m->ts, m->d, pg(m, m->params[1]), 0, s);
     };
     P.add(std::move(t));
   }
+  adam_param(1);
 }
 
 void build_optimizer(nnt_model* m) {
   // one AdamW task per chunk of the flat parameter buffers (<= 256 Mi elements)
+  if (m->offload) return;  // offloaded models update inside the fused backward only
   const int64_t chunk = 256ll << 20;
   for (int64_t o = 0; o < m->n_flat; o += chunk) {
     const int64_t n = std::min(chunk, m->n_flat - o);
@@ -1033,18 +1292,13 @@ void make_grids(nnt_model* m) {
   m->gkeys = new_grid(m, 1);
   // parameter gradients: weights tiled [out tile, in tile], vectors by their axis
   for (const ParamInfo& p : m->params) {
-    auto axis_tile = [&](int64_t n) -> int {
-      if (n == m->d) return m->te;
-      if (n == 3 * (int64_t)m->d) return m->te;
-      if (n == m->f) return m->ti;
-      if (n == m->V) return m->tv;
-      if (n == m->S) return m->ts;
-      return (int)n;
-    };
-    int a = tiles_of((int)p.shape0, axis_tile(p.shape0));
-    int bcount = p.shape1 ? tiles_of((int)p.shape1, axis_tile(p.shape1)) : 1;
+    int a = tiles_of((int)p.shape0, axis_tile(m, p.shape0));
+    int bcount = p.shape1 ? tiles_of((int)p.shape1, axis_tile(m, p.shape1)) : 1;
     m->ggrad.push_back(new_grid(m, a, bcount));
   }
+  for (size_t i = 0; i < m->params.size(); ++i)
+    m->gpchunk.push_back(new_grid(m, (int)m->chunks_of[i].size()));
+  m->gring = new_grid(m, std::max(1, m->n_ring));
 }
 
 nnt_status wait_event(nnt_model* m, cudaEvent_t ev) {
@@ -1091,6 +1345,8 @@ void free_model(nnt_model* m) {
   for (void* p : m->dev_allocs) cudaFree(p);
   m->dev_allocs.clear();
   if (m->loss_host) cudaFreeHost(m->loss_host);
+  if (m->host_m) cudaFreeHost(m->host_m);
+  if (m->host_v) cudaFreeHost(m->host_v);
   if (m->done_event) cudaEventDestroy(m->done_event);
   cudaStream_t own = m->ex.main_;
   bool owned = m->opts.stream == nullptr;
@@ -1151,7 +1407,7 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
       return fail(nullptr, NNT_ERR_CUDA);
     }
   }
-  s = m->ex.init(main, m->opts.n_streams, false, m->opts.trace != 0, TT_COUNT);
+  s = m->ex.init(main, m->opts.n_streams, true, m->opts.trace != 0, TT_COUNT);
   if (s == NNT_OK && cudaEventCreateWithFlags(&m->done_event, cudaEventDisableTiming) != cudaSuccess)
     s = NNT_ERR_CUDA;
   if (s == NNT_OK) s = alloc_all(m);
@@ -1159,10 +1415,12 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
   if (s == NNT_OK) {
     make_grids(m);
     build_forward(m);
-    build_backward(m);
+    if (!m->offload) build_backward(m, m->bwd, false);
+    build_backward(m, m->bwdf, true);
     build_optimizer(m);
     m->fwd.finalize(m->opts.n_streams);
     m->bwd.finalize(m->opts.n_streams);
+    m->bwdf.finalize(m->opts.n_streams);
     m->opt.finalize(1);
     s = sync_model(m);
   }
@@ -1222,6 +1480,11 @@ nnt_status nnt_backward(nnt_model* m) {
     set_thread_error("nnt_backward needs a preceding nnt_forward");
     return fail(m, NNT_ERR_STATE);
   }
+  if (m->offload) {
+    set_thread_error("this model offloads AdamW moments: gradients are not kept whole; use "
+                     "nnt_backward_adamw");
+    return fail(m, NNT_ERR_STATE);
+  }
   auto t0 = std::chrono::steady_clock::now();
   nnt_status s = m->ex.run(m->bwd, m->opts.use_cuda_graph ? 1 : -1);
   if (s != NNT_OK) return fail(m, s);
@@ -1242,6 +1505,10 @@ nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp) {
   }
   if (m->state != 2) {
     set_thread_error("nnt_adamw_step needs a preceding nnt_backward");
+    return fail(m, NNT_ERR_STATE);
+  }
+  if (m->offload) {
+    set_thread_error("this model offloads AdamW moments; use nnt_backward_adamw");
     return fail(m, NNT_ERR_STATE);
   }
   if (!(hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1) ||
@@ -1267,6 +1534,47 @@ nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp) {
     if (s == NNT_OK) s = m->ex.collect_trace(m->opt);
     if (s != NNT_OK) return fail(m, s);
     m->last_opt_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  }
+  return NNT_OK;
+}
+
+nnt_status nnt_backward_adamw(nnt_model* m, const nnt_adamw* hp) {
+  if (!m || !hp) {
+    set_thread_error("NULL model or hyper-parameters");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  if (m->state != 1) {
+    set_thread_error("nnt_backward_adamw needs a preceding nnt_forward");
+    return fail(m, NNT_ERR_STATE);
+  }
+  if (!(hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1) ||
+      !(hp->eps > 0) || !(hp->weight_decay >= 0)) {
+    set_thread_error("invalid AdamW hyper-parameters");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  auto t0 = std::chrono::steady_clock::now();
+  const int64_t t = m->step + 1;
+  AdamHyperDev& h = m->hyper_host;
+  h.lr = hp->lr; h.b1 = hp->beta1; h.b2 = hp->beta2; h.eps = hp->eps; h.wd = hp->weight_decay;
+  h.bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
+  h.bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
+  h.pad = 0;
+  if (cudaMemcpyAsync(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_) != cudaSuccess)
+    return fail(m, NNT_ERR_CUDA);
+  nnt_status s = m->ex.run(m->bwdf, m->opts.use_cuda_graph ? 3 : -1);
+  if (s != NNT_OK) return fail(m, s);
+  m->step = t;
+  m->state = 0;
+  for (const Chunk& c : m->chunks)
+    if (c.host) {
+      m->h2d_bytes += (uint64_t)c.n * 8;  // m and v read over C2C
+      m->d2h_bytes += (uint64_t)c.n * 8;  // and written back
+    }
+  if (m->opts.trace) {
+    s = sync_model(m);
+    if (s == NNT_OK) s = m->ex.collect_trace(m->bwdf);
+    if (s != NNT_OK) return fail(m, s);
+    m->last_bwd_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
   }
   return NNT_OK;
 }
@@ -1321,14 +1629,45 @@ nnt_status nnt_set_param(nnt_model* m, int32_t i, const float* host_buf) {
   return copy_param(m, i, m ? m->master : nullptr, const_cast<float*>(host_buf), true);
 }
 nnt_status nnt_get_grad(nnt_model* m, int32_t i, float* host_buf) {
-  return copy_param(m, i, m ? m->grad : nullptr, host_buf, false);
+  if (m && i >= 0 && i < (int32_t)m->params.size() && m->params[i].goff < 0) {
+    set_thread_error("gradients of %s are streamed through the ring and not kept",
+                     m->params[i].name.c_str());
+    return fail(m, NNT_ERR_STATE);
+  }
+  if (m && i >= 0 && i < (int32_t)m->params.size() && host_buf) {
+    const ParamInfo& p = m->params[i];
+    if (cudaMemcpyAsync(host_buf, m->grad + p.goff, p.n * 4, cudaMemcpyDeviceToHost, m->ex.main_) !=
+        cudaSuccess)
+      return fail(m, NNT_ERR_CUDA);
+    nnt_status s = sync_model(m);
+    return s == NNT_OK ? s : fail(m, s);
+  }
+  set_thread_error("bad model, buffer or parameter index");
+  return fail(m, NNT_ERR_INVALID_ARG);
 }
 nnt_status nnt_get_adam_state(nnt_model* m, int32_t i, int32_t which, float* host_buf) {
   if (which != 0 && which != 1) {
     set_thread_error("which must be 0 (m) or 1 (v)");
     return fail(m, NNT_ERR_INVALID_ARG);
   }
-  return copy_param(m, i, m ? (which ? m->mom2 : m->mom1) : nullptr, host_buf, false);
+  if (!m || !host_buf || i < 0 || i >= (int32_t)m->params.size()) {
+    set_thread_error("bad model, buffer or parameter index");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  nnt_status s = sync_model(m);
+  if (s != NNT_OK) return fail(m, s);
+  for (int ci : m->chunks_of[i]) {
+    const Chunk& c = m->chunks[ci];
+    float* dst = host_buf + c.e0;
+    if (c.host) {
+      memcpy(dst, (which ? m->host_v : m->host_m) + c.mv_off, (size_t)c.n * 4);
+    } else if (cudaMemcpyAsync(dst, (which ? m->mom2 : m->mom1) + c.mv_off, (size_t)c.n * 4,
+                               cudaMemcpyDeviceToHost, m->ex.main_) != cudaSuccess) {
+      return fail(m, NNT_ERR_CUDA);
+    }
+  }
+  s = sync_model(m);
+  return s == NNT_OK ? s : fail(m, s);
 }
 
 nnt_status nnt_get_logits(nnt_model* m, float* host_buf) {
@@ -1369,8 +1708,11 @@ nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out) {
   out->n_tiles = m->next_tile;
   out->n_params = m->n_scalar;
   out->n_streams = m->opts.n_streams;
+  out->offload_active = m->offload ? 1 : 0;
+  out->h2d_bytes = m->h2d_bytes;
+  out->d2h_bytes = m->d2h_bytes;
   out->kernels_forward = m->fwd.kernels();
-  out->kernels_backward = m->bwd.kernels();
+  out->kernels_backward = m->offload ? m->bwdf.kernels() : m->bwd.kernels();
   out->kernels_adamw = m->opt.kernels();
   return NNT_OK;
 }
@@ -1403,6 +1745,7 @@ nnt_status nnt_set_trace(nnt_model* m, int32_t on) {
   const int ns = on ? 1 : m->opts.n_streams;
   m->fwd.finalize(ns);
   m->bwd.finalize(ns);
+  m->bwdf.finalize(ns);
   m->ex.drop_graphs();
   return NNT_OK;
 }

@@ -74,6 +74,7 @@ _SIGS = {
     "nnt_forward": (C.c_int, [_P, _P, _I32, C.POINTER(_F)]),
     "nnt_backward": (C.c_int, [_P]),
     "nnt_adamw_step": (C.c_int, [_P, C.POINTER(AdamW)]),
+    "nnt_backward_adamw": (C.c_int, [_P, C.POINTER(AdamW)]),
     "nnt_destroy": (None, [_P]),
     "nnt_num_params": (_I32, [_P]),
     "nnt_param_info": (C.c_int, [_P, _I32, C.POINTER(C.c_char_p), C.POINTER(_I64)]),
@@ -214,6 +215,11 @@ class Model:
     def adamw_step(self, lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1):
         hp = AdamW(lr, beta1, beta2, eps, weight_decay)
         check(lib().nnt_adamw_step(self.h, C.byref(hp)), self.h)
+
+    def backward_adamw(self, lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1):
+        """Backward with each chunk's AdamW update fused in (nnt_backward_adamw)."""
+        hp = AdamW(lr, beta1, beta2, eps, weight_decay)
+        check(lib().nnt_backward_adamw(self.h, C.byref(hp)), self.h)
 
     # ---- parity surface
     def _get(self, fn, i, *extra):
