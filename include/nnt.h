@@ -93,9 +93,17 @@ typedef struct {
 /* AdamW hyper-parameters (README: --optimizer=fusedadamw, --optimizer-eps=1e-8,
  * --weight-decay=0.1, --lr=3e-4; decoupled weight decay per the pages' reference
  * "Decoupled Weight Decay Regularization"). Betas are not on the pages: 0.9 and
- * 0.999 are used by the tests. */
+ * 0.999 are used by the tests.
+ * Warm-up (README: --start-lr, --full-lr-iter): AdamW iteration t (1-based,
+ * counted by the model) uses start_lr at t = 1, lr from t = full_lr_iter on,
+ * and the straight line between them in between (the pages give the two end
+ * points only). full_lr_iter <= 1 (e.g. a zero-initialised struct) applies lr
+ * from the first iteration. INVALID_ARG for a negative rate, weight decay or
+ * full_lr_iter, eps <= 0, or a beta outside [0, 1). */
 typedef struct {
   float lr, beta1, beta2, eps, weight_decay;
+  float start_lr;       /* rate of iteration 1 when full_lr_iter > 1 */
+  int32_t full_lr_iter; /* first iteration at the full rate lr */
 } nnt_adamw;
 
 typedef struct nnt_model nnt_model;
@@ -139,8 +147,22 @@ nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_d
  * the model offloads AdamW moments (use nnt_backward_adamw). */
 nnt_status nnt_backward(nnt_model* m);
 
-/* One fused AdamW update of every parameter tile from the current gradients;
- * the step counter starts at 1 and grows by one per call. STATE error if no
+/* Gradient accumulation over minibatches (README: --batch sequences per
+ * optimizer step, processed --minibatch at a time; the step happens once the
+ * whole batch's gradients are collected). Backward pass of the last forward
+ * whose gradients are ADDED to those stored since the last AdamW update; the
+ * first call after an update (or after nnt_backward's overwrite) starts the
+ * sum. nnt_adamw_step then uses the mean of the k summed minibatch gradients,
+ * which for minibatches of equal token count is the gradient of the mean loss
+ * over the whole batch. Call pattern for a batch of k minibatches:
+ * k x (nnt_forward, nnt_backward_accumulate), then nnt_adamw_step. Same
+ * STATE rules as nnt_backward; a failed call leaves the sum undefined, so the
+ * next call starts a new one. */
+nnt_status nnt_backward_accumulate(nnt_model* m);
+
+/* One fused AdamW update of every parameter tile from the current gradients
+ * (their mean over the minibatches accumulated since the last update); the
+ * step counter starts at 1 and grows by one per call. STATE error if no
  * backward preceded it since the last update. */
 nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp);
 
@@ -155,6 +177,8 @@ nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp);
  * in place in pinned, device-mapped host memory (over NVLink-C2C on GB300).
  * Same STATE/INVALID_ARG rules as nnt_backward / nnt_adamw_step. */
 nnt_status nnt_backward_adamw(nnt_model* m, const nnt_adamw* hp);
+/* (nnt_backward_adamw does not add to accumulated gradients: STATE error while
+ * minibatch gradients are pending an nnt_adamw_step.) */
 
 /* Free everything the model owns. NULL-safe; always succeeds. */
 void nnt_destroy(nnt_model* m);

@@ -22,7 +22,15 @@ Readings where the pages are silent (each also listed in the design notes):
   * LayerNorm eps 1e-5, biased variance.
   * GELU: the tanh approximation used by GPT2.
   * attention scale 1/sqrt(head_dim); causal mask = probability exactly 0.
-  * no dropout, no gradient clipping, constant lr, AdamW betas (0.9, 0.999).
+  * no dropout, no gradient clipping, AdamW betas (0.9, 0.999).
+  * learning-rate warm-up (README flags --start-lr, --full-lr-iter): the pages
+    give the rate of the first iteration and the iteration from which the full
+    rate applies; in between the rate is read as the straight line joining
+    them. With full_lr_iter <= 1 (the default here) the rate is constant.
+  * gradient accumulation (README flags --batch, --minibatch): the optimizer
+    step uses the gradient of the mean loss over the whole batch, i.e. the
+    mean of the minibatch gradients when every minibatch holds the same
+    number of tokens.
   * weight decay applied to every parameter (one --weight-decay flag, no
     exclusion list on the pages).
   * tied LM head (wte used as the output projection, no LM bias); the two
@@ -70,6 +78,8 @@ class AdamWHyper:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.1
+    start_lr: float = 0.0  # rate of iteration 1 when full_lr_iter > 1
+    full_lr_iter: int = 0  # first iteration at the full rate (<= 1: always)
 
 
 def param_order(cfg: GPT2Config):
@@ -454,8 +464,26 @@ def backward(cfg: GPT2Config, params, cache, dtype=np.float64):
     return grads
 
 
+def scheduled_lr(hp: AdamWHyper, step: int) -> float:
+    """Rate of AdamW iteration ``step`` (1-based) under the warm-up flags.
+
+    README "Minimal working GPT example": --start-lr is the rate used for the
+    first batch and --full-lr-iter the AdamW iteration that first uses the full
+    --lr (1 = full rate from the start). Between the two the rate rises along a
+    straight line (a reading: the pages name only the end points).
+    """
+    if hp.full_lr_iter <= 1 or step >= hp.full_lr_iter:
+        return hp.lr
+    return hp.start_lr + (hp.lr - hp.start_lr) * (step - 1) / (hp.full_lr_iter - 1)
+
+
 def adamw_step(params, grads, m, v, step, hp: AdamWHyper, dtype=np.float64):
-    """AdamW over every parameter; returns new (params, m, v) dictionaries."""
+    """AdamW over every parameter; returns new (params, m, v) dictionaries.
+
+    The rate is that of iteration ``step`` under the warm-up schedule.
+    """
+    hp = AdamWHyper(lr=scheduled_lr(hp, step), beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps,
+                    weight_decay=hp.weight_decay)
     new_p, new_m, new_v = {}, {}, {}
     for k in params:
         w = np.asarray(params[k], dtype=dtype)
@@ -473,6 +501,46 @@ def train_step(cfg: GPT2Config, params, windows, hp: AdamWHyper = AdamWHyper(),
     grads = backward(cfg, params, cache, dtype)
     new_p, new_m, new_v = adamw_step(params, grads, m, v, step, hp, dtype)
     return loss, grads, new_p, new_m, new_v
+
+
+def batch_gradient(cfg: GPT2Config, params, minibatches, dtype=np.float64):
+    """Loss and gradient of one optimizer batch given as a list of minibatches.
+
+    README "Minimal working GPT example": --batch sequences form the batch, the
+    optimizer step happens after the gradients of the whole batch are
+    collected, and --minibatch sequences are processed at a time; the loss is
+    the mean over all tokens (--loss-reduction=mean). Every minibatch here has
+    the same shape, so the batch loss and its gradient are the means of the
+    minibatch losses and gradients.
+    """
+    losses, total = [], None
+    for windows in minibatches:
+        loss, cache = forward(cfg, params, windows, dtype)
+        grads = backward(cfg, params, cache, dtype)
+        del cache
+        losses.append(loss)
+        total = grads if total is None else {n: total[n] + grads[n] for n in total}
+    k = len(minibatches)
+    return sum(losses) / k, {n: g / k for n, g in total.items()}
+
+
+def train_batch(cfg: GPT2Config, params, minibatches, hp: AdamWHyper = AdamWHyper(),
+                m=None, v=None, step=1, dtype=np.float64):
+    """One optimizer step over a batch of minibatches; same returns as train_step."""
+    loss, grads = batch_gradient(cfg, params, minibatches, dtype)
+    new_p, new_m, new_v = adamw_step(params, grads, m, v, step, hp, dtype)
+    return loss, grads, new_p, new_m, new_v
+
+
+def train(cfg: GPT2Config, params, batches, hp: AdamWHyper = AdamWHyper(), dtype=np.float64):
+    """Several optimizer steps; ``batches[i]`` is the list of minibatch windows of
+    step i + 1. Returns (per-step batch losses, final params, m, v)."""
+    m = v = None
+    losses = []
+    for i, mbs in enumerate(batches):
+        loss, _, params, m, v = train_batch(cfg, params, mbs, hp, m, v, i + 1, dtype)
+        losses.append(loss)
+    return losses, params, m, v
 
 
 def step_flops(cfg: GPT2Config) -> float:

@@ -413,3 +413,65 @@ def test_bf16_precision_model_reduces_to_exact_step_with_identity_rounding():
     gb = O.backward_bf16_operands(cfg, p, cb)
     for k in g0:
         assert np.abs(gb[k] - g0[k]).max() <= 3e-2 * np.abs(g0[k]).max() + 1e-12, k
+
+
+# ------------------------------------- gradient accumulation and lr warm-up
+
+def test_warmup_schedule_end_points_from_readme():
+    """README flags: --start-lr is the rate of the first batch, --full-lr-iter the
+    iteration that first uses --lr, and 1 means the full rate throughout."""
+    with open(os.path.join(GOLDEN, "readme_hyperparams.json")) as fh:
+        hpj = json.load(fh)
+    hp = O.AdamWHyper(lr=hpj["lr"], start_lr=hpj["start_lr"], full_lr_iter=hpj["full_lr_iter"])
+    assert O.scheduled_lr(hp, 1) == hpj["start_lr"]
+    assert O.scheduled_lr(hp, hpj["full_lr_iter"]) == hpj["lr"]
+    assert O.scheduled_lr(hp, hpj["full_lr_iter"] + 5) == hpj["lr"]
+    rates = [O.scheduled_lr(hp, t) for t in range(1, hpj["full_lr_iter"] + 1)]
+    assert all(a < b for a, b in zip(rates, rates[1:]))  # strictly rising to the full rate
+    for t in (1, 2, 7, 100):
+        assert O.scheduled_lr(O.AdamWHyper(lr=hpj["lr"], start_lr=0.0, full_lr_iter=1), t) == hpj["lr"]
+    # the constant-rate default
+    assert O.scheduled_lr(O.AdamWHyper(), 1) == O.AdamWHyper().lr
+
+
+def test_zero_start_rate_leaves_weights_unchanged_on_first_step():
+    """lr = 0 multiplies both the decay and the Adam term: w stays bit-identical,
+    while the moments still take the first gradient."""
+    cfg = O.GPT2Config(n_layer=1, d_model=8, n_head=2, d_ff=16, vocab=11, seq=4, batch=2)
+    p = _rand_params(cfg, 31)
+    hp = O.AdamWHyper(start_lr=0.0, full_lr_iter=4)
+    loss, grads, new, m, v = O.train_step(cfg, p, _windows(cfg, 32), hp)
+    for n in p:
+        np.testing.assert_array_equal(new[n], p[n])
+        np.testing.assert_allclose(m[n], 0.1 * grads[n], rtol=1e-14)
+
+
+def test_minibatch_accumulation_equals_whole_batch_gradient():
+    """The mean loss over a batch is the mean of its equal-sized minibatches'
+    mean losses, so accumulated minibatch gradients / k must equal the gradient
+    of the batch processed at once (batch linearity, computed another way)."""
+    big = O.GPT2Config(n_layer=2, d_model=8, n_head=2, d_ff=16, vocab=13, seq=5, batch=4)
+    small = O.GPT2Config(n_layer=2, d_model=8, n_head=2, d_ff=16, vocab=13, seq=5, batch=2)
+    p = _rand_params(big, 33)
+    win = _windows(big, 34)
+    loss_all, cache = O.forward(big, p, win)
+    g_all = O.backward(big, p, cache)
+    loss_acc, g_acc = O.batch_gradient(small, p, [win[:2], win[2:]])
+    assert abs(loss_acc - loss_all) < 1e-13
+    for n in g_all:
+        np.testing.assert_allclose(g_acc[n], g_all[n], rtol=1e-10, atol=1e-14)
+    # a wrong normaliser (sum instead of mean) is caught
+    assert not np.allclose(2 * g_acc["wte"], g_all["wte"])
+
+
+def test_training_on_one_batch_lowers_the_loss():
+    """Several AdamW steps on a repeated batch must lower its loss (descent on a
+    smooth objective with a small rate); the warm-up schedule's first step at
+    rate 0 leaves the loss of step 2 equal to that of step 1."""
+    cfg = O.GPT2Config(n_layer=1, d_model=16, n_head=2, d_ff=32, vocab=17, seq=6, batch=2)
+    p = _rand_params(cfg, 35, std=0.1)
+    mbs = [_windows(cfg, 36), _windows(cfg, 37)]
+    hp = O.AdamWHyper(lr=1e-2, start_lr=0.0, full_lr_iter=3)
+    losses, final, _, _ = O.train(cfg, p, [mbs] * 6, hp)
+    assert losses[1] == losses[0]
+    assert all(b < a for a, b in zip(losses[1:], losses[2:])), losses

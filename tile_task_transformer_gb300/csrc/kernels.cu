@@ -281,6 +281,22 @@ static int row_tpr(int cols) {
   return tpr;
 }
 
+// float4 groups per thread actually needed (1, 2, 4, 6 or 8), so register
+// arrays are no larger than the row.
+static int row_maxv(int cols, int tpr) {
+  const int need = (int)ceil_div(cols / 4, tpr);
+  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : 8;
+}
+
+#define NNT_MAXV_DISPATCH(mv, ...)                               \
+  switch (mv) {                                                  \
+    case 1: { constexpr int MV = 1; __VA_ARGS__; } break;        \
+    case 2: { constexpr int MV = 2; __VA_ARGS__; } break;        \
+    case 4: { constexpr int MV = 4; __VA_ARGS__; } break;        \
+    case 6: { constexpr int MV = 6; __VA_ARGS__; } break;        \
+    default: { constexpr int MV = 8; __VA_ARGS__; } break;       \
+  }
+
 #define NNT_TPR_DISPATCH(tpr, ...)                          \
   switch (tpr) {                                            \
     case 32: { constexpr int TPR = 32; __VA_ARGS__; } break;     \
@@ -301,12 +317,13 @@ nnt_status launch_layernorm_fwd(const float* x, const float* g, const float* b, 
   const int block = std::max(256, tpr);
   const int rpc = block / tpr;
   const int64_t grid = ceil_div(rows, rpc);
-  NNT_TPR_DISPATCH(tpr, {
+  const int mv = row_maxv(cols, tpr);
+  NNT_TPR_DISPATCH(tpr, NNT_MAXV_DISPATCH(mv, {
     if (act_dtype == NNT_BF16)
-      ln_fwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>(x, g, b, (bf16*)y, mean, rstd, rows, cols, eps);
+      ln_fwd_kernel<TPR, MV, bf16><<<grid, block, 0, st>>>(x, g, b, (bf16*)y, mean, rstd, rows, cols, eps);
     else
-      ln_fwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>(x, g, b, (float*)y, mean, rstd, rows, cols, eps);
-  });
+      ln_fwd_kernel<TPR, MV, float><<<grid, block, 0, st>>>(x, g, b, (float*)y, mean, rstd, rows, cols, eps);
+  }));
   return launch_check("layernorm_fwd");
 }
 
@@ -379,12 +396,13 @@ nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* me
   const int tpr = row_tpr(cols);
   const int block = std::max(256, tpr);
   const int64_t grid = ceil_div(rows, block / tpr);
-  NNT_TPR_DISPATCH(tpr, {
+  const int mv = row_maxv(cols, tpr);
+  NNT_TPR_DISPATCH(tpr, NNT_MAXV_DISPATCH(mv, {
     if (act_dtype == NNT_BF16)
-      ln_bwd_kernel<TPR, 8, bf16><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols);
+      ln_bwd_kernel<TPR, MV, bf16><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols);
     else
-      ln_bwd_kernel<TPR, 8, float><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols);
-  });
+      ln_bwd_kernel<TPR, MV, float><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols);
+  }));
   return launch_check("layernorm_bwd");
 }
 
@@ -441,14 +459,15 @@ int64_t ln_colsum_chunks(int64_t rows) { return std::min<int64_t>(128, std::max<
 
 nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* mean,
                                  const float* rstd, const float* out, int64_t rows, int cols,
-                                 float* part, float* dg, float* db, float* dbias, cudaStream_t st) {
+                                 float* part, float* dg, float* db, float* dbias, int accumulate,
+                                 cudaStream_t st) {
   NNT_CHECK_ARG(cols % 4 == 0, "layernorm colsums: cols must be a multiple of 4");
   const int64_t nch = ln_colsum_chunks(rows);
   const int64_t rpc = ceil_div(rows, nch);
   dim3 grid((unsigned)ceil_div(cols, 128), (unsigned)nch);
   ln_bwd_colsums_kernel<<<grid, 256, 0, st>>>(dy, x, mean, rstd, out, rows, cols, rpc, part);
   NNT_TRY(launch_check("ln_bwd_colsums"));
-  return launch_sum_parts3(part, nch, cols, dg, db, out ? dbias : nullptr, st);
+  return launch_sum_parts3(part, nch, cols, dg, db, out ? dbias : nullptr, accumulate, st);
 }
 
 // out[c] (+)= sum_p part[p*ld + c]. A CTA owns 32 columns; its 8 warps take
@@ -484,7 +503,7 @@ __global__ void sum_parts_kernel(const float* __restrict__ part, int64_t nparts,
 }
 
 __global__ void sum_parts3_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
-                                  float* o0, float* o1, float* o2) {
+                                  float* o0, float* o1, float* o2, int accumulate) {
   float* outs[3] = {o0, o1, o2};
   float* out = outs[blockIdx.y];
   if (!out) return;
@@ -502,15 +521,15 @@ __global__ void sum_parts3_kernel(const float* __restrict__ part, int64_t nparts
     float t = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) t += red[i][lane];
-    out[c] = t;
+    out[c] = accumulate ? out[c] + t : t;
   }
 }
 
 nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, float* o0, float* o1,
-                             float* o2, cudaStream_t st) {
+                             float* o2, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
   dim3 grid((unsigned)ceil_div(cols, 32), 3);
-  sum_parts3_kernel<<<grid, 256, 0, st>>>(part, nparts, cols, o0, o1, o2);
+  sum_parts3_kernel<<<grid, 256, 0, st>>>(part, nparts, cols, o0, o1, o2, accumulate);
   return launch_check("sum_parts3");
 }
 
@@ -576,152 +595,218 @@ nnt_status launch_colsum(const void* a, int a_dtype, int64_t rows, int64_t cols,
 // causal softmax over score rows (scores already scaled by 1/sqrt(hd))
 // =====================================================================
 
-template <int TPR, int MAXV, typename T>
-__global__ void softmax_fwd_kernel(const float* __restrict__ s, T* __restrict__ p, int64_t S,
-                                   ZMap zm, int nz, int q0, int nq) {
-  __shared__ float red[32];
-  const int rpc = blockDim.x / TPR;
-  const int lane = threadIdx.x % TPR;
-  const int64_t r = (int64_t)blockIdx.x * rpc + threadIdx.x / TPR;
-  const bool active = r < (int64_t)nz * nq;
-  const int64_t rr = active ? r : 0;
-  const int q = q0 + (int)(rr % nq);
-  const int64_t z = zm.z((int)(rr / nq));
+// One warp per score row. Rows of up to 1024 causal entries stay in registers
+// (8 float4 per lane); longer rows are swept in 1024-entry segments with an
+// online (max, sum) and re-read (from L2) for the output. Only the q+1 valid
+// entries are loaded and exponentiated; entries past q up to the 128-key block
+// boundary are written as 0. No block-level barriers.
+template <typename T>
+__global__ void __launch_bounds__(256) softmax_fwd_kernel(const float* __restrict__ s,
+                                                          T* __restrict__ p, int64_t S, ZMap zm,
+                                                          int nz, int q0, int nq) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= (int64_t)nz * nq) return;
+  const int q = q0 + (int)(r % nq);
+  const int64_t z = zm.z((int)(r / nq));
   const float* sr = s + (z * S + q) * S;
   T* pr = p + (z * S + q) * S;
   const int valid = q + 1;
   const int wend = (int)std::min<int64_t>(S, round_up(valid, kCausalBlock));
-  const int nvv = (valid + 3) >> 2;
-  float4 v[MAXV];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int c = lane + i * TPR;
-    if (active && c < nvv) {
-      v[i] = load4_stream(sr + 4 * c);
-      if (4 * c + 1 > q) v[i].y = -INFINITY;
-      if (4 * c + 2 > q) v[i].z = -INFINITY;
-      if (4 * c + 3 > q) v[i].w = -INFINITY;
-      mx = fmaxf(mx, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
-    } else {
-      v[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-  }
-  mx = group_max<TPR>(mx, red);
-  const float ms = mx * kLog2e;
-  float sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    v[i].x = exp2f(v[i].x * kLog2e - ms);
-    v[i].y = exp2f(v[i].y * kLog2e - ms);
-    v[i].z = exp2f(v[i].z * kLog2e - ms);
-    v[i].w = exp2f(v[i].w * kLog2e - ms);
-    sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-  }
-  sum = group_sum<TPR>(sum, red);
-  if (!active) return;
-  const float inv = 1.0f / sum;
+  const int nvv = (valid + 3) >> 2;  // float4 groups holding valid entries
   const int nw = wend >> 2;
+  if (nvv <= 256) {
+    float4 v[8];
+    float mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int c = lane + i * TPR;
-    if (c < nw) {
-      float4 o = make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv);
-      store4(pr + 4 * c, o);  // masked lanes hold exp2(-inf) = 0
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvv) {
+        v[i] = load4_stream(sr + 4 * c);
+        if (4 * c + 1 > q) v[i].y = -INFINITY;
+        if (4 * c + 2 > q) v[i].z = -INFINITY;
+        if (4 * c + 3 > q) v[i].w = -INFINITY;
+        mx = fmaxf(mx, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
+      }
     }
+    mx = warp_max(mx);
+    const float ms = mx * kLog2e;
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvv) {
+        v[i].x = exp2f(v[i].x * kLog2e - ms);
+        v[i].y = exp2f(v[i].y * kLog2e - ms);
+        v[i].z = exp2f(v[i].z * kLog2e - ms);
+        v[i].w = exp2f(v[i].w * kLog2e - ms);
+        sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      }
+    }
+    const float inv = 1.0f / warp_sum(sum);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvv) store4(pr + 4 * c, make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv));
+      else if (c < nw) store4(pr + 4 * c, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    return;
+  }
+  // long rows: online max/sum over the valid entries, then a second sweep
+  float mx = -INFINITY, sum = 0.f;
+  for (int c = lane; c < nvv; c += 32) {
+    float4 v = load4(sr + 4 * c);
+    if (4 * c + 1 > q) v.y = -INFINITY;
+    if (4 * c + 2 > q) v.z = -INFINITY;
+    if (4 * c + 3 > q) v.w = -INFINITY;
+    const float lm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (lm > mx) {
+      sum *= exp2f((mx - lm) * kLog2e);
+      mx = lm;
+    }
+    sum += exp2f((v.x - mx) * kLog2e) + exp2f((v.y - mx) * kLog2e) + exp2f((v.z - mx) * kLog2e) +
+           exp2f((v.w - mx) * kLog2e);
+  }
+  const float M = warp_max(mx);
+  sum = (mx == -INFINITY) ? 0.f : sum * exp2f((mx - M) * kLog2e);
+  const float inv = 1.0f / warp_sum(sum);
+  const float ms = M * kLog2e;
+  for (int c = lane; c < nw; c += 32) {
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nvv) {
+      const float4 v = load4(sr + 4 * c);
+      o.x = exp2f(v.x * kLog2e - ms) * inv;
+      o.y = 4 * c + 1 > q ? 0.f : exp2f(v.y * kLog2e - ms) * inv;
+      o.z = 4 * c + 2 > q ? 0.f : exp2f(v.z * kLog2e - ms) * inv;
+      o.w = 4 * c + 3 > q ? 0.f : exp2f(v.w * kLog2e - ms) * inv;
+    }
+    store4(pr + 4 * c, o);
   }
 }
 
-template <int TPR, int MAXV, typename T>
-__global__ void softmax_bwd_kernel(const T* __restrict__ p, const float* __restrict__ dp,
-                                   T* __restrict__ ds, int64_t S, ZMap zm, int nz, int q0, int nq,
-                                   float scale) {
-  __shared__ float red[32];
-  const int rpc = blockDim.x / TPR;
-  const int lane = threadIdx.x % TPR;
-  const int64_t r = (int64_t)blockIdx.x * rpc + threadIdx.x / TPR;
-  const bool active = r < (int64_t)nz * nq;
-  const int64_t rr = active ? r : 0;
-  const int q = q0 + (int)(rr % nq);
-  const int64_t z = zm.z((int)(rr / nq));
+// Four entries of a probability row kept in their storage type (bf16 rows
+// stay packed in two registers) and widened when used.
+template <typename T> struct Raw4;
+template <> struct Raw4<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ float4 get() const { return v; }
+};
+template <> struct Raw4<bf16> {
+  uint2 u;
+  __device__ __forceinline__ void load(const bf16* p) { u = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ float4 get() const {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+};
+
+// dS = scale * P * (dP - rowsum(dP * P)) over the valid entries, 0 beyond q up
+// to the block boundary; one warp per row, as the forward. The register path
+// keeps P (in its storage type) and P*dP, so dS = scale * (P*dP - P*dot).
+template <typename T>
+__global__ void __launch_bounds__(256, 3) softmax_bwd_kernel(const T* __restrict__ p,
+                                                             const float* __restrict__ dp,
+                                                             T* __restrict__ ds, int64_t S, ZMap zm,
+                                                             int nz, int q0, int nq, float scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= (int64_t)nz * nq) return;
+  const int q = q0 + (int)(r % nq);
+  const int64_t z = zm.z((int)(r / nq));
   const int64_t off = (z * S + q) * S;
   const int valid = q + 1;
   const int wend = (int)std::min<int64_t>(S, round_up(valid, kCausalBlock));
   const int nvv = (valid + 3) >> 2;
-  float4 pv[MAXV], dv[MAXV];
-  float dot = 0.f;
-#pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int c = lane + i * TPR;
-    if (active && c < nvv) {
-      pv[i] = load4(p + off + 4 * c);
-      dv[i] = load4_stream(dp + off + 4 * c);
-      // P is exactly 0 beyond q; clear dP there too so 0*garbage cannot leak in
-      if (4 * c + 1 > q) { pv[i].y = 0.f; dv[i].y = 0.f; }
-      if (4 * c + 2 > q) { pv[i].z = 0.f; dv[i].z = 0.f; }
-      if (4 * c + 3 > q) { pv[i].w = 0.f; dv[i].w = 0.f; }
-      dot += (pv[i].x * dv[i].x + pv[i].y * dv[i].y) + (pv[i].z * dv[i].z + pv[i].w * dv[i].w);
-    } else {
-      pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dv[i] = pv[i];
-    }
-  }
-  dot = group_sum<TPR>(dot, red);
-  if (!active) return;
   const int nw = wend >> 2;
+  auto masked = [q](float4& a, int c) {
+    if (4 * c + 1 > q) a.y = 0.f;
+    if (4 * c + 2 > q) a.z = 0.f;
+    if (4 * c + 3 > q) a.w = 0.f;
+  };
+  if (nvv <= 256) {
+    Raw4<T> pr[8];
+    float4 pd[8];
+    float dot = 0.f;
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int c = lane + i * TPR;
-    if (c < nw) {
-      float4 o;
-      o.x = scale * pv[i].x * (dv[i].x - dot);
-      o.y = scale * pv[i].y * (dv[i].y - dot);
-      o.z = scale * pv[i].z * (dv[i].z - dot);
-      o.w = scale * pv[i].w * (dv[i].w - dot);
-      store4(ds + off + 4 * c, o);
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvv) {
+        pr[i].load(p + off + 4 * c);
+        pd[i] = load4_stream(dp + off + 4 * c);
+      }
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvv) {
+        float4 a = pr[i].get();
+        masked(a, c);
+        masked(pd[i], c);  // P is 0 past q; clear dP there too so 0*garbage cannot leak in
+        pd[i] = make_float4(a.x * pd[i].x, a.y * pd[i].y, a.z * pd[i].z, a.w * pd[i].w);
+        dot += (pd[i].x + pd[i].y) + (pd[i].z + pd[i].w);
+      }
+    }
+    dot = warp_sum(dot);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvv) {
+        float4 a = pr[i].get();
+        masked(a, c);
+        store4(ds + off + 4 * c, make_float4(scale * (pd[i].x - a.x * dot), scale * (pd[i].y - a.y * dot),
+                                             scale * (pd[i].z - a.z * dot), scale * (pd[i].w - a.w * dot)));
+      } else if (c < nw) {
+        store4(ds + off + 4 * c, make_float4(0.f, 0.f, 0.f, 0.f));
+      }
+    }
+    return;
   }
-}
-
-// Threads per row such that a row needs at most 4 float4 per thread: fewer
-// registers, so more rows (and more loads) are in flight per SM.
-static int softmax_tpr(int64_t S) {
-  int tpr = 32;
-  while ((int64_t)tpr * 4 * 4 < S && tpr < 1024) tpr <<= 1;
-  return tpr;
+  float dot = 0.f;
+  for (int c = lane; c < nvv; c += 32) {
+    float4 a = load4(p + off + 4 * c), b = load4(dp + off + 4 * c);
+    masked(a, c);
+    masked(b, c);
+    dot += (a.x * b.x + a.y * b.y) + (a.z * b.z + a.w * b.w);
+  }
+  dot = warp_sum(dot);
+  for (int c = lane; c < nw; c += 32) {
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nvv) {
+      float4 a = load4(p + off + 4 * c), b = load4(dp + off + 4 * c);
+      masked(a, c);
+      masked(b, c);
+      o = make_float4(scale * a.x * (b.x - dot), scale * a.y * (b.y - dot), scale * a.z * (b.z - dot),
+                      scale * a.w * (b.w - dot));
+    }
+    store4(ds + off + 4 * c, o);
+  }
 }
 
 nnt_status launch_softmax_fwd(const float* s, void* p, int64_t S, ZMap zm, int nz, int q0, int nq,
                               int act_dtype, cudaStream_t st) {
-  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 16384, "softmax: seq must be a multiple of 4 <= 16384");
+  NNT_CHECK_ARG(S % 4 == 0 && S > 0, "softmax: seq must be a positive multiple of 4");
   const int64_t rows = (int64_t)nz * nq;
   if (rows == 0) return NNT_OK;
-  const int tpr = softmax_tpr(S);
-  const int block = std::max(256, tpr);
-  const int64_t grid = ceil_div(rows, block / tpr);
-  NNT_TPR_DISPATCH(tpr, {
-    if (act_dtype == NNT_BF16)
-      softmax_fwd_kernel<TPR, 4, bf16><<<grid, block, 0, st>>>(s, (bf16*)p, S, zm, nz, q0, nq);
-    else
-      softmax_fwd_kernel<TPR, 4, float><<<grid, block, 0, st>>>(s, (float*)p, S, zm, nz, q0, nq);
-  });
+  const int64_t grid = ceil_div(rows, 8);
+  if (act_dtype == NNT_BF16)
+    softmax_fwd_kernel<bf16><<<grid, 256, 0, st>>>(s, (bf16*)p, S, zm, nz, q0, nq);
+  else
+    softmax_fwd_kernel<float><<<grid, 256, 0, st>>>(s, (float*)p, S, zm, nz, q0, nq);
   return launch_check("softmax_fwd");
 }
 
 nnt_status launch_softmax_bwd(const void* p, const float* dp, void* ds, int64_t S, ZMap zm, int nz,
                               int q0, int nq, float scale, int act_dtype, cudaStream_t st) {
-  NNT_CHECK_ARG(S % 4 == 0 && S > 0 && S <= 16384, "softmax bwd: seq must be a multiple of 4 <= 16384");
+  NNT_CHECK_ARG(S % 4 == 0 && S > 0, "softmax bwd: seq must be a positive multiple of 4");
   const int64_t rows = (int64_t)nz * nq;
   if (rows == 0) return NNT_OK;
-  const int tpr = softmax_tpr(S);
-  const int block = std::max(256, tpr);
-  const int64_t grid = ceil_div(rows, block / tpr);
-  NNT_TPR_DISPATCH(tpr, {
-    if (act_dtype == NNT_BF16)
-      softmax_bwd_kernel<TPR, 4, bf16><<<grid, block, 0, st>>>((const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
-    else
-      softmax_bwd_kernel<TPR, 4, float><<<grid, block, 0, st>>>((const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
-  });
+  const int64_t grid = ceil_div(rows, 8);
+  if (act_dtype == NNT_BF16)
+    softmax_bwd_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
+  else
+    softmax_bwd_kernel<float><<<grid, 256, 0, st>>>((const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
   return launch_check("softmax_bwd");
 }
 
@@ -802,15 +887,26 @@ __global__ void __launch_bounds__(512) cross_entropy_kernel(
   const float* zr = z + r * ldz;
   const int64_t n4 = cols >> 2;  // full float4s
   float m = -INFINITY, s = 0.f;
-  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
-    float4 v = load4(zr + 4 * i);
-    float lm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  // four float4 per thread in flight per iteration, then the online update
+  const int64_t bs = blockDim.x;
+  for (int64_t i0 = threadIdx.x; i0 < n4; i0 += 4 * bs) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = (i0 + u * bs < n4) ? load4(zr + 4 * (i0 + u * bs))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float lm = m;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) lm = fmaxf(lm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
     if (lm > m) {
       s *= exp2f((m - lm) * kLog2e);
       m = lm;
     }
-    s += exp2f((v.x - m) * kLog2e) + exp2f((v.y - m) * kLog2e) + exp2f((v.z - m) * kLog2e) +
-         exp2f((v.w - m) * kLog2e);
+    const float ms = m * kLog2e;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      s += exp2f(v[u].x * kLog2e - ms) + exp2f(v[u].y * kLog2e - ms) + exp2f(v[u].z * kLog2e - ms) +
+           exp2f(v[u].w * kLog2e - ms);
   }
   for (int64_t c = 4 * n4 + threadIdx.x; c < cols; c += blockDim.x) {
     float v = zr[c];
@@ -850,6 +946,7 @@ __global__ void __launch_bounds__(512) cross_entropy_kernel(
   if (threadIdx.x == 0) row_loss[r] = lse - zr[y];
   const float ls = lse * kLog2e;
   T* dr = dz + r * lddz;
+#pragma unroll 4
   for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
     float4 v = load4(zr + 4 * i);
     float4 o;
@@ -922,17 +1019,24 @@ nnt_status launch_mean_loss(const float* row_loss, int64_t rows, float* loss, cu
 // AdamW (decoupled weight decay), fp32 state, optional bf16 copy out
 // =====================================================================
 
+// Every operation is rounded explicitly (no contraction left to the compiler),
+// so each instantiation of the kernel below -- and thus the device-moment and
+// host-moment paths -- produces the same bits for the same inputs.
 __device__ __forceinline__ void adamw_one(float& w, float g, float& m, float& v, float lr, float b1,
                                           float b2, float eps, float wd, float bc1, float bc2) {
-  m = b1 * m + (1.f - b1) * g;
-  v = b2 * v + (1.f - b2) * g * g;
-  const float mhat = m / bc1;
-  const float vhat = v / bc2;
-  w = w - lr * wd * w - lr * mhat / (sqrtf(vhat) + eps);
+  m = __fmaf_rn(b1, m, __fmul_rn(1.f - b1, g));
+  v = __fmaf_rn(b2, v, __fmul_rn(__fmul_rn(1.f - b2, g), g));
+  const float mhat = __fdiv_rn(m, bc1);
+  const float vhat = __fdiv_rn(v, bc2);
+  const float decay = __fmul_rn(__fmul_rn(lr, wd), w);
+  const float step = __fdiv_rn(__fmul_rn(lr, mhat), __fadd_rn(__fsqrt_rn(vhat), eps));
+  w = __fsub_rn(__fsub_rn(w, decay), step);
 }
 
-// hyper (optional, device): lr, beta1, beta2, eps, wd, bc1, bc2 -- overrides the
-// by-value arguments so a captured graph can be replayed with new values.
+// hyper (optional, device): lr, beta1, beta2, eps, wd, bc1, bc2, gscale --
+// overrides the by-value arguments so a captured graph can be replayed with new
+// values. The gradient used is g * gscale (1 for a single backward; 1/k for the
+// sum of k accumulated minibatch gradients, i.e. their mean).
 // UNROLL float4 groups per thread per iteration: all their loads are issued
 // before any math, which keeps enough bytes in flight when m and v sit behind
 // the slower host link.
@@ -941,9 +1045,10 @@ __global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
                              float* __restrict__ m, float* __restrict__ v, bf16* __restrict__ wb,
                              int64_t n, float lr, float b1, float b2, float eps, float wd,
                              float bc1, float bc2, const float* __restrict__ hyper) {
+  float gs = 1.f;
   if (hyper) {
     lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; eps = hyper[3]; wd = hyper[4];
-    bc1 = hyper[5]; bc2 = hyper[6];
+    bc1 = hyper[5]; bc2 = hyper[6]; gs = hyper[7];
   }
   const int64_t n4 = n >> 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -963,10 +1068,10 @@ __global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t i = i0 + u * stride;
       if (i < n4) {
-        adamw_one(W[u].x, G[u].x, M[u].x, V[u].x, lr, b1, b2, eps, wd, bc1, bc2);
-        adamw_one(W[u].y, G[u].y, M[u].y, V[u].y, lr, b1, b2, eps, wd, bc1, bc2);
-        adamw_one(W[u].z, G[u].z, M[u].z, V[u].z, lr, b1, b2, eps, wd, bc1, bc2);
-        adamw_one(W[u].w, G[u].w, M[u].w, V[u].w, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].x, __fmul_rn(G[u].x, gs), M[u].x, V[u].x, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].y, __fmul_rn(G[u].y, gs), M[u].y, V[u].y, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].z, __fmul_rn(G[u].z, gs), M[u].z, V[u].z, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(W[u].w, __fmul_rn(G[u].w, gs), M[u].w, V[u].w, lr, b1, b2, eps, wd, bc1, bc2);
         store4_stream(w + 4 * i, W[u]);
         store4_stream(m + 4 * i, M[u]);
         store4_stream(v + 4 * i, V[u]);
@@ -978,7 +1083,7 @@ __global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
   const int64_t t = 4 * n4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (t < n) {
     float W = w[t], M = m[t], V = v[t];
-    adamw_one(W, g[t], M, V, lr, b1, b2, eps, wd, bc1, bc2);
+    adamw_one(W, __fmul_rn(g[t], gs), M, V, lr, b1, b2, eps, wd, bc1, bc2);
     w[t] = W;
     m[t] = M;
     v[t] = V;

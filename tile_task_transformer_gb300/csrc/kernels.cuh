@@ -31,14 +31,16 @@ nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* me
                                 const float* rstd, const float* g, const float* resid, float* dx,
                                 void* dx_act, int64_t rows, int cols, int act_dtype,
                                 cudaStream_t st);
-// dg = sum_rows dy*xhat, db = sum_rows dy and (out != NULL) dbias = sum_rows out,
-// in a fixed order; part: scratch of ln_colsum_chunks(rows) * 3 * cols floats
+// dg (+)= sum_rows dy*xhat, db (+)= sum_rows dy and (out != NULL) dbias (+)=
+// sum_rows out, in a fixed order; part: scratch of ln_colsum_chunks(rows) * 3 *
+// cols floats
 int64_t ln_colsum_chunks(int64_t rows);
 nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* mean,
                                  const float* rstd, const float* out, int64_t rows, int cols,
-                                 float* part, float* dg, float* db, float* dbias, cudaStream_t st);
+                                 float* part, float* dg, float* db, float* dbias, int accumulate,
+                                 cudaStream_t st);
 nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, float* o0, float* o1,
-                             float* o2, cudaStream_t st);
+                             float* o2, int accumulate, cudaStream_t st);
 
 // out[c] (=|+=) sum over p of part[p][c], p in increasing order
 nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,
@@ -74,8 +76,8 @@ nnt_status launch_adamw(float* w, const float* g, float* m, float* v, bf16* w_bf
                         float lr, float b1, float b2, float eps, float wd, float bc1, float bc2,
                         cudaStream_t st);
 
-// same, hyper-parameters read on the device from hyper_dev[0..6] =
-// (lr, beta1, beta2, eps, weight_decay, 1-beta1^t, 1-beta2^t)
+// same, hyper-parameters read on the device from hyper_dev[0..7] =
+// (lr, beta1, beta2, eps, weight_decay, 1-beta1^t, 1-beta2^t, gradient scale)
 // max_ctas > 0 caps the grid (moments in host memory: a few CTAs keep NVLink-C2C
 // busy without taking SMs from concurrent tasks)
 nnt_status launch_adamw_dev(float* w, const float* g, float* m, float* v, bf16* w_bf16, int64_t n,

@@ -74,8 +74,11 @@ struct Chunk {
   int64_t mv_off = -1;     // offset in the device or host moment pool
 };
 
+// graph slot of the accumulating backward (0-3: forward, backward, AdamW, fused)
+constexpr int kSlotBwdAcc = 8;
+
 struct AdamHyperDev {
-  float lr, b1, b2, eps, wd, bc1, bc2, pad;
+  float lr, b1, b2, eps, wd, bc1, bc2, gscale;
 };
 
 thread_local std::string t_model_err;
@@ -153,9 +156,11 @@ struct nnt_model {
   uint64_t h2d_bytes = 0, d2h_bytes = 0;
 
   Program fwd, bwd, bwdf, opt;
+  Program bwda;  // backward that adds into the gradients (minibatch accumulation)
   Executor ex;
   cudaEvent_t done_event = nullptr;
   int state = 0;  // 0: created, 1: forward done, 2: backward done
+  int n_acc = 0;  // minibatch gradients summed in the gradient buffers since the last update
   int64_t step = 0;
   double last_fwd_ms = 0, last_bwd_ms = 0, last_opt_ms = 0;
 };
@@ -842,8 +847,12 @@ void build_forward(nnt_model* m) {
 // its gradient is final and every task that reads the old weights has been
 // issued (weight reads are declared, so the executor orders the update after
 // them); moments in pinned host memory are updated in place over NVLink-C2C.
-void build_backward(nnt_model* m, Program& P, bool fused) {
+// fused: each chunk's AdamW update follows its final gradient. acc (not with
+// fused): every gradient write adds to the stored gradient instead of
+// replacing it.
+void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
   Builder b{m};
+  const int GW = acc ? ACC_RW : ACC_W;  // access of the tasks that write parameter gradients
   const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
   const size_t as = m->act_size;
   const int act = m->act;
@@ -934,10 +943,11 @@ void build_backward(nnt_model* m, Program& P, bool fused) {
         g.A = dY; g.lda = ldy; g.a_trans = 1;
         g.B = X; g.ldb = ldx; g.b_trans = 1;
         g.C = pg(m, W); g.ldc = Nin; g.c_dtype = NNT_F32;
+        g.beta = acc ? 1 : 0;
         std::vector<TileUse> u;
         box(u, gdY, ACC_R);
         box(u, gX, ACC_R);
-        box(u, m->ggrad[gidx], ACC_W, ot0, ot1, it0, it1);
+        box(u, m->ggrad[gidx], GW, ot0, ot1, it0, it1);
         b.gemm_task(P, TT_GEMM_DW, g, std::move(u), 2.0 * (o1 - o0) * (i1 - i0) * T);
       }
   };
@@ -947,11 +957,12 @@ void build_backward(nnt_model* m, Program& P, bool fused) {
     t.kernels = 2;
     box(t.uses, ga, ACC_R);
     box(t.uses, m->gcol_part, ACC_RW);
-    box(t.uses, m->ggrad[gidx], ACC_W);
+    box(t.uses, m->ggrad[gidx], GW);
     t.bytes = (double)T * N * (a_dtype == NNT_BF16 ? 2 : 4);
     float* out = pg(m, bp);
+    const int accum = acc ? 1 : 0;
     t.fn = [=](cudaStream_t s) {
-      return launch_colsum(a, a_dtype, T, N, N, m->col_part, out, 0, s);
+      return launch_colsum(a, a_dtype, T, N, N, m->col_part, out, accum, s);
     };
     P.add(std::move(t));
     adam_param(gidx);
@@ -989,16 +1000,17 @@ void build_backward(nnt_model* m, Program& P, bool fused) {
     box(t.uses, gst, ACC_R);
     box(t.uses, m->gdres, ACC_R);
     box(t.uses, m->gln_part, ACC_RW);
-    box(t.uses, m->ggrad[gidx_g], ACC_W);
-    box(t.uses, m->ggrad[gidx_b], ACC_W);
-    if (bias_idx >= 0) box(t.uses, m->ggrad[bias_idx], ACC_W);
+    box(t.uses, m->ggrad[gidx_g], GW);
+    box(t.uses, m->ggrad[gidx_b], GW);
+    if (bias_idx >= 0) box(t.uses, m->ggrad[bias_idx], GW);
     t.bytes = (double)T * d * 4 * (bias_idx >= 0 ? 3 : 2);
     float* og = pg(m, gm);
     float* ob = pg(m, bt_);
     float* obias = bias_idx >= 0 ? pg(m, m->params[bias_idx]) : nullptr;
+    const int accum = acc ? 1 : 0;
     t.fn = [=](cudaStream_t s) {
       return launch_ln_bwd_colsums(dy, xin, mu, rs, obias ? m->dres : nullptr, T, d, m->ln_part_g, og,
-                                   ob, obias, s);
+                                   ob, obias, accum, s);
     };
     P.add(std::move(t));
     adam_param(gidx_g);
@@ -1033,10 +1045,11 @@ void build_backward(nnt_model* m, Program& P, bool fused) {
       g.A = m->dz; g.lda = m->lddz; g.a_trans = 1;
       g.B = m->y; g.ldb = d; g.b_trans = 1;
       g.C = pg(m, m->params[0]); g.ldc = d; g.c_dtype = NNT_F32;
+      g.beta = acc ? 1 : 0;
       std::vector<TileUse> u;
       box(u, m->gdz, ACC_R);
       box(u, m->gy, ACC_R);
-      box(u, m->ggrad[0], ACC_W, vt, vt + 1, t0, t1);
+      box(u, m->ggrad[0], GW, vt, vt + 1, t0, t1);
       b.gemm_task(P, TT_GEMM_LM_DW, g, std::move(u), 2.0 * (v1 - v0) * (c1 - c0) * T);
     }
   // final LN backward (no residual input: dres starts here)
@@ -1230,11 +1243,12 @@ void build_backward(nnt_model* m, Program& P, bool fused) {
     Task t;
     t.type = TT_WPE_GRAD;
     for (int bt = 0; bt < m->n_bt; ++bt) box(t.uses, m->gdres, ACC_R, bt * m->n_st + st, bt * m->n_st + st + 1);
-    box(t.uses, m->ggrad[1], ACC_W, st, st + 1);
+    box(t.uses, m->ggrad[1], GW, st, st + 1);
     t.bytes = (double)T / m->n_st * d * 4 + (double)m->ts * d * 4;
     const int s0 = st * m->ts;
-    t.fn = [m, s0](cudaStream_t s) {
-      return launch_wpe_grad(m->dres, m->tm, m->B, s0, m->ts, m->d, pg(m, m->params[1]), 0, s);
+    const int accum = acc ? 1 : 0;
+    t.fn = [m, s0, accum](cudaStream_t s) {
+      return launch_wpe_grad(m->dres, m->tm, m->B, s0, m->ts, m->d, pg(m, m->params[1]), accum, s);
     };
     P.add(std::move(t));
   }
@@ -1355,6 +1369,77 @@ void free_model(nnt_model* m) {
   if (owned && own) cudaStreamDestroy(own);
 }
 
+// Learning rate of AdamW iteration t (1-based) under the README's warm-up
+// flags: --start-lr is the rate of the first iteration and --full-lr-iter the
+// iteration from which the full --lr applies. The pages do not say how the
+// rate moves in between; it is read as a straight line from start_lr at t = 1
+// to lr at t = full_lr_iter. full_lr_iter <= 1 means the full rate throughout.
+double scheduled_lr(const nnt_adamw* hp, int64_t t) {
+  if (hp->full_lr_iter <= 1 || t >= hp->full_lr_iter) return hp->lr;
+  const double frac = (double)(t - 1) / (double)(hp->full_lr_iter - 1);
+  return (double)hp->start_lr + ((double)hp->lr - (double)hp->start_lr) * frac;
+}
+
+bool valid_adamw(const nnt_adamw* hp) {
+  if (!(hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1) ||
+      !(hp->eps > 0) || !(hp->weight_decay >= 0) || !(hp->start_lr >= 0) || hp->full_lr_iter < 0) {
+    set_thread_error("invalid AdamW hyper-parameters");
+    return false;
+  }
+  return true;
+}
+
+// Device copy of the hyper-parameters of iteration t: the captured AdamW
+// graphs read them from there, so one graph serves every step.
+nnt_status upload_hyper(nnt_model* m, const nnt_adamw* hp, int64_t t, float gscale) {
+  AdamHyperDev& h = m->hyper_host;
+  h.lr = (float)scheduled_lr(hp, t);
+  h.b1 = hp->beta1; h.b2 = hp->beta2; h.eps = hp->eps; h.wd = hp->weight_decay;
+  h.bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
+  h.bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
+  h.gscale = gscale;
+  if (cudaMemcpyAsync(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_) != cudaSuccess) {
+    set_thread_error("hyper-parameter upload failed: %s", cudaGetErrorString(cudaGetLastError()));
+    return NNT_ERR_CUDA;
+  }
+  return NNT_OK;
+}
+
+// nnt_backward (acc = false) and nnt_backward_accumulate (acc = true).
+nnt_status run_backward(nnt_model* m, bool acc, const char* who) {
+  if (!m) {
+    set_thread_error("NULL model");
+    return fail(m, NNT_ERR_INVALID_ARG);
+  }
+  if (m->state != 1) {
+    set_thread_error("%s needs a preceding nnt_forward", who);
+    return fail(m, NNT_ERR_STATE);
+  }
+  if (m->offload) {
+    set_thread_error("this model offloads AdamW moments: gradients are not kept whole; use "
+                     "nnt_backward_adamw");
+    return fail(m, NNT_ERR_STATE);
+  }
+  // the first minibatch after an update writes the gradients, later ones add
+  const bool add = acc && m->n_acc > 0;
+  auto t0 = std::chrono::steady_clock::now();
+  nnt_status s = add ? m->ex.run(m->bwda, m->opts.use_cuda_graph ? kSlotBwdAcc : -1)
+                     : m->ex.run(m->bwd, m->opts.use_cuda_graph ? 1 : -1);
+  if (s != NNT_OK) {
+    m->n_acc = 0;  // the gradients are no longer a known sum
+    return fail(m, s);
+  }
+  m->n_acc = add ? m->n_acc + 1 : 1;
+  m->state = 2;
+  if (m->opts.trace) {
+    s = sync_model(m);
+    if (s == NNT_OK) s = m->ex.collect_trace(add ? m->bwda : m->bwd);
+    if (s != NNT_OK) return fail(m, s);
+    m->last_bwd_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  }
+  return NNT_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -1415,7 +1500,10 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
   if (s == NNT_OK) {
     make_grids(m);
     build_forward(m);
-    if (!m->offload) build_backward(m, m->bwd, false);
+    if (!m->offload) {
+      build_backward(m, m->bwd, false);
+      build_backward(m, m->bwda, false, true);
+    }
     build_backward(m, m->bwdf, true);
     build_optimizer(m);
     m->fwd.finalize(m->opts.n_streams);
@@ -1471,31 +1559,10 @@ nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_d
   return NNT_OK;
 }
 
-nnt_status nnt_backward(nnt_model* m) {
-  if (!m) {
-    set_thread_error("NULL model");
-    return fail(m, NNT_ERR_INVALID_ARG);
-  }
-  if (m->state != 1) {
-    set_thread_error("nnt_backward needs a preceding nnt_forward");
-    return fail(m, NNT_ERR_STATE);
-  }
-  if (m->offload) {
-    set_thread_error("this model offloads AdamW moments: gradients are not kept whole; use "
-                     "nnt_backward_adamw");
-    return fail(m, NNT_ERR_STATE);
-  }
-  auto t0 = std::chrono::steady_clock::now();
-  nnt_status s = m->ex.run(m->bwd, m->opts.use_cuda_graph ? 1 : -1);
-  if (s != NNT_OK) return fail(m, s);
-  m->state = 2;
-  if (m->opts.trace) {
-    s = sync_model(m);
-    if (s == NNT_OK) s = m->ex.collect_trace(m->bwd);
-    if (s != NNT_OK) return fail(m, s);
-    m->last_bwd_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
-  }
-  return NNT_OK;
+nnt_status nnt_backward(nnt_model* m) { return run_backward(m, false, "nnt_backward"); }
+
+nnt_status nnt_backward_accumulate(nnt_model* m) {
+  return run_backward(m, true, "nnt_backward_accumulate");
 }
 
 nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp) {
@@ -1503,32 +1570,23 @@ nnt_status nnt_adamw_step(nnt_model* m, const nnt_adamw* hp) {
     set_thread_error("NULL model or hyper-parameters");
     return fail(m, NNT_ERR_INVALID_ARG);
   }
-  if (m->state != 2) {
-    set_thread_error("nnt_adamw_step needs a preceding nnt_backward");
+  if (m->n_acc < 1) {
+    set_thread_error("nnt_adamw_step needs a preceding nnt_backward or nnt_backward_accumulate");
     return fail(m, NNT_ERR_STATE);
   }
   if (m->offload) {
     set_thread_error("this model offloads AdamW moments; use nnt_backward_adamw");
     return fail(m, NNT_ERR_STATE);
   }
-  if (!(hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1) ||
-      !(hp->eps > 0) || !(hp->weight_decay >= 0)) {
-    set_thread_error("invalid AdamW hyper-parameters");
-    return fail(m, NNT_ERR_INVALID_ARG);
-  }
+  if (!valid_adamw(hp)) return fail(m, NNT_ERR_INVALID_ARG);
   auto t0 = std::chrono::steady_clock::now();
   const int64_t t = m->step + 1;
-  AdamHyperDev& h = m->hyper_host;
-  h.lr = hp->lr; h.b1 = hp->beta1; h.b2 = hp->beta2; h.eps = hp->eps; h.wd = hp->weight_decay;
-  h.bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
-  h.bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
-  h.pad = 0;
-  if (cudaMemcpyAsync(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_) != cudaSuccess)
-    return fail(m, NNT_ERR_CUDA);
+  if (upload_hyper(m, hp, t, 1.0f / (float)m->n_acc) != NNT_OK) return fail(m, NNT_ERR_CUDA);
   nnt_status s = m->ex.run(m->opt, m->opts.use_cuda_graph ? 2 : -1);
   if (s != NNT_OK) return fail(m, s);
   m->step = t;
   m->state = 0;
+  m->n_acc = 0;
   if (m->opts.trace) {
     s = sync_model(m);
     if (s == NNT_OK) s = m->ex.collect_trace(m->opt);
@@ -1547,20 +1605,15 @@ nnt_status nnt_backward_adamw(nnt_model* m, const nnt_adamw* hp) {
     set_thread_error("nnt_backward_adamw needs a preceding nnt_forward");
     return fail(m, NNT_ERR_STATE);
   }
-  if (!(hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1) ||
-      !(hp->eps > 0) || !(hp->weight_decay >= 0)) {
-    set_thread_error("invalid AdamW hyper-parameters");
-    return fail(m, NNT_ERR_INVALID_ARG);
+  if (m->n_acc > 0) {
+    set_thread_error("nnt_backward_adamw cannot add to accumulated gradients: finish the "
+                     "accumulation with nnt_backward_accumulate + nnt_adamw_step");
+    return fail(m, NNT_ERR_STATE);
   }
+  if (!valid_adamw(hp)) return fail(m, NNT_ERR_INVALID_ARG);
   auto t0 = std::chrono::steady_clock::now();
   const int64_t t = m->step + 1;
-  AdamHyperDev& h = m->hyper_host;
-  h.lr = hp->lr; h.b1 = hp->beta1; h.b2 = hp->beta2; h.eps = hp->eps; h.wd = hp->weight_decay;
-  h.bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
-  h.bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
-  h.pad = 0;
-  if (cudaMemcpyAsync(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_) != cudaSuccess)
-    return fail(m, NNT_ERR_CUDA);
+  if (upload_hyper(m, hp, t, 1.0f) != NNT_OK) return fail(m, NNT_ERR_CUDA);
   nnt_status s = m->ex.run(m->bwdf, m->opts.use_cuda_graph ? 3 : -1);
   if (s != NNT_OK) return fail(m, s);
   m->step = t;

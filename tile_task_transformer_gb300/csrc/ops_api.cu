@@ -81,7 +81,7 @@ nnt_status nnt_op_layernorm_bwd(const float* dy_dev, const float* x_dev, const f
     void* part = nullptr;
     NNT_TRY(scratch((size_t)ln_colsum_chunks(rows) * 3 * cols * 4, &part));
     NNT_TRY(launch_ln_bwd_colsums(dy_dev, x_dev, mean_dev, rstd_dev, nullptr, rows, (int)cols,
-                                  (float*)part, dg_dev, db_dev, nullptr, st));
+                                  (float*)part, dg_dev, db_dev, nullptr, 0, st));
   }
   return NNT_OK;
 }

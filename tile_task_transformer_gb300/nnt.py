@@ -51,7 +51,7 @@ class Options(C.Structure):
 
 class AdamW(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
-                ("weight_decay", C.c_float)]
+                ("weight_decay", C.c_float), ("start_lr", C.c_float), ("full_lr_iter", C.c_int32)]
 
 
 class Stats(C.Structure):
@@ -73,6 +73,7 @@ _SIGS = {
     "nnt_create_model": (C.c_int, [C.POINTER(Config), C.POINTER(Tiles), C.POINTER(Options), C.POINTER(_P)]),
     "nnt_forward": (C.c_int, [_P, _P, _I32, C.POINTER(_F)]),
     "nnt_backward": (C.c_int, [_P]),
+    "nnt_backward_accumulate": (C.c_int, [_P]),
     "nnt_adamw_step": (C.c_int, [_P, C.POINTER(AdamW)]),
     "nnt_backward_adamw": (C.c_int, [_P, C.POINTER(AdamW)]),
     "nnt_destroy": (None, [_P]),
@@ -209,16 +210,21 @@ class Model:
         check(lib().nnt_forward(self.h, ptr, on_dev, C.byref(loss) if want_loss else None), self.h)
         return loss.value if want_loss else None
 
-    def backward(self):
-        check(lib().nnt_backward(self.h), self.h)
+    def backward(self, accumulate=False):
+        """Gradients of the last forward; accumulate=True adds them to the ones
+        summed since the last update (nnt_backward_accumulate)."""
+        fn = lib().nnt_backward_accumulate if accumulate else lib().nnt_backward
+        check(fn(self.h), self.h)
 
-    def adamw_step(self, lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1):
-        hp = AdamW(lr, beta1, beta2, eps, weight_decay)
+    def adamw_step(self, lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1,
+                   start_lr=0.0, full_lr_iter=0):
+        hp = AdamW(lr, beta1, beta2, eps, weight_decay, start_lr, full_lr_iter)
         check(lib().nnt_adamw_step(self.h, C.byref(hp)), self.h)
 
-    def backward_adamw(self, lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1):
+    def backward_adamw(self, lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1,
+                       start_lr=0.0, full_lr_iter=0):
         """Backward with each chunk's AdamW update fused in (nnt_backward_adamw)."""
-        hp = AdamW(lr, beta1, beta2, eps, weight_decay)
+        hp = AdamW(lr, beta1, beta2, eps, weight_decay, start_lr, full_lr_iter)
         check(lib().nnt_backward_adamw(self.h, C.byref(hp)), self.h)
 
     # ---- parity surface
