@@ -264,6 +264,31 @@ nnt_status nnt_op_softmax_causal_bwd(const void* p_dev, const float* dp_dev, voi
                                      int64_t nmat, int64_t seq, float scale, int32_t dtype,
                                      void* stream);
 
+/* Fused causal attention (the README's --flashattention option; the pages
+ * list it as a memory-saving flag whose kernel NNTile does not have yet):
+ * O = softmax_causal(Q K^T / sqrt(hd)) V without materialising the scores.
+ * q, k, v, o: bf16 [Z][S][hd] device buffers (Z = sequences x heads, rows of
+ * one (sequence, head) contiguous, 16-byte aligned); lse: fp32 [Z][S], the
+ * base-2 log-sum-exp of each row's scaled scores, so that the probabilities
+ * are 2^(s * log2(e) / sqrt(hd) - lse) (saved for the backward). hd must be 64
+ * or 128 (INVALID_ARG otherwise); any S >= 1. Scores and P are bf16 MMA
+ * operands with fp32 accumulation, P rounded to bf16 before P V. Runs on
+ * `stream`; the library keeps no reference to the buffers. A bounded wait
+ * that runs out is reported through nnt_op_read_error. */
+nnt_status nnt_op_flash_attention_fwd(const void* q_dev, const void* k_dev, const void* v_dev,
+                                      void* o_dev, float* lse_dev, int64_t Z, int64_t S,
+                                      int64_t hd, void* stream);
+
+/* Backward of nnt_op_flash_attention_fwd: dq, dk, dv (bf16 [Z][S][hd],
+ * overwritten) from q, k, v, the forward's o and lse, and do = dL/dO (bf16
+ * [Z][S][hd]). P is recomputed from lse; D = rowsum(do * o) goes to a
+ * library-owned scratch buffer (grown with cudaMalloc when too small). Sums run
+ * in a fixed order (no atomics): same inputs, same bits. */
+nnt_status nnt_op_flash_attention_bwd(const void* q_dev, const void* k_dev, const void* v_dev,
+                                      const void* o_dev, const void* do_dev, const float* lse_dev,
+                                      void* dq_dev, void* dk_dev, void* dv_dev, int64_t Z,
+                                      int64_t S, int64_t hd, void* stream);
+
 /* tanh-form GELU over n elements: g = gelu(u) (u fp32, g act) and its
  * backward du = dg * gelu'(u) (dg act, du act). */
 nnt_status nnt_op_gelu_fwd(const float* u_dev, void* g_dev, int64_t n, int32_t dtype, void* stream);

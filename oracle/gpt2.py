@@ -197,6 +197,18 @@ def causal_softmax_forward(scores):
     return e / e.sum(axis=-1, keepdims=True)
 
 
+def causal_logsumexp(scores):
+    """Natural log of each row's softmax normaliser over the causal entries:
+    lse[q] = log sum_{k <= q} exp(scores[q, k]), so that the causal softmax is
+    exp(scores - lse) on those entries. (A fused attention keeps this per row
+    instead of the probabilities.)"""
+    S_q, S_k = scores.shape[-2:]
+    mask = np.triu(np.ones((S_q, S_k), dtype=bool), k=1)
+    s = np.where(mask, -np.inf, scores)
+    m = s.max(axis=-1)
+    return m + np.log(np.exp(s - m[..., None]).sum(axis=-1))
+
+
 def causal_softmax_backward(dP, P):
     """dS = P * (dP - rowsum(dP * P)); masked entries (P = 0) give 0."""
     return P * (dP - (dP * P).sum(axis=-1, keepdims=True))

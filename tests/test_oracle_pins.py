@@ -475,3 +475,19 @@ def test_training_on_one_batch_lowers_the_loss():
     losses, final, _, _ = O.train(cfg, p, [mbs] * 6, hp)
     assert losses[1] == losses[0]
     assert all(b < a for a, b in zip(losses[1:], losses[2:])), losses
+
+
+def test_causal_logsumexp_normalises_the_causal_softmax():
+    """exp(scores - lse) must reproduce the (separately pinned) causal softmax on
+    the causal entries, and lse of a single-entry row is that entry."""
+    rng = np.random.default_rng(41)
+    sc = 4.0 * rng.standard_normal((3, 7, 7))
+    lse = O.causal_logsumexp(sc)
+    P = O.causal_softmax_forward(sc)
+    tri = np.tril(np.ones((7, 7), dtype=bool))
+    np.testing.assert_allclose(np.exp(sc - lse[..., None])[:, tri], P[:, tri], rtol=1e-12)
+    np.testing.assert_array_equal(lse[:, 0], sc[:, 0, 0])
+    # a brute-force row
+    q = 5
+    ref = math.log(sum(math.exp(sc[1, q, k]) for k in range(q + 1)))
+    assert abs(lse[1, q] - ref) < 1e-12

@@ -23,6 +23,15 @@ nnt_status read_and_clear_device_error(uint32_t* code_host, cudaStream_t st);
 
 const char* status_name(nnt_status s);
 void set_thread_error(const char* fmt, ...);
+// Status of the last kernel launch on this thread (error text set on failure).
+inline nnt_status launch_check(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_thread_error("launch of %s failed: %s", what, cudaGetErrorString(e));
+    return NNT_ERR_CUDA;
+  }
+  return NNT_OK;
+}
 const char* thread_error();
 
 #define NNT_CUDA_TRY(expr)                                                        \

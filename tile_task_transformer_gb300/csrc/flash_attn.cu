@@ -1,0 +1,809 @@
+// Fused causal attention tile task ("flash attention") for sm_103a.
+//
+// The README's example command turns on --flashattention, which the pages list
+// as a memory-saving option whose kernel NNTile does not have yet (README
+// "Minimal working GPT example", flag list). Here it is a tile task of its
+// own: the score tile S = Q K^T / sqrt(hd) of one (sequence, head) and 128
+// queries lives in tensor memory, the causal softmax is taken row by row with
+// a running maximum and sum (online softmax), P reaches P V through shared
+// memory, and nothing of size S x S is written to HBM. The backward pass
+// recomputes P from the per-row log-sum-exp saved by the forward.
+//
+// Every kernel runs 128 threads (4 warps). Thread t owns row t of the current
+// tile, which is TMEM lane t (warp w reads lanes 32w..32w+31). Thread 0 also
+// issues the TMA copies and the tcgen05.mma instructions; the other threads
+// only wait for their results. Tiles are [128 rows][hd] bf16 loaded by TMA
+// with a 128-byte swizzle as hd/64 chunks of 16 KB; the same smem tile serves
+// as a K-major operand (rows = M or N, K = hd) or an MN-major one (N = hd,
+// K = rows) through its descriptor. P and dS tiles written by the threads use
+// the K-major layout TMA would produce.
+//
+//   flash_fwd_kernel     item x query block: O and the log-sum-exp
+//   flash_bwd_d_kernel   D = rowsum(dO * O)
+//   flash_bwd_kv_kernel  item x key block: dK, dV over the query blocks at or after it
+//   flash_bwd_q_kernel   item x query block: dQ over the key blocks at or before it
+// dK/dV and dQ come from separate passes, so every sum has a fixed order (no
+// atomics). Every mbarrier wait is bounded: on expiry the kernel records the
+// device error word, waits (bounded) for its own copies and MMAs in flight,
+// frees its TMEM and returns.
+#include <math.h>
+
+#include <mutex>
+
+#include "flash.cuh"
+#include "tc_ptx.cuh"
+
+namespace nnt {
+namespace {
+
+constexpr int FB = 128;              // queries or keys per block
+constexpr int kThreads = 128;
+constexpr int CHUNK = FB * 128;      // one [128 rows][64 bf16] swizzled chunk: 16 KB
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Descriptor of K step kk (16 elements) of a [128][*] tile used K-major.
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
+  return make_sdesc(base + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32), 16, 1024);
+}
+// Descriptor of K step kk (16 rows) of a [128][hd] tile used MN-major (N = hd).
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
+  return make_sdesc(base + (uint32_t)(kk * 2048), CHUNK, 1024);
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Columns 8g..8g+7 of row r of a [128][128] bf16 K-major tile (two chunks).
+__device__ __forceinline__ void put8(uint8_t* tile, int r, int g, const float* v) {
+  uint4 pk;
+  pk.x = pack_bf2(v[0], v[1]);
+  pk.y = pack_bf2(v[2], v[3]);
+  pk.z = pack_bf2(v[4], v[5]);
+  pk.w = pack_bf2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(tile + (g >> 3) * CHUNK + r * 128 + (((g & 7) ^ (r & 7)) << 4)) = pk;
+}
+
+// One [128][HD] tile starting at sequence row `row` of item z.
+template <int HD>
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int row,
+                                          int z) {
+#pragma unroll
+  for (int c = 0; c < HD / 64; ++c) tma_load_3d(dst + c * CHUNK, map, bar, 64 * c, row, z);
+}
+
+// HD/32 chunks of 32 TMEM columns of this thread's row, scaled, to bf16 at dst.
+template <int HD>
+__device__ __forceinline__ void store_row(uint32_t taddr, bool row_ok, bf16* dst, float scale) {
+#pragma unroll
+  for (int c = 0; c < HD / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32_nw(taddr + 32 * c, o);
+    tmem_wait_ld();
+    if (row_ok) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 pk;
+        pk.x = pack_bf2(__uint_as_float(o[8 * k + 0]) * scale, __uint_as_float(o[8 * k + 1]) * scale);
+        pk.y = pack_bf2(__uint_as_float(o[8 * k + 2]) * scale, __uint_as_float(o[8 * k + 3]) * scale);
+        pk.z = pack_bf2(__uint_as_float(o[8 * k + 4]) * scale, __uint_as_float(o[8 * k + 5]) * scale);
+        pk.w = pack_bf2(__uint_as_float(o[8 * k + 6]) * scale, __uint_as_float(o[8 * k + 7]) * scale);
+        *reinterpret_cast<uint4*>(dst + 32 * c + 8 * k) = pk;
+      }
+    }
+  }
+}
+
+// Bounded waits for every copy a barrier still owes (n issued, *w waited).
+__device__ __forceinline__ void drain(uint64_t* bar, int n, int* w) {
+  for (; *w < n; ++*w) mbar_wait(bar, (uint32_t)(*w & 1));
+}
+
+// ================================================================ forward
+
+template <int HD>
+struct FwdCfg {
+  static constexpr int TILE = FB * HD * 2;
+  // Q, K (two stages), V (one buffer), P
+  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 4 * TILE;
+  static constexpr int OFF_BAR = OFF_P + 2 * CHUNK;
+  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  static constexpr uint32_t TMEM_COLS = FB + HD <= 256 ? 256 : 512;  // S: 128 columns, O: HD
+};
+
+// Per CTA: item blockIdx % nz, query block nqb-1 - blockIdx / nz (largest
+// first). Key blocks 0..qb in order; K is double-buffered (block j+2 loads once
+// S_j is done), V single-buffered (block j loads once P V_{j-1} is done, and
+// lands while the softmax of block j runs).
+//
+// Softmax of row r at key block j: m = running maximum of the scaled scores
+// in base 2, l = running sum of 2^(s*c2 - m). The maximum actually used is
+// raised only when a row's new maximum exceeds it by more than 8 (P stays
+// below 2^8, exact in fp32 and in bf16's range); then l and the row of O are
+// multiplied by 2^(m_old - m_new) (O read and written back through TMEM).
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const FlashArgs a, int nqb, float c2,
+                     uint32_t* err) {
+  using C = FwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* bar_k = bar_q + 1;  // two stages
+  uint64_t* bar_v = bar_q + 3;
+  uint64_t* bar_s = bar_q + 4;
+  uint64_t* bar_o = bar_q + 5;
+  uint64_t* bar_x = bar_q + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int qb = nqb - 1 - (int)(blockIdx.x / a.nz);
+  const int item = (int)(blockIdx.x % a.nz);
+  const int z = (int)a.zm.z(item);
+  const int q0 = qb * FB, nkb = qb + 1;
+  const int q = q0 + tid;
+
+  if (tid == 0) {
+    for (int i = 0; i < 7; ++i) mbar_init(bar_q + i, 1);
+    mbar_fence_init();
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_v = smem_u32(sm + C::OFF_V), s_p = smem_u32(sm + C::OFF_P);
+
+  int n_k[2] = {0, 0}, w_k[2] = {0, 0}, n_v = 0, w_v = 0, w_q = 0;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_q, C::TILE);
+    load_tile<HD>(&tmQ, sm + C::OFF_Q, bar_q, q0, z);
+    mbar_arrive_expect_tx(&bar_k[0], C::TILE);
+    load_tile<HD>(&tmK, sm + C::OFF_K, &bar_k[0], 0, z);
+    n_k[0] = 1;
+    mbar_arrive_expect_tx(bar_v, C::TILE);
+    load_tile<HD>(&tmV, sm + C::OFF_V, bar_v, 0, z);
+    n_v = 1;
+    if (nkb > 1) {
+      mbar_arrive_expect_tx(&bar_k[1], C::TILE);
+      load_tile<HD>(&tmK, sm + C::OFF_K + C::TILE, &bar_k[1], FB, z);
+      n_k[1] = 1;
+    }
+  }
+
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true, aborted = false;
+  for (int j = 0; j < nkb; ++j) {
+    const int st = j & 1;
+    if (tid == 0) {
+      if (j == 0) {
+        ok = mbar_wait(bar_q, 0);
+        w_q = ok ? 1 : 0;
+      }
+      if (ok) {
+        ok = mbar_wait(&bar_k[st], (uint32_t)((j >> 1) & 1));
+        if (ok) ++w_k[st];
+      }
+      if (ok) {
+        tc_fence_after();
+        const uint32_t s_k = smem_u32(sm + C::OFF_K + st * C::TILE);
+        constexpr uint32_t idesc = make_idesc(FB, FB, false, false);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem, desc_k(s_q, kk), desc_k(s_k, kk), idesc, kk > 0 ? 1u : 0u);
+        umma_commit(bar_s);
+      }
+    }
+    if (ok) ok = mbar_wait(bar_s, (uint32_t)(j & 1));
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    tc_fence_after();
+    if (tid == 0) {  // S_j done, and with it P V_{j-1}: K stage st and the V buffer are free
+      if (j + 2 < nkb) {
+        mbar_arrive_expect_tx(&bar_k[st], C::TILE);
+        load_tile<HD>(&tmK, sm + C::OFF_K + st * C::TILE, &bar_k[st], (j + 2) * FB, z);
+        ++n_k[st];
+      }
+      if (j >= 1) {
+        mbar_arrive_expect_tx(bar_v, C::TILE);
+        load_tile<HD>(&tmV, sm + C::OFF_V, bar_v, j * FB, z);
+        ++n_v;
+      }
+    }
+    // ---- softmax of row `tid` over keys [j*128, j*128 + 128)
+    uint32_t u[FB];
+#pragma unroll
+    for (int c = 0; c < FB / 32; ++c) tmem_ld32_nw(t_row + 32 * c, u + 32 * c);
+    tmem_wait_ld();
+    const bool diag = j == nkb - 1;  // keys past the query only in the last block
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < FB; ++c) {
+      float x = __uint_as_float(u[c]);
+      if (diag && c > tid) x = -INFINITY;
+      u[c] = __float_as_uint(x);
+      mx = fmaxf(mx, x);
+    }
+    const float m_new = fmaxf(m_used, mx * c2);
+    if (j == 0) {
+      m_used = m_new;
+    } else {
+      const bool need = m_new > m_used + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2f(m_used - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m_used = m_new;
+        }
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32_nw(t_row + FB + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(t_row + FB + 32 * c, o);
+        }
+        tmem_wait_st();
+      }
+    }
+    float sum = 0.f;
+    uint8_t* pt = sm + C::OFF_P;
+#pragma unroll
+    for (int g = 0; g < FB / 8; ++g) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[e] = ex2f(fmaf(__uint_as_float(u[8 * g + e]), c2, -m_used));
+        sum += v[e];
+      }
+      put8(pt, tid, g, v);
+    }
+    l += sum;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+      ok = mbar_wait(bar_v, (uint32_t)(j & 1));
+      if (ok) {
+        ++w_v;
+        tc_fence_after();
+        constexpr uint32_t idesc = make_idesc(FB, HD, false, true);
+#pragma unroll
+        for (int kk = 0; kk < FB / 16; ++kk)
+          umma_bf16(tmem + FB, desc_k(s_p, kk), desc_mn(s_v, kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+    }
+  }
+  if (!aborted) {
+    if (tid == 0 && ok) umma_commit(bar_o);
+    if (ok) ok = mbar_wait(bar_o, 0);
+    if (__syncthreads_or(!ok)) aborted = true;
+  }
+  if (!aborted) {
+    tc_fence_after();
+    const int b = a.zm.b(item), h = a.zm.h(item);
+    const bool row_ok = q < a.S;
+    bf16* orow = a.o + (row_ok ? a.tm.row(b, q) * a.ldo + a.o_col + (int64_t)h * HD : 0);
+    store_row<HD>(t_row + FB, row_ok, orow, 1.f / l);
+    if (row_ok) a.lse[(int64_t)z * a.S + q] = m_used + log2f(l);
+  } else if (tid == 0) {
+    atomicOr(err, DEVERR_WAIT_TIMEOUT);
+    drain(bar_q, 1, &w_q);
+    drain(&bar_k[0], n_k[0], &w_k[0]);
+    drain(&bar_k[1], n_k[1], &w_k[1]);
+    drain(bar_v, n_v, &w_v);
+    umma_commit(bar_x);
+    mbar_wait(bar_x, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ================================================================ backward
+
+// D[z][s] = sum_j dO[z][s][j] * O(z, s, j); one warp per row.
+__global__ void __launch_bounds__(256) flash_bwd_d_kernel(const bf16* __restrict__ dO, const FlashArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= (int64_t)a.nz * a.S) return;
+  const int item = (int)(r / a.S), s = (int)(r % a.S);
+  const int64_t z = a.zm.z(item);
+  const bf16* dr = dO + (z * a.S + s) * a.hd;
+  const bf16* orow = a.o + a.tm.row(a.zm.b(item), s) * a.ldo + a.o_col + (int64_t)a.zm.h(item) * a.hd;
+  float acc = 0.f;
+  for (int j = 4 * lane; j < a.hd; j += 128) {
+    const float4 x = load4(dr + j), y = load4(orow + j);
+    acc += (x.x * y.x + x.y * y.y) + (x.z * y.z + x.w * y.w);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) a.D[z * a.S + s] = acc;
+}
+
+template <int HD>
+struct KvCfg {
+  static constexpr int TILE = FB * HD * 2;
+  static constexpr int NS = HD <= 64 ? 2 : 1;  // stages of (Q, dO)
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_ST = 2 * TILE;  // stage s: Q, then dO
+  static constexpr int OFF_PT = OFF_ST + NS * 2 * TILE, OFF_DS = OFF_PT + 2 * CHUNK;
+  static constexpr int OFF_ROW = OFF_DS + 2 * CHUNK;  // lse and D of the current query block
+  static constexpr int OFF_BAR = OFF_ROW + 2 * FB * 4;
+  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+};
+
+// Per CTA: key block kb = blockIdx / nz (the first ones have the most query
+// blocks), item blockIdx % nz. For each query block i >= kb:
+//   S^T = K Q_i^T, dP^T = V dO_i^T            (TMEM columns 0..127, 128..255)
+//   P^T = 2^(S^T c2 - lse), dS^T = scale * P^T (dP^T - D)   (rows = keys, in smem)
+//   dV += P^T dO_i, dK += dS^T Q_i              (TMEM columns 256.., 256+HD..)
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                        const FlashArgs a, int nqb, float c2, float scale, uint32_t* err) {
+  using C = KvCfg<HD>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_kv = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* bar_ld = bar_kv + 1;    // [2]
+  uint64_t* bar_free = bar_kv + 3;  // [2]
+  uint64_t* bar_s = bar_kv + 5;
+  uint64_t* bar_o = bar_kv + 6;
+  uint64_t* bar_x = bar_kv + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kv + 8);
+  float* lse_s = reinterpret_cast<float*>(sm + C::OFF_ROW);
+  float* d_s = lse_s + FB;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int kb = (int)(blockIdx.x / a.nz);
+  const int item = (int)(blockIdx.x % a.nz);
+  const int z = (int)a.zm.z(item);
+  const int n = nqb - kb;
+  const int key = kb * FB + tid;
+
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(bar_kv + i, 1);
+    mbar_fence_init();
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+    tma_prefetch_map(&tmdO);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t s_k = smem_u32(sm + C::OFF_K), s_v = smem_u32(sm + C::OFF_V);
+  const uint32_t s_pt = smem_u32(sm + C::OFF_PT), s_ds = smem_u32(sm + C::OFF_DS);
+
+  auto load_qdo = [&](int s, int i) {
+    uint8_t* dst = sm + C::OFF_ST + s * 2 * C::TILE;
+    mbar_arrive_expect_tx(&bar_ld[s], 2 * C::TILE);
+    load_tile<HD>(&tmQ, dst, &bar_ld[s], i * FB, z);
+    load_tile<HD>(&tmdO, dst + C::TILE, &bar_ld[s], i * FB, z);
+  };
+  int n_ld[2] = {0, 0}, w_ld[2] = {0, 0}, w_kv = 0;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
+    load_tile<HD>(&tmK, sm + C::OFF_K, bar_kv, kb * FB, z);
+    load_tile<HD>(&tmV, sm + C::OFF_V, bar_kv, kb * FB, z);
+    for (int it = 0; it < NS && it < n; ++it) {
+      load_qdo(it, kb + it);
+      n_ld[it] = 1;
+    }
+  }
+
+  bool ok = true, aborted = false;
+  for (int it = 0; it < n; ++it) {
+    const int i = kb + it, st = it % NS;
+    const int qc = i * FB + tid;  // this thread's column of the query block
+    const float lse_c = qc < a.S ? a.lse[(int64_t)z * a.S + qc] : 0.f;
+    const float d_c = qc < a.S ? a.D[(int64_t)z * a.S + qc] : 0.f;
+    if (tid == 0) {
+      if (it == 0) {
+        ok = mbar_wait(bar_kv, 0);
+        w_kv = ok ? 1 : 0;
+      }
+      if (ok && it >= 1 && it + NS - 1 < n) {  // refill the stage freed by iteration it-1
+        const int s2 = (it + NS - 1) % NS;
+        ok = mbar_wait(&bar_free[s2], (uint32_t)(((it - 1) / NS) & 1));
+        if (ok) {
+          load_qdo(s2, i + NS - 1);
+          ++n_ld[s2];
+        }
+      }
+      if (ok) {
+        ok = mbar_wait(&bar_ld[st], (uint32_t)((it / NS) & 1));
+        if (ok) ++w_ld[st];
+      }
+      if (ok) {
+        tc_fence_after();
+        const uint32_t s_qt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE), s_do = s_qt + C::TILE;
+        constexpr uint32_t idesc = make_idesc(FB, FB, false, false);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem, desc_k(s_k, kk), desc_k(s_qt, kk), idesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + FB, desc_k(s_v, kk), desc_k(s_do, kk), idesc, kk > 0 ? 1u : 0u);
+        umma_commit(bar_s);
+      }
+    }
+    lse_s[tid] = lse_c;
+    d_s[tid] = d_c;
+    if (ok) ok = mbar_wait(bar_s, (uint32_t)(it & 1));
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    tc_fence_after();
+    const bool diag = i == kb;
+    uint8_t* pt = sm + C::OFF_PT;
+    uint8_t* dst = sm + C::OFF_DS;
+#pragma unroll
+    for (int c = 0; c < FB / 32; ++c) {
+      uint32_t sv[32], dv[32];
+      tmem_ld32_nw(t_row + 32 * c, sv);
+      tmem_ld32_nw(t_row + FB + 32 * c, dv);
+      tmem_wait_ld();
+      float p[32], ds[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int qq = 32 * c + e;
+        const bool valid = i * FB + qq < a.S && (!diag || qq >= tid);
+        const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_s[qq])) : 0.f;
+        p[e] = pv;
+        ds[e] = pv * (__uint_as_float(dv[e]) - d_s[qq]) * scale;
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        put8(pt, tid, 4 * c + g, p + 8 * g);
+        put8(dst, tid, 4 * c + g, ds + 8 * g);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint32_t s_qt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE), s_do = s_qt + C::TILE;
+      constexpr uint32_t idesc = make_idesc(FB, HD, false, true);
+#pragma unroll
+      for (int kk = 0; kk < FB / 16; ++kk)
+        umma_bf16(tmem + 2 * FB, desc_k(s_pt, kk), desc_mn(s_do, kk), idesc, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < FB / 16; ++kk)
+        umma_bf16(tmem + 2 * FB + HD, desc_k(s_ds, kk), desc_mn(s_qt, kk), idesc,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&bar_free[st]);
+    }
+  }
+  if (!aborted) {
+    if (tid == 0 && ok) umma_commit(bar_o);
+    if (ok) ok = mbar_wait(bar_o, 0);
+    if (__syncthreads_or(!ok)) aborted = true;
+  }
+  if (!aborted) {
+    tc_fence_after();
+    const int b = a.zm.b(item), h = a.zm.h(item);
+    const bool row_ok = key < a.S;
+    const int64_t row = row_ok ? a.tm.row(b, key) * a.ldd : 0;
+    store_row<HD>(t_row + 2 * FB, row_ok, a.dv + row + a.dv_col + (int64_t)h * HD, 1.f);
+    store_row<HD>(t_row + 2 * FB + HD, row_ok, a.dk + row + a.dk_col + (int64_t)h * HD, 1.f);
+  } else if (tid == 0) {
+    atomicOr(err, DEVERR_WAIT_TIMEOUT);
+    drain(bar_kv, 1, &w_kv);
+    drain(&bar_ld[0], n_ld[0], &w_ld[0]);
+    drain(&bar_ld[1], n_ld[1], &w_ld[1]);
+    umma_commit(bar_x);
+    mbar_wait(bar_x, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD>
+struct QCfg {
+  static constexpr int TILE = FB * HD * 2;
+  static constexpr int NS = 2;  // stages of (K, V)
+  static constexpr int OFF_Q = 0, OFF_DO = TILE, OFF_ST = 2 * TILE;  // stage s: K, then V
+  static constexpr int OFF_DS = OFF_ST + NS * 2 * TILE;
+  static constexpr int OFF_BAR = OFF_DS + 2 * CHUNK;
+  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+};
+
+// Per CTA: query block qb = nqb-1 - blockIdx / nz, item blockIdx % nz. For
+// each key block j <= qb:
+//   S = Q K_j^T, dP = dO V_j^T                  (TMEM columns 0..127, 128..255)
+//   dS = scale * P (dP - D), P = 2^(S c2 - lse)  (rows = queries, in smem)
+//   dQ += dS K_j                                (TMEM columns 256..)
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const FlashArgs a, int nqb, float c2, float scale, uint32_t* err) {
+  using C = QCfg<HD>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_qd = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* bar_ld = bar_qd + 1;    // [2]
+  uint64_t* bar_free = bar_qd + 3;  // [2]
+  uint64_t* bar_s = bar_qd + 5;
+  uint64_t* bar_o = bar_qd + 6;
+  uint64_t* bar_x = bar_qd + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_qd + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int qb = nqb - 1 - (int)(blockIdx.x / a.nz);
+  const int item = (int)(blockIdx.x % a.nz);
+  const int z = (int)a.zm.z(item);
+  const int n = qb + 1;
+  const int q = qb * FB + tid;
+  const float lse_r = q < a.S ? a.lse[(int64_t)z * a.S + q] : 0.f;
+  const float d_r = q < a.S ? a.D[(int64_t)z * a.S + q] : 0.f;
+
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(bar_qd + i, 1);
+    mbar_fence_init();
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+    tma_prefetch_map(&tmdO);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_do = smem_u32(sm + C::OFF_DO);
+  const uint32_t s_ds = smem_u32(sm + C::OFF_DS);
+
+  auto load_kv = [&](int s, int j) {
+    uint8_t* dst = sm + C::OFF_ST + s * 2 * C::TILE;
+    mbar_arrive_expect_tx(&bar_ld[s], 2 * C::TILE);
+    load_tile<HD>(&tmK, dst, &bar_ld[s], j * FB, z);
+    load_tile<HD>(&tmV, dst + C::TILE, &bar_ld[s], j * FB, z);
+  };
+  int n_ld[2] = {0, 0}, w_ld[2] = {0, 0}, w_qd = 0;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_qd, 2 * C::TILE);
+    load_tile<HD>(&tmQ, sm + C::OFF_Q, bar_qd, qb * FB, z);
+    load_tile<HD>(&tmdO, sm + C::OFF_DO, bar_qd, qb * FB, z);
+    for (int it = 0; it < NS && it < n; ++it) {
+      load_kv(it, it);
+      n_ld[it] = 1;
+    }
+  }
+
+  bool ok = true, aborted = false;
+  for (int j = 0; j < n; ++j) {
+    const int st = j % NS;
+    if (tid == 0) {
+      if (j == 0) {
+        ok = mbar_wait(bar_qd, 0);
+        w_qd = ok ? 1 : 0;
+      }
+      if (ok && j >= 1 && j + NS - 1 < n) {
+        const int s2 = (j + NS - 1) % NS;
+        ok = mbar_wait(&bar_free[s2], (uint32_t)(((j - 1) / NS) & 1));
+        if (ok) {
+          load_kv(s2, j + NS - 1);
+          ++n_ld[s2];
+        }
+      }
+      if (ok) {
+        ok = mbar_wait(&bar_ld[st], (uint32_t)((j / NS) & 1));
+        if (ok) ++w_ld[st];
+      }
+      if (ok) {
+        tc_fence_after();
+        const uint32_t s_kt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE), s_vt = s_kt + C::TILE;
+        constexpr uint32_t idesc = make_idesc(FB, FB, false, false);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem, desc_k(s_q, kk), desc_k(s_kt, kk), idesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + FB, desc_k(s_do, kk), desc_k(s_vt, kk), idesc, kk > 0 ? 1u : 0u);
+        umma_commit(bar_s);
+      }
+    }
+    if (ok) ok = mbar_wait(bar_s, (uint32_t)(j & 1));
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    tc_fence_after();
+    const bool diag = j == qb;
+    uint8_t* dst = sm + C::OFF_DS;
+#pragma unroll
+    for (int c = 0; c < FB / 32; ++c) {
+      uint32_t sv[32], dv[32];
+      tmem_ld32_nw(t_row + 32 * c, sv);
+      tmem_ld32_nw(t_row + FB + 32 * c, dv);
+      tmem_wait_ld();
+      float ds[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const bool valid = !diag || 32 * c + e <= tid;
+        const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_r)) : 0.f;
+        ds[e] = pv * (__uint_as_float(dv[e]) - d_r) * scale;
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) put8(dst, tid, 4 * c + g, ds + 8 * g);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint32_t s_kt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE);
+      constexpr uint32_t idesc = make_idesc(FB, HD, false, true);
+#pragma unroll
+      for (int kk = 0; kk < FB / 16; ++kk)
+        umma_bf16(tmem + 2 * FB, desc_k(s_ds, kk), desc_mn(s_kt, kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&bar_free[st]);
+    }
+  }
+  if (!aborted) {
+    if (tid == 0 && ok) umma_commit(bar_o);
+    if (ok) ok = mbar_wait(bar_o, 0);
+    if (__syncthreads_or(!ok)) aborted = true;
+  }
+  if (!aborted) {
+    tc_fence_after();
+    const int b = a.zm.b(item), h = a.zm.h(item);
+    const bool row_ok = q < a.S;
+    const int64_t row = row_ok ? a.tm.row(b, q) * a.ldd : 0;
+    store_row<HD>(t_row + 2 * FB, row_ok, a.dq + row + a.dq_col + (int64_t)h * HD, 1.f);
+  } else if (tid == 0) {
+    atomicOr(err, DEVERR_WAIT_TIMEOUT);
+    drain(bar_qd, 1, &w_qd);
+    drain(&bar_ld[0], n_ld[0], &w_ld[0]);
+    drain(&bar_ld[1], n_ld[1], &w_ld[1]);
+    umma_commit(bar_x);
+    mbar_wait(bar_x, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+// Opt a kernel into `bytes` of dynamic shared memory, once per kernel: each
+// caller passes its own once_flag and result slot (kernels of one signature
+// share a function-pointer type, so a static inside a template on that type
+// would be shared between them).
+template <typename K>
+nnt_status allow_smem(K kern, int bytes, std::once_flag& once, cudaError_t& e) {
+  std::call_once(once, [&] { e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
+  if (e != cudaSuccess) {
+    set_thread_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    return NNT_ERR_CUDA;
+  }
+  return NNT_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+nnt_status check_args(const FlashArgs& a, const void* q, const void* k, const void* v) {
+  NNT_CHECK_ARG(flash_supported(a.hd), "flash attention: head size %d (supported: 64, 128)", a.hd);
+  NNT_CHECK_ARG(a.S > 0 && a.nz > 0 && a.z_total > 0, "flash attention: empty problem");
+  NNT_CHECK_ARG(a.zm.z(a.nz - 1) < a.z_total && a.zm.z(0) >= 0, "flash attention: item out of range");
+  NNT_CHECK_ARG(q && k && v && aligned16(q) && aligned16(k) && aligned16(v),
+                "flash attention: q, k, v must be 16-byte aligned device pointers");
+  NNT_CHECK_ARG(a.o && aligned16(a.o) && a.ldo % 8 == 0 && a.o_col % 8 == 0 && a.lse,
+                "flash attention: O must be 16-byte aligned with ldo, o_col multiples of 8; lse needed");
+  return NNT_OK;
+}
+
+nnt_status qkv_maps(const FlashArgs& a, const bf16* q, const bf16* k, const bf16* v, CUtensorMap* mq,
+                    CUtensorMap* mk, CUtensorMap* mv) {
+  const int64_t hd = a.hd, S = a.S;
+  NNT_TRY(make_map(mq, q, hd, S, hd, S * hd, a.z_total, 64, FB));
+  NNT_TRY(make_map(mk, k, hd, S, hd, S * hd, a.z_total, 64, FB));
+  return make_map(mv, v, hd, S, hd, S * hd, a.z_total, 64, FB);
+}
+
+template <int HD>
+nnt_status fwd_hd(const bf16* q, const bf16* k, const bf16* v, const FlashArgs& a, cudaStream_t st) {
+  auto kern = flash_fwd_kernel<HD>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  NNT_TRY(allow_smem(kern, FwdCfg<HD>::SMEM, once, attr));
+  CUtensorMap mq, mk, mv;
+  NNT_TRY(qkv_maps(a, q, k, v, &mq, &mk, &mv));
+  uint32_t* err = device_error_word();
+  NNT_CHECK_ARG(err != nullptr, "device error word unavailable");
+  const int nqb = (int)ceil_div(a.S, FB);
+  const float c2 = (float)(1.4426950408889634 / sqrt((double)HD));
+  kern<<<(unsigned)(nqb * a.nz), kThreads, FwdCfg<HD>::SMEM, st>>>(mq, mk, mv, a, nqb, c2, err);
+  return launch_check("flash_fwd");
+}
+
+template <int HD>
+nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, const FlashArgs& a,
+                  cudaStream_t st) {
+  auto kv = flash_bwd_kv_kernel<HD>;
+  auto qk = flash_bwd_q_kernel<HD>;
+  static std::once_flag once_kv, once_q;
+  static cudaError_t attr_kv = cudaSuccess, attr_q = cudaSuccess;
+  NNT_TRY(allow_smem(kv, KvCfg<HD>::SMEM, once_kv, attr_kv));
+  NNT_TRY(allow_smem(qk, QCfg<HD>::SMEM, once_q, attr_q));
+  CUtensorMap mq, mk, mv, mdo;
+  NNT_TRY(qkv_maps(a, q, k, v, &mq, &mk, &mv));
+  NNT_TRY(make_map(&mdo, dO, a.hd, a.S, a.hd, (int64_t)a.S * a.hd, a.z_total, 64, FB));
+  uint32_t* err = device_error_word();
+  NNT_CHECK_ARG(err != nullptr, "device error word unavailable");
+  const int nqb = (int)ceil_div(a.S, FB);
+  const double scale = 1.0 / sqrt((double)HD);
+  const float c2 = (float)(1.4426950408889634 * scale);
+  flash_bwd_d_kernel<<<(unsigned)ceil_div((int64_t)a.nz * a.S, 8), 256, 0, st>>>(dO, a);
+  NNT_TRY(launch_check("flash_bwd_d"));
+  kv<<<(unsigned)(nqb * a.nz), kThreads, KvCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+  NNT_TRY(launch_check("flash_bwd_kv"));
+  qk<<<(unsigned)(nqb * a.nz), kThreads, QCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+  return launch_check("flash_bwd_q");
+}
+
+}  // namespace
+
+bool flash_supported(int hd) { return hd == 64 || hd == 128; }
+
+nnt_status launch_flash_fwd(const bf16* q, const bf16* k, const bf16* v, const FlashArgs& a,
+                            cudaStream_t st) {
+  NNT_TRY(check_args(a, q, k, v));
+  return a.hd == 64 ? fwd_hd<64>(q, k, v, a, st) : fwd_hd<128>(q, k, v, a, st);
+}
+
+nnt_status launch_flash_bwd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO,
+                            const FlashArgs& a, cudaStream_t st) {
+  NNT_TRY(check_args(a, q, k, v));
+  NNT_CHECK_ARG(dO && aligned16(dO) && a.D && a.dq && a.dk && a.dv && aligned16(a.dq) &&
+                    aligned16(a.dk) && aligned16(a.dv) && a.ldd % 8 == 0 && a.dq_col % 8 == 0 &&
+                    a.dk_col % 8 == 0 && a.dv_col % 8 == 0,
+                "flash attention backward: dO, D and 16-byte aligned dq, dk, dv (ldd and column "
+                "offsets multiples of 8) needed");
+  return a.hd == 64 ? bwd_hd<64>(q, k, v, dO, a, st) : bwd_hd<128>(q, k, v, dO, a, st);
+}
+
+}  // namespace nnt

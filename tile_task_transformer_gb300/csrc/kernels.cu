@@ -46,15 +46,6 @@ void set_thread_error(const char* fmt, ...) {
 }
 const char* thread_error() { return t_err; }
 
-static inline nnt_status launch_check(const char* what) {
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    set_thread_error("launch of %s failed: %s", what, cudaGetErrorString(e));
-    return NNT_ERR_CUDA;
-  }
-  return NNT_OK;
-}
-
 static constexpr float kLog2e = 1.4426950408889634f;
 
 // =====================================================================

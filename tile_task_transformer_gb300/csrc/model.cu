@@ -1805,7 +1805,7 @@ nnt_status nnt_set_trace(nnt_model* m, int32_t on) {
 
 const char* nnt_last_error(const nnt_model* m) {
   if (m) return m->err.c_str();
-  return t_model_err.c_str();
+  return thread_error();  // the last error of any call on this thread
 }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "flash.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
 
@@ -103,6 +104,57 @@ nnt_status nnt_op_softmax_causal_bwd(const void* p_dev, const float* dp_dev, voi
   ZMap zm{0, 0, 1, 1};
   return launch_softmax_bwd(p_dev, dp_dev, ds_dev, seq, zm, (int)nmat, 0, (int)seq, scale, dtype,
                             (cudaStream_t)stream);
+}
+
+namespace {
+// FlashArgs of the op-level calls: plain [Z][S][hd] buffers (one head per item).
+FlashArgs plain_flash(int64_t Z, int64_t S, int64_t hd) {
+  FlashArgs a;
+  a.S = (int)S;
+  a.hd = (int)hd;
+  a.nz = (int)Z;
+  a.zm = ZMap{0, 0, 1, 1};
+  a.z_total = Z;
+  a.tm = TokMap{(int)S, (int)Z, (int)S, 1};
+  a.ldo = hd;
+  a.ldd = hd;
+  return a;
+}
+}  // namespace
+
+nnt_status nnt_op_flash_attention_fwd(const void* q_dev, const void* k_dev, const void* v_dev,
+                                      void* o_dev, float* lse_dev, int64_t Z, int64_t S,
+                                      int64_t hd, void* stream) {
+  NNT_CHECK_ARG(q_dev && k_dev && v_dev && o_dev && lse_dev, "NULL pointer");
+  NNT_CHECK_ARG(Z > 0 && S > 0 && Z * S < (1ll << 31) && flash_supported((int)hd),
+                "bad size (Z, S >= 1, Z*S < 2^31, hd 64 or 128)");
+  FlashArgs a = plain_flash(Z, S, hd);
+  a.o = static_cast<bf16*>(o_dev);
+  a.lse = lse_dev;
+  return launch_flash_fwd(static_cast<const bf16*>(q_dev), static_cast<const bf16*>(k_dev),
+                          static_cast<const bf16*>(v_dev), a, (cudaStream_t)stream);
+}
+
+nnt_status nnt_op_flash_attention_bwd(const void* q_dev, const void* k_dev, const void* v_dev,
+                                      const void* o_dev, const void* do_dev, const float* lse_dev,
+                                      void* dq_dev, void* dk_dev, void* dv_dev, int64_t Z,
+                                      int64_t S, int64_t hd, void* stream) {
+  NNT_CHECK_ARG(q_dev && k_dev && v_dev && o_dev && do_dev && lse_dev && dq_dev && dk_dev && dv_dev,
+                "NULL pointer");
+  NNT_CHECK_ARG(Z > 0 && S > 0 && Z * S < (1ll << 31) && flash_supported((int)hd),
+                "bad size (Z, S >= 1, Z*S < 2^31, hd 64 or 128)");
+  void* D = nullptr;
+  NNT_TRY(scratch((size_t)(Z * S) * sizeof(float), &D));
+  FlashArgs a = plain_flash(Z, S, hd);
+  a.o = const_cast<bf16*>(static_cast<const bf16*>(o_dev));
+  a.lse = const_cast<float*>(lse_dev);
+  a.D = static_cast<float*>(D);
+  a.dq = static_cast<bf16*>(dq_dev);
+  a.dk = static_cast<bf16*>(dk_dev);
+  a.dv = static_cast<bf16*>(dv_dev);
+  return launch_flash_bwd(static_cast<const bf16*>(q_dev), static_cast<const bf16*>(k_dev),
+                          static_cast<const bf16*>(v_dev), static_cast<const bf16*>(do_dev), a,
+                          (cudaStream_t)stream);
 }
 
 nnt_status nnt_op_gelu_fwd(const float* u_dev, void* g_dev, int64_t n, int32_t dtype, void* stream) {

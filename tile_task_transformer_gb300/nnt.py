@@ -93,6 +93,8 @@ _SIGS = {
     "nnt_op_layernorm_bwd": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _P]),
     "nnt_op_softmax_causal_fwd": (C.c_int, [_P, _P, _I64, _I64, _I32, _P]),
     "nnt_op_softmax_causal_bwd": (C.c_int, [_P, _P, _P, _I64, _I64, _F, _I32, _P]),
+    "nnt_op_flash_attention_fwd": (C.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "nnt_op_flash_attention_bwd": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "nnt_op_gelu_fwd": (C.c_int, [_P, _P, _I64, _I32, _P]),
     "nnt_op_gelu_bwd": (C.c_int, [_P, _P, _P, _I64, _I32, _P]),
     "nnt_op_cross_entropy": (C.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P]),
@@ -301,6 +303,17 @@ def op_softmax_causal_fwd(s, p, nmat, seq, dtype, stream=None):
 def op_softmax_causal_bwd(p, dp, ds, nmat, seq, scale, dtype, stream=None):
     check(lib().nnt_op_softmax_causal_bwd(_ptr(p), _ptr(dp), _ptr(ds), nmat, seq, scale, dtype,
                                           _stream(stream)))
+
+
+def op_flash_attention_fwd(q, k, v, o, lse, Z, S, hd, stream=None):
+    """Fused causal attention forward on bf16 [Z][S][hd] buffers (lse fp32 [Z][S])."""
+    check(lib().nnt_op_flash_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), Z, S, hd,
+                                           _stream(stream)))
+
+
+def op_flash_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, Z, S, hd, stream=None):
+    check(lib().nnt_op_flash_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                           _ptr(dq), _ptr(dk), _ptr(dv), Z, S, hd, _stream(stream)))
 
 
 def op_gelu_fwd(u, g, n, dtype, stream=None):
