@@ -88,6 +88,11 @@ typedef struct {
   int32_t trace;               /* 1: time every task with CUDA events (nnt_get_task_times) */
   int32_t gemm_min_task_cols;  /* consecutive output column tiles share one GEMM launch until it
                                   is this wide (0 = 8192; negative = one launch per tile) */
+  int32_t flash_attention;     /* README --flashattention: fused attention tile tasks that keep
+                                  the scores on chip (no [B,H,S,S] buffers). 0 = on when usable
+                                  (bf16, tensor-core GEMMs, head size 64 or 128), 1 = required
+                                  (INVALID_ARG when not usable), -1 = off (materialised scores,
+                                  softmax and P V as separate tasks) */
 } nnt_options;
 
 /* AdamW hyper-parameters (README: --optimizer=fusedadamw, --optimizer-eps=1e-8,
@@ -119,6 +124,7 @@ typedef struct {
   int32_t n_streams;
   int32_t offload_active;
   int64_t kernels_forward, kernels_backward, kernels_adamw; /* kernel launches per call */
+  int32_t flash_attention;      /* 1 when the fused attention tasks are in use */
 } nnt_stats;
 
 /* ---------------------------------------------------------------- model API */

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "executor.h"
+#include "flash.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
 
@@ -37,14 +38,15 @@ enum TaskType : int {
   TT_GEMM_FC, TT_GEMM_MLP_PROJ, TT_GEMM_LM_HEAD, TT_XENT, TT_LOSS,
   TT_GEMM_LM_DX, TT_GEMM_LM_DW, TT_LN_BWD, TT_LN_PARTS, TT_GEMM_DX, TT_GEMM_DW, TT_COLSUM,
   TT_GEMM_ATTN_BWD, TT_SOFTMAX_BWD, TT_EMB_SORT, TT_EMB_SCATTER, TT_WPE_GRAD, TT_ADAMW,
-  TT_ADAMW_HOST, TT_COUNT
+  TT_ADAMW_HOST, TT_FLASH_FWD, TT_FLASH_BWD, TT_COUNT
 };
 const char* kTaskNames[TT_COUNT] = {
     "embedding_fwd", "layernorm_fwd", "gemm_qkv", "gemm_qk", "softmax_fwd", "gemm_pv",
     "gemm_attn_out", "gemm_fc_gelu", "gemm_mlp_proj", "gemm_lm_head", "cross_entropy",
     "mean_loss", "gemm_lm_dx", "gemm_lm_dw", "layernorm_bwd", "layernorm_param_grads",
     "gemm_dx", "gemm_dw", "bias_grads", "gemm_attn_bwd", "softmax_bwd", "token_sort",
-    "embedding_scatter", "wpe_grad", "adamw", "adamw_host_moments"};
+    "embedding_scatter", "wpe_grad", "adamw", "adamw_host_moments", "flash_attn_fwd",
+    "flash_attn_bwd"};
 
 
 struct ParamInfo {
@@ -117,6 +119,11 @@ struct nnt_model {
   std::vector<float*> x, xmid, mu1, r1, mu2, r2, u;
   std::vector<void*> h1, qkvh, P, O, h2, g;
   float* scores = nullptr;  // [B*H][S][S] fp32, reused by every layer (fwd scores, bwd dP)
+  // fused attention (flash): per-layer row log-sum-exp [B*H][S] and the
+  // backward's D = rowsum(dO * O) scratch [B*H][S]; no P or scores buffers
+  bool flash = false;
+  std::vector<float*> lse;
+  float* attn_d = nullptr;
   void* y = nullptr;
   float *muf = nullptr, *rf = nullptr;
   float* z = nullptr;
@@ -135,7 +142,8 @@ struct nnt_model {
   uint32_t* sort_keys = nullptr;
 
   // tile grids
-  std::vector<TGrid> gx, gxmid, gh1, gqkvh, gP, gO, gh2, gu, gg, gstat1, gstat2;
+  std::vector<TGrid> gx, gxmid, gh1, gqkvh, gP, gO, gh2, gu, gg, gstat1, gstat2, glse;
+  TGrid gattn_d;
   TGrid gscores, gy, gstatf, gz, gdz, grow_loss, gloss, gtok;
   TGrid gdres, gdres_act, gdtmp, gdu, gdOh, gdqkv, gln_part, gcol_part, gkeys;
   std::vector<TGrid> gparam, ggrad;
@@ -477,6 +485,7 @@ nnt_status alloc_all(nnt_model* m) {
   m->h1.resize(L);
   m->qkvh.resize(L);
   m->P.resize(L);
+  m->lse.resize(L);
   m->O.resize(L);
   m->h2.resize(L);
   m->g.resize(L);
@@ -490,13 +499,19 @@ nnt_status alloc_all(nnt_model* m) {
     NNT_TRY(dalloc(m, m->r2[l], (size_t)T * 4));
     NNT_TRY(dalloc(m, m->h1[l], Td * as));
     NNT_TRY(dalloc(m, m->qkvh[l], 3 * Td * as));
-    NNT_TRY(dalloc(m, m->P[l], (size_t)B * H * S * S * as));
+    if (m->flash)
+      NNT_TRY(dalloc(m, m->lse[l], (size_t)B * H * S * 4));
+    else
+      NNT_TRY(dalloc(m, m->P[l], (size_t)B * H * S * S * as));
     NNT_TRY(dalloc(m, m->O[l], Td * as));
     NNT_TRY(dalloc(m, m->h2[l], Td * as));
     NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * 4));
     NNT_TRY(dalloc(m, m->g[l], (size_t)T * f * as));
   }
-  NNT_TRY(dalloc(m, m->scores, (size_t)B * H * S * S * 4));
+  if (m->flash)
+    NNT_TRY(dalloc(m, m->attn_d, (size_t)B * H * S * 4));
+  else
+    NNT_TRY(dalloc(m, m->scores, (size_t)B * H * S * S * 4));
   NNT_TRY(dalloc(m, m->y, Td * as));
   NNT_TRY(dalloc(m, m->muf, (size_t)T * 4));
   NNT_TRY(dalloc(m, m->rf, (size_t)T * 4));
@@ -608,6 +623,19 @@ struct Builder {
 };
 
 // -------------------------------------------------------------- forward
+// Fused-attention arguments for the (sequence, head) items of one (batch tile,
+// head tile) of the step's buffers.
+FlashArgs flash_args(const nnt_model* m, int bt, int ht) {
+  FlashArgs a;
+  a.S = m->S;
+  a.hd = m->hd;
+  a.nz = m->tb * m->th;
+  a.zm = ZMap{bt * m->tb, ht * m->th, m->th, m->H};
+  a.z_total = (int64_t)m->B * m->H;
+  a.tm = m->tm;
+  return a;
+}
+
 void build_forward(nnt_model* m) {
   Builder b{m};
   Program& P = m->fwd;
@@ -684,7 +712,26 @@ void build_forward(nnt_model* m) {
     const size_t zq = (size_t)S * hd;  // elements of one head's q (or k, v)
     const char* qkv_base = (const char*)m->qkvh[l];
     const int64_t BH = (int64_t)m->B * H;
-    for (int bt = 0; bt < m->n_bt; ++bt)
+    if (m->flash) {
+      // one fused task per (batch tile, head tile): O and the row log-sum-exp
+      const bf16* qp = reinterpret_cast<const bf16*>(qkv_base);
+      for (int bt = 0; bt < m->n_bt; ++bt)
+        for (int ht = 0; ht < m->n_ht; ++ht) {
+          FlashArgs fa = flash_args(m, bt, ht);
+          fa.o = static_cast<bf16*>(m->O[l]);
+          fa.ldo = d;
+          fa.lse = m->lse[l];
+          Task t;
+          t.type = TT_FLASH_FWD;
+          box(t.uses, m->gqkvh[l], ACC_R, 0, 3, bt, bt + 1, ht, ht + 1);
+          box(t.uses, m->gO[l], ACC_W, bt * m->n_st, (bt + 1) * m->n_st);
+          box(t.uses, m->glse[l], ACC_W, bt, bt + 1, ht, ht + 1);
+          t.flops = 2 * 2.0 * hd * causal_rows(0, S) * fa.nz;  // Q K^T and P V, causal half
+          t.fn = [=](cudaStream_t s) { return launch_flash_fwd(qp, qp + BH * zq, qp + 2 * BH * zq, fa, s); };
+          P.add(std::move(t));
+        }
+    }
+    for (int bt = 0; bt < (m->flash ? 0 : m->n_bt); ++bt)
       for (int ht = 0; ht < m->n_ht; ++ht)
         for (int st = 0; st < m->n_st; ++st) {
           const int nz = m->tb * m->th;
@@ -1111,7 +1158,39 @@ void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
             P_(m, l, OW), pi + OW);
     // attention backward per (batch tile, head tile)
     const char* qkv_base = (const char*)m->qkvh[l];
-    for (int bt = 0; bt < m->n_bt; ++bt)
+    if (m->flash) {
+      // fused: recomputes P from the saved log-sum-exp; dQ, dK, dV head-merged into dqkv
+      const bf16* qp = reinterpret_cast<const bf16*>(qkv_base);
+      for (int bt = 0; bt < m->n_bt; ++bt)
+        for (int ht = 0; ht < m->n_ht; ++ht) {
+          FlashArgs fa = flash_args(m, bt, ht);
+          fa.o = static_cast<bf16*>(m->O[l]);
+          fa.ldo = d;
+          fa.lse = m->lse[l];
+          fa.D = m->attn_d;
+          fa.dq = fa.dk = fa.dv = static_cast<bf16*>(m->dqkv);
+          fa.ldd = 3 * d;
+          fa.dq_col = 0;
+          fa.dk_col = d;
+          fa.dv_col = 2 * d;
+          Task t;
+          t.type = TT_FLASH_BWD;
+          t.kernels = 3;
+          box(t.uses, m->gqkvh[l], ACC_R, 0, 3, bt, bt + 1, ht, ht + 1);
+          box(t.uses, m->gO[l], ACC_R, bt * m->n_st, (bt + 1) * m->n_st);
+          box(t.uses, m->glse[l], ACC_R, bt, bt + 1, ht, ht + 1);
+          box(t.uses, m->gdOh, ACC_R, 0, 1, bt, bt + 1, ht, ht + 1);
+          box(t.uses, m->gattn_d, ACC_RW, bt, bt + 1, ht, ht + 1);
+          box(t.uses, m->gdqkv, ACC_W, 0, 3, bt * m->n_st, (bt + 1) * m->n_st, ht, ht + 1);
+          t.flops = 4 * 2.0 * hd * causal_rows(0, S) * fa.nz;  // dV, dP, dQ, dK, causal half
+          const bf16* dO = static_cast<const bf16*>(m->dOh);
+          t.fn = [=](cudaStream_t s) {
+            return launch_flash_bwd(qp, qp + BH * zq, qp + 2 * BH * zq, dO, fa, s);
+          };
+          P.add(std::move(t));
+        }
+    }
+    for (int bt = 0; bt < (m->flash ? 0 : m->n_bt); ++bt)
       for (int ht = 0; ht < m->n_ht; ++ht) {
         const int nz = m->tb * m->th;
         ZMap zm{bt * m->tb, ht * m->th, m->th, H};
@@ -1281,6 +1360,7 @@ void make_grids(nnt_model* m) {
     m->gstat1.push_back(new_grid(m, m->n_tok));
     m->gqkvh.push_back(new_grid(m, 3, m->n_bt, m->n_ht, m->n_st));
     m->gP.push_back(new_grid(m, m->n_bt, m->n_ht, m->n_st));
+    m->glse.push_back(new_grid(m, m->n_bt, m->n_ht));
     m->gO.push_back(new_grid(m, m->n_tok, m->nce));
     m->gh2.push_back(new_grid(m, m->n_tok, m->nce));
     m->gstat2.push_back(new_grid(m, m->n_tok));
@@ -1288,6 +1368,7 @@ void make_grids(nnt_model* m) {
     m->gg.push_back(new_grid(m, m->n_tok, m->ncf));
   }
   m->gscores = new_grid(m, m->n_bt, m->n_ht, m->n_st);
+  m->gattn_d = new_grid(m, m->n_bt, m->n_ht);
   m->gy = new_grid(m, m->n_tok, m->nce);
   m->gstatf = new_grid(m, m->n_tok);
   m->gz = new_grid(m, m->n_tok, m->ncv);
@@ -1482,6 +1563,16 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
   m->gemm_min_cols = m->opts.gemm_min_task_cols == 0 ? 8192 : std::max(0, m->opts.gemm_min_task_cols);
   if (m->opts.n_streams <= 0) m->opts.n_streams = 2;
   m->opts.n_streams = std::min(m->opts.n_streams, 8);
+  {
+    const bool usable = m->act == NNT_BF16 && m->backend == 0 && flash_supported(m->hd);
+    if (m->opts.flash_attention > 0 && !usable) {
+      set_thread_error("flash attention needs bf16, tensor-core GEMMs and head size 64 or 128 "
+                       "(head size %d)", m->hd);
+      delete m;
+      return fail(nullptr, NNT_ERR_INVALID_ARG);
+    }
+    m->flash = m->opts.flash_attention >= 0 && usable;
+  }
 
   cudaStream_t main = (cudaStream_t)m->opts.stream;
   if (!main) {
@@ -1508,6 +1599,7 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
     build_optimizer(m);
     m->fwd.finalize(m->opts.n_streams);
     m->bwd.finalize(m->opts.n_streams);
+    m->bwda.finalize(m->opts.n_streams);
     m->bwdf.finalize(m->opts.n_streams);
     m->opt.finalize(1);
     s = sync_model(m);
@@ -1767,6 +1859,7 @@ nnt_status nnt_get_stats(const nnt_model* m, nnt_stats* out) {
   out->kernels_forward = m->fwd.kernels();
   out->kernels_backward = m->offload ? m->bwdf.kernels() : m->bwd.kernels();
   out->kernels_adamw = m->opt.kernels();
+  out->flash_attention = m->flash ? 1 : 0;
   return NNT_OK;
 }
 

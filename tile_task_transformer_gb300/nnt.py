@@ -46,7 +46,7 @@ class Options(C.Structure):
                 ("init_std", C.c_float), ("init_zero_bias", C.c_int32), ("n_streams", C.c_int32),
                 ("use_cuda_graph", C.c_int32), ("timeout_ms", C.c_uint32),
                 ("gemm_backend", C.c_int32), ("trace", C.c_int32),
-                ("gemm_min_task_cols", C.c_int32)]
+                ("gemm_min_task_cols", C.c_int32), ("flash_attention", C.c_int32)]
 
 
 class AdamW(C.Structure):
@@ -62,7 +62,8 @@ class Stats(C.Structure):
                 ("n_tasks_backward", C.c_int64), ("n_tasks_adamw", C.c_int64),
                 ("n_tiles", C.c_int64), ("n_params", C.c_int64), ("n_streams", C.c_int32),
                 ("offload_active", C.c_int32), ("kernels_forward", C.c_int64),
-                ("kernels_backward", C.c_int64), ("kernels_adamw", C.c_int64)]
+                ("kernels_backward", C.c_int64), ("kernels_adamw", C.c_int64),
+                ("flash_attention", C.c_int32)]
 
 
 _P = C.c_void_p
@@ -166,14 +167,15 @@ class Model:
     def __init__(self, n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype=BF16,
                  ln_eps=1e-5, tiles=None, seed=0, init_std=0.0, zero_bias=False, stream=None,
                  n_streams=2, use_cuda_graph=False, timeout_ms=0, gemm_backend=0, trace=False,
-                 allow_host_offload=False, hbm_budget_bytes=0, gemm_min_task_cols=0):
+                 allow_host_offload=False, hbm_budget_bytes=0, gemm_min_task_cols=0,
+                 flash_attention=0):
         self.cfg = Config(n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype, ln_eps)
         t = tiles or {}
         self.tiles = Tiles(t.get("batch_tile", 0), t.get("seq_tile", 0), t.get("embd_tile", 0),
                            t.get("inner_tile", 0), t.get("head_tile", 0), t.get("vocab_tile", 0))
         self.opts = Options(_stream(stream), hbm_budget_bytes, int(allow_host_offload), seed,
                             init_std, int(zero_bias), n_streams, int(use_cuda_graph), timeout_ms,
-                            gemm_backend, int(trace), gemm_min_task_cols)
+                            gemm_backend, int(trace), gemm_min_task_cols, flash_attention)
         h = C.c_void_p()
         check(lib().nnt_create_model(C.byref(self.cfg), C.byref(self.tiles), C.byref(self.opts),
                                      C.byref(h)))
