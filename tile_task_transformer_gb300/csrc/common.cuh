@@ -15,6 +15,7 @@ enum DeviceError : uint32_t {
   DEVERR_TOKEN_RANGE = 1u << 0,   // token id >= vocab
   DEVERR_WAIT_TIMEOUT = 1u << 1,  // a bounded mbarrier wait ran out
   DEVERR_BAD_TILE = 1u << 2,      // a tile index out of range (checks build)
+  DEVERR_SMEM_ALIGN = 1u << 3,    // dynamic shared memory not at the alignment a kernel needs
 };
 // Device address of the error word on the current device (for kernels in other
 // translation units), and a stream-ordered read-and-clear of it.

@@ -9,10 +9,11 @@
 // memory, and nothing of size S x S is written to HBM. The backward pass
 // recomputes P from the per-row log-sum-exp saved by the forward.
 //
-// Every kernel runs 128 threads (4 warps). Thread t owns row t of the current
-// tile, which is TMEM lane t (warp w reads lanes 32w..32w+31). Thread 0 also
-// issues the TMA copies and the tcgen05.mma instructions; the other threads
-// only wait for their results. Tiles are [128 rows][hd] bf16 loaded by TMA
+// The tensor-core kernels run 256 threads (8 warps): threads t and t+128 own
+// row t of the current tile, which is TMEM lane t (warp w reads lanes
+// 32(w%4)..32(w%4)+31), each taking one half of the row's columns. Thread 0
+// also issues the TMA copies and the tcgen05.mma instructions; the other
+// threads only wait for their results. Tiles are [128 rows][hd] bf16 loaded by TMA
 // with a 128-byte swizzle as hd/64 chunks of 16 KB; the same smem tile serves
 // as a K-major operand (rows = M or N, K = hd) or an MN-major one (N = hd,
 // K = rows) through its descriptor. P and dS tiles written by the threads use
@@ -37,7 +38,8 @@ namespace nnt {
 namespace {
 
 constexpr int FB = 128;              // queries or keys per block
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;     // forward: two threads per row, one per half of the columns
+constexpr int kBwdThreads = 256;  // backward: the same split
 constexpr int CHUNK = FB * 128;      // one [128 rows][64 bf16] swizzled chunk: 16 KB
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -78,11 +80,11 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint8_t* dst, 
   for (int c = 0; c < HD / 64; ++c) tma_load_3d(dst + c * CHUNK, map, bar, 64 * c, row, z);
 }
 
-// HD/32 chunks of 32 TMEM columns of this thread's row, scaled, to bf16 at dst.
-template <int HD>
+// NCOL (a multiple of 32) TMEM columns of this thread's row, scaled, to bf16 at dst.
+template <int NCOL>
 __device__ __forceinline__ void store_row(uint32_t taddr, bool row_ok, bf16* dst, float scale) {
 #pragma unroll
-  for (int c = 0; c < HD / 32; ++c) {
+  for (int c = 0; c < NCOL / 32; ++c) {
     uint32_t o[32];
     tmem_ld32_nw(taddr + 32 * c, o);
     tmem_wait_ld();
@@ -110,48 +112,62 @@ __device__ __forceinline__ void drain(uint64_t* bar, int n, int* w) {
 template <int HD>
 struct FwdCfg {
   static constexpr int TILE = FB * HD * 2;
-  // Q, K (two stages), V (one buffer), P
-  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 4 * TILE;
+  // Q, K (two stages), V (two stages), P. The halves' row maxima and sums
+  // ([2][128] floats) borrow the start of P while P is free.
+  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE;
+  static constexpr int OFF_RED = OFF_P;
   static constexpr int OFF_BAR = OFF_P + 2 * CHUNK;
-  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  // head size 64: no room to re-align the base by hand if two CTAs are to fit
+  // on an SM; the kernel then requires a 1024-byte aligned dynamic base
+  static constexpr bool FIXED_BASE = HD <= 64;
+  static constexpr int SMEM = OFF_BAR + 128 + (FIXED_BASE ? 0 : 1024);
   static constexpr uint32_t TMEM_COLS = FB + HD <= 256 ? 256 : 512;  // S: 128 columns, O: HD
 };
 
 // Per CTA: item blockIdx % nz, query block nqb-1 - blockIdx / nz (largest
-// first). Key blocks 0..qb in order; K is double-buffered (block j+2 loads once
-// S_j is done), V single-buffered (block j loads once P V_{j-1} is done, and
-// lands while the softmax of block j runs).
+// first). Key blocks 0..qb in order; K and V are double-buffered: once S_j is
+// done (and with it P V_{j-1}), K_{j+2} and V_{j+1} load into the freed
+// stages.
 //
-// Softmax of row r at key block j: m = running maximum of the scaled scores
-// in base 2, l = running sum of 2^(s*c2 - m). The maximum actually used is
-// raised only when a row's new maximum exceeds it by more than 8 (P stays
-// below 2^8, exact in fp32 and in bf16's range); then l and the row of O are
-// multiplied by 2^(m_old - m_new) (O read and written back through TMEM).
+// Two threads per row, one per half of the columns (256 threads; warps w and
+// w+4 share TMEM lanes 32(w%4)..). Softmax of row r at key block j: m =
+// running maximum of the scaled scores in base 2 (the halves' maxima meet in
+// shared memory), l = running sum of 2^(s*c2 - m), kept per half and added at
+// the end. The maximum actually used is raised only when a row's new maximum
+// exceeds it by more than 8 (P stays below 2^8, exact in fp32 and in bf16's
+// range); then l and the row of O are multiplied by 2^(m_old - m_new), each
+// thread rescaling its half of O through TMEM.
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
     flash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FlashArgs a, int nqb, float c2,
                      uint32_t* err) {
   using C = FwdCfg<HD>;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (C::FIXED_BASE && sm != smem_raw) {  // 128-byte swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicOr(err, DEVERR_SMEM_ALIGN);
+    return;
+  }
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* bar_k = bar_q + 1;  // two stages
-  uint64_t* bar_v = bar_q + 3;
-  uint64_t* bar_s = bar_q + 4;
-  uint64_t* bar_o = bar_q + 5;
-  uint64_t* bar_x = bar_q + 6;
+  uint64_t* bar_v = bar_q + 3;  // two stages
+  uint64_t* bar_s = bar_q + 5;
+  uint64_t* bar_o = bar_q + 6;
+  uint64_t* bar_x = bar_q + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
+  float* red = reinterpret_cast<float*>(sm + C::OFF_RED);  // [2][FB]: row maxima, then row sums
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid & (FB - 1), hf = tid >> 7;  // row of the tile, column half
   const int qb = nqb - 1 - (int)(blockIdx.x / a.nz);
   const int item = (int)(blockIdx.x % a.nz);
   const int z = (int)a.zm.z(item);
   const int q0 = qb * FB, nkb = qb + 1;
-  const int q = q0 + tid;
+  const int q = q0 + r;
 
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(bar_q + i, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(bar_q + i, 1);
     mbar_fence_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -165,23 +181,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_v = smem_u32(sm + C::OFF_V), s_p = smem_u32(sm + C::OFF_P);
+  constexpr int HC = FB / 2;  // score columns per thread
+  constexpr int HO = HD / 2;  // O columns per thread
 
-  int n_k[2] = {0, 0}, w_k[2] = {0, 0}, n_v = 0, w_v = 0, w_q = 0;
+  int n_k[2] = {0, 0}, w_k[2] = {0, 0}, n_v[2] = {0, 0}, w_v[2] = {0, 0}, w_q = 0;
+  auto load_kv = [&](const CUtensorMap* map, int off, uint64_t* bar, int blk) {
+    mbar_arrive_expect_tx(bar, C::TILE);
+    load_tile<HD>(map, sm + off + (blk & 1) * C::TILE, bar, blk * FB, z);
+  };
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_q, C::TILE);
     load_tile<HD>(&tmQ, sm + C::OFF_Q, bar_q, q0, z);
-    mbar_arrive_expect_tx(&bar_k[0], C::TILE);
-    load_tile<HD>(&tmK, sm + C::OFF_K, &bar_k[0], 0, z);
-    n_k[0] = 1;
-    mbar_arrive_expect_tx(bar_v, C::TILE);
-    load_tile<HD>(&tmV, sm + C::OFF_V, bar_v, 0, z);
-    n_v = 1;
-    if (nkb > 1) {
-      mbar_arrive_expect_tx(&bar_k[1], C::TILE);
-      load_tile<HD>(&tmK, sm + C::OFF_K + C::TILE, &bar_k[1], FB, z);
-      n_k[1] = 1;
+    for (int blk = 0; blk < 2 && blk < nkb; ++blk) {
+      load_kv(&tmK, C::OFF_K, &bar_k[blk], blk);
+      load_kv(&tmV, C::OFF_V, &bar_v[blk], blk);
+      n_k[blk] = n_v[blk] = 1;
     }
   }
 
@@ -214,32 +230,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
     tc_fence_after();
-    if (tid == 0) {  // S_j done, and with it P V_{j-1}: K stage st and the V buffer are free
+    if (tid == 0) {  // S_j done, and with it P V_{j-1}: K stage j&1 and V stage (j+1)&1 are free
       if (j + 2 < nkb) {
-        mbar_arrive_expect_tx(&bar_k[st], C::TILE);
-        load_tile<HD>(&tmK, sm + C::OFF_K + st * C::TILE, &bar_k[st], (j + 2) * FB, z);
+        load_kv(&tmK, C::OFF_K, &bar_k[st], j + 2);
         ++n_k[st];
       }
-      if (j >= 1) {
-        mbar_arrive_expect_tx(bar_v, C::TILE);
-        load_tile<HD>(&tmV, sm + C::OFF_V, bar_v, j * FB, z);
-        ++n_v;
+      if (j >= 1 && j + 1 < nkb) {
+        load_kv(&tmV, C::OFF_V, &bar_v[st ^ 1], j + 1);
+        ++n_v[st ^ 1];
       }
     }
-    // ---- softmax of row `tid` over keys [j*128, j*128 + 128)
-    uint32_t u[FB];
+    // ---- softmax of row r over keys [j*128, j*128 + 128), columns [hf*64, hf*64 + 64)
+    uint32_t u[HC];
 #pragma unroll
-    for (int c = 0; c < FB / 32; ++c) tmem_ld32_nw(t_row + 32 * c, u + 32 * c);
+    for (int c = 0; c < HC / 32; ++c) tmem_ld32_nw(t_row + hf * HC + 32 * c, u + 32 * c);
     tmem_wait_ld();
     const bool diag = j == nkb - 1;  // keys past the query only in the last block
     float mx = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < FB; ++c) {
+    for (int c = 0; c < HC; ++c) {
       float x = __uint_as_float(u[c]);
-      if (diag && c > tid) x = -INFINITY;
+      if (diag && hf * HC + c > r) x = -INFINITY;
       u[c] = __float_as_uint(x);
       mx = fmaxf(mx, x);
     }
+    red[hf * FB + r] = mx;
+    __syncthreads();
+    mx = fmaxf(mx, red[(hf ^ 1) * FB + r]);
+    __syncthreads();  // the scratch lies in P, written below
     const float m_new = fmaxf(m_used, mx * c2);
     if (j == 0) {
       m_used = m_new;
@@ -252,13 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HO / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32_nw(t_row + FB + 32 * c, o);
+          const uint32_t ta = t_row + FB + hf * HO + 32 * c;
+          tmem_ld32_nw(ta, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(t_row + FB + 32 * c, o);
+          tmem_st32(ta, o);
         }
         tmem_wait_st();
       }
@@ -266,28 +285,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sum = 0.f;
     uint8_t* pt = sm + C::OFF_P;
 #pragma unroll
-    for (int g = 0; g < FB / 8; ++g) {
+    for (int g = 0; g < HC / 8; ++g) {
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         v[e] = ex2f(fmaf(__uint_as_float(u[8 * g + e]), c2, -m_used));
         sum += v[e];
       }
-      put8(pt, tid, g, v);
+      put8(pt, r, hf * (HC / 8) + g, v);
     }
     l += sum;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
-      ok = mbar_wait(bar_v, (uint32_t)(j & 1));
+      ok = mbar_wait(&bar_v[st], (uint32_t)((j >> 1) & 1));
       if (ok) {
-        ++w_v;
+        ++w_v[st];
         tc_fence_after();
+        const uint32_t s_vt = s_v + (uint32_t)(st * C::TILE);
         constexpr uint32_t idesc = make_idesc(FB, HD, false, true);
 #pragma unroll
         for (int kk = 0; kk < FB / 16; ++kk)
-          umma_bf16(tmem + FB, desc_k(s_p, kk), desc_mn(s_v, kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(tmem + FB, desc_k(s_p, kk), desc_mn(s_vt, kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
       }
     }
   }
@@ -297,18 +317,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__syncthreads_or(!ok)) aborted = true;
   }
   if (!aborted) {
+    red[hf * FB + r] = l;  // P's last reader (the final P V) is done
+    __syncthreads();
+    l += red[(hf ^ 1) * FB + r];
     tc_fence_after();
     const int b = a.zm.b(item), h = a.zm.h(item);
     const bool row_ok = q < a.S;
-    bf16* orow = a.o + (row_ok ? a.tm.row(b, q) * a.ldo + a.o_col + (int64_t)h * HD : 0);
-    store_row<HD>(t_row + FB, row_ok, orow, 1.f / l);
-    if (row_ok) a.lse[(int64_t)z * a.S + q] = m_used + log2f(l);
+    bf16* orow = a.o + (row_ok ? a.tm.row(b, q) * a.ldo + a.o_col + (int64_t)h * HD + hf * HO : 0);
+    store_row<HO>(t_row + FB + hf * HO, row_ok, orow, 1.f / l);
+    if (row_ok && hf == 0) a.lse[(int64_t)z * a.S + q] = m_used + log2f(l);
   } else if (tid == 0) {
     atomicOr(err, DEVERR_WAIT_TIMEOUT);
     drain(bar_q, 1, &w_q);
     drain(&bar_k[0], n_k[0], &w_k[0]);
     drain(&bar_k[1], n_k[1], &w_k[1]);
-    drain(bar_v, n_v, &w_v);
+    drain(&bar_v[0], n_v[0], &w_v[0]);
+    drain(&bar_v[1], n_v[1], &w_v[1]);
     umma_commit(bar_x);
     mbar_wait(bar_x, 0);
   }
@@ -322,22 +346,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================ backward
 
-// D[z][s] = sum_j dO[z][s][j] * O(z, s, j); one warp per row.
-__global__ void __launch_bounds__(256) flash_bwd_d_kernel(const bf16* __restrict__ dO, const FlashArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= (int64_t)a.nz * a.S) return;
-  const int item = (int)(r / a.S), s = (int)(r % a.S);
-  const int64_t z = a.zm.z(item);
-  const bf16* dr = dO + (z * a.S + s) * a.hd;
-  const bf16* orow = a.o + a.tm.row(a.zm.b(item), s) * a.ldo + a.o_col + (int64_t)a.zm.h(item) * a.hd;
+__device__ __forceinline__ float dot8_bf16(uint4 x, uint4 y) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
   float acc = 0.f;
-  for (int j = 4 * lane; j < a.hd; j += 128) {
-    const float4 x = load4(dr + j), y = load4(orow + j);
-    acc += (x.x * y.x + x.y * y.y) + (x.z * y.z + x.w * y.w);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[i]));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[i]));
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
   }
-  acc = warp_sum(acc);
-  if (lane == 0) a.D[z * a.S + s] = acc;
+  return acc;
+}
+
+// D[z][s] = sum_j dO[z][s][j] * O(z, s, j). CTA: 32 rows of item blockIdx.y;
+// eight lanes per row, 16 bytes of dO and of O each per step.
+__global__ void __launch_bounds__(256) flash_bwd_d_kernel(const bf16* __restrict__ dO, const FlashArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int item = blockIdx.y;
+  const int s = blockIdx.x * 32 + warp * 4 + (lane >> 3);
+  const int sub = lane & 7;
+  const int64_t z = a.zm.z(item);
+  float acc = 0.f;
+  if (s < a.S) {
+    const bf16* dr = dO + (z * a.S + s) * a.hd;
+    const bf16* orow = a.o + a.tm.row(a.zm.b(item), s) * a.ldo + a.o_col + (int64_t)a.zm.h(item) * a.hd;
+    for (int j = 8 * sub; j < a.hd; j += 64)
+      acc += dot8_bf16(*reinterpret_cast<const uint4*>(dr + j), *reinterpret_cast<const uint4*>(orow + j));
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  if (sub == 0 && s < a.S) a.D[z * a.S + s] = acc;
 }
 
 template <int HD>
@@ -357,7 +397,7 @@ struct KvCfg {
 //   P^T = 2^(S^T c2 - lse), dS^T = scale * P^T (dP^T - D)   (rows = keys, in smem)
 //   dV += P^T dO_i, dK += dS^T Q_i              (TMEM columns 256.., 256+HD..)
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     flash_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                         const FlashArgs a, int nqb, float c2, float scale, uint32_t* err) {
@@ -376,11 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* d_s = lse_s + FB;
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid & (FB - 1), hf = tid >> 7;  // row of the tile, column half
   const int kb = (int)(blockIdx.x / a.nz);
   const int item = (int)(blockIdx.x % a.nz);
   const int z = (int)a.zm.z(item);
   const int n = nqb - kb;
-  const int key = kb * FB + tid;
+  const int key = kb * FB + r;
 
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(bar_kv + i, 1);
@@ -398,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t s_k = smem_u32(sm + C::OFF_K), s_v = smem_u32(sm + C::OFF_V);
   const uint32_t s_pt = smem_u32(sm + C::OFF_PT), s_ds = smem_u32(sm + C::OFF_DS);
 
@@ -420,24 +461,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   bool ok = true, aborted = false;
+  // column r of query block i: lse (first half of the threads) or D (second);
+  // the next block's value is loaded one iteration ahead
+  const float* rowsrc = hf ? a.D : a.lse;
+  auto row_val = [&](int i) {
+    const int qc = i * FB + r;
+    return qc < a.S ? rowsrc[(int64_t)z * a.S + qc] : 0.f;
+  };
+  // refill the stage freed by iteration it-1 with the operands of iteration it+NS-1
+  auto refill = [&](int it) {
+    if (ok && it >= 1 && it + NS - 1 < n) {
+      const int s2 = (it + NS - 1) % NS;
+      ok = mbar_wait(&bar_free[s2], (uint32_t)(((it - 1) / NS) & 1));
+      if (ok) {
+        load_qdo(s2, kb + it + NS - 1);
+        ++n_ld[s2];
+      }
+    }
+  };
+  float row_next = row_val(kb);
   for (int it = 0; it < n; ++it) {
     const int i = kb + it, st = it % NS;
-    const int qc = i * FB + tid;  // this thread's column of the query block
-    const float lse_c = qc < a.S ? a.lse[(int64_t)z * a.S + qc] : 0.f;
-    const float d_c = qc < a.S ? a.D[(int64_t)z * a.S + qc] : 0.f;
+    const float row_c = row_next;
+    if (it + 1 < n) row_next = row_val(i + 1);
     if (tid == 0) {
       if (it == 0) {
         ok = mbar_wait(bar_kv, 0);
         w_kv = ok ? 1 : 0;
       }
-      if (ok && it >= 1 && it + NS - 1 < n) {  // refill the stage freed by iteration it-1
-        const int s2 = (it + NS - 1) % NS;
-        ok = mbar_wait(&bar_free[s2], (uint32_t)(((it - 1) / NS) & 1));
-        if (ok) {
-          load_qdo(s2, i + NS - 1);
-          ++n_ld[s2];
-        }
-      }
+      if (NS == 1) refill(it);  // single stage: the operands of this iteration
       if (ok) {
         ok = mbar_wait(&bar_ld[st], (uint32_t)((it / NS) & 1));
         if (ok) ++w_ld[st];
@@ -454,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tmem + FB, desc_k(s_v, kk), desc_k(s_do, kk), idesc, kk > 0 ? 1u : 0u);
         umma_commit(bar_s);
       }
+      if (NS > 1) refill(it);  // after the issue, so the MMAs queue back to back
     }
-    lse_s[tid] = lse_c;
-    d_s[tid] = d_c;
+    (hf ? d_s : lse_s)[r] = row_c;
     if (ok) ok = mbar_wait(bar_s, (uint32_t)(it & 1));
     if (__syncthreads_or(!ok)) {
       aborted = true;
@@ -467,7 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* pt = sm + C::OFF_PT;
     uint8_t* dst = sm + C::OFF_DS;
 #pragma unroll
-    for (int c = 0; c < FB / 32; ++c) {
+    for (int cc = 0; cc < 2; ++cc) {  // this thread's 64 query columns
+      const int c = 2 * hf + cc;
       uint32_t sv[32], dv[32];
       tmem_ld32_nw(t_row + 32 * c, sv);
       tmem_ld32_nw(t_row + FB + 32 * c, dv);
@@ -476,15 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int qq = 32 * c + e;
-        const bool valid = i * FB + qq < a.S && (!diag || qq >= tid);
+        const bool valid = i * FB + qq < a.S && (!diag || qq >= r);
         const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_s[qq])) : 0.f;
         p[e] = pv;
         ds[e] = pv * (__uint_as_float(dv[e]) - d_s[qq]) * scale;
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        put8(pt, tid, 4 * c + g, p + 8 * g);
-        put8(dst, tid, 4 * c + g, ds + 8 * g);
+        put8(pt, r, 4 * c + g, p + 8 * g);
+        put8(dst, r, 4 * c + g, ds + 8 * g);
       }
     }
     fence_async_smem();
@@ -514,8 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = a.zm.b(item), h = a.zm.h(item);
     const bool row_ok = key < a.S;
     const int64_t row = row_ok ? a.tm.row(b, key) * a.ldd : 0;
-    store_row<HD>(t_row + 2 * FB, row_ok, a.dv + row + a.dv_col + (int64_t)h * HD, 1.f);
-    store_row<HD>(t_row + 2 * FB + HD, row_ok, a.dk + row + a.dk_col + (int64_t)h * HD, 1.f);
+    const int c0 = hf * (HD / 2);  // this thread's half of the columns
+    store_row<HD / 2>(t_row + 2 * FB + c0, row_ok, a.dv + row + a.dv_col + (int64_t)h * HD + c0, 1.f);
+    store_row<HD / 2>(t_row + 2 * FB + HD + c0, row_ok, a.dk + row + a.dk_col + (int64_t)h * HD + c0, 1.f);
   } else if (tid == 0) {
     atomicOr(err, DEVERR_WAIT_TIMEOUT);
     drain(bar_kv, 1, &w_kv);
@@ -548,7 +602,7 @@ struct QCfg {
 //   dS = scale * P (dP - D), P = 2^(S c2 - lse)  (rows = queries, in smem)
 //   dQ += dS K_j                                (TMEM columns 256..)
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     flash_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const FlashArgs a, int nqb, float c2, float scale, uint32_t* err) {
@@ -565,11 +619,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_qd + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid & (FB - 1), hf = tid >> 7;  // row of the tile, column half
   const int qb = nqb - 1 - (int)(blockIdx.x / a.nz);
   const int item = (int)(blockIdx.x % a.nz);
   const int z = (int)a.zm.z(item);
   const int n = qb + 1;
-  const int q = qb * FB + tid;
+  const int q = qb * FB + r;
   const float lse_r = q < a.S ? a.lse[(int64_t)z * a.S + q] : 0.f;
   const float d_r = q < a.S ? a.D[(int64_t)z * a.S + q] : 0.f;
 
@@ -589,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_do = smem_u32(sm + C::OFF_DO);
   const uint32_t s_ds = smem_u32(sm + C::OFF_DS);
 
@@ -618,14 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar_qd, 0);
         w_qd = ok ? 1 : 0;
       }
-      if (ok && j >= 1 && j + NS - 1 < n) {
-        const int s2 = (j + NS - 1) % NS;
-        ok = mbar_wait(&bar_free[s2], (uint32_t)(((j - 1) / NS) & 1));
-        if (ok) {
-          load_kv(s2, j + NS - 1);
-          ++n_ld[s2];
-        }
-      }
       if (ok) {
         ok = mbar_wait(&bar_ld[st], (uint32_t)((j / NS) & 1));
         if (ok) ++w_ld[st];
@@ -642,6 +689,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tmem + FB, desc_k(s_do, kk), desc_k(s_vt, kk), idesc, kk > 0 ? 1u : 0u);
         umma_commit(bar_s);
       }
+      // refill the stage freed by iteration j-1 (after the issue, so the MMAs
+      // queue back to back)
+      if (ok && j >= 1 && j + NS - 1 < n) {
+        const int s2 = (j + NS - 1) % NS;
+        ok = mbar_wait(&bar_free[s2], (uint32_t)(((j - 1) / NS) & 1));
+        if (ok) {
+          load_kv(s2, j + NS - 1);
+          ++n_ld[s2];
+        }
+      }
     }
     if (ok) ok = mbar_wait(bar_s, (uint32_t)(j & 1));
     if (__syncthreads_or(!ok)) {
@@ -652,7 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool diag = j == qb;
     uint8_t* dst = sm + C::OFF_DS;
 #pragma unroll
-    for (int c = 0; c < FB / 32; ++c) {
+    for (int cc = 0; cc < 2; ++cc) {  // this thread's 64 key columns
+      const int c = 2 * hf + cc;
       uint32_t sv[32], dv[32];
       tmem_ld32_nw(t_row + 32 * c, sv);
       tmem_ld32_nw(t_row + FB + 32 * c, dv);
@@ -660,12 +718,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float ds[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const bool valid = !diag || 32 * c + e <= tid;
+        const bool valid = !diag || 32 * c + e <= r;
         const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_r)) : 0.f;
         ds[e] = pv * (__uint_as_float(dv[e]) - d_r) * scale;
       }
 #pragma unroll
-      for (int g = 0; g < 4; ++g) put8(dst, tid, 4 * c + g, ds + 8 * g);
+      for (int g = 0; g < 4; ++g) put8(dst, r, 4 * c + g, ds + 8 * g);
     }
     fence_async_smem();
     tc_fence_before();
@@ -690,7 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = a.zm.b(item), h = a.zm.h(item);
     const bool row_ok = q < a.S;
     const int64_t row = row_ok ? a.tm.row(b, q) * a.ldd : 0;
-    store_row<HD>(t_row + 2 * FB, row_ok, a.dq + row + a.dq_col + (int64_t)h * HD, 1.f);
+    const int c0 = hf * (HD / 2);
+    store_row<HD / 2>(t_row + 2 * FB + c0, row_ok, a.dq + row + a.dq_col + (int64_t)h * HD + c0, 1.f);
   } else if (tid == 0) {
     atomicOr(err, DEVERR_WAIT_TIMEOUT);
     drain(bar_qd, 1, &w_qd);
@@ -728,6 +787,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 nnt_status check_args(const FlashArgs& a, const void* q, const void* k, const void* v) {
   NNT_CHECK_ARG(flash_supported(a.hd), "flash attention: head size %d (supported: 64, 128)", a.hd);
   NNT_CHECK_ARG(a.S > 0 && a.nz > 0 && a.z_total > 0, "flash attention: empty problem");
+  NNT_CHECK_ARG(a.nz <= 65535, "flash attention: more than 65535 (sequence, head) items in one launch");
   NNT_CHECK_ARG(a.zm.z(a.nz - 1) < a.z_total && a.zm.z(0) >= 0, "flash attention: item out of range");
   NNT_CHECK_ARG(q && k && v && aligned16(q) && aligned16(k) && aligned16(v),
                 "flash attention: q, k, v must be 16-byte aligned device pointers");
@@ -777,11 +837,11 @@ nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, c
   const int nqb = (int)ceil_div(a.S, FB);
   const double scale = 1.0 / sqrt((double)HD);
   const float c2 = (float)(1.4426950408889634 * scale);
-  flash_bwd_d_kernel<<<(unsigned)ceil_div((int64_t)a.nz * a.S, 8), 256, 0, st>>>(dO, a);
+  flash_bwd_d_kernel<<<dim3((unsigned)ceil_div(a.S, 32), (unsigned)a.nz), 256, 0, st>>>(dO, a);
   NNT_TRY(launch_check("flash_bwd_d"));
-  kv<<<(unsigned)(nqb * a.nz), kThreads, KvCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+  kv<<<(unsigned)(nqb * a.nz), kBwdThreads, KvCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
   NNT_TRY(launch_check("flash_bwd_kv"));
-  qk<<<(unsigned)(nqb * a.nz), kThreads, QCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+  qk<<<(unsigned)(nqb * a.nz), kBwdThreads, QCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
   return launch_check("flash_bwd_q");
 }
 

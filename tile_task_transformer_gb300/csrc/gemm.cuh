@@ -52,6 +52,10 @@ struct GemmArgs {
   float alpha = 1.f;
   int beta = 0;
   int epi = EPI_STORE;
+  // fp32 workspace for splitting K across CTAs (plain fp32 stores only; see
+  // gemm_split_k): partial products go here, then a fixed-order sum into C
+  float* ws = nullptr;
+  int64_t ws_elems = 0;
   const float* bias = nullptr;
   const float* resid = nullptr;
   int64_t ld_resid = 0;
@@ -130,5 +134,12 @@ nnt_status gemm(const GemmArgs& g, int backend, cudaStream_t st);
 nnt_status gemm_simt(const GemmArgs& g, cudaStream_t st);
 nnt_status gemm_tc(const GemmArgs& g, cudaStream_t st);  // NNT_ERR_INVALID_ARG if unsupported
 bool gemm_tc_supported(const GemmArgs& g);
+// Number of K slices the tensor-core path uses for g when a workspace of
+// ws_elems floats is available (1 = no split). A split GEMM computes the
+// slices as a batch of products into the workspace and sums them in slice
+// order into C, so the result does not depend on scheduling. Only plain fp32
+// outputs without bias, residual or activation, one batch item, alpha 1, and
+// few output tiles for the SM count qualify.
+int gemm_split_k(const GemmArgs& g, int64_t ws_elems);
 
 }  // namespace nnt

@@ -85,8 +85,8 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int STAGES = BN >= 192 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int TMEM_COLS = BN == 192 ? 512 : 2 * BN;  // two accumulators, power of two
   static constexpr int BAR_BYTES = 256;
   // per epilogue warp: a 32x32 output chunk (4 KB) and a 32x32 fp32 GELU input chunk (4 KB)
   static constexpr int STAGING_BYTES = 4 * 8192;
@@ -137,12 +137,33 @@ __device__ __forceinline__ TileCoord tile_at(const GemmArgs& g, const TileSpace&
   return c;
 }
 
+// tanh-form GELU and its derivative with the hardware tanh approximation
+// (relative error about 2^-11, below the bf16 rounding of the values these
+// epilogues produce; the CUDA-core path keeps the library tanhf).
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_fwd_fast(float u) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  return 0.5f * u * (1.0f + tanh_fast(c * (u + a * u * u * u)));
+}
+__device__ __forceinline__ float gelu_grad_fast(float u) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float t = tanh_fast(c * (u + a * u * u * u));
+  return 0.5f * (1.0f + t) + 0.5f * u * (1.0f - t * t) * c * (1.0f + 3.0f * a * u * u);
+}
+
 // Elementwise epilogue of one 32-column chunk of row m held in registers
 // (columns nb..nb+31; `full`: all of them inside the window). Bias loads are
-// the same address across the warp (broadcast); residual / GELU-input loads
-// read each thread's own row segment.
+// the same address across the warp (broadcast). `pre` holds this row's 32
+// residual (EPI_STORE) or GELU-input (EPI_GELU_BWD) values when the chunk lies
+// wholly inside the window (loaded coalesced and transposed through shared
+// memory by the caller); otherwise they are read here element by element.
 __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool row_ok, int nb,
-                                          int n_lo, int n_hi, bool full, float* v, float* u_out) {
+                                          int n_lo, int n_hi, bool full, float* v, float* u_out,
+                                          const float* pre) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] *= g.alpha;
   if (g.bias) {
@@ -159,16 +180,12 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool 
     }
   }
   if (g.epi == EPI_STORE) {
-    const float* add = nullptr;
-    if (g.resid) add = g.resid + (int64_t)m * g.ld_resid;
-    if (add && row_ok) {
-      if (full) {
+    if (g.resid && row_ok) {
+      if (pre) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 r = *(reinterpret_cast<const float4*>(add + nb) + k);
-          v[4 * k] += r.x; v[4 * k + 1] += r.y; v[4 * k + 2] += r.z; v[4 * k + 3] += r.w;
-        }
+        for (int j = 0; j < 32; ++j) v[j] += pre[j];
       } else {
+        const float* add = g.resid + (int64_t)m * g.ld_resid;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (nb + j >= n_lo && nb + j < n_hi) v[j] += add[nb + j];
@@ -183,21 +200,17 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool 
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       u_out[j] = v[j];
-      v[j] = gelu_fwd_dev(v[j]);
+      v[j] = gelu_fwd_fast(v[j]);
     }
   } else if (row_ok) {  // EPI_GELU_BWD
-    const float* u = g.aux + (int64_t)m * g.ld_aux;
-    if (full) {
+    if (pre) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 r = *(reinterpret_cast<const float4*>(u + nb) + k);
-        v[4 * k] *= gelu_grad_dev(r.x); v[4 * k + 1] *= gelu_grad_dev(r.y);
-        v[4 * k + 2] *= gelu_grad_dev(r.z); v[4 * k + 3] *= gelu_grad_dev(r.w);
-      }
+      for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_fast(pre[j]);
     } else {
+      const float* u = g.aux + (int64_t)m * g.ld_aux;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= gelu_grad_dev(u[nb + j]);
+        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= gelu_grad_fast(u[nb + j]);
     }
   }
 }
@@ -378,6 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stage_base = smem + C::STAGES * C::STAGE + (warp - 2) * 8192;
     const bool cbf = g.c_dtype == NNT_BF16;
     const bool gelu = g.epi == EPI_GELU;
+    // residual (EPI_STORE) or GELU input (EPI_GELU_BWD): each chunk's 32x32
+    // block is read coalesced one chunk ahead and turned into one row per lane
+    // through the chunk's (free) output staging buffer
+    const float* src = g.epi == EPI_GELU_BWD ? g.aux : (g.epi == EPI_STORE ? g.resid : nullptr);
+    const int64_t ld_src = g.epi == EPI_GELU_BWD ? g.ld_aux : g.ld_resid;
     int buf = 0;
     int issued = 0;  // bulk store groups of this warp so far
     int acc = 0;
@@ -396,11 +414,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m >= c.m_start && m < c.m_end;
       const bool rows_full = row0 >= c.m_start && row0 + 32 <= c.m_end;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+      // lane reads rows 4*rr + lane/8 of the block, 16 bytes at column 4*(lane%8)
+      float4 pf[8];
+      auto prefetch = [&](int nb_) {
+        const bool whole = src && rows_full && nb_ >= c.n_start && nb_ + 32 <= c.n_end;
+        if (whole) {
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr)
+            pf[rr] = __ldg(reinterpret_cast<const float4*>(src + (int64_t)(row0 + 4 * rr + (lane >> 3)) * ld_src +
+                                                           nb_ + 4 * (lane & 7)));
+        }
+        return whole;
+      };
+      bool have = prefetch(c.n_box);
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         const int nb = c.n_box + ch * 32;
         if (nb >= c.n_end) break;  // uniform across the warp
-        float v[32], u[32];
+        float v[32], u[32], pre[32];
         tmem_ld32(tbase + ch * 32, v);
         if (row0 >= c.m_end) continue;  // no row of this warp in the window (uniform)
         const bool cols_full = nb >= c.n_start && nb + 32 <= c.n_end;
@@ -408,7 +439,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ts.c_mode == 1) tma = row0 >= c.m_start && nb >= c.n_start;
         else tma = ts.c_mode > 1 && rows_full && cols_full;
         if (tma && g.epi == EPI_GELU && !ts.aux_tma) tma = false;
-        epi_chunk(g, c.i, m, row_ok, nb, c.n_start, c.n_end, cols_full, v, u);
+        uint8_t* stage_c = stage_base + (gelu ? 0 : buf * 4096);
+        uint8_t* stage_u = stage_base + 4096;
+        const bool have_cur = have;
+        if ((tma || have_cur) && issued >= (gelu ? 1 : 2)) {
+          // the group that last used this buffer must have finished reading it
+          if (lane == 0) {
+            if (gelu) bulk_wait_read();
+            else bulk_wait_read1();
+          }
+          __syncwarp();
+        }
+        if (have_cur) {
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            const int rl = 4 * rr + (lane >> 3);
+            *reinterpret_cast<float4*>(stage_c + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4)) = pf[rr];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 x = *reinterpret_cast<const float4*>(stage_c + lane * 128 + ((k ^ (lane & 7)) << 4));
+            pre[4 * k] = x.x; pre[4 * k + 1] = x.y; pre[4 * k + 2] = x.z; pre[4 * k + 3] = x.w;
+          }
+          __syncwarp();
+        }
+        have = ch + 1 < BN / 32 && prefetch(nb + 32);  // next chunk's block, in flight meanwhile
+        epi_chunk(g, c.i, m, row_ok, nb, c.n_start, c.n_end, cols_full, v, u, have_cur ? pre : nullptr);
         if (!tma) {
           if (row_ok) {
 #pragma unroll
@@ -422,16 +479,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           continue;
-        }
-        uint8_t* stage_c = stage_base + (gelu ? 0 : buf * 4096);
-        uint8_t* stage_u = stage_base + 4096;
-        if (issued >= (gelu ? 1 : 2)) {
-          // the group that last used this buffer must have finished reading it
-          if (lane == 0) {
-            if (gelu) bulk_wait_read();
-            else bulk_wait_read1();
-          }
-          __syncwarp();
         }
         if (cbf) stage_bf16(stage_c, lane, v);
         else stage_f32(stage_c, lane, v);
@@ -632,7 +679,7 @@ int bn_override() {
   if (v < 0) {
     const char* e = getenv("NNT_GEMM_BN");
     v = e ? atoi(e) : 0;
-    if (v != 64 && v != 128 && v != 256) v = 0;
+    if (v != 64 && v != 128 && v != 192 && v != 256) v = 0;
   }
   return v;
 }
@@ -643,11 +690,12 @@ int choose_bn(const GemmArgs& g) {
   const int sms = num_sms();
   double best = 0;
   int best_bn = 64;
-  for (int bn : {256, 128, 64}) {
+  for (int bn : {256, 192, 128, 64}) {
     if (bn > 64 && g.nt <= bn / 2) continue;
     const TileSpace t = tile_space(g, bn);
     const double waves = std::ceil((double)t.total / sms);
-    const double eff = (double)t.total / (waves * sms) * (bn == 256 ? 1.0 : bn == 128 ? 0.8 : 0.35);
+    const double eff = (double)t.total / (waves * sms) *
+                       (bn == 256 ? 1.0 : bn == 192 ? 0.95 : bn == 128 ? 0.8 : 0.35);
     if (eff > best + 1e-9) {
       best = eff;
       best_bn = bn;
@@ -676,16 +724,90 @@ bool gemm_tc_supported(const GemmArgs& g) {
   return true;
 }
 
+nnt_status gemm_tc_one(const GemmArgs& g, cudaStream_t st) {
+  switch (choose_bn(g)) {
+    case 256: return launch_bn<256>(g, st);
+    case 192: return launch_bn<192>(g, st);
+    case 128: return launch_bn<128>(g, st);
+    default: return launch_bn<64>(g, st);
+  }
+}
+
+// out[(m - c_row0) * ldc + n] (+)= sum over slices s in order of
+// ws[s][m - m0][n - n0], for the window rows m and columns n.
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t mt, int nt,
+                                     float* C, int64_t ldc, int accumulate) {
+  const int64_t n4 = (int64_t)mt * (nt / 4);
+  const int64_t win = (int64_t)mt * nt;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / (nt / 4);
+    const int c = (int)(i - r * (nt / 4)) * 4;
+    float4 t = *reinterpret_cast<const float4*>(ws + r * nt + c);
+    for (int s = 1; s < split; ++s) {
+      const float4 u = *reinterpret_cast<const float4*>(ws + s * win + r * nt + c);
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    float4* o = reinterpret_cast<float4*>(C + r * ldc + c);
+    if (accumulate) {
+      const float4 p = *o;
+      t.x += p.x; t.y += p.y; t.z += p.z; t.w += p.w;
+    }
+    *o = t;
+  }
+}
+
+// K split into `split` equal slices run as batch items of one launch (operand
+// offsets of i*K/split along K, outputs to workspace slice i), then summed.
+nnt_status gemm_tc_split(const GemmArgs& g, int split, cudaStream_t st) {
+  NNT_CHECK_ARG(g.nt % 4 == 0 && g.ldc % 4 == 0, "split GEMM: output width and ldc must be multiples of 4");
+  const int ks = g.K / split;
+  GemmArgs b = g;
+  b.K = ks;
+  b.nbatch = split;
+  b.zm = ZMap{0, 0, 1, 1};
+  b.a_zs = g.a_trans ? (int64_t)ks * g.lda : ks;
+  b.b_zs = g.b_trans ? (int64_t)ks * g.ldb : ks;
+  b.C = g.ws - g.n0;  // slice z row m, column n at ws[z * mt*nt + (m - m0) * nt + (n - n0)]
+  b.c_row0 = g.m0;
+  b.ldc = g.nt;
+  b.c_zs = (int64_t)g.mt * g.nt;
+  b.beta = 0;
+  b.ws = nullptr;
+  NNT_TRY(gemm_tc_one(b, st));
+  float* out = static_cast<float*>(g.C) + (int64_t)(g.m0 - g.c_row0) * g.ldc + g.n0;
+  const int64_t n4 = (int64_t)g.mt * (g.nt / 4);
+  const int grid = (int)std::min<int64_t>((n4 + 255) / 256, 4 * num_sms());
+  splitk_reduce_kernel<<<grid, 256, 0, st>>>(g.ws, split, g.mt, g.nt, out, g.ldc, g.beta);
+  return launch_check("splitk_reduce");
+}
+
 nnt_status gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if (!gemm_tc_supported(g)) {
     set_thread_error("gemm_tc: unsupported shape/layout");
     return NNT_ERR_INVALID_ARG;
   }
-  switch (choose_bn(g)) {
-    case 256: return launch_bn<256>(g, st);
-    case 128: return launch_bn<128>(g, st);
-    default: return launch_bn<64>(g, st);
+  const int split = gemm_split_k(g, g.ws ? g.ws_elems : 0);
+  if (split > 1) return gemm_tc_split(g, split, st);
+  return gemm_tc_one(g, st);
+}
+
+int gemm_split_k(const GemmArgs& g, int64_t ws_elems) {
+  if (ws_elems <= 0 || g.out_mode != OUT_PLAIN || g.epi != EPI_STORE || g.c_dtype != NNT_F32 ||
+      g.bias || g.resid || g.aux || g.nbatch != 1 || g.alpha != 1.f || g.causal != CAUSAL_NONE)
+    return 1;
+  const int sms = num_sms();
+  const int tiles = tile_space(g, choose_bn(g)).total;
+  if (2 * tiles > sms) return 1;
+  // the most slices that fill the SMs once, each at least 8 k-blocks deep and
+  // an exact share of K (the slices are batch items of one launch)
+  int best = 1;
+  for (int s = 2; s <= 8; s *= 2) {
+    if (tiles * s > sms || g.K % (s * BK) != 0 || g.K / (s * BK) < 8) break;
+    if ((int64_t)s * g.mt * g.nt > ws_elems) break;
+    best = s;
   }
+  return best;
 }
 
 }  // namespace nnt

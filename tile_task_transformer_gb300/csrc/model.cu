@@ -140,12 +140,15 @@ struct nnt_model {
   float *ln_part_g = nullptr, *ln_part_b = nullptr;
   float* col_part = nullptr;
   uint32_t* sort_keys = nullptr;
+  // split-K workspace of the weight-gradient GEMMs (few output tiles, K = all tokens)
+  float* splitk_ws = nullptr;
+  int64_t splitk_elems = 0;
 
   // tile grids
   std::vector<TGrid> gx, gxmid, gh1, gqkvh, gP, gO, gh2, gu, gg, gstat1, gstat2, glse;
   TGrid gattn_d;
   TGrid gscores, gy, gstatf, gz, gdz, grow_loss, gloss, gtok;
-  TGrid gdres, gdres_act, gdtmp, gdu, gdOh, gdqkv, gln_part, gcol_part, gkeys;
+  TGrid gdres, gdres_act, gdtmp, gdu, gdOh, gdqkv, gln_part, gcol_part, gkeys, gsplitk;
   std::vector<TGrid> gparam, ggrad;
   int64_t next_tile = 0;
 
@@ -528,6 +531,10 @@ nnt_status alloc_all(nnt_model* m) {
   NNT_TRY(dalloc(m, m->ln_part_g, (size_t)ln_colsum_chunks(T) * 3 * d * 4));
   const int64_t maxcols = std::max<int64_t>(3 * d, f);
   NNT_TRY(dalloc(m, m->col_part, (size_t)colsum_nparts(T) * maxcols * 4));
+  if (m->act == NNT_BF16 && m->backend == 0) {  // 32 MB: the split weight-gradient GEMMs of small models
+    m->splitk_elems = 8ll << 20;
+    NNT_TRY(dalloc(m, m->splitk_ws, (size_t)m->splitk_elems * 4));
+  }
   NNT_TRY(dalloc(m, m->sort_keys, (size_t)T * 4));
   // padding columns of the logits must stay finite: zero them once
   NNT_CUDA_TRY(cudaMemset(m->z, 0, (size_t)T * m->ldz * 4));
@@ -576,12 +583,21 @@ struct Builder {
   int st_of(int rt) const { return rt % m->n_st; }
 
   // GEMM task helper
-  void gemm_task(Program& P, int type, const GemmArgs& g, std::vector<TileUse> uses, double flops) {
+  void gemm_task(Program& P, int type, const GemmArgs& g0, std::vector<TileUse> uses, double flops) {
     Task t;
     t.type = type;
+    GemmArgs g = g0;
+    const int be = m->backend;
+    // GEMMs with too few output tiles for the SMs (the weight gradients of small
+    // layers) split K through the shared workspace, one such task at a time
+    if (m->splitk_ws && be == 0 && gemm_tc_supported(g) && gemm_split_k(g, m->splitk_elems) > 1) {
+      g.ws = m->splitk_ws;
+      g.ws_elems = m->splitk_elems;
+      box(uses, m->gsplitk, ACC_RW);
+      t.kernels = 2;
+    }
     t.uses = std::move(uses);
     t.flops = flops;
-    const int be = m->backend;
     t.fn = [g, be](cudaStream_t s) { return gemm(g, be, s); };
     P.add(std::move(t));
   }
@@ -1385,6 +1401,7 @@ void make_grids(nnt_model* m) {
   m->gln_part = new_grid(m, m->n_tok);
   m->gcol_part = new_grid(m, 1);
   m->gkeys = new_grid(m, 1);
+  m->gsplitk = new_grid(m, 1);
   // parameter gradients: weights tiled [out tile, in tile], vectors by their axis
   for (const ParamInfo& p : m->params) {
     int a = tiles_of((int)p.shape0, axis_tile(m, p.shape0));
