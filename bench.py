@@ -68,7 +68,7 @@ def gemm_traffic(workload):
         d = json.load(fh)
     csrc = os.path.join(ROOT, "tile_task_transformer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "gemm.cuh"):
+    for f in ("gemm_tc.cu", "gemm.cuh", "tc_ptx.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return d["bytes_per_launch"] if h.hexdigest() == d.get("source_sha256") else None
