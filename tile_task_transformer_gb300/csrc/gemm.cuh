@@ -10,7 +10,7 @@ namespace nnt {
 
 enum EpiKind : int {
   EPI_STORE = 0,     // C = alpha*acc (+ bias[n]) (+ resid[m, n]) (+ C if beta)
-  EPI_GELU = 1,      // u = alpha*acc + bias[n] -> aux (fp32); C = gelu(u)
+  EPI_GELU = 1,      // u = alpha*acc + bias[n] -> aux (aux_dtype); C = gelu(u)
   EPI_GELU_BWD = 2,  // C = alpha*acc * gelu'(aux[m, n])
 };
 
@@ -59,8 +59,9 @@ struct GemmArgs {
   const float* bias = nullptr;
   const float* resid = nullptr;
   int64_t ld_resid = 0;
-  float* aux = nullptr;
+  void* aux = nullptr;  // GELU input u: written by EPI_GELU, read by EPI_GELU_BWD
   int64_t ld_aux = 0;
+  int aux_dtype = NNT_F32;  // NNT_F32 or NNT_BF16
   int causal = CAUSAL_NONE;
 };
 
@@ -72,6 +73,17 @@ __device__ __forceinline__ float gelu_grad_dev(float u) {
   const float c = 0.7978845608028654f, a = 0.044715f;
   const float t = tanhf(c * (u + a * u * u * u));
   return 0.5f * (1.0f + t) + 0.5f * u * (1.0f - t * t) * c * (1.0f + 3.0f * a * u * u);
+}
+
+__device__ __forceinline__ float aux_load(const GemmArgs& g, int64_t idx) {
+  return g.aux_dtype == NNT_BF16 ? __bfloat162float(static_cast<const bf16*>(g.aux)[idx])
+                                 : static_cast<const float*>(g.aux)[idx];
+}
+__device__ __forceinline__ void aux_store(const GemmArgs& g, int64_t idx, float v) {
+  if (g.aux_dtype == NNT_BF16)
+    static_cast<bf16*>(g.aux)[idx] = __float2bfloat16_rn(v);
+  else
+    static_cast<float*>(g.aux)[idx] = v;
 }
 
 // Element offset of output (i, m, n) in C.
@@ -99,10 +111,10 @@ __device__ __forceinline__ void epilogue_one(const GemmArgs& g, int i, int m, in
     if (g.beta) v += static_cast<const float*>(g.C)[o];
   } else if (g.epi == EPI_GELU) {
     if (g.bias) v += g.bias[n];
-    g.aux[(int64_t)m * g.ld_aux + n] = v;
+    aux_store(g, (int64_t)m * g.ld_aux + n, v);
     v = gelu_fwd_dev(v);
   } else {  // EPI_GELU_BWD
-    v *= gelu_grad_dev(g.aux[(int64_t)m * g.ld_aux + n]);
+    v *= gelu_grad_dev(aux_load(g, (int64_t)m * g.ld_aux + n));
   }
   if (g.c_dtype == NNT_BF16)
     static_cast<bf16*>(g.C)[o] = __float2bfloat16_rn(v);

@@ -207,10 +207,10 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool 
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_fast(pre[j]);
     } else {
-      const float* u = g.aux + (int64_t)m * g.ld_aux;
+      const int64_t ub = (int64_t)m * g.ld_aux;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= gelu_grad_fast(u[nb + j]);
+        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= gelu_grad_fast(aux_load(g, ub + nb + j));
     }
   }
 }
@@ -385,16 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
     const int q = warp & 3;
-    // Staging: 8 KB per warp. GELU epilogues use it as output chunk + GELU input
-    // chunk (one store group in flight); the others ping-pong two 4 KB output
-    // buffers (two store groups in flight).
+    // Staging: 8 KB per warp, two 4 KB halves ping-ponged so that two
+    // bulk-store groups can be in flight; a GELU epilogue with bf16 output and
+    // bf16 u puts both 2 KB chunks in one half. With an fp32 u the whole 8 KB
+    // serves one chunk (one group in flight).
     uint8_t* stage_base = smem + C::STAGES * C::STAGE + (warp - 2) * 8192;
     const bool cbf = g.c_dtype == NNT_BF16;
     const bool gelu = g.epi == EPI_GELU;
+    const bool ubf = g.aux_dtype == NNT_BF16;
+    const bool single = gelu && !(cbf && ubf);
     // residual (EPI_STORE) or GELU input (EPI_GELU_BWD): each chunk's 32x32
     // block is read coalesced one chunk ahead and turned into one row per lane
     // through the chunk's (free) output staging buffer
-    const float* src = g.epi == EPI_GELU_BWD ? g.aux : (g.epi == EPI_STORE ? g.resid : nullptr);
+    const void* src = g.epi == EPI_GELU_BWD ? g.aux : (g.epi == EPI_STORE ? g.resid : nullptr);
+    const bool src_bf = g.epi == EPI_GELU_BWD && ubf;
     const int64_t ld_src = g.epi == EPI_GELU_BWD ? g.ld_aux : g.ld_resid;
     int buf = 0;
     int issued = 0;  // bulk store groups of this warp so far
@@ -414,15 +418,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m >= c.m_start && m < c.m_end;
       const bool rows_full = row0 >= c.m_start && row0 + 32 <= c.m_end;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      // lane reads rows 4*rr + lane/8 of the block, 16 bytes at column 4*(lane%8)
-      float4 pf[8];
+      // fp32: lane reads rows 4*rr + lane/8 of the block, 16 bytes at column
+      // 4*(lane%8); bf16: rows 8*rr + lane/4, 16 bytes at column 8*(lane%4)
+      uint4 pf[8];
       auto prefetch = [&](int nb_) {
         const bool whole = src && rows_full && nb_ >= c.n_start && nb_ + 32 <= c.n_end;
         if (whole) {
+          if (src_bf) {
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr)
-            pf[rr] = __ldg(reinterpret_cast<const float4*>(src + (int64_t)(row0 + 4 * rr + (lane >> 3)) * ld_src +
-                                                           nb_ + 4 * (lane & 7)));
+            for (int rr = 0; rr < 4; ++rr)
+              pf[rr] = __ldg(reinterpret_cast<const uint4*>(static_cast<const bf16*>(src) +
+                                                            (int64_t)(row0 + 8 * rr + (lane >> 2)) * ld_src +
+                                                            nb_ + 8 * (lane & 3)));
+          } else {
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr)
+              pf[rr] = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(src) +
+                                                            (int64_t)(row0 + 4 * rr + (lane >> 3)) * ld_src +
+                                                            nb_ + 4 * (lane & 7)));
+          }
         }
         return whole;
       };
@@ -439,28 +453,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ts.c_mode == 1) tma = row0 >= c.m_start && nb >= c.n_start;
         else tma = ts.c_mode > 1 && rows_full && cols_full;
         if (tma && g.epi == EPI_GELU && !ts.aux_tma) tma = false;
-        uint8_t* stage_c = stage_base + (gelu ? 0 : buf * 4096);
-        uint8_t* stage_u = stage_base + 4096;
+        uint8_t* stage_c = stage_base + (single ? 0 : buf * 4096);
+        uint8_t* stage_u = single ? stage_base + 4096 : stage_c + 2048;
         const bool have_cur = have;
-        if ((tma || have_cur) && issued >= (gelu ? 1 : 2)) {
+        if ((tma || have_cur) && issued >= (single ? 1 : 2)) {
           // the group that last used this buffer must have finished reading it
           if (lane == 0) {
-            if (gelu) bulk_wait_read();
+            if (single) bulk_wait_read();
             else bulk_wait_read1();
           }
           __syncwarp();
         }
         if (have_cur) {
+          if (src_bf) {
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {
-            const int rl = 4 * rr + (lane >> 3);
-            *reinterpret_cast<float4*>(stage_c + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4)) = pf[rr];
-          }
-          __syncwarp();
+            for (int rr = 0; rr < 4; ++rr) {
+              const int rl = 8 * rr + (lane >> 2);
+              *reinterpret_cast<uint4*>(stage_c + rl * 64 + (((lane & 3) ^ ((rl >> 1) & 3)) << 4)) = pf[rr];
+            }
+            __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 x = *reinterpret_cast<const float4*>(stage_c + lane * 128 + ((k ^ (lane & 7)) << 4));
-            pre[4 * k] = x.x; pre[4 * k + 1] = x.y; pre[4 * k + 2] = x.z; pre[4 * k + 3] = x.w;
+            for (int k = 0; k < 4; ++k) {
+              const uint4 x = *reinterpret_cast<const uint4*>(stage_c + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4));
+              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+                pre[8 * k + 2 * e] = f2.x;
+                pre[8 * k + 2 * e + 1] = f2.y;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+              const int rl = 4 * rr + (lane >> 3);
+              *reinterpret_cast<uint4*>(stage_c + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4)) = pf[rr];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float4 x = *reinterpret_cast<const float4*>(stage_c + lane * 128 + ((k ^ (lane & 7)) << 4));
+              pre[4 * k] = x.x; pre[4 * k + 1] = x.y; pre[4 * k + 2] = x.z; pre[4 * k + 3] = x.w;
+            }
           }
           __syncwarp();
         }
@@ -472,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 32; ++j) {
               const int n = nb + j;
               if (n < c.n_start || n >= c.n_end) continue;
-              if (g.epi == EPI_GELU) g.aux[(int64_t)m * g.ld_aux + n] = u[j];
+              if (g.epi == EPI_GELU) aux_store(g, (int64_t)m * g.ld_aux + n, u[j]);
               const int64_t o = out_offset(g, c.i, m, n);
               if (cbf) static_cast<bf16*>(g.C)[o] = __float2bfloat16_rn(v[j]);
               else static_cast<float*>(g.C)[o] = v[j];
@@ -482,7 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (cbf) stage_bf16(stage_c, lane, v);
         else stage_f32(stage_c, lane, v);
-        if (gelu) stage_f32(stage_u, lane, u);
+        if (gelu) {
+          if (ubf) stage_bf16(stage_u, lane, u);
+          else stage_f32(stage_u, lane, u);
+        }
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -585,11 +622,13 @@ nnt_status store_maps(const GemmArgs& g, int64_t zmax, CUtensorMap* mc, CUtensor
     }
   }
   if (g.epi == EPI_GELU && c_mode == 1) {
-    const char* base = reinterpret_cast<const char*>(g.aux) + ((int64_t)g.m0 * g.ld_aux + g.n0) * 4;
-    if (al16((int64_t)(uintptr_t)base) && al16(g.ld_aux * 4)) {
+    const bool ub = g.aux_dtype == NNT_BF16;
+    const int64_t ues = ub ? 2 : 4;
+    const char* base = reinterpret_cast<const char*>(g.aux) + ((int64_t)g.m0 * g.ld_aux + g.n0) * ues;
+    if (al16((int64_t)(uintptr_t)base) && al16(g.ld_aux * ues)) {
       cuuint64_t dims[2] = {(cuuint64_t)g.nt, (cuuint64_t)g.mt};
-      cuuint64_t str[1] = {(cuuint64_t)(g.ld_aux * 4)};
-      NNT_TRY(make_store_map(mu, base, false, 2, dims, str));
+      cuuint64_t str[1] = {(cuuint64_t)(g.ld_aux * ues)};
+      NNT_TRY(make_store_map(mu, base, ub, 2, dims, str));
       aux_tma = 1;
     }
   }
@@ -720,7 +759,7 @@ bool gemm_tc_supported(const GemmArgs& g) {
   if (g.out_mode != OUT_PLAIN && (g.hs_hd % 8 || g.c_col_off % 8)) return false;
   if (g.bias && !aligned16(g.bias)) return false;
   if (g.resid && (!aligned16(g.resid) || g.ld_resid % 4)) return false;
-  if (g.aux && (!aligned16(g.aux) || g.ld_aux % 4)) return false;
+  if (g.aux && (!aligned16(g.aux) || g.ld_aux % (g.aux_dtype == NNT_BF16 ? 8 : 4))) return false;
   return true;
 }
 
