@@ -48,6 +48,33 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
+// Packed two-lane fp32 arithmetic (one instruction for two values).
+__device__ __forceinline__ uint64_t f2_bits(float2 a) {
+  uint64_t u;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(a.x), "f"(a.y));
+  return u;
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t u) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(u));
+  return a;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+
 // Descriptor of K step kk (16 elements) of a [128][*] tile used K-major.
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
   return make_sdesc(base + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32), 16, 1024);
@@ -247,12 +274,22 @@ __global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
     tmem_wait_ld();
     const bool diag = j == nkb - 1;  // keys past the query only in the last block
     float mx = -INFINITY;
+    if (diag) {
 #pragma unroll
-    for (int c = 0; c < HC; ++c) {
-      float x = __uint_as_float(u[c]);
-      if (diag && hf * HC + c > r) x = -INFINITY;
-      u[c] = __float_as_uint(x);
-      mx = fmaxf(mx, x);
+      for (int c = 0; c < HC; ++c) {
+        float x = __uint_as_float(u[c]);
+        if (hf * HC + c > r) x = -INFINITY;
+        u[c] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
+      }
+    } else {
+      float m2 = -INFINITY;  // two chains
+#pragma unroll
+      for (int c = 0; c < HC; c += 2) {
+        mx = fmaxf(mx, __uint_as_float(u[c]));
+        m2 = fmaxf(m2, __uint_as_float(u[c + 1]));
+      }
+      mx = fmaxf(mx, m2);
     }
     red[hf * FB + r] = mx;
     __syncthreads();
@@ -282,19 +319,23 @@ __global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
         tmem_wait_st();
       }
     }
-    float sum = 0.f;
+    float2 sum2 = make_float2(0.f, 0.f);
+    const float2 c22 = make_float2(c2, c2), mm = make_float2(-m_used, -m_used);
     uint8_t* pt = sm + C::OFF_P;
 #pragma unroll
     for (int g = 0; g < HC / 8; ++g) {
       float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v[e] = ex2f(fmaf(__uint_as_float(u[8 * g + e]), c2, -m_used));
-        sum += v[e];
+      for (int e = 0; e < 8; e += 2) {
+        const float2 t = fma2(make_float2(__uint_as_float(u[8 * g + e]), __uint_as_float(u[8 * g + e + 1])), c22, mm);
+        const float2 pv = make_float2(ex2f(t.x), ex2f(t.y));
+        v[e] = pv.x;
+        v[e + 1] = pv.y;
+        sum2 = add2(sum2, pv);
       }
       put8(pt, r, hf * (HC / 8) + g, v);
     }
-    l += sum;
+    l += sum2.x + sum2.y;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -525,14 +566,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32_nw(t_row + 32 * c, sv);
       tmem_ld32_nw(t_row + FB + 32 * c, dv);
       tmem_wait_ld();
-      float p[32], ds[32];
+      // the chunk's 32 lse and D values: the same addresses across the warp (broadcast)
+      float ls[32], dd[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int qq = 32 * c + e;
-        const bool valid = i * FB + qq < a.S && (!diag || qq >= r);
-        const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_s[qq])) : 0.f;
-        p[e] = pv;
-        ds[e] = pv * (__uint_as_float(dv[e]) - d_s[qq]) * scale;
+      for (int k = 0; k < 8; ++k) {
+        const float4 x = reinterpret_cast<const float4*>(lse_s + 32 * c)[k];
+        const float4 y = reinterpret_cast<const float4*>(d_s + 32 * c)[k];
+        ls[4 * k] = x.x; ls[4 * k + 1] = x.y; ls[4 * k + 2] = x.z; ls[4 * k + 3] = x.w;
+        dd[4 * k] = y.x; dd[4 * k + 1] = y.y; dd[4 * k + 2] = y.z; dd[4 * k + 3] = y.w;
+      }
+      float p[32], ds[32];
+      if (!diag && i * FB + 32 * c + 32 <= a.S) {  // every entry of the chunk is causal and in range
+        const float2 c22 = make_float2(c2, c2), sc2 = make_float2(scale, scale);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 t = fma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22,
+                                make_float2(-ls[e], -ls[e + 1]));
+          const float2 pv = make_float2(ex2f(t.x), ex2f(t.y));
+          const float2 dq = add2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                 make_float2(-dd[e], -dd[e + 1]));
+          const float2 d2 = mul2(mul2(pv, sc2), dq);
+          p[e] = pv.x; p[e + 1] = pv.y;
+          ds[e] = d2.x; ds[e + 1] = d2.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qq = 32 * c + e;
+          const bool valid = i * FB + qq < a.S && (!diag || qq >= r);
+          const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -ls[e])) : 0.f;
+          p[e] = pv;
+          ds[e] = pv * scale * (__uint_as_float(dv[e]) - dd[e]);
+        }
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -716,11 +781,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32_nw(t_row + FB + 32 * c, dv);
       tmem_wait_ld();
       float ds[32];
+      if (!diag) {
+        const float2 c22 = make_float2(c2, c2), ml = make_float2(-lse_r, -lse_r);
+        const float2 sc2 = make_float2(scale, scale), md = make_float2(-d_r, -d_r);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const bool valid = !diag || 32 * c + e <= r;
-        const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_r)) : 0.f;
-        ds[e] = pv * (__uint_as_float(dv[e]) - d_r) * scale;
+        for (int e = 0; e < 32; e += 2) {
+          const float2 t = fma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22, ml);
+          const float2 pv = make_float2(ex2f(t.x), ex2f(t.y));
+          const float2 dq = add2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), md);
+          const float2 d2 = mul2(mul2(pv, sc2), dq);
+          ds[e] = d2.x; ds[e + 1] = d2.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const bool valid = 32 * c + e <= r;
+          const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lse_r)) : 0.f;
+          ds[e] = pv * scale * (__uint_as_float(dv[e]) - d_r);
+        }
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g) put8(dst, r, 4 * c + g, ds + 8 * g);

@@ -397,6 +397,131 @@ nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* me
   return launch_check("layernorm_bwd");
 }
 
+// Layer-norm backward with its column sums in the same pass, for rows of at
+// most 1024 columns (one warp per row, MAXV float4 groups per lane). Each warp
+// takes rows blockIdx*8 + warp, then every gridDim*8-th; besides dx (as
+// ln_bwd_kernel) it accumulates, per column, sum dy*xhat, sum dy and
+// (want_out) sum dx. The eight warps' sums are added in warp order through
+// shared memory and the CTA writes part[blockIdx][3][cols]; sum_parts3 adds
+// the CTAs in order. dy, x and the new residual gradient are read once.
+template <int MAXV, typename T>
+__global__ void __launch_bounds__(256, 2) ln_bwd_fused_kernel(
+    const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ mean,
+    const float* __restrict__ rstd, const float* __restrict__ g, const float* resid, float* dx,
+    T* __restrict__ dx_act, int64_t rows, int cols, float* __restrict__ part, int want_out) {
+  extern __shared__ float red[];  // [8 warps][3][cols]
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nv = cols >> 2;
+  const float inv_n = 1.0f / (float)cols;
+  float4 ag[MAXV], ab[MAXV], ao[MAXV];
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) ag[i] = ab[i] = ao[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t row = (int64_t)blockIdx.x * 8 + w; row < rows; row += (int64_t)gridDim.x * 8) {
+    const float mu = mean[row], rs = rstd[row];
+    float4 dv[MAXV], xh[MAXV];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nv) {
+        dv[i] = load4(dy + row * cols + 4 * c);
+        const float4 xv = load4(x + row * cols + 4 * c);
+        const float4 gm = __ldg(reinterpret_cast<const float4*>(g) + c);
+        xh[i] = make_float4((xv.x - mu) * rs, (xv.y - mu) * rs, (xv.z - mu) * rs, (xv.w - mu) * rs);
+        const float4 gd = make_float4(gm.x * dv[i].x, gm.y * dv[i].y, gm.z * dv[i].z, gm.w * dv[i].w);
+        s1 += (gd.x + gd.y) + (gd.z + gd.w);
+        s2 += (gd.x * xh[i].x + gd.y * xh[i].y) + (gd.z * xh[i].z + gd.w * xh[i].w);
+      } else {
+        dv[i] = xh[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    s1 = warp_sum(s1) * inv_n;
+    s2 = warp_sum(s2) * inv_n;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nv) {
+        const float4 gm = __ldg(reinterpret_cast<const float4*>(g) + c);
+        float4 o;
+        o.x = rs * (gm.x * dv[i].x - s1 - xh[i].x * s2);
+        o.y = rs * (gm.y * dv[i].y - s1 - xh[i].y * s2);
+        o.z = rs * (gm.z * dv[i].z - s1 - xh[i].z * s2);
+        o.w = rs * (gm.w * dv[i].w - s1 - xh[i].w * s2);
+        if (resid) {
+          const float4 q = load4(resid + row * cols + 4 * c);
+          o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
+        }
+        store4(dx + row * cols + 4 * c, o);
+        if (dx_act) store4(dx_act + row * cols + 4 * c, o);
+        ag[i].x += dv[i].x * xh[i].x; ag[i].y += dv[i].y * xh[i].y;
+        ag[i].z += dv[i].z * xh[i].z; ag[i].w += dv[i].w * xh[i].w;
+        ab[i].x += dv[i].x; ab[i].y += dv[i].y; ab[i].z += dv[i].z; ab[i].w += dv[i].w;
+        ao[i].x += o.x; ao[i].y += o.y; ao[i].z += o.z; ao[i].w += o.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nv) {
+      float* r0 = red + (w * 3) * cols + 4 * c;
+      *reinterpret_cast<float4*>(r0) = ag[i];
+      *reinterpret_cast<float4*>(r0 + cols) = ab[i];
+      *reinterpret_cast<float4*>(r0 + 2 * cols) = ao[i];
+    }
+  }
+  __syncthreads();
+  const int nsum = (want_out ? 3 : 2) * cols;
+  for (int k = threadIdx.x; k < nsum; k += blockDim.x) {
+    float t = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) t += red[ww * 3 * cols + k];
+    part[(int64_t)blockIdx.x * 3 * cols + k] = t;
+  }
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+int ln_bwd_fused_ctas(int64_t rows) {
+  return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(rows, 8), 2 * sm_count()));
+}
+
+nnt_status launch_ln_bwd_fused(const float* dy, const float* x, const float* mean, const float* rstd,
+                               const float* g, const float* resid, float* dx, void* dx_act,
+                               int64_t rows, int cols, int act_dtype, float* part, int want_out,
+                               cudaStream_t st) {
+  NNT_CHECK_ARG(cols % 4 == 0 && cols > 0 && cols <= 1024,
+                "fused layernorm bwd: cols must be a multiple of 4 in [4, 1024] (got %d)", cols);
+  if (rows == 0) return NNT_OK;
+  const int grid = ln_bwd_fused_ctas(rows);
+  const size_t smem = (size_t)8 * 3 * cols * 4;
+  const int mv = row_maxv(cols, 32);
+  NNT_MAXV_DISPATCH(mv, {
+    // the largest smem any call needs (1024 columns), allowed once per instantiation
+    if (act_dtype == NNT_BF16) {
+      auto k = ln_bwd_fused_kernel<MV, bf16>;
+      static const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 3 * 1024 * 4);
+      NNT_CUDA_TRY(attr);
+      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols, part, want_out);
+    } else {
+      auto k = ln_bwd_fused_kernel<MV, float>;
+      static const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 3 * 1024 * 4);
+      NNT_CUDA_TRY(attr);
+      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols, part, want_out);
+    }
+  });
+  return launch_check("layernorm_bwd_fused");
+}
+
 // Column sums of the layer-norm backward over a chunk of rows: sum dy*xhat
 // (gain gradient), sum dy (shift gradient) and, when `out` is given, sum out
 // (the bias gradient of the linear layer whose output gradient `out` is).
@@ -504,8 +629,19 @@ __global__ void sum_parts3_kernel(const float* __restrict__ part, int64_t nparts
   const int64_t ld = 3 * cols;
   const float* p0 = part + blockIdx.y * cols;
   float s = 0.f;
-  if (c < cols)
-    for (int64_t p = w; p < nparts; p += 8) s += p0[p * ld + c];
+  if (c < cols) {
+    // four loads in flight per warp; each warp still adds its rows in a fixed order
+    int64_t p = w;
+    for (; p + 24 < nparts; p += 32) {
+      const float a0 = p0[p * ld + c], a1 = p0[(p + 8) * ld + c];
+      const float a2 = p0[(p + 16) * ld + c], a3 = p0[(p + 24) * ld + c];
+      s += a0;
+      s += a1;
+      s += a2;
+      s += a3;
+    }
+    for (; p < nparts; p += 8) s += p0[p * ld + c];
+  }
   red[w][lane] = s;
   __syncthreads();
   if (w == 0 && c < cols) {

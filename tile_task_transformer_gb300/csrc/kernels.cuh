@@ -41,6 +41,15 @@ nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* m
                                  cudaStream_t st);
 nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, float* o0, float* o1,
                              float* o2, int accumulate, cudaStream_t st);
+// Layer-norm backward (as launch_layernorm_bwd) that also writes the column
+// sums sum dy*xhat, sum dy and (want_out) sum dx of its rows as
+// ln_bwd_fused_ctas(rows) partial rows part[p][3][cols] (cols <= 1024; add
+// them with launch_sum_parts3). dy, x and dx are read or written once.
+int ln_bwd_fused_ctas(int64_t rows);
+nnt_status launch_ln_bwd_fused(const float* dy, const float* x, const float* mean, const float* rstd,
+                               const float* g, const float* resid, float* dx, void* dx_act,
+                               int64_t rows, int cols, int act_dtype, float* part, int want_out,
+                               cudaStream_t st);
 
 // out[c] (=|+=) sum over p of part[p][c], p in increasing order
 nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,

@@ -529,7 +529,9 @@ nnt_status alloc_all(nnt_model* m) {
   NNT_TRY(dalloc(m, m->du, (size_t)T * f * as));
   NNT_TRY(dalloc(m, m->dOh, Td * as));
   NNT_TRY(dalloc(m, m->dqkv, 3 * Td * as));
-  NNT_TRY(dalloc(m, m->ln_part_g, (size_t)ln_colsum_chunks(T) * 3 * d * 4));
+  NNT_TRY(dalloc(m, m->ln_part_g,
+                 (size_t)std::max<int64_t>(ln_colsum_chunks(T), (int64_t)m->n_tok * ln_bwd_fused_ctas(m->TT)) *
+                     3 * d * 4));
   const int64_t maxcols = std::max<int64_t>(3 * d, f);
   NNT_TRY(dalloc(m, m->col_part, (size_t)colsum_nparts(T) * maxcols * 4));
   if (m->act == NNT_BF16 && m->backend == 0) {  // 32 MB: the split weight-gradient GEMMs of small models
@@ -916,6 +918,9 @@ void build_forward(nnt_model* m) {
 // replacing it.
 void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
   Builder b{m};
+  // rows of at most 1024 features: LayerNorm backward with its column sums in one pass
+  const bool fused_ln = m->d <= 1024;
+  const int ln_g = ln_bwd_fused_ctas(m->TT);  // partial rows per token tile
   const int GW = acc ? ACC_RW : ACC_W;  // access of the tasks that write parameter gradients
   const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
   const size_t as = m->act_size;
@@ -1049,33 +1054,55 @@ void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
       t.bytes = (double)m->TT * d * (4 * (has_resid ? 4 : 3) + as);
       const int64_t r0 = (int64_t)rt * m->TT;
       const float* gam = pm(m, gm);
-      t.fn = [=](cudaStream_t s) {
-        return launch_layernorm_bwd(dy + r0 * d, xin + r0 * d, mu + r0, rs + r0, gam,
-                                    has_resid ? m->dres + r0 * d : nullptr, m->dres + r0 * d,
-                                    (char*)m->dres_act + r0 * d * as, m->TT, d, act, s);
-      };
+      if (fused_ln) {
+        // the column sums of this token tile go to its slice of the partials
+        box(t.uses, m->gln_part, ACC_W, rt, rt + 1);
+        float* part = m->ln_part_g + (int64_t)rt * ln_g * 3 * d;
+        const int want_out = bias_idx >= 0;
+        t.fn = [=](cudaStream_t s) {
+          return launch_ln_bwd_fused(dy + r0 * d, xin + r0 * d, mu + r0, rs + r0, gam,
+                                     has_resid ? m->dres + r0 * d : nullptr, m->dres + r0 * d,
+                                     (char*)m->dres_act + r0 * d * as, m->TT, d, act, part, want_out, s);
+        };
+      } else {
+        t.fn = [=](cudaStream_t s) {
+          return launch_layernorm_bwd(dy + r0 * d, xin + r0 * d, mu + r0, rs + r0, gam,
+                                      has_resid ? m->dres + r0 * d : nullptr, m->dres + r0 * d,
+                                      (char*)m->dres_act + r0 * d * as, m->TT, d, act, s);
+        };
+      }
       P.add(std::move(t));
     }
     Task t;
     t.type = TT_LN_PARTS;
-    t.kernels = 2;
-    box(t.uses, gdy, ACC_R);
-    box(t.uses, gxin, ACC_R);
-    box(t.uses, gst, ACC_R);
-    box(t.uses, m->gdres, ACC_R);
-    box(t.uses, m->gln_part, ACC_RW);
+    t.kernels = fused_ln ? 1 : 2;
+    if (!fused_ln) {
+      box(t.uses, gdy, ACC_R);
+      box(t.uses, gxin, ACC_R);
+      box(t.uses, gst, ACC_R);
+      box(t.uses, m->gdres, ACC_R);
+    }
+    box(t.uses, m->gln_part, fused_ln ? ACC_R : ACC_RW);
     box(t.uses, m->ggrad[gidx_g], GW);
     box(t.uses, m->ggrad[gidx_b], GW);
     if (bias_idx >= 0) box(t.uses, m->ggrad[bias_idx], GW);
-    t.bytes = (double)T * d * 4 * (bias_idx >= 0 ? 3 : 2);
     float* og = pg(m, gm);
     float* ob = pg(m, bt_);
     float* obias = bias_idx >= 0 ? pg(m, m->params[bias_idx]) : nullptr;
     const int accum = acc ? 1 : 0;
-    t.fn = [=](cudaStream_t s) {
-      return launch_ln_bwd_colsums(dy, xin, mu, rs, obias ? m->dres : nullptr, T, d, m->ln_part_g, og,
-                                   ob, obias, accum, s);
-    };
+    if (fused_ln) {
+      const int64_t np = (int64_t)m->n_tok * ln_g;
+      t.bytes = (double)np * 3 * d * 4;
+      t.fn = [=](cudaStream_t s) {
+        return launch_sum_parts3(m->ln_part_g, np, d, og, ob, obias, accum, s);
+      };
+    } else {
+      t.bytes = (double)T * d * 4 * (bias_idx >= 0 ? 3 : 2);
+      t.fn = [=](cudaStream_t s) {
+        return launch_ln_bwd_colsums(dy, xin, mu, rs, obias ? m->dres : nullptr, T, d, m->ln_part_g, og,
+                                     ob, obias, accum, s);
+      };
+    }
     P.add(std::move(t));
     adam_param(gidx_g);
     adam_param(gidx_b);
