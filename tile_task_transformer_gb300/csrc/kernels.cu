@@ -586,44 +586,46 @@ nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* m
   return launch_sum_parts3(part, nch, cols, dg, db, out ? dbias : nullptr, accumulate, st);
 }
 
-// out[c] (+)= sum_p part[p*ld + c]. A CTA owns 32 columns; its 8 warps take
-// every 8th partial row (lane = column, so each row read is one coalesced
-// 128-byte segment) and the 8 warp sums are added in warp order: a fixed
-// summation order, independent of scheduling.
-__global__ void sum_parts_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
+// out[c] (+)= sum_p part[p*ld + c]. A CTA owns 32 columns; its kSumWarps warps
+// take every kSumWarps-th partial row (lane = column, so each row read is one
+// coalesced 128-byte segment; four rows in flight per warp) and the warp sums
+// are added in warp order: a fixed summation order, independent of scheduling.
+constexpr int kSumWarps = 32;
+
+__global__ void __launch_bounds__(32 * kSumWarps) sum_parts_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
                                  int64_t ld, float* __restrict__ out, int accumulate) {
-  __shared__ float red[8][33];
+  __shared__ float red[kSumWarps][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = blockIdx.x * 32ll + lane;
   float s = 0.f;
   if (c < cols) {
     int64_t p = w;
-    for (; p + 24 < nparts; p += 32) {
-      const float a0 = part[p * ld + c], a1 = part[(p + 8) * ld + c];
-      const float a2 = part[(p + 16) * ld + c], a3 = part[(p + 24) * ld + c];
+    for (; p + 3 * kSumWarps < nparts; p += 4 * kSumWarps) {
+      const float a0 = part[p * ld + c], a1 = part[(p + kSumWarps) * ld + c];
+      const float a2 = part[(p + 2 * kSumWarps) * ld + c], a3 = part[(p + 3 * kSumWarps) * ld + c];
       s += a0;
       s += a1;
       s += a2;
       s += a3;
     }
-    for (; p < nparts; p += 8) s += part[p * ld + c];
+    for (; p < nparts; p += kSumWarps) s += part[p * ld + c];
   }
   red[w][lane] = s;
   __syncthreads();
   if (w == 0 && c < cols) {
     float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t += red[i][lane];
+    for (int i = 0; i < kSumWarps; ++i) t += red[i][lane];
     out[c] = accumulate ? out[c] + t : t;
   }
 }
 
-__global__ void sum_parts3_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
+__global__ void __launch_bounds__(32 * kSumWarps) sum_parts3_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
                                   float* o0, float* o1, float* o2, int accumulate) {
   float* outs[3] = {o0, o1, o2};
   float* out = outs[blockIdx.y];
   if (!out) return;
-  __shared__ float red[8][33];
+  __shared__ float red[kSumWarps][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = blockIdx.x * 32ll + lane;
   const int64_t ld = 3 * cols;
@@ -632,22 +634,22 @@ __global__ void sum_parts3_kernel(const float* __restrict__ part, int64_t nparts
   if (c < cols) {
     // four loads in flight per warp; each warp still adds its rows in a fixed order
     int64_t p = w;
-    for (; p + 24 < nparts; p += 32) {
-      const float a0 = p0[p * ld + c], a1 = p0[(p + 8) * ld + c];
-      const float a2 = p0[(p + 16) * ld + c], a3 = p0[(p + 24) * ld + c];
+    for (; p + 3 * kSumWarps < nparts; p += 4 * kSumWarps) {
+      const float a0 = p0[p * ld + c], a1 = p0[(p + kSumWarps) * ld + c];
+      const float a2 = p0[(p + 2 * kSumWarps) * ld + c], a3 = p0[(p + 3 * kSumWarps) * ld + c];
       s += a0;
       s += a1;
       s += a2;
       s += a3;
     }
-    for (; p < nparts; p += 8) s += p0[p * ld + c];
+    for (; p < nparts; p += kSumWarps) s += p0[p * ld + c];
   }
   red[w][lane] = s;
   __syncthreads();
   if (w == 0 && c < cols) {
     float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t += red[i][lane];
+    for (int i = 0; i < kSumWarps; ++i) t += red[i][lane];
     out[c] = accumulate ? out[c] + t : t;
   }
 }
@@ -656,14 +658,14 @@ nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, fl
                              float* o2, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
   dim3 grid((unsigned)ceil_div(cols, 32), 3);
-  sum_parts3_kernel<<<grid, 256, 0, st>>>(part, nparts, cols, o0, o1, o2, accumulate);
+  sum_parts3_kernel<<<grid, 32 * kSumWarps, 0, st>>>(part, nparts, cols, o0, o1, o2, accumulate);
   return launch_check("sum_parts3");
 }
 
 nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,
                             float* out, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
-  sum_parts_kernel<<<(unsigned)ceil_div(cols, 32), 256, 0, st>>>(part, nparts, cols, ld, out,
+  sum_parts_kernel<<<(unsigned)ceil_div(cols, 32), 32 * kSumWarps, 0, st>>>(part, nparts, cols, ld, out,
                                                                   accumulate);
   return launch_check("sum_parts");
 }
