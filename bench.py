@@ -375,7 +375,7 @@ def run_sweep(args):
     dev = "cuda"
     kernels = args.sweep_kernel.split(",") if args.sweep_kernel else [
         "layernorm_fwd", "layernorm_bwd", "softmax_fwd", "softmax_bwd", "gelu_fwd", "gelu_bwd",
-        "cross_entropy", "adamw", "gemm"]
+        "cross_entropy", "adamw", "gemm", "flash_attention"]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def timeit(fn):
@@ -427,8 +427,9 @@ def run_sweep(args):
                             db = torch.empty(Cc, device=dev)
                             ms = timeit(lambda: nnt.op_layernorm_bwd(dy, x, mu, rs, g, None, dx, dxa, dg, db,
                                                                      R, Cc, dt))
-                            # dx pass (read dy, x; write dx, copy) + gain/shift column pass (read dy, x)
-                            emit("layernorm_bwd", [R, Cc], dt_name, ms, nbytes=R * Cc * (8 + 4 + es + 8))
+                            # algorithmic: read dy, x; write dx and its activation-dtype copy (rows
+                            # over 1024 columns read dy, x a second time for the column sums)
+                            emit("layernorm_bwd", [R, Cc], dt_name, ms, nbytes=R * Cc * (8 + 4 + es))
                         del x, y
                 if ("gelu_fwd" in kernels or "gelu_bwd" in kernels):
                     n = R * Cc
@@ -489,6 +490,20 @@ def run_sweep(args):
             ms = timeit(lambda: nnt.op_gemm(A, N, 0, B, N, 0, Cm, N, nnt.BF16, N, N, N, dtype=nnt.BF16))
             emit("gemm", [N, N, N], "bf16", ms, flops=2.0 * N ** 3)
             del A, B, Cm
+    if "flash_attention" in kernels:
+        # fused causal attention on [Z][S][hd] bf16 (GPT2-small and wide layer shapes);
+        # algorithmic flops on the causal half: forward QK^T, PV; backward dV, dP, dQ, dK
+        for Z, S, hd in ((48, 1024, 64), (128, 1024, 128)):
+            q, k, v, do = (torch.randn(Z, S, hd, device=dev).to(torch.bfloat16) for _ in range(4))
+            o = torch.empty_like(q)
+            lse = torch.empty(Z, S, device=dev)
+            dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+            pairs = Z * S * (S + 1) / 2
+            ms = timeit(lambda: nnt.op_flash_attention_fwd(q, k, v, o, lse, Z, S, hd))
+            emit("flash_attention_fwd", [Z, S, hd], "bf16", ms, flops=2 * 2.0 * hd * pairs)
+            ms = timeit(lambda: nnt.op_flash_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, Z, S, hd))
+            emit("flash_attention_bwd", [Z, S, hd], "bf16", ms, flops=4 * 2.0 * hd * pairs)
+            del q, k, v, do, o, dq, dk, dv
     print(json.dumps({"sweep_device_error": nnt.read_device_error()}))
     return 0
 

@@ -103,6 +103,7 @@ def test_flash_saves_the_score_buffers():
     a.close()
     b.close()
     B, H, S, L = cfg.batch, cfg.n_head, cfg.seq, cfg.n_layer
-    # P per layer (bf16) and one fp32 score buffer, less the per-layer lse and D
-    expect = L * B * H * S * S * 2 + B * H * S * S * 4 - (L + 1) * B * H * S * 4
+    # P per layer (bf16) and one fp32 score buffer, less the per-layer lse, D and
+    # the one bf16 dS^T buffer of the fused backward
+    expect = L * B * H * S * S * 2 + B * H * S * S * 4 - (L + 1) * B * H * S * 4 - B * H * S * S * 2
     assert abs(saved - expect) <= 4096 * (L + 2), (saved, expect)

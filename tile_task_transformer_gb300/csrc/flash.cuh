@@ -24,6 +24,10 @@ struct FlashArgs {
   // backward: D = rowsum(dO * O) scratch [Zall][S]; gradient outputs in the
   // same token-row layout (ldd, columns dq_col / dk_col / dv_col + h * hd)
   float* D = nullptr;
+  // optional [Zall][S][S] bf16 scratch (S a multiple of 8): the dK/dV pass then
+  // also stores dS^T (row = key, column = query) and dQ = dS K runs as a
+  // tensor-core GEMM instead of a second recomputing pass
+  bf16* ds = nullptr;
   bf16* dq = nullptr;
   bf16* dk = nullptr;
   bf16* dv = nullptr;

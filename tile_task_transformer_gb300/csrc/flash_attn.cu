@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "flash.cuh"
+#include "gemm.cuh"
 #include "tc_ptx.cuh"
 
 namespace nnt {
@@ -441,7 +442,8 @@ template <int HD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     flash_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                        const FlashArgs a, int nqb, float c2, float scale, uint32_t* err) {
+                        const __grid_constant__ CUtensorMap tmDS, int store_ds, const FlashArgs a,
+                        int nqb, float c2, float scale, uint32_t* err) {
   using C = KvCfg<HD>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -525,6 +527,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int i = kb + it, st = it % NS;
     const float row_c = row_next;
     if (it + 1 < n) row_next = row_val(i + 1);
+    // the previous dS^T tile must have left shared memory before it is rewritten
+    if (store_ds && tid == 32 && it > 0) bulk_wait_read();
     if (tid == 0) {
       if (it == 0) {
         ok = mbar_wait(bar_kv, 0);
@@ -608,6 +612,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (store_ds && tid == 32) {  // dS^T tile to global: rows kb*128.., columns i*128..
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tma_store_3d(&tmDS, dst + c * CHUNK, i * FB + 64 * c, kb * FB, z);
+      bulk_commit();
+    }
     if (tid == 0 && ok) {
       tc_fence_after();
       const uint32_t s_qt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE), s_do = s_qt + C::TILE;
@@ -643,6 +652,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     umma_commit(bar_x);
     mbar_wait(bar_x, 0);
   }
+  if (store_ds && tid == 32) bulk_wait_all();  // stores finished before shared memory goes
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -917,10 +927,29 @@ nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, c
   const float c2 = (float)(1.4426950408889634 * scale);
   flash_bwd_d_kernel<<<dim3((unsigned)ceil_div(a.S, 32), (unsigned)a.nz), 256, 0, st>>>(dO, a);
   NNT_TRY(launch_check("flash_bwd_d"));
-  kv<<<(unsigned)(nqb * a.nz), kBwdThreads, KvCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+  const bool via_gemm = a.ds && a.S % 8 == 0;
+  CUtensorMap mds = mq;  // unused unless via_gemm
+  if (via_gemm) NNT_TRY(make_map(&mds, a.ds, a.S, a.S, a.S, (int64_t)a.S * a.S, a.z_total, 64, FB));
+  kv<<<(unsigned)(nqb * a.nz), kBwdThreads, KvCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a,
+                                                                   nqb, c2, (float)scale, err);
   NNT_TRY(launch_check("flash_bwd_kv"));
-  qk<<<(unsigned)(nqb * a.nz), kBwdThreads, QCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
-  return launch_check("flash_bwd_q");
+  if (!via_gemm) {
+    qk<<<(unsigned)(nqb * a.nz), kBwdThreads, QCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+    return launch_check("flash_bwd_q");
+  }
+  // dQ[q] = sum_{k <= q} dS[q][k] K[k]: A = dS^T read MN-major, causal key range per query tile
+  GemmArgs g;
+  g.M = a.S; g.N = HD; g.K = a.S;
+  g.nbatch = a.nz; g.zm = a.zm;
+  g.m0 = 0; g.mt = a.S; g.n0 = 0; g.nt = HD;
+  g.A = a.ds; g.lda = a.S; g.a_zs = (int64_t)a.S * a.S; g.a_trans = 1;
+  g.B = k; g.ldb = HD; g.b_zs = (int64_t)a.S * HD; g.b_trans = 1;
+  g.op_dtype = NNT_BF16;
+  g.C = a.dq; g.ldc = a.ldd; g.c_dtype = NNT_BF16; g.out_mode = OUT_HEADMERGE;
+  g.c_col_off = a.dq_col; g.hs_hd = HD; g.hs_H = a.zm.H; g.hs_B = (int)(a.z_total / a.zm.H); g.hs_S = a.S;
+  g.tm = a.tm;
+  g.causal = CAUSAL_K_UPPER;
+  return gemm(g, 0, st);
 }
 
 }  // namespace

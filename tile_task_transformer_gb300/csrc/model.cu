@@ -125,6 +125,7 @@ struct nnt_model {
   bool flash = false;
   std::vector<float*> lse;
   float* attn_d = nullptr;
+  bf16* attn_ds = nullptr;  // [B*H][S][S] dS^T of the backward (its dQ is then a GEMM)
   void* y = nullptr;
   float *muf = nullptr, *rf = nullptr;
   float* z = nullptr;
@@ -512,8 +513,10 @@ nnt_status alloc_all(nnt_model* m) {
     NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * as));
     NNT_TRY(dalloc(m, m->g[l], (size_t)T * f * as));
   }
-  if (m->flash)
+  if (m->flash) {
     NNT_TRY(dalloc(m, m->attn_d, (size_t)B * H * S * 4));
+    if (S % 8 == 0) NNT_TRY(dalloc(m, m->attn_ds, (size_t)B * H * S * S * 2));
+  }
   else
     NNT_TRY(dalloc(m, m->scores, (size_t)B * H * S * S * 4));
   NNT_TRY(dalloc(m, m->y, Td * as));
@@ -1213,6 +1216,7 @@ void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
           fa.ldo = d;
           fa.lse = m->lse[l];
           fa.D = m->attn_d;
+          fa.ds = m->attn_ds;
           fa.dq = fa.dk = fa.dv = static_cast<bf16*>(m->dqkv);
           fa.ldd = 3 * d;
           fa.dq_col = 0;

@@ -151,9 +151,13 @@ nnt_status nnt_op_flash_attention_bwd(const void* q_dev, const void* k_dev, cons
                 "NULL pointer");
   NNT_CHECK_ARG(Z > 0 && S > 0 && Z * S < (1ll << 31) && flash_supported((int)hd),
                 "bad size (Z, S >= 1, Z*S < 2^31, hd 64 or 128)");
+  // scratch: D [Z][S] fp32, then (S a multiple of 8) dS^T [Z][S][S] bf16
+  const size_t d_bytes = ((size_t)(Z * S) * sizeof(float) + 255) / 256 * 256;
+  const bool with_ds = S % 8 == 0;
   void* D = nullptr;
-  NNT_TRY(scratch((size_t)(Z * S) * sizeof(float), &D));
+  NNT_TRY(scratch(d_bytes + (with_ds ? (size_t)Z * S * S * 2 : 0), &D));
   FlashArgs a = plain_flash(Z, S, hd);
+  if (with_ds) a.ds = reinterpret_cast<bf16*>(static_cast<char*>(D) + d_bytes);
   a.o = const_cast<bf16*>(static_cast<const bf16*>(o_dev));
   a.lse = const_cast<float*>(lse_dev);
   a.D = static_cast<float*>(D);
