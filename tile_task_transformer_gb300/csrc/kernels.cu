@@ -398,59 +398,82 @@ nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* me
 }
 
 // Layer-norm backward with its column sums in the same pass, for rows of at
-// most 1024 columns (one warp per row, MAXV float4 groups per lane). Each warp
-// takes rows blockIdx*8 + warp, then every gridDim*8-th; besides dx (as
-// ln_bwd_kernel) it accumulates, per column, sum dy*xhat, sum dy and
-// (want_out) sum dx. The eight warps' sums are added in warp order through
-// shared memory and the CTA writes part[blockIdx][3][cols]; sum_parts3 adds
-// the CTAs in order. dy, x and the new residual gradient are read once.
-template <int MAXV, typename T>
+// most 1024 columns. A row belongs to a group of RW warps (RW = 1 or 2; each
+// lane holds MAXV float4 groups of the row: dy, x and the residual are all
+// loaded before the row statistics are reduced, so a row costs one memory
+// round trip); the two warps of a pair swap their partial sums through shared
+// memory with a 64-thread named barrier. Row groups take rows blockIdx*G + g,
+// then every gridDim*G-th (G = 8 / RW). Besides dx it accumulates, per column,
+// sum dy*xhat, sum dy and (want_out) sum dx; the row groups' sums are added in
+// group order through shared memory and the CTA writes part[blockIdx][3][cols]
+// (sum_parts3 adds the CTAs in order). dy, x and the residual are read once.
+template <int RW, int MAXV, typename T>
 __global__ void __launch_bounds__(256, 2) ln_bwd_fused_kernel(
     const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ mean,
     const float* __restrict__ rstd, const float* __restrict__ g, const float* resid, float* dx,
     T* __restrict__ dx_act, int64_t rows, int cols, float* __restrict__ part, int want_out) {
-  extern __shared__ float red[];  // [8 warps][3][cols]
+  constexpr int G = 8 / RW;  // row groups per CTA
+  extern __shared__ float red[];  // [G][3][cols]
+  __shared__ float xch[2][8][2];  // pair exchange: [parity][warp][s1, s2]
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int grp = w / RW, half = w % RW;
   const int nv = cols >> 2;
   const float inv_n = 1.0f / (float)cols;
   float4 ag[MAXV], ab[MAXV], ao[MAXV];
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) ag[i] = ab[i] = ao[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t row = (int64_t)blockIdx.x * 8 + w; row < rows; row += (int64_t)gridDim.x * 8) {
+  int parity = 0;
+  for (int64_t row = (int64_t)blockIdx.x * G + grp; row < rows; row += (int64_t)gridDim.x * G) {
     const float mu = mean[row], rs = rstd[row];
-    float4 dv[MAXV], xh[MAXV];
+    float4 dv[MAXV], xh[MAXV], q[MAXV];
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int c = half * 32 + lane + 32 * RW * i;
+      if (c < nv) {
+        dv[i] = load4(dy + row * cols + 4 * c);
+        xh[i] = load4(x + row * cols + 4 * c);
+        q[i] = resid ? load4(resid + row * cols + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        dv[i] = xh[i] = q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
-      const int c = lane + 32 * i;
+      const int c = half * 32 + lane + 32 * RW * i;
       if (c < nv) {
-        dv[i] = load4(dy + row * cols + 4 * c);
-        const float4 xv = load4(x + row * cols + 4 * c);
         const float4 gm = __ldg(reinterpret_cast<const float4*>(g) + c);
-        xh[i] = make_float4((xv.x - mu) * rs, (xv.y - mu) * rs, (xv.z - mu) * rs, (xv.w - mu) * rs);
+        xh[i] = make_float4((xh[i].x - mu) * rs, (xh[i].y - mu) * rs, (xh[i].z - mu) * rs, (xh[i].w - mu) * rs);
         const float4 gd = make_float4(gm.x * dv[i].x, gm.y * dv[i].y, gm.z * dv[i].z, gm.w * dv[i].w);
         s1 += (gd.x + gd.y) + (gd.z + gd.w);
         s2 += (gd.x * xh[i].x + gd.y * xh[i].y) + (gd.z * xh[i].z + gd.w * xh[i].w);
-      } else {
-        dv[i] = xh[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    s1 = warp_sum(s1) * inv_n;
-    s2 = warp_sum(s2) * inv_n;
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    if constexpr (RW == 2) {
+      if (lane == 0) {
+        xch[parity][w][0] = s1;
+        xch[parity][w][1] = s2;
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + grp) : "memory");
+      const int p0 = grp * 2;  // the pair's sums in warp order
+      s1 = xch[parity][p0][0] + xch[parity][p0 + 1][0];
+      s2 = xch[parity][p0][1] + xch[parity][p0 + 1][1];
+      parity ^= 1;  // the next row writes the other slot, so no second barrier is needed
+    }
+    s1 *= inv_n;
+    s2 *= inv_n;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
-      const int c = lane + 32 * i;
+      const int c = half * 32 + lane + 32 * RW * i;
       if (c < nv) {
         const float4 gm = __ldg(reinterpret_cast<const float4*>(g) + c);
         float4 o;
-        o.x = rs * (gm.x * dv[i].x - s1 - xh[i].x * s2);
-        o.y = rs * (gm.y * dv[i].y - s1 - xh[i].y * s2);
-        o.z = rs * (gm.z * dv[i].z - s1 - xh[i].z * s2);
-        o.w = rs * (gm.w * dv[i].w - s1 - xh[i].w * s2);
-        if (resid) {
-          const float4 q = load4(resid + row * cols + 4 * c);
-          o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
-        }
+        o.x = rs * (gm.x * dv[i].x - s1 - xh[i].x * s2) + q[i].x;
+        o.y = rs * (gm.y * dv[i].y - s1 - xh[i].y * s2) + q[i].y;
+        o.z = rs * (gm.z * dv[i].z - s1 - xh[i].z * s2) + q[i].z;
+        o.w = rs * (gm.w * dv[i].w - s1 - xh[i].w * s2) + q[i].w;
         store4(dx + row * cols + 4 * c, o);
         if (dx_act) store4(dx_act + row * cols + 4 * c, o);
         ag[i].x += dv[i].x * xh[i].x; ag[i].y += dv[i].y * xh[i].y;
@@ -462,9 +485,9 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_fused_kernel(
   }
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
-    const int c = lane + 32 * i;
+    const int c = half * 32 + lane + 32 * RW * i;
     if (c < nv) {
-      float* r0 = red + (w * 3) * cols + 4 * c;
+      float* r0 = red + (grp * 3) * cols + 4 * c;
       *reinterpret_cast<float4*>(r0) = ag[i];
       *reinterpret_cast<float4*>(r0 + cols) = ab[i];
       *reinterpret_cast<float4*>(r0 + 2 * cols) = ao[i];
@@ -475,7 +498,7 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_fused_kernel(
   for (int k = threadIdx.x; k < nsum; k += blockDim.x) {
     float t = 0.f;
 #pragma unroll
-    for (int ww = 0; ww < 8; ++ww) t += red[ww * 3 * cols + k];
+    for (int gg = 0; gg < G; ++gg) t += red[gg * 3 * cols + k];
     part[(int64_t)blockIdx.x * 3 * cols + k] = t;
   }
 }
@@ -491,8 +514,12 @@ static int sm_count() {
   return n;
 }
 
-int ln_bwd_fused_ctas(int64_t rows) {
-  return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(rows, 8), 2 * sm_count()));
+// rows of more than 512 columns: two warps per row
+static int ln_rw(int cols) { return cols > 512 ? 2 : 1; }
+
+int ln_bwd_fused_ctas(int64_t rows, int cols) {
+  const int G = 8 / ln_rw(cols);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(rows, G), 2 * sm_count()));
 }
 
 nnt_status launch_ln_bwd_fused(const float* dy, const float* x, const float* mean, const float* rstd,
@@ -502,23 +529,35 @@ nnt_status launch_ln_bwd_fused(const float* dy, const float* x, const float* mea
   NNT_CHECK_ARG(cols % 4 == 0 && cols > 0 && cols <= 1024,
                 "fused layernorm bwd: cols must be a multiple of 4 in [4, 1024] (got %d)", cols);
   if (rows == 0) return NNT_OK;
-  const int grid = ln_bwd_fused_ctas(rows);
-  const size_t smem = (size_t)8 * 3 * cols * 4;
-  const int mv = row_maxv(cols, 32);
-  NNT_MAXV_DISPATCH(mv, {
-    // the largest smem any call needs (1024 columns), allowed once per instantiation
-    if (act_dtype == NNT_BF16) {
-      auto k = ln_bwd_fused_kernel<MV, bf16>;
-      static const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 3 * 1024 * 4);
-      NNT_CUDA_TRY(attr);
-      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols, part, want_out);
-    } else {
-      auto k = ln_bwd_fused_kernel<MV, float>;
-      static const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 3 * 1024 * 4);
-      NNT_CUDA_TRY(attr);
-      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols, part, want_out);
-    }
-  });
+  const int rw = ln_rw(cols);
+  const int grid = ln_bwd_fused_ctas(rows, cols);
+  const size_t smem = (size_t)(8 / rw) * 3 * cols * 4;
+  const int mv = row_maxv(cols, 32 * rw);
+  // the largest dynamic smem any call needs (1024 columns), allowed once per instantiation
+#define NNT_LN_FUSED_LAUNCH(RWV)                                                                   \
+  NNT_MAXV_DISPATCH(mv, {                                                                        \
+    if (act_dtype == NNT_BF16) {                                                                 \
+      auto k = ln_bwd_fused_kernel<RWV, MV, bf16>;                                              \
+      static const cudaError_t attr =                                                            \
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 / RWV * 3 * 1024 * 4); \
+      NNT_CUDA_TRY(attr);                                                                        \
+      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols, part, \
+                                 want_out);                                                      \
+    } else {                                                                                     \
+      auto k = ln_bwd_fused_kernel<RWV, MV, float>;                                             \
+      static const cudaError_t attr =                                                            \
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 / RWV * 3 * 1024 * 4); \
+      NNT_CUDA_TRY(attr);                                                                        \
+      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols,      \
+                                 part, want_out);                                                \
+    }                                                                                            \
+  })
+  if (rw == 2) {
+    NNT_LN_FUSED_LAUNCH(2);
+  } else {
+    NNT_LN_FUSED_LAUNCH(1);
+  }
+#undef NNT_LN_FUSED_LAUNCH
   return launch_check("layernorm_bwd_fused");
 }
 

@@ -45,7 +45,7 @@ nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, fl
 // sums sum dy*xhat, sum dy and (want_out) sum dx of its rows as
 // ln_bwd_fused_ctas(rows) partial rows part[p][3][cols] (cols <= 1024; add
 // them with launch_sum_parts3). dy, x and dx are read or written once.
-int ln_bwd_fused_ctas(int64_t rows);
+int ln_bwd_fused_ctas(int64_t rows, int cols);
 nnt_status launch_ln_bwd_fused(const float* dy, const float* x, const float* mean, const float* rstd,
                                const float* g, const float* resid, float* dx, void* dx_act,
                                int64_t rows, int cols, int act_dtype, float* part, int want_out,

@@ -533,7 +533,7 @@ nnt_status alloc_all(nnt_model* m) {
   NNT_TRY(dalloc(m, m->dOh, Td * as));
   NNT_TRY(dalloc(m, m->dqkv, 3 * Td * as));
   NNT_TRY(dalloc(m, m->ln_part_g,
-                 (size_t)std::max<int64_t>(ln_colsum_chunks(T), (int64_t)m->n_tok * ln_bwd_fused_ctas(m->TT)) *
+                 (size_t)std::max<int64_t>(ln_colsum_chunks(T), (int64_t)m->n_tok * ln_bwd_fused_ctas(m->TT, m->d)) *
                      3 * d * 4));
   const int64_t maxcols = std::max<int64_t>(3 * d, f);
   NNT_TRY(dalloc(m, m->col_part, (size_t)colsum_nparts(T) * maxcols * 4));
@@ -923,7 +923,7 @@ void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
   Builder b{m};
   // rows of at most 1024 features: LayerNorm backward with its column sums in one pass
   const bool fused_ln = m->d <= 1024;
-  const int ln_g = ln_bwd_fused_ctas(m->TT);  // partial rows per token tile
+  const int ln_g = ln_bwd_fused_ctas(m->TT, m->d);  // partial rows per token tile
   const int GW = acc ? ACC_RW : ACC_W;  // access of the tasks that write parameter gradients
   const int d = m->d, f = m->f, T = m->T, S = m->S, H = m->H, hd = m->hd, V = m->V;
   const size_t as = m->act_size;

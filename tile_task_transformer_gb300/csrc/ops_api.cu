@@ -72,7 +72,7 @@ nnt_status nnt_op_layernorm_bwd(const float* dy_dev, const float* x_dev, const f
   NNT_CHECK_ARG(rows >= 0 && cols > 0 && cols <= 32768 && dtype_ok(dtype), "bad size or dtype");
   cudaStream_t st = (cudaStream_t)stream;
   if (dg_dev && rows > 0 && cols <= 1024) {  // one pass: rows and their column sums
-    const int64_t np = ln_bwd_fused_ctas(rows);
+    const int64_t np = ln_bwd_fused_ctas(rows, (int)cols);
     void* part = nullptr;
     NNT_TRY(scratch((size_t)np * 3 * cols * 4, &part));
     NNT_TRY(launch_ln_bwd_fused(dy_dev, x_dev, mean_dev, rstd_dev, g_dev, resid_dev, dx_dev, dx_act_dev,
