@@ -21,8 +21,11 @@
 //
 //   flash_fwd_kernel     item x query block: O and the log-sum-exp
 //   flash_bwd_d_kernel   D = rowsum(dO * O)
-//   flash_bwd_kv_kernel  item x key block: dK, dV over the query blocks at or after it
+//   flash_bwd_kv_kernel  item x key block: dK, dV over the query blocks at or after it,
+//                        and (given a dS^T buffer) each dS^T tile stored by TMA, after
+//                        which dQ = dS K is the causal tensor-core GEMM
 //   flash_bwd_q_kernel   item x query block: dQ over the key blocks at or before it
+//                        (recomputing S and dP; used without a dS^T buffer)
 // dK/dV and dQ come from separate passes, so every sum has a fixed order (no
 // atomics). Every mbarrier wait is bounded: on expiry the kernel records the
 // device error word, waits (bounded) for its own copies and MMAs in flight,
