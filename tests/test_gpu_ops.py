@@ -144,10 +144,14 @@ def test_gelu(dtype):
     chk(n(du), O.gelu_backward(n(dgt).astype(np.float64), u.astype(np.float64)))
 
 
-@pytest.mark.parametrize("rows,cols", [(5, 256), (64, 50257), (3, 1000)])
+# Rows of up to 56320 logits are held in shared memory (one CTA per SM, more
+# rows than SMs in the 300-row case, a quarter of the row past the columns in
+# the padded case); 60000 logits take the two-pass kernel.
+@pytest.mark.parametrize("rows,cols,pad", [(5, 256, 0), (64, 50257, 0), (3, 1000, 0),
+                                           (300, 50257, 0), (7, 1000, 4000), (3, 60000, 0)])
 @pytest.mark.parametrize("dtype", [nnt.F32, nnt.BF16])
-def test_cross_entropy(rows, cols, dtype):
-    ldz = (cols + 3) // 4 * 4
+def test_cross_entropy(rows, cols, pad, dtype):
+    ldz = (cols + 3) // 4 * 4 + pad
     lddz = (cols + 7) // 8 * 8
     z = np.zeros((rows, ldz), np.float32)
     z[:, :cols] = synth.normal_matrix(8, 1, (rows, cols), 3.0)

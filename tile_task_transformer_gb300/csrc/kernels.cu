@@ -1152,6 +1152,9 @@ nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t
   NNT_CHECK_ARG(ldz % 4 == 0 && lddz % 4 == 0 && ldz >= cols && lddz >= cols,
                 "cross entropy: leading dimensions must be multiples of 4 and >= cols");
   if (nrows == 0) return NNT_OK;
+  if (cols > 0 && cross_entropy_smem_fits(ldz) && reinterpret_cast<uintptr_t>(z) % 16 == 0)
+    return launch_cross_entropy_smem(z, ldz, r0, nrows, cols, tok_ids, tm, tgt, tgt_stride, dz, lddz,
+                                     row_loss, inv_rows, act_dtype, sm_count(), st);
   // two CTAs per SM walk the rows, so the rows being re-read (pass 2) stay in L2
   const unsigned grid = (unsigned)std::min<int64_t>(nrows, 2 * 152);
   if (act_dtype == NNT_BF16)
