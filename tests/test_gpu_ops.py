@@ -144,13 +144,18 @@ def test_gelu(dtype):
     chk(n(du), O.gelu_backward(n(dgt).astype(np.float64), u.astype(np.float64)))
 
 
-# Rows of up to 56320 logits are held in shared memory (one CTA per SM, more
-# rows than SMs in the 300-row case, a quarter of the row past the columns in
-# the padded case); 60000 logits take the two-pass kernel.
+# Both kernels on every shape. The cluster-pair kernel holds rows of up to 55296
+# logits in shared memory, half a row per CTA: more rows than clusters in the
+# 300-row case, padding past the columns, a second half that is empty (3
+# columns) or holds only the tail (5); 60000 logits always take the two-pass
+# kernel.
 @pytest.mark.parametrize("rows,cols,pad", [(5, 256, 0), (64, 50257, 0), (3, 1000, 0),
-                                           (300, 50257, 0), (7, 1000, 4000), (3, 60000, 0)])
+                                           (300, 50257, 0), (7, 1000, 4000), (9, 3, 0),
+                                           (2, 5, 0), (3, 60000, 0)])
 @pytest.mark.parametrize("dtype", [nnt.F32, nnt.BF16])
-def test_cross_entropy(rows, cols, pad, dtype):
+@pytest.mark.parametrize("kernel", ["pair", "twopass"])
+def test_cross_entropy(rows, cols, pad, dtype, kernel, monkeypatch):
+    monkeypatch.setenv("NNT_CE_KERNEL", kernel)
     ldz = (cols + 3) // 4 * 4 + pad
     lddz = (cols + 7) // 8 * 8
     z = np.zeros((rows, ldz), np.float32)

@@ -36,6 +36,7 @@
 
 #include "flash.cuh"
 #include "gemm.cuh"
+#include "ptx_math.cuh"
 #include "tc_ptx.cuh"
 
 namespace nnt {
@@ -45,39 +46,6 @@ constexpr int FB = 128;              // queries or keys per block
 constexpr int kThreads = 256;     // forward: two threads per row, one per half of the columns
 constexpr int kBwdThreads = 256;  // backward: the same split
 constexpr int CHUNK = FB * 128;      // one [128 rows][64 bf16] swizzled chunk: 16 KB
-
-__device__ __forceinline__ float ex2f(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Packed two-lane fp32 arithmetic (one instruction for two values).
-__device__ __forceinline__ uint64_t f2_bits(float2 a) {
-  uint64_t u;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(a.x), "f"(a.y));
-  return u;
-}
-__device__ __forceinline__ float2 bits_f2(uint64_t u) {
-  float2 a;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(u));
-  return a;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
 
 // Descriptor of K step kk (16 elements) of a [128][*] tile used K-major.
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {

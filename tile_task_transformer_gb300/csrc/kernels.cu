@@ -10,6 +10,8 @@
 // fixed order, so results do not depend on scheduling.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 
@@ -1152,7 +1154,15 @@ nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t
   NNT_CHECK_ARG(ldz % 4 == 0 && lddz % 4 == 0 && ldz >= cols && lddz >= cols,
                 "cross entropy: leading dimensions must be multiples of 4 and >= cols");
   if (nrows == 0) return NNT_OK;
-  if (cols > 0 && cross_entropy_smem_fits(ldz) && reinterpret_cast<uintptr_t>(z) % 16 == 0)
+  // Rows from 32768 logits up to what shared memory holds take the cluster-pair
+  // kernel (one HBM read); shorter rows stay in L2 between the two passes here,
+  // which measured faster. NNT_CE_KERNEL=pair or twopass forces one of them.
+  const char* force_env = getenv("NNT_CE_KERNEL");
+  const char* force = force_env ? force_env : "";
+  const bool pair_ok = cross_entropy_smem_fits(cols) && reinterpret_cast<uintptr_t>(z) % 16 == 0;
+  const bool pair = pair_ok && (strcmp(force, "pair") == 0 ||
+                                (strcmp(force, "twopass") != 0 && cols >= 32768));
+  if (pair)
     return launch_cross_entropy_smem(z, ldz, r0, nrows, cols, tok_ids, tm, tgt, tgt_stride, dz, lddz,
                                      row_loss, inv_rows, act_dtype, sm_count(), st);
   // two CTAs per SM walk the rows, so the rows being re-read (pass 2) stay in L2

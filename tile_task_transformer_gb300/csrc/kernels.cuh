@@ -78,9 +78,10 @@ nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t
                                 int64_t cols, const uint16_t* tok_ids, TokMap tm,
                                 const uint16_t* tgt, int64_t tgt_stride, void* dz, int64_t lddz,
                                 float* row_loss, float inv_rows, int act_dtype, cudaStream_t st);
-// The same with the row held in shared memory (one HBM read of the logits);
-// rows of at most 56320 fp32 logits (ldz a multiple of 4, z 16-byte aligned).
-bool cross_entropy_smem_fits(int64_t ldz);
+// The same with the row held in shared memory, half a row per CTA of a
+// two-CTA cluster (one HBM read of the logits); rows of 1 to 55296 logits
+// (ldz, lddz multiples of 4, z 16-byte aligned).
+bool cross_entropy_smem_fits(int64_t cols);
 nnt_status launch_cross_entropy_smem(const float* z, int64_t ldz, int64_t r0, int64_t nrows,
                                      int64_t cols, const uint16_t* tok_ids, TokMap tm,
                                      const uint16_t* tgt, int64_t tgt_stride, void* dz, int64_t lddz,
