@@ -122,6 +122,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values of x, on every rank (x itself for one
+    rank): the job is as slow as its slowest replica."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_rate(world, tokens_per_rank, seconds):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / seconds
+
+
 def oracle_sample(name, seed, batch=1):
     """CPU oracle step on `batch` sequences of the workload; returns (tokens, seconds, cores)."""
     import numpy as np
@@ -232,13 +249,8 @@ def run_gpu(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        tmax = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        ms = tmax.item()
-    value = world * T / (ms / 1000.0)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, "cuda")
+    value = job_rate(world, T, ms / 1000.0)
 
     # ---- end to end through the C ABI: pinned host tokens in, loss out, every step
     torch.cuda.synchronize()
@@ -249,8 +261,8 @@ def run_gpu(args):
         losses.append(step(tok_pin, True))
     torch.cuda.synchronize()
     barrier()
-    e2e_s = (time.perf_counter() - t0) / args.steps
-    e2e_value = world * T / e2e_s
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, "cuda")
+    e2e_value = job_rate(world, T, e2e_s)
     assert all(np.isfinite(losses)), losses
 
     # ---- per-task timing pass (CUDA events on each task's stream) for the roofline
