@@ -228,6 +228,43 @@ nnt_status nnt_set_trace(nnt_model* m, int32_t on);
 /* Last error message of this model (or of the calling thread when m is NULL). */
 const char* nnt_last_error(const nnt_model* m);
 
+/* ------------------------------------------------------ executor schedule
+ *
+ * The executor's plan for a task graph given only by its tile accesses, as the
+ * model's own programs get it: tasks are submitted in program order, each
+ * declaring the tiles it reads and writes, and the dependencies follow from
+ * those accesses (review page "The reading" / "What carries the argument";
+ * first page, abstract: a sequential task flow whose runtime infers the
+ * dependencies). Host only: no device work and no CUDA call, so it runs without
+ * a GPU; it exposes the scheduler for inspection and tests.
+ *
+ * Tasks are 0..n_tasks-1 in program order. Task i's accesses are entries
+ * use_off[i] .. use_off[i+1]-1 (use_off has n_tasks + 1 entries, use_off[0] = 0,
+ * non-decreasing) of use_tile (any int64 tile id) and use_mode (1 read,
+ * 2 write, 3 read and write). copy_task (NULL = none) marks host<->device copy
+ * tasks, which run on one extra copy stream; stream_hint (NULL = none) pins a
+ * task to a compute stream (>= 0, clamped to n_streams - 1) or leaves it to the
+ * scheduler (-1). n_streams >= 1 compute streams.
+ *
+ * Outputs (caller-owned, n_tasks entries unless stated): stream_out[i] in
+ * 0..n_streams-1, or n_streams for the copy stream; task i's direct
+ * dependencies are dep_task[dep_off[i] .. dep_off[i+1]-1] (the last writer of
+ * each tile it uses, and for a tile it writes the readers since that writer;
+ * ascending), and the tasks it waits for on other streams (one event wait
+ * each; dependencies already implied by stream order or by earlier waits are
+ * left out) are wait_task[wait_off[i] .. wait_off[i+1]-1]. dep_off and wait_off
+ * have n_tasks + 1 entries. dep_cap and wait_cap are the capacities of dep_task
+ * and wait_task: when one is too small the call fills both offset arrays,
+ * writes nothing else and returns INVALID_ARG, so the caller can size the
+ * arrays from dep_off[n_tasks] and wait_off[n_tasks] and call again. Also
+ * INVALID_ARG on n_tasks < 0, n_streams < 1, a NULL required array, bad
+ * offsets or a mode outside 1..3. */
+nnt_status nnt_plan_schedule(int32_t n_tasks, const int64_t* use_off, const int64_t* use_tile,
+                             const int32_t* use_mode, const int32_t* copy_task,
+                             const int32_t* stream_hint, int32_t n_streams, int32_t* stream_out,
+                             int64_t* dep_off, int32_t* dep_task, int64_t dep_cap,
+                             int64_t* wait_off, int32_t* wait_task, int64_t wait_cap);
+
 /* ------------------------------------------------------ single tile tasks
  *
  * The step's tile kernels as stand-alone calls on caller device buffers, used

@@ -101,6 +101,57 @@ void Program::finalize(int n_streams) {
   for (char u : used) n_streams_used_ += u;
 }
 
+}  // namespace nnt
+
+extern "C" nnt_status nnt_plan_schedule(int32_t n_tasks, const int64_t* use_off,
+                                        const int64_t* use_tile, const int32_t* use_mode,
+                                        const int32_t* copy_task, const int32_t* stream_hint,
+                                        int32_t n_streams, int32_t* stream_out, int64_t* dep_off,
+                                        int32_t* dep_task, int64_t dep_cap, int64_t* wait_off,
+                                        int32_t* wait_task, int64_t wait_cap) {
+  using namespace nnt;
+  NNT_CHECK_ARG(n_tasks >= 0 && n_streams >= 1, "plan_schedule: n_tasks %d, n_streams %d", n_tasks,
+                n_streams);
+  NNT_CHECK_ARG(use_off && stream_out && dep_off && wait_off, "plan_schedule: NULL array");
+  NNT_CHECK_ARG(use_off[0] == 0, "plan_schedule: use_off[0] must be 0");
+  for (int32_t i = 0; i < n_tasks; ++i)
+    NNT_CHECK_ARG(use_off[i + 1] >= use_off[i], "plan_schedule: use_off decreases at task %d", i);
+  const int64_t n_uses = use_off[n_tasks];
+  NNT_CHECK_ARG(n_uses == 0 || (use_tile && use_mode), "plan_schedule: NULL tile or mode array");
+  for (int64_t u = 0; u < n_uses; ++u)
+    NNT_CHECK_ARG(use_mode[u] >= 1 && use_mode[u] <= 3, "plan_schedule: mode %d at use %lld",
+                  use_mode[u], (long long)u);
+  Program p;
+  for (int32_t i = 0; i < n_tasks; ++i) {
+    Task t;
+    for (int64_t u = use_off[i]; u < use_off[i + 1]; ++u) t.uses.push_back({use_tile[u], use_mode[u]});
+    t.copy_engine = copy_task ? (copy_task[i] != 0) : 0;
+    t.stream_hint = stream_hint ? std::max(-1, stream_hint[i]) : -1;
+    p.add(std::move(t));
+  }
+  p.finalize(n_streams);
+  dep_off[0] = 0;
+  wait_off[0] = 0;
+  for (int32_t i = 0; i < n_tasks; ++i) {
+    dep_off[i + 1] = dep_off[i] + (int64_t)p.deps()[i].size();
+    wait_off[i + 1] = wait_off[i] + (int64_t)p.tasks()[i].waits.size();
+  }
+  NNT_CHECK_ARG(dep_off[n_tasks] <= dep_cap && wait_off[n_tasks] <= wait_cap,
+                "plan_schedule: %lld dependencies and %lld waits do not fit capacities %lld, %lld",
+                (long long)dep_off[n_tasks], (long long)wait_off[n_tasks], (long long)dep_cap,
+                (long long)wait_cap);
+  NNT_CHECK_ARG((dep_off[n_tasks] == 0 || dep_task) && (wait_off[n_tasks] == 0 || wait_task),
+                "plan_schedule: NULL dependency or wait array");
+  for (int32_t i = 0; i < n_tasks; ++i) {
+    stream_out[i] = p.tasks()[i].stream;
+    std::copy(p.deps()[i].begin(), p.deps()[i].end(), dep_task + dep_off[i]);
+    std::copy(p.tasks()[i].waits.begin(), p.tasks()[i].waits.end(), wait_task + wait_off[i]);
+  }
+  return NNT_OK;
+}
+
+namespace nnt {
+
 Executor::~Executor() {
   for (auto g : graphs_)
     if (g) cudaGraphExecDestroy(g);

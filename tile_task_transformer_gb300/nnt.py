@@ -106,6 +106,7 @@ _SIGS = {
     "nnt_op_gemm": (C.c_int, [_P, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32, _I64, _I64, _I64, _F,
                               _F, _I32, _I32, _P]),
     "nnt_op_read_error": (C.c_int, [C.POINTER(C.c_uint32), _P]),
+    "nnt_plan_schedule": (C.c_int, [_I32, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _I64, _P, _P, _I64]),
 }
 
 _lib = None
@@ -362,3 +363,42 @@ def read_device_error(stream=None) -> int:
     code = C.c_uint32(0)
     check(lib().nnt_op_read_error(C.byref(code), _stream(stream)))
     return code.value
+
+
+def plan_schedule(uses, n_streams, copy=None, hints=None):
+    """The executor's plan for tasks given by their tile accesses (host only).
+
+    ``uses[i]`` lists task i's ``(tile, mode)`` pairs (mode 1 read, 2 write,
+    3 both); ``copy`` and ``hints`` are optional per-task lists (copy-stream
+    task; pinned compute stream or -1). Returns ``(streams, deps, waits)``:
+    each task's stream, its direct dependencies and its cross-stream waits."""
+    n = len(uses)
+    off = np.zeros(n + 1, np.int64)
+    off[1:] = np.cumsum([len(u) for u in uses])
+    tiles = np.array([t for u in uses for t, _ in u], np.int64)
+    modes = np.array([m for u in uses for _, m in u], np.int32)
+    cp = None if copy is None else np.ascontiguousarray(copy, np.int32)
+    hi = None if hints is None else np.ascontiguousarray(hints, np.int32)
+    streams = np.zeros(n, np.int32)
+    dep_off = np.zeros(n + 1, np.int64)
+    wait_off = np.zeros(n + 1, np.int64)
+    cap_d = cap_w = 0
+    dep = wait = np.zeros(0, np.int32)
+    for _ in range(2):  # the first call sizes the outputs
+        st = lib().nnt_plan_schedule(n, _ptr(off), _ptr(tiles) if tiles.size else None,
+                                     _ptr(modes) if modes.size else None, _ptr(cp), _ptr(hi),
+                                     n_streams, _ptr(streams), _ptr(dep_off),
+                                     _ptr(dep) if dep.size else None, cap_d, _ptr(wait_off),
+                                     _ptr(wait) if wait.size else None, cap_w)
+        if st == OK:
+            break
+        if dep_off[n] <= cap_d and wait_off[n] <= cap_w:
+            check(st)
+        cap_d, cap_w = int(dep_off[n]), int(wait_off[n])
+        dep = np.zeros(max(cap_d, 1), np.int32)
+        wait = np.zeros(max(cap_w, 1), np.int32)
+    else:
+        check(st)
+    deps = [dep[dep_off[i]:dep_off[i + 1]].tolist() for i in range(n)]
+    waits = [wait[wait_off[i]:wait_off[i + 1]].tolist() for i in range(n)]
+    return streams.tolist(), deps, waits
