@@ -53,3 +53,32 @@ def test_null_safety(L):
     assert L.nnt_backward(None) == nnt.ERR_INVALID_ARG
     st = L.nnt_create_model(None, None, None, None)
     assert st == nnt.ERR_INVALID_ARG
+
+
+# Stand-alone tile tasks: invalid arguments are rejected before any device work,
+# so these run without a GPU (the pointers are never dereferenced).
+P = 4096  # a non-NULL stand-in address
+
+
+@pytest.mark.parametrize("call,why", [
+    (lambda: nnt.op_flash_attention_fwd(P, P, P, P, P, 2, 128, 32), "head size 32 has no fused kernel"),
+    (lambda: nnt.op_flash_attention_fwd(P, None, P, P, P, 2, 128, 64), "NULL k"),
+    (lambda: nnt.op_flash_attention_bwd(P, P, P, P, P, P, P, P, P, 0, 128, 64), "Z = 0"),
+    (lambda: nnt.op_cross_entropy(P, 0, 100, 100, P, 1, P, 100, P, P, nnt.F32), "no rows"),
+    (lambda: nnt.op_cross_entropy(P, 4, 0, 4, P, 1, P, 4, P, P, nnt.F32), "no columns"),
+    (lambda: nnt.op_cross_entropy(P, 4, 100, 100, P, 1, P, 100, P, P, 5), "dtype"),
+    (lambda: nnt.op_gemm(P, 8, 0, P, 8, 1, P, 16, nnt.F32, 16, 16, 16), "lda < K"),
+    (lambda: nnt.op_gemm(P, 16, 0, P, 16, 1, P, 16, nnt.F32, 16, 16, 16, beta=0.5), "beta 0.5"),
+    (lambda: nnt.op_gemm(P, 16, 0, P, 16, 1, P, 16, nnt.BF16, 16, 16, 16, beta=1.0), "beta 1 with bf16 C"),
+    (lambda: nnt.op_adamw(P, P, P, P, None, 10, 3e-4, 0.9, 0.999, 0.0, 0.1, 0.1, 0.001), "eps 0"),
+    (lambda: nnt.op_adamw(P, P, P, P, None, 10, 3e-4, 0.9, 0.999, 1e-8, 0.1, 0.0, 0.001), "bc1 0"),
+    (lambda: nnt.op_embedding_fwd(P, 32, P, P, P, 2, 32, 64, 70000), "vocab over uint16"),
+    (lambda: nnt.op_embedding_fwd(P, 16, P, P, P, 2, 32, 64, 256), "ids stride < seq"),
+    (lambda: nnt.op_layernorm_fwd(P, P, P, P, P, P, 4, 40000, 1e-5, nnt.F32), "cols > 32768"),
+    (lambda: nnt.op_gelu_fwd(P, P, 10, 9), "dtype"),
+])
+def test_op_arguments_rejected_before_device_work(L, call, why):
+    with pytest.raises(nnt.NNTError) as e:
+        call()
+    assert e.value.status == nnt.ERR_INVALID_ARG, why
+    assert L.nnt_last_error(None)
