@@ -25,9 +25,11 @@
  *   - Token windows are uint16 [batch, seq + 1] (the nanoGPT-style uint16 token
  *     stream of the README's "Minimal working GPT example"): inputs are
  *     columns 0..seq-1, next-token targets columns 1..seq.
- *   - All work is issued on one CUDA stream (nnt_options.stream, or the legacy
- *     default stream when NULL) plus library-owned side streams that are joined
- *     back into it before each call returns.
+ *   - A model issues its work on one CUDA stream (nnt_options.stream; when that
+ *     is NULL, a blocking stream the model creates and destroys, which the
+ *     legacy default stream orders against) plus library-owned side streams
+ *     that are joined back into it before each call returns. The stand-alone
+ *     tile tasks (nnt_op_*) run on the stream they are given.
  */
 #ifndef NNT_H
 #define NNT_H
@@ -75,7 +77,7 @@ typedef struct {
 
 /* Library options. Zero-initialised options are valid defaults. */
 typedef struct {
-  void* stream;                /* cudaStream_t the step runs on (NULL = legacy default) */
+  void* stream;                /* cudaStream_t the step runs on (NULL = a stream of the model's own) */
   uint64_t hbm_budget_bytes;   /* device bytes the model may use; 0 = free memory - 2 GiB */
   int32_t allow_host_offload;  /* 1: tiles that do not fit go to pinned host RAM */
   uint64_t init_seed;          /* weights drawn on the device from this seed ... */
