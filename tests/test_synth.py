@@ -1,5 +1,6 @@
 """Seeded input generators: splitmix64 against its published sequence, recipes."""
 import numpy as np
+import pytest
 
 from tile_task_transformer_gb300 import synth
 
@@ -35,3 +36,13 @@ def test_param_recipe():
     assert list(p) == names and len(names) == 2 + 12 * 2 + 2
     assert np.all(p["h0.ln1.g"] == 1) and np.all(p["ln_f.b"] == 0)
     assert sum(v.size for v in p.values()) == 118528
+
+
+@pytest.mark.parametrize("L,d,f,V,S,stated,half_unit", [
+    (12, 768, 3072, 50257, 1024, 124.4e6, 0.05e6),  # GPT2-small shape (124.4M)
+    (4, 8192, 32768, 50257, 1024, 3.6e9, 0.05e9),   # wide-4, stated as about 3.6B parameters
+    (8, 16384, 65536, 50257, 1024, 26.6e9, 0.05e9), # wide-8, stated as about 26.6B parameters
+])
+def test_parameter_counts_match_the_stated_model_sizes(L, d, f, V, S, stated, half_unit):
+    n = sum(int(np.prod(s)) for _, s in synth.param_names_shapes(L, d, f, V, S))
+    assert abs(n - stated) <= half_unit, (n, stated)  # equal after rounding to the stated digits
