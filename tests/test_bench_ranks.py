@@ -1,4 +1,4 @@
-"""The bench's multi-rank bookkeeping on the CPU: max over ranks through a
+"""The bench's bookkeeping on the CPU: max over ranks through a
 world-size-2 gloo process group, the whole-job rate, and the reference arm
 running on rank 0 alone. (On GPUs the same helpers run over NCCL, one rank per
 GPU; every rank is an independent replica, so there is no data-path
@@ -63,3 +63,13 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = argparse.Namespace(workload="tiny", warmup=3, steps=2, gpus=2)
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+@pytest.mark.parametrize("L,d,H,f,V,S,B", [(12, 768, 12, 3072, 50257, 1024, 4),
+                                           (4, 8192, 64, 32768, 50257, 1024, 8),
+                                           (2, 64, 4, 256, 256, 32, 2)])
+def test_model_flops_agree_with_the_pinned_oracle_count(L, d, H, f, V, S, B):
+    from oracle import gpt2 as O
+
+    cfg = O.GPT2Config(n_layer=L, d_model=d, n_head=H, d_ff=f, vocab=V, seq=S, batch=B)
+    assert bench.model_step_flops(L, d, H, f, V, S, B) == O.step_flops(cfg)
