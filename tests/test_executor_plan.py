@@ -18,6 +18,8 @@ R, W, RW = 1, 2, 3
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
+    from tile_task_transformer_gb300 import build
+    build.build()  # host compile only; no GPU needed
     nnt.lib()
 
 
