@@ -30,6 +30,11 @@
  *     legacy default stream orders against) plus library-owned side streams
  *     that are joined back into it before each call returns. The stand-alone
  *     tile tasks (nnt_op_*) run on the stream they are given.
+ *   - Environment (for measurement; the defaults choose per shape):
+ *     NNT_GEMM_BN=64|128|192|256 forces the width of the tensor-core GEMM's
+ *     128 x BN output tiles; NNT_CE_KERNEL=pair|twopass forces the
+ *     cross-entropy kernel (the two-CTA-cluster kernel holds rows of up to
+ *     55296 logits in shared memory; the two-pass kernel takes any row).
  */
 #ifndef NNT_H
 #define NNT_H
@@ -344,7 +349,9 @@ nnt_status nnt_op_gelu_bwd(const void* dg_dev, const float* u_dev, void* du_dev,
  * columns valid; README --loss-reduction=mean) with uint16 targets
  * (tgt_dev[r * tgt_stride]) and its gradient dz = (softmax(z) - onehot)/rows
  * written as act [rows, lddz] (columns cols..lddz-1 written as 0). loss_dev: one
- * fp32 (the mean). row_loss_dev: fp32 [rows] scratch for per-row losses. */
+ * fp32 (the mean). row_loss_dev: fp32 [rows] scratch for per-row losses.
+ * ldz and lddz are multiples of 4 and at least cols (INVALID_ARG otherwise);
+ * a target >= cols sets the device error word (nnt_op_read_error). */
 nnt_status nnt_op_cross_entropy(const float* z_dev, int64_t rows, int64_t cols, int64_t ldz,
                                 const uint16_t* tgt_dev, int64_t tgt_stride, void* dz_dev,
                                 int64_t lddz, float* row_loss_dev, float* loss_dev,

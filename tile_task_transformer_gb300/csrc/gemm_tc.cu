@@ -709,10 +709,7 @@ nnt_status launch_bn(const GemmArgs& g, cudaStream_t st) {
   return launch_tc<BN, false, false>(g, st);
 }
 
-// Tile width: the widest of 256/128/64 whose persistent schedule wastes at most
-// a little more than the narrower ones (tiles per CTA rounded up).
-// Relative tensor-pipe efficiency of a 128 x BN tile (smem operand traffic per
-// MMA grows as BN shrinks), measured on GB300 for K >= 768.
+// NNT_GEMM_BN=64|128|192|256 forces the tile width (for measurement).
 int bn_override() {
   static int v = -1;
   if (v < 0) {
@@ -723,6 +720,10 @@ int bn_override() {
   return v;
 }
 
+// Tile width BN of the 128 x BN output tiles: the one with the best product of
+// wave efficiency (tiles over whole waves of one tile per SM) and the relative
+// tensor-pipe efficiency of a 128 x BN tile (shared-memory operand traffic per
+// MMA grows as BN shrinks), measured on GB300 for K >= 768.
 int choose_bn(const GemmArgs& g) {
   if (bn_override()) return bn_override();
   if (g.nt <= 64) return 64;
