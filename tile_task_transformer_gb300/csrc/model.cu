@@ -916,9 +916,8 @@ void build_forward(nnt_model* m) {
 // its gradient is final and every task that reads the old weights has been
 // issued (weight reads are declared, so the executor orders the update after
 // them); moments in pinned host memory are updated in place over NVLink-C2C.
-// fused: each chunk's AdamW update follows its final gradient. acc (not with
-// fused): every gradient write adds to the stored gradient instead of
-// replacing it.
+// acc (not with fused): every gradient write adds to the stored gradient
+// instead of replacing it.
 void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
   Builder b{m};
   // rows of at most 1024 features: LayerNorm backward with its column sums in one pass
