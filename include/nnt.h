@@ -142,7 +142,7 @@ typedef struct {
  * Errors: INVALID_ARG if n_ctx % seq_tile, n_head % head_tile,
  * batch % batch_tile or d_model % n_head is non-zero, if d_model, d_ff or the
  * head size is not a multiple of 8 (bf16: head size a multiple of 16), if vocab
- * > 65536, or if batch*n_ctx > 16384; OOM if the tiles do not fit and offload is
+ * > 65536, or if batch*n_ctx > 1048576; OOM if the tiles do not fit and offload is
  * off. *out is NULL on error. */
 nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
                             const nnt_options* opts, nnt_model** out);
@@ -372,18 +372,19 @@ nnt_status nnt_op_embedding_fwd(const uint16_t* ids_dev, int64_t ids_stride, con
 
 /* Embedding scatter-add, deterministic: dwte[ids[t]] += dx[t] for token
  * t = b*seq + s in increasing t order, dwpe[s] += dx[b, s] in increasing b
- * order (fp32). Needs batch*seq <= 16384. */
+ * order (fp32). Needs batch*seq <= 1048576; uses library scratch of
+ * 4*batch*seq bytes (allocated once per device and grown on demand). */
 nnt_status nnt_op_embedding_bwd(const uint16_t* ids_dev, int64_t ids_stride, const float* dx_dev,
                                 float* dwte_dev, float* dwpe_dev, int64_t batch, int64_t seq,
                                 int64_t d, int64_t vocab, void* stream);
 
 /* Same as nnt_op_embedding_bwd (same results, bit for bit), but it allocates
  * nothing. It is meant for callers that cannot allocate device memory while
- * they run: code enqueuing work inside a CUDA stream capture (cudaMalloc is not
- * capturable), hosts that own all device memory through their own allocator or
- * a fixed budget, and loops that cannot afford an allocation's implicit
- * synchronisation. The NNTile pages have no counterpart of this call; it only
- * changes where the scratch lives.
+ * they run: hosts that own all device memory through their own allocator or a
+ * fixed budget (a library allocation would bypass it, or fail), and loops that
+ * cannot afford the implicit device synchronisation of an allocation. The
+ * NNTile pages have no counterpart of this call; it only changes where the
+ * scratch lives.
  * Scratch: one fixed array of 16384 uint32 sort keys (64 KiB) compiled into
  * the library, present on every device that loads it until the process exits;
  * so batch*seq must be <= 16384 (INVALID_ARG otherwise, before any work).
@@ -412,6 +413,39 @@ nnt_status nnt_op_gemm(const void* a_dev, int64_t lda, int32_t a_trans, const vo
 /* Device error word of the kernels (bad token ids, exhausted bounded waits):
  * read and clear. 0 = none. */
 nnt_status nnt_op_read_error(uint32_t* code_out, void* stream);
+
+/* ---- failure detection (tests) ----------------------------------------
+ * Host-side fault injection, off by default: after
+ * nnt_set_fault_injection(kind, n) the n-th call of that kind from now on
+ * fails the way the real failure would, without any GPU work failing:
+ *   NNT_FAULT_DEVICE_ALLOC  a device allocation of nnt_create_model -> NNT_ERR_OOM
+ *   NNT_FAULT_HOST_ALLOC    a pinned host allocation (loss word, offloaded
+ *                           AdamW moments) -> NNT_ERR_OOM
+ *   NNT_FAULT_COPY          an async copy submission of the model API (token
+ *                           upload, loss read-back, parameter/gradient/state
+ *                           copies) -> NNT_ERR_CUDA, the copy not issued
+ *   NNT_FAULT_EVENT_WAIT    a host wait for the model's stream -> NNT_ERR_TIMEOUT
+ *                           (the device work itself still completes)
+ * n = 0 disarms. Calls of other kinds are not counted. After an injected
+ * failure the model (if created) stays valid and destroyable; nnt_create_model
+ * frees everything it had allocated and sets *out to NULL.
+ * Thread-safe; the counters are process-wide. */
+typedef enum {
+  NNT_FAULT_DEVICE_ALLOC = 0,
+  NNT_FAULT_HOST_ALLOC = 1,
+  NNT_FAULT_COPY = 2,
+  NNT_FAULT_EVENT_WAIT = 3
+} nnt_fault_kind;
+nnt_status nnt_set_fault_injection(int32_t kind, int64_t nth);
+
+/* Bounded device wait, self-test: one CTA waits on an mbarrier phase that
+ * nothing completes (arrive = 0) or that its own thread completes first
+ * (arrive = 1), giving up after limit_ns nanoseconds of %globaltimer (1 us ..
+ * 1 s, INVALID_ARG otherwise). On giving up it ORs the wait-timeout bit (2)
+ * into the device error word (nnt_op_read_error) and returns; the GPU context
+ * stays usable. The same bounded wait guards every mbarrier wait of the
+ * tensor-core kernels (their limit: 5 s). */
+nnt_status nnt_op_wait_selftest(int64_t limit_ns, int32_t arrive, void* stream);
 
 #ifdef __cplusplus
 }

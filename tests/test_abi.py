@@ -38,7 +38,7 @@ def _create(cfg, tiles=None):
     (nnt.Config(2, 64, 4, 256, 70000, 32, 2, 0, 1e-5), None, "vocab"),
     (nnt.Config(2, 64, 4, 256, 256, 32, 2, 7, 1e-5), None, "dtype"),
     (nnt.Config(2, 68, 4, 256, 256, 32, 2, 0, 1e-5), None, "multiple of 8"),
-    (nnt.Config(2, 64, 4, 256, 256, 8192, 4, 0, 1e-5), None, "batch*n_ctx"),
+    (nnt.Config(2, 64, 4, 256, 256, 8192, 129, 0, 1e-5), None, "batch*n_ctx"),  # > 2^20 tokens
 ])
 def test_invalid_shapes_rejected_before_device_work(L, cfg, tiles, why):
     st, h = _create(cfg, tiles)
@@ -82,3 +82,17 @@ def test_op_arguments_rejected_before_device_work(L, call, why):
         call()
     assert e.value.status == nnt.ERR_INVALID_ARG, why
     assert L.nnt_last_error(None)
+
+
+def test_fault_injection_arguments_checked_on_host(L):
+    assert L.nnt_set_fault_injection(4, 1) == nnt.ERR_INVALID_ARG
+    assert L.nnt_set_fault_injection(-1, 1) == nnt.ERR_INVALID_ARG
+    assert L.nnt_set_fault_injection(nnt.FAULT_COPY, -2) == nnt.ERR_INVALID_ARG
+    for k in range(4):  # arm and disarm: host-only, no device call
+        assert L.nnt_set_fault_injection(k, 3) == nnt.OK
+        assert L.nnt_set_fault_injection(k, 0) == nnt.OK
+
+
+def test_wait_selftest_limit_checked_before_device_work(L):
+    assert L.nnt_op_wait_selftest(999, 0, None) == nnt.ERR_INVALID_ARG
+    assert L.nnt_op_wait_selftest(1_000_000_001, 0, None) == nnt.ERR_INVALID_ARG

@@ -3,13 +3,10 @@
 * GPT2-small shape (12 x 768, vocab 50257, 4 x 1024 tokens, tiles of the
   NNTile README example): the whole step against the fp64 oracle.
 * wide-4 (4 x 8192, 64 heads, d_ff 32768, 8 x 1024 tokens, 3.6B parameters):
-  too large for the oracle as a whole, so it is checked through properties that
-  hold at any size, each computable by the oracle on one sequence:
-    - the batch's 8 windows are copies of one sequence, so the mean-loss
-      gradient (and the loss) equal those of that single sequence;
-    - the logits of every sequence depend on that sequence only, so the
-      logits of the replicated batch equal the single-sequence logits;
-    - with wte = 0 every logit is 0 and the loss is ln V exactly.
+  the batch holds two distinct sequences four times each, so the loss, the
+  gradients and the AdamW update equal those of the two sequences alone, which
+  the oracle computes; with wte = 0 every logit is 0 and the loss is ln V
+  exactly.
 """
 import math
 
@@ -58,21 +55,11 @@ def test_gpt2_small_full_step_matches_oracle():
     grads = m.grads()
     m.adamw_step()
     new = m.params()
+    mom1 = {n: m.get_adam_state(i, 0) for i, n in enumerate(m.names)}
     m.close()
-    rloss, rgrads, rnew, _, _ = O.train_step(cfg, params, win)
+    rloss, rgrads, rnew, rm, _ = O.train_step(cfg, params, win)
     assert abs(loss - rloss) < 1e-3, (loss, rloss)
-    worst = {}
-    for n in rgrads:
-        e = relerr(grads[n], rgrads[n])
-        worst[n] = e
-        assert e < TOL, (n, e)
-        w0 = params[n].astype(np.float64)
-        if np.abs(w0).max() > 0:
-            assert relerr(new[n], rnew[n]) < TOL, n
-        bound = 2 * 3e-4 * (1 + TOL) + TOL * np.abs(rnew[n]).max()
-        assert np.abs(new[n] - rnew[n]).max() <= bound, n
-        sel = np.abs(rgrads[n]) > 0.2 * np.abs(rgrads[n]).max()
-        assert relerr((new[n] - w0)[sel], (rnew[n] - w0)[sel]) < TOL, n
+    worst = _step_checks(grads, new, mom1, params, rgrads, rnew, rm)
     print("worst normwise grad error", max(worst.values()))
 
 
@@ -85,46 +72,68 @@ def test_wide4_zero_embedding_loss_is_log_vocab():
     assert abs(loss - math.log(cfg.vocab)) < 1e-4
 
 
-def test_wide4_replicated_batch_matches_single_sequence_oracle():
+def _step_checks(grads, new, mom1, params, rgrads, rnew, rm):
+    """Normwise gradient, first-moment and updated-weight errors of one step."""
+    worst = {}
+    for n in rgrads:
+        e = relerr(grads[n], rgrads[n])
+        worst[n] = e
+        assert e < TOL, (n, e)
+        assert relerr(mom1[n], rm[n]) < TOL, n
+        w0 = params[n].astype(np.float64)
+        if np.abs(w0).max() > 0:
+            assert relerr(new[n], rnew[n]) < TOL, n
+        # at t = 1 the update is -lr (wd w + g/(|g| + eps)): a gradient that is
+        # ~0 in both may flip sign, which moves the weight by 2 lr
+        bound = 2 * 3e-4 * (1 + TOL) + TOL * np.abs(rnew[n]).max()
+        assert np.abs(new[n] - rnew[n]).max() <= bound, n
+        sel = np.abs(rgrads[n]) > 0.2 * np.abs(rgrads[n]).max()
+        assert relerr((new[n] - w0)[sel], (rnew[n] - w0)[sel]) < TOL, n
+    return worst
+
+
+def test_wide4_step_matches_bf16_operand_oracle():
+    """The whole wide-4 step (forward, backward, AdamW at t = 1) on a batch of
+    two distinct sequences, each repeated 4 times: the mean over the 8 windows
+    equals the mean over the two, which the oracle computes.
+
+    The reference is the oracle with every matrix-product operand rounded to
+    bf16 (the stated precision: bf16 GEMM operands, fp32 accumulation and fp32
+    everything else): loss within 1e-3 of it, gradients, first moments and
+    updated weights within 2e-2 normwise. The departures of the same step from
+    the unrounded oracle are printed, not asserted (except the logits); at
+    d_model 8192 they come from the bf16 operands themselves."""
     cfg = WIDE4
-    one = O.GPT2Config(n_layer=cfg.n_layer, d_model=cfg.d_model, n_head=cfg.n_head, d_ff=cfg.d_ff,
-                       vocab=cfg.vocab, seq=cfg.seq, batch=1)
+    two = O.GPT2Config(n_layer=cfg.n_layer, d_model=cfg.d_model, n_head=cfg.n_head, d_ff=cfg.d_ff,
+                       vocab=cfg.vocab, seq=cfg.seq, batch=2)
     params = synth.gpt2_params(3, cfg.n_layer, cfg.d_model, cfg.d_ff, cfg.vocab, cfg.seq)
-    seq = synth.token_windows(3, 1, cfg.seq, cfg.vocab)
-    win = np.ascontiguousarray(np.repeat(seq, cfg.batch, axis=0))
+    seqs = np.concatenate([synth.token_windows(3, 1, cfg.seq, cfg.vocab),
+                           synth.token_windows(4, 1, cfg.seq, cfg.vocab)])
+    win = np.ascontiguousarray(np.tile(seqs, (cfg.batch // 2, 1)))  # s0, s1, s0, s1, ...
     m = make(cfg, WIDE4_TILES)
     m.set_params(params)
     loss = m.forward(win)
-    logits = m.logits()[: cfg.seq]  # rows of sequence 0 (token tiles hold whole sequences)
+    logits = m.logits()[: 2 * cfg.seq]  # windows 0 and 1: rows b * S + s
     m.backward()
-    grads = {n: m.get_grad(i) for i, n in enumerate(m.names)}
+    grads = m.grads()
+    m.adamw_step()
+    new = m.params()
+    mom1 = {n: m.get_adam_state(i, 0) for i, n in enumerate(m.names)}
     m.close()
-    # The tensor-core path multiplies bf16 operands; the oracle's bf16 precision
-    # model rounds the same operands (and the gradients kept only as operands)
-    # at the same points. At d_model 8192 that rounding alone moves the loss by
-    # ~2.3e-3 and the gradients by up to ~4% (normwise, growing with depth) from
-    # the unrounded oracle, so for this configuration the tolerances are read
-    # against the model: loss within 1e-3 of it; each gradient within
-    # max(2e-2, the model's own deviation) of it, and no further from the
-    # unrounded oracle than the model is, plus 2e-2.
-    bloss, bcache = O.forward(one, params, seq, dtype=np.float32, gemm_operands="bf16")
-    assert abs(loss - bloss) < 1e-3, (loss, bloss)
-    bgrads = O.backward_bf16_operands(one, params, bcache, dtype=np.float32)
+
+    bloss, bcache = O.forward(two, params, seqs, dtype=np.float32, gemm_operands="bf16")
+    bgrads = O.backward_bf16_operands(two, params, bcache, dtype=np.float32)
     del bcache
-    # single-sequence unrounded oracle in float32 (its float32 mode agrees with
-    # float64 to 1e-4, a test of the oracle's own)
-    rloss, cache = O.forward(one, params, seq, dtype=np.float32)
-    assert abs(loss - rloss) < abs(bloss - rloss) + 1e-3, (loss, rloss, bloss)
+    bnew, bm, _ = O.adamw_step(params, bgrads, None, None, 1, O.AdamWHyper(), np.float32)
+    assert abs(loss - bloss) < 1e-3, (loss, bloss)
+    worst = _step_checks(grads, new, mom1, params, bgrads, bnew, bm)
+    del bnew, bm
+
+    rloss, cache = O.forward(two, params, seqs, dtype=np.float32)
     assert relerr(logits, cache["z"]) < TOL
-    rgrads = O.backward(one, params, cache, dtype=np.float32)
+    rgrads = O.backward(two, params, cache, dtype=np.float32)
     del cache
-    worst = {}
+    print(f"loss: gpu {loss:.6f} bf16-operand oracle {bloss:.6f} unrounded oracle {rloss:.6f}")
     for n in rgrads:
-        model_dev = relerr(bgrads[n], rgrads[n])
-        e_model = relerr(grads[n], bgrads[n])
-        e_exact = relerr(grads[n], rgrads[n])
-        worst[n] = (e_model, e_exact, model_dev)
-        assert e_model < max(TOL, model_dev), (n, e_model, model_dev)
-        assert e_exact < model_dev + TOL, (n, e_exact, model_dev)
-    k = max(worst, key=lambda n: worst[n][1])
-    print("largest gradient deviation (gpu-model, gpu-exact, model-exact):", k, worst[k])
+        print(f"{n}: gpu-vs-bf16 {worst[n]:.4f} gpu-vs-unrounded {relerr(grads[n], rgrads[n]):.4f} "
+              f"bf16-vs-unrounded {relerr(bgrads[n], rgrads[n]):.4f}")

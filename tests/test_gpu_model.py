@@ -114,6 +114,17 @@ def test_tiny_fp32_tile_invariance(tiles, min_cols):
     np.testing.assert_array_equal(got["grads"]["wpe"], ref["grads"]["wpe"])
 
 
+LONG = O.GPT2Config(n_layer=1, d_model=64, n_head=4, d_ff=256, vocab=256, seq=1024, batch=32)
+
+
+def test_step_beyond_one_token_sort_block():
+    """32 x 1024 tokens (more than the 16384 one CTA of the token sort holds,
+    the README's minibatch of 4 sequences of 1024 scaled up 8 times): the
+    fp32 step still matches the oracle."""
+    got = run_step(LONG, nnt.F32, {"seq_tile": 512, "batch_tile": 8})
+    check_step(LONG, got, tol=1e-4)
+
+
 @pytest.mark.parametrize("n_streams,graph", [(1, False), (4, False), (3, True)])
 def test_tiny_fp32_streams_and_graphs(n_streams, graph):
     got = run_step(TINY, nnt.F32, TINY_TILES, n_streams=n_streams, use_cuda_graph=graph)

@@ -1,9 +1,15 @@
 """The allocation-free embedding scatter-add against the regular one (GPU).
 
 nnt_op_embedding_bwd_noalloc serves callers that cannot allocate device memory
-while they run (stream capture, caller-owned memory budgets). It must give the
-same bits as nnt_op_embedding_bwd, call after call, although every call reuses
-the same fixed scratch array. This file is collected last on purpose.
+while they run: hosts that own all device memory through their own allocator
+or a fixed budget, and loops that cannot afford an allocation's implicit
+device synchronisation. It must give the same bits as nnt_op_embedding_bwd,
+call after call, although every call reuses the same fixed scratch array, and
+it must leave the device's free memory unchanged.
+
+The file is collected last (``zz``) so that a run stopping at the first
+failure has run every other test first; the tests themselves need no state
+from earlier tests and also pass alone in a fresh process.
 """
 import numpy as np
 import pytest
@@ -21,10 +27,33 @@ def _case(seed, B, S, d, V):
     return ids, dx, w0, p0
 
 
-def test_noalloc_matches_regular_call_twice():
+def _torch():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    return torch
+
+
+def test_noalloc_allocates_nothing():
+    """Free device memory is the same before and after calls (the fixed
+    scratch is part of the library's image). One call first: with lazy module
+    loading, the kernels' code is loaded onto the device at their first launch."""
+    torch = _torch()
+    B, S, d, V = 2, 512, 64, 1000
+    ids, dx, w0, p0 = _case(20, B, S, d, V)
+    idt = torch.as_tensor(ids.view(np.int16)).cuda()
+    dxt, wt, pt = torch.as_tensor(dx).cuda(), torch.as_tensor(w0).cuda(), torch.as_tensor(p0).cuda()
+    nnt.op_embedding_bwd_noalloc(idt, S + 1, dxt, wt, pt, B, S, d, V)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(2):
+        nnt.op_embedding_bwd_noalloc(idt, S + 1, dxt, wt, pt, B, S, d, V)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+
+
+def test_noalloc_matches_regular_call_twice():
+    torch = _torch()
     for seed, (B, S, d, V) in [(21, (4, 1024, 768, 50257)), (22, (16, 1024, 64, 1000))]:
         ids, dx, w0, p0 = _case(seed, B, S, d, V)
         idt = torch.as_tensor(ids.view(np.int16)).cuda()
@@ -39,9 +68,7 @@ def test_noalloc_matches_regular_call_twice():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    torch = pytest.importorskip("torch")
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
+    torch = _torch()
     B, S, d, V = 17, 1024, 8, 100  # 17408 tokens > 16384
     x = torch.zeros(8, device="cuda")
     with pytest.raises(nnt.NNTError) as e:

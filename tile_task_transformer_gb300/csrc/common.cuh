@@ -22,6 +22,17 @@ enum DeviceError : uint32_t {
 uint32_t* device_error_word();
 nnt_status read_and_clear_device_error(uint32_t* code_host, cudaStream_t st);
 
+// Host-side fault injection (nnt_set_fault_injection): counts one call of
+// `kind`; true for the call that the armed count designates.
+enum FaultKind : int {
+  FAULT_DEVICE_ALLOC = NNT_FAULT_DEVICE_ALLOC,
+  FAULT_HOST_ALLOC = NNT_FAULT_HOST_ALLOC,
+  FAULT_COPY = NNT_FAULT_COPY,
+  FAULT_EVENT_WAIT = NNT_FAULT_EVENT_WAIT,
+  FAULT_KINDS = 4
+};
+bool fault_hit(FaultKind kind);
+
 const char* status_name(nnt_status s);
 void set_thread_error(const char* fmt, ...);
 // Status of the last kernel launch on this thread (error text set on failure).

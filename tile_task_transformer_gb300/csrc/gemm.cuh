@@ -63,6 +63,9 @@ struct GemmArgs {
   int64_t ld_aux = 0;
   int aux_dtype = NNT_F32;  // NNT_F32 or NNT_BF16
   int causal = CAUSAL_NONE;
+  // limit of every mbarrier wait of the tensor-core kernel (%globaltimer ns);
+  // on expiry it sets the device error word and returns
+  uint64_t wait_ns = 5000000000ull;
 };
 
 __device__ __forceinline__ float gelu_fwd_dev(float u) {
@@ -153,5 +156,10 @@ bool gemm_tc_supported(const GemmArgs& g);
 // outputs without bias, residual or activation, one batch item, alpha 1, and
 // few output tiles for the SM count qualify.
 int gemm_split_k(const GemmArgs& g, int64_t ws_elems);
+
+// One bounded mbarrier wait (the tensor-core kernels' wait) on a phase that
+// nothing completes (arrive false) or that is completed first (arrive true);
+// on giving up after limit_ns it sets DEVERR_WAIT_TIMEOUT and returns.
+nnt_status launch_wait_selftest(uint64_t limit_ns, bool arrive, cudaStream_t st);
 
 }  // namespace nnt

@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!c.needed) continue;
         const int z = (int)g.zm.z(c.i);
         for (int kb = c.kb_lo; kb < c.kb_hi; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1)) {
+          if (!mbar_wait(&empty[s], ph ^ 1, g.wait_ns)) {
             atomicOr(err, DEVERR_WAIT_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ss = C::STAGES - 1;
           pp ^= 1;
         }
-        if (!mbar_wait(&full[ss], pp)) atomicOr(err, DEVERR_WAIT_TIMEOUT);
+        if (!mbar_wait(&full[ss], pp, g.wait_ns)) atomicOr(err, DEVERR_WAIT_TIMEOUT);
       }
     }
   } else if (warp == 1) {
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
         const TileCoord c = tile_at<BN>(g, ts, t);
         if (!c.needed) continue;
-        if (!mbar_wait(&tempty[acc], aph ^ 1)) {
+        if (!mbar_wait(&tempty[acc], aph ^ 1, g.wait_ns)) {
           atomicOr(err, DEVERR_WAIT_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = c.kb_lo; kb < c.kb_hi; ++kb) {
-          if (!mbar_wait(&full[s], ph)) {
+          if (!mbar_wait(&full[s], ph, g.wait_ns)) {
             atomicOr(err, DEVERR_WAIT_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
       const TileCoord c = tile_at<BN>(g, ts, t);
       if (!c.needed) continue;
-      if (!mbar_wait(&tfull[acc], aph)) {
+      if (!mbar_wait(&tfull[acc], aph, g.wait_ns)) {
         atomicOr(err, DEVERR_WAIT_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -830,6 +830,27 @@ nnt_status gemm_tc(const GemmArgs& g, cudaStream_t st) {
   const int split = gemm_split_k(g, g.ws ? g.ws_elems : 0);
   if (split > 1) return gemm_tc_split(g, split, st);
   return gemm_tc_one(g, st);
+}
+
+namespace {
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int arrive, uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  mbar_fence_init();
+  if (arrive) mbar_arrive(&bar);
+  if (!mbar_wait(&bar, 0, limit_ns)) atomicOr(err, DEVERR_WAIT_TIMEOUT);
+}
+}  // namespace
+
+nnt_status launch_wait_selftest(uint64_t limit_ns, bool arrive, cudaStream_t st) {
+  uint32_t* err = device_error_word();
+  if (!err) {
+    set_thread_error("device error word unavailable");
+    return NNT_ERR_CUDA;
+  }
+  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, arrive ? 1 : 0, err);
+  return launch_check("wait_selftest");
 }
 
 int gemm_split_k(const GemmArgs& g, int64_t ws_elems) {

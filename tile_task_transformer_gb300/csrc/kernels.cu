@@ -92,18 +92,24 @@ nnt_status launch_embedding_fwd(const uint16_t* ids, int64_t ids_stride, const f
   return launch_check("embedding_fwd");
 }
 
-// One CTA sorts the keys id*T + t (t = b*S + s) of all T tokens with a bitonic
-// network in shared memory. Keys are unique, so the order of tokens that share
-// an id is their token order.
+// Token sort for the embedding scatter-add. The T tokens are cut into blocks
+// of Bs = min(T, kTokenSortBlock) consecutive tokens; CTA b sorts the keys
+// id*Bs + j (j = local index of token t = b*Bs + j) of block b with a bitonic
+// network in shared memory and writes them to keys_out[b*Bs ...]. Keys are
+// unique, so inside a block the tokens that share an id stay in token order;
+// the blocks themselves are in token order.
 __global__ void token_sort_kernel(const uint16_t* __restrict__ ids, int64_t ids_stride, int B,
-                                  int S, uint32_t* __restrict__ keys_out, int npow2) {
+                                  int S, uint32_t* __restrict__ keys_out, int Bs, int npow2) {
   extern __shared__ uint32_t sk[];
   const int T = B * S;
+  const int t0 = blockIdx.x * Bs;
+  const int n = min(Bs, T - t0);
   for (int i = threadIdx.x; i < npow2; i += blockDim.x) {
     uint32_t k = 0xFFFFFFFFu;
-    if (i < T) {
-      int b = i / S, s = i % S;
-      k = (uint32_t)ids[(int64_t)b * ids_stride + s] * (uint32_t)T + (uint32_t)i;
+    if (i < n) {
+      const int t = t0 + i;
+      const int b = t / S, s = t % S;
+      k = (uint32_t)ids[(int64_t)b * ids_stride + s] * (uint32_t)Bs + (uint32_t)i;
     }
     sk[i] = k;
   }
@@ -123,44 +129,82 @@ __global__ void token_sort_kernel(const uint16_t* __restrict__ ids, int64_t ids_
       __syncthreads();
     }
   }
-  for (int i = threadIdx.x; i < T; i += blockDim.x) keys_out[i] = sk[i];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) keys_out[t0 + i] = sk[i];
 }
+
+int token_sort_block(int T) { return T < kTokenSortBlock ? T : kTokenSortBlock; }
 
 nnt_status launch_token_sort(const uint16_t* ids, int64_t ids_stride, int B, int S,
                              uint32_t* keys_out, cudaStream_t st) {
-  const int T = B * S;
-  NNT_CHECK_ARG(T > 0 && T <= 16384, "token sort: batch*seq must be in [1, 16384] (got %d)", T);
+  const int64_t T64 = (int64_t)B * S;
+  NNT_CHECK_ARG(T64 > 0 && T64 <= kMaxTokens, "token sort: batch*seq must be in [1, %d] (got %lld)",
+                kMaxTokens, (long long)T64);
+  const int T = (int)T64;
+  const int Bs = token_sort_block(T);
   int npow2 = 1;
-  while (npow2 < T) npow2 <<= 1;
+  while (npow2 < Bs) npow2 <<= 1;
   size_t smem = (size_t)npow2 * 4;
   if (smem > 48 * 1024)
     NNT_CUDA_TRY(cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
-  token_sort_kernel<<<1, 1024, smem, st>>>(ids, ids_stride, B, S, keys_out, npow2);
+  token_sort_kernel<<<(T + Bs - 1) / Bs, 1024, smem, st>>>(ids, ids_stride, B, S, keys_out, Bs, npow2);
   return launch_check("token_sort");
 }
 
-// CTA i handles sorted position i when it starts a run of equal ids: it adds the
-// dx rows of that run, in token order, onto dwte[id].
-__global__ void embedding_scatter_kernel(const uint32_t* __restrict__ keys, int T,
+// First position in keys[0, n) whose key is >= v (keys ascending).
+__device__ __forceinline__ int lower_bound_u32(const uint32_t* keys, int n, uint32_t v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (keys[mid] < v) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// CTA p looks at sorted position p (block b = p / Bs). It works only when p
+// starts the run of its id inside block b and no earlier block holds that id;
+// it then adds the dx rows of every token with that id -- block by block from
+// b on, each block's run in token order, so in increasing token order -- onto
+// dwte[id].
+constexpr int kScatterMaxBlocks = kMaxTokens / kTokenSortBlock;
+__global__ void embedding_scatter_kernel(const uint32_t* __restrict__ keys, int T, int Bs,
                                          const float* __restrict__ dx, TokMap tm, int S,
                                          float* __restrict__ dwte, int d, int vocab) {
-  const int i = blockIdx.x;
-  const uint32_t id = keys[i] / (uint32_t)T;
-  if (i > 0 && keys[i - 1] / (uint32_t)T == id) return;
+  __shared__ int run_lo[kScatterMaxBlocks], run_hi[kScatterMaxBlocks];
+  __shared__ int in_earlier;
+  const int p = blockIdx.x;
+  const int blk = p / Bs;
+  const uint32_t id = keys[p] / (uint32_t)Bs;
+  if (p > blk * Bs && keys[p - 1] / (uint32_t)Bs == id) return;  // uniform over the CTA
   if (id >= (uint32_t)vocab) return;
-  int j_end = i + 1;
-  while (j_end < T && keys[j_end] / (uint32_t)T == id) ++j_end;
+  const int nblk = (T + Bs - 1) / Bs;
+  if (threadIdx.x == 0) in_earlier = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+    const int n = min(Bs, T - b * Bs);
+    const uint32_t* kb = keys + (int64_t)b * Bs;
+    const int lo = b == blk ? p - blk * Bs : lower_bound_u32(kb, n, id * (uint32_t)Bs);
+    const int hi = lower_bound_u32(kb, n, (id + 1) * (uint32_t)Bs);
+    run_lo[b] = lo;
+    run_hi[b] = hi;
+    if (b < blk && hi > lo) in_earlier = 1;
+  }
+  __syncthreads();
+  if (in_earlier) return;  // that block's CTA covers this id
   const int nv = d >> 2;
   for (int c = threadIdx.x; c < nv; c += blockDim.x) {
     float4 acc = load4(dwte + (int64_t)id * d + 4 * c);
-    for (int j = i; j < j_end; ++j) {
-      int t = (int)(keys[j] % (uint32_t)T);
-      float4 g = load4(dx + tm.row(t / S, t % S) * d + 4 * c);
-      acc.x += g.x;
-      acc.y += g.y;
-      acc.z += g.z;
-      acc.w += g.w;
+    for (int b = blk; b < nblk; ++b) {
+      const uint32_t* kb = keys + (int64_t)b * Bs;
+      for (int j = run_lo[b]; j < run_hi[b]; ++j) {
+        const int t = b * Bs + (int)(kb[j] % (uint32_t)Bs);
+        float4 g = load4(dx + tm.row(t / S, t % S) * d + 4 * c);
+        acc.x += g.x;
+        acc.y += g.y;
+        acc.z += g.z;
+        acc.w += g.w;
+      }
     }
     store4(dwte + (int64_t)id * d + 4 * c, acc);
   }
@@ -169,9 +213,11 @@ __global__ void embedding_scatter_kernel(const uint32_t* __restrict__ keys, int 
 nnt_status launch_embedding_scatter(const uint32_t* keys, int T, const float* dx, TokMap tm, int S,
                                     float* dwte, int d, int vocab, cudaStream_t st) {
   NNT_CHECK_ARG(d % 4 == 0, "embedding scatter: d must be a multiple of 4");
+  NNT_CHECK_ARG(T >= 0 && T <= kMaxTokens, "embedding scatter: too many tokens (%d)", T);
   if (T == 0) return NNT_OK;
   int threads = std::min(256, std::max(32, (d / 4 + 31) / 32 * 32));
-  embedding_scatter_kernel<<<T, threads, 0, st>>>(keys, T, dx, tm, S, dwte, d, vocab);
+  embedding_scatter_kernel<<<T, threads, 0, st>>>(keys, T, token_sort_block(T), dx, tm, S, dwte, d,
+                                                  vocab);
   return launch_check("embedding_scatter");
 }
 

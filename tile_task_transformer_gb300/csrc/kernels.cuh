@@ -13,10 +13,16 @@ namespace nnt {
 nnt_status launch_embedding_fwd(const uint16_t* ids, int64_t ids_stride, const float* wte,
                                 const float* wpe, float* x, int d, int vocab, TokMap tm, int b0,
                                 int nb, int s0, int ns, cudaStream_t st);
-// sort keys id*T + t of all T tokens of the window (single CTA bitonic sort)
+// Tokens per batch*seq window the embedding backward handles, and the block
+// of consecutive tokens one CTA of the token sort orders in shared memory.
+constexpr int kMaxTokens = 1 << 20;
+constexpr int kTokenSortBlock = 16384;
+// Sort keys of the T = B*S tokens, T <= kMaxTokens (keys_out: T entries):
+// blocks of min(T, kTokenSortBlock) tokens, each sorted by (id, token) in one
+// CTA; key id*Bs + j for token j of its block.
 nnt_status launch_token_sort(const uint16_t* ids, int64_t ids_stride, int B, int S,
                              uint32_t* keys_out, cudaStream_t st);
-// dwte[id] += dx rows of that id in token order (needs sorted keys)
+// dwte[id] += dx rows of that id in token order (keys from launch_token_sort)
 nnt_status launch_embedding_scatter(const uint32_t* keys, int T, const float* dx, TokMap tm,
                                     int S, float* dwte, int d, int vocab, cudaStream_t st);
 // dwpe[s] (+)= sum_b dx[b, s] in b order, for s in [s0, s0+ns)

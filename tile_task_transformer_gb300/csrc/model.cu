@@ -186,10 +186,31 @@ nnt_status fail(nnt_model* m, nnt_status s) {
   return s;
 }
 
+// cudaMemcpyAsync behind the copy fault hook; `what` names the copy in the error text.
+nnt_status copy_async(void* dst, const void* src, size_t n, cudaMemcpyKind k, cudaStream_t st,
+                      const char* what) {
+  if (fault_hit(FAULT_COPY)) {
+    set_thread_error("%s: async copy submission failed (injected)", what);
+    return NNT_ERR_CUDA;
+  }
+  cudaError_t e = cudaMemcpyAsync(dst, src, n, k, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_thread_error("%s: %s", what, cudaGetErrorString(e));
+    return NNT_ERR_CUDA;
+  }
+  return NNT_OK;
+}
+
 template <typename Ptr>
 nnt_status dalloc(nnt_model* m, Ptr*& p, size_t bytes) {
   void* q = nullptr;
   if (bytes == 0) bytes = 16;
+  if (fault_hit(FAULT_DEVICE_ALLOC)) {
+    set_thread_error("cudaMalloc of %zu bytes failed (injected); %llu bytes already held", bytes,
+                     (unsigned long long)m->device_bytes);
+    return NNT_ERR_OOM;
+  }
   cudaError_t e = cudaMalloc(&q, bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -252,7 +273,7 @@ nnt_status validate(const nnt_gpt2_config* c, const nnt_tiles* t) {
   NNT_CHECK_ARG(c->dtype == NNT_F32 || hd % 16 == 0, "bf16 needs a head size multiple of 16");
   NNT_CHECK_ARG(c->vocab <= 65536, "vocab must be <= 65536 (uint16 token ids)");
   NNT_CHECK_ARG(c->n_ctx % 4 == 0, "n_ctx must be a multiple of 4");
-  NNT_CHECK_ARG((int64_t)c->batch * c->n_ctx <= 16384, "batch*n_ctx must be <= 16384");
+  NNT_CHECK_ARG((int64_t)c->batch * c->n_ctx <= kMaxTokens, "batch*n_ctx must be <= %d", kMaxTokens);
   NNT_CHECK_ARG(c->d_model <= 32768, "d_model must be <= 32768");
   if (t) {
     NNT_CHECK_ARG(t->batch_tile >= 0 && t->seq_tile >= 0 && t->embd_tile >= 0 && t->inner_tile >= 0 &&
@@ -412,8 +433,8 @@ nnt_status alloc_param_state(nnt_model* m, uint64_t budget) {
     void* hm = nullptr;
     void* hv = nullptr;
     const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
-    if (cudaHostAlloc(&hm, (size_t)host_mv * 4, fl) != cudaSuccess ||
-        cudaHostAlloc(&hv, (size_t)host_mv * 4, fl) != cudaSuccess) {
+    if (fault_hit(FAULT_HOST_ALLOC) || cudaHostAlloc(&hm, (size_t)host_mv * 4, fl) != cudaSuccess ||
+        fault_hit(FAULT_HOST_ALLOC) || cudaHostAlloc(&hv, (size_t)host_mv * 4, fl) != cudaSuccess) {
       cudaGetLastError();
       if (hm) cudaFreeHost(hm);
       set_thread_error("pinned host allocation of 2 x %lld bytes for AdamW moments failed",
@@ -546,6 +567,10 @@ nnt_status alloc_all(nnt_model* m) {
   NNT_CUDA_TRY(cudaMemset(m->z, 0, (size_t)T * m->ldz * 4));
   NNT_CUDA_TRY(cudaMemset(m->dz, 0, (size_t)T * m->lddz * as));
   void* lh = nullptr;
+  if (fault_hit(FAULT_HOST_ALLOC)) {
+    set_thread_error("pinned host allocation of the loss word failed (injected)");
+    return NNT_ERR_OOM;
+  }
   NNT_CUDA_TRY(cudaMallocHost(&lh, 64));
   m->loss_host = (float*)lh;
   m->host_bytes += 64;
@@ -1447,6 +1472,10 @@ void make_grids(nnt_model* m) {
 
 nnt_status wait_event(nnt_model* m, cudaEvent_t ev) {
   const uint32_t tmo = m->opts.timeout_ms ? m->opts.timeout_ms : 600000u;
+  if (fault_hit(FAULT_EVENT_WAIT)) {
+    set_thread_error("wait for the device timed out after %u ms (injected)", tmo);
+    return NNT_ERR_TIMEOUT;
+  }
   auto t0 = std::chrono::steady_clock::now();
   for (;;) {
     cudaError_t e = cudaEventQuery(ev);
@@ -1528,11 +1557,8 @@ nnt_status upload_hyper(nnt_model* m, const nnt_adamw* hp, int64_t t, float gsca
   h.bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
   h.bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
   h.gscale = gscale;
-  if (cudaMemcpyAsync(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_) != cudaSuccess) {
-    set_thread_error("hyper-parameter upload failed: %s", cudaGetErrorString(cudaGetLastError()));
-    return NNT_ERR_CUDA;
-  }
-  return NNT_OK;
+  return copy_async(m->hyper_dev, &h, sizeof h, cudaMemcpyHostToDevice, m->ex.main_,
+                    "hyper-parameter upload");
 }
 
 // nnt_backward (acc = false) and nnt_backward_accumulate (acc = true).
@@ -1673,18 +1699,18 @@ nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_d
   const size_t tb = (size_t)m->B * (m->S + 1) * 2;
   cudaStream_t st = m->ex.main_;
   nnt_status s = NNT_OK;
-  if (cudaMemcpyAsync(m->tokens_dev, tokens, tb,
-                      tokens_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
-                      st) != cudaSuccess) {
-    set_thread_error("token copy failed: %s", cudaGetErrorString(cudaGetLastError()));
-    return fail(m, NNT_ERR_CUDA);
-  }
+  s = copy_async(m->tokens_dev, tokens, tb, tokens_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                 st, "token copy");
+  if (s != NNT_OK) return fail(m, s);
   s = m->ex.run(m->fwd, m->opts.use_cuda_graph ? 0 : -1);
   if (s != NNT_OK) return fail(m, s);
   m->state = 1;
   if (loss_out || m->opts.trace) {
-    if (cudaMemcpyAsync(m->loss_host, m->loss_dev, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-      return fail(m, NNT_ERR_CUDA);
+    s = copy_async(m->loss_host, m->loss_dev, 4, cudaMemcpyDeviceToHost, st, "loss read-back");
+    if (s != NNT_OK) {
+      m->state = 0;
+      return fail(m, s);
+    }
     s = check_device_error(m);
     if (s != NNT_OK) {
       m->state = 0;
@@ -1802,15 +1828,15 @@ static nnt_status copy_param(nnt_model* m, int32_t i, float* base, float* host, 
   const ParamInfo& p = m->params[i];
   cudaStream_t st = m->ex.main_;
   if (to_dev) {
-    if (cudaMemcpyAsync(base + p.off, host, p.n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return fail(m, NNT_ERR_CUDA);
+    nnt_status c = copy_async(base + p.off, host, p.n * 4, cudaMemcpyHostToDevice, st, "parameter upload");
+    if (c != NNT_OK) return fail(m, c);
     if (base == m->master) {
       nnt_status s = launch_cast_bf16(m->master + p.off, m->wbf + p.off, p.n, st);
       if (s != NNT_OK) return fail(m, s);
     }
   } else {
-    if (cudaMemcpyAsync(host, base + p.off, p.n * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-      return fail(m, NNT_ERR_CUDA);
+    nnt_status c = copy_async(host, base + p.off, p.n * 4, cudaMemcpyDeviceToHost, st, "parameter read-back");
+    if (c != NNT_OK) return fail(m, c);
   }
   nnt_status s = sync_model(m);
   return s == NNT_OK ? s : fail(m, s);
@@ -1830,10 +1856,10 @@ nnt_status nnt_get_grad(nnt_model* m, int32_t i, float* host_buf) {
   }
   if (m && i >= 0 && i < (int32_t)m->params.size() && host_buf) {
     const ParamInfo& p = m->params[i];
-    if (cudaMemcpyAsync(host_buf, m->grad + p.goff, p.n * 4, cudaMemcpyDeviceToHost, m->ex.main_) !=
-        cudaSuccess)
-      return fail(m, NNT_ERR_CUDA);
-    nnt_status s = sync_model(m);
+    nnt_status s = copy_async(host_buf, m->grad + p.goff, p.n * 4, cudaMemcpyDeviceToHost, m->ex.main_,
+                              "gradient read-back");
+    if (s != NNT_OK) return fail(m, s);
+    s = sync_model(m);
     return s == NNT_OK ? s : fail(m, s);
   }
   set_thread_error("bad model, buffer or parameter index");
@@ -1855,9 +1881,10 @@ nnt_status nnt_get_adam_state(nnt_model* m, int32_t i, int32_t which, float* hos
     float* dst = host_buf + c.e0;
     if (c.host) {
       memcpy(dst, (which ? m->host_v : m->host_m) + c.mv_off, (size_t)c.n * 4);
-    } else if (cudaMemcpyAsync(dst, (which ? m->mom2 : m->mom1) + c.mv_off, (size_t)c.n * 4,
-                               cudaMemcpyDeviceToHost, m->ex.main_) != cudaSuccess) {
-      return fail(m, NNT_ERR_CUDA);
+    } else {
+      s = copy_async(dst, (which ? m->mom2 : m->mom1) + c.mv_off, (size_t)c.n * 4, cudaMemcpyDeviceToHost,
+                     m->ex.main_, "AdamW state read-back");
+      if (s != NNT_OK) return fail(m, s);
     }
   }
   s = sync_model(m);
@@ -1876,6 +1903,10 @@ nnt_status nnt_get_logits(nnt_model* m, float* host_buf) {
       for (int bl = 0; bl < m->tb; ++bl) {
         const int b = bt * m->tb + bl, s0 = st * m->ts;
         const int64_t src_row = m->tm.row(b, s0);
+        if (fault_hit(FAULT_COPY)) {
+          set_thread_error("logits read-back: async copy submission failed (injected)");
+          return fail(m, NNT_ERR_CUDA);
+        }
         if (cudaMemcpy2DAsync(host_buf + ((int64_t)b * m->S + s0) * m->V, (size_t)m->V * 4,
                               m->z + src_row * m->ldz, (size_t)m->ldz * 4, (size_t)m->V * 4, m->ts,
                               cudaMemcpyDeviceToHost, m->ex.main_) != cudaSuccess)

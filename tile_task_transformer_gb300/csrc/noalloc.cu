@@ -1,13 +1,14 @@
 // Allocation-free variant of the embedding scatter-add (nnt_op_embedding_bwd).
 //
-// Some callers cannot allocate device memory while they run: code that
-// enqueues work inside a CUDA stream capture (cudaMalloc is not capturable),
-// hosts that own all device memory through their own allocator or a fixed
-// budget, and latency-critical loops where an allocation's implicit
-// synchronisation is not acceptable. nnt_op_embedding_bwd takes its scratch
+// Some callers cannot allocate device memory while they run: hosts that own
+// all device memory through their own allocator or a fixed budget (a library
+// allocation would bypass it or fail), and latency-critical loops where the
+// implicit device synchronisation of cudaMalloc/cudaFree is not acceptable.
+// nnt_op_embedding_bwd takes its scratch
 // (the token sort keys) from a library-owned buffer that it grows with
 // cudaMalloc; this variant instead uses a fixed array compiled into the
 // library, so it never calls cudaMalloc, cudaFree or any allocating routine.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -17,8 +18,9 @@ using namespace nnt;
 
 namespace {
 
-// Largest batch*seq the fixed scratch serves: one 32-bit sort key per token.
-constexpr int kNoAllocMaxTokens = 16384;
+// Largest batch*seq the fixed scratch serves: one 32-bit sort key per token,
+// as many tokens as one CTA of the token sort orders (64 KiB of keys).
+constexpr int kNoAllocMaxTokens = kTokenSortBlock;
 
 // The scratch itself: 64 KiB in every device's global memory for as long as
 // the library is loaded. In host code this name is only a stand-in for the
@@ -27,25 +29,31 @@ static __device__ __align__(256) uint32_t g_noalloc_sort_keys[kNoAllocMaxTokens]
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-uint32_t* g_keys_dev[kMaxDevices] = {};
+std::atomic<uint32_t*> g_keys_dev[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the first call on each device does this set-up).
+// per device (the first call on each device does this set-up). Later calls
+// read it without taking the lock.
 nnt_status keys_on_current_device(uint32_t** out) {
   int dev = 0;
   NNT_CUDA_TRY(cudaGetDevice(&dev));
   NNT_CHECK_ARG(dev >= 0 && dev < kMaxDevices, "device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lk(g_setup_mu);
-  if (!g_keys_dev[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_sort_keys);
-    if (e != cudaSuccess || !p) {
-      set_thread_error("cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
-      return NNT_ERR_CUDA;
+  uint32_t* k = g_keys_dev[dev].load(std::memory_order_acquire);
+  if (!k) {
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    k = g_keys_dev[dev].load(std::memory_order_relaxed);
+    if (!k) {
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_sort_keys);
+      if (e != cudaSuccess || !p) {
+        set_thread_error("cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+        return NNT_ERR_CUDA;
+      }
+      k = static_cast<uint32_t*>(p);
+      g_keys_dev[dev].store(k, std::memory_order_release);
     }
-    g_keys_dev[dev] = static_cast<uint32_t*>(p);
   }
-  *out = g_keys_dev[dev];
+  *out = k;
   return NNT_OK;
 }
 

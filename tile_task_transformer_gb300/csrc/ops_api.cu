@@ -217,9 +217,9 @@ nnt_status nnt_op_embedding_bwd(const uint16_t* ids_dev, int64_t ids_stride, con
                                 float* dwte_dev, float* dwpe_dev, int64_t batch, int64_t seq,
                                 int64_t d, int64_t vocab, void* stream) {
   NNT_CHECK_ARG(ids_dev && dx_dev && dwte_dev && dwpe_dev, "NULL pointer");
-  NNT_CHECK_ARG(batch > 0 && seq > 0 && batch * seq <= 16384 && d > 0 && vocab > 0 &&
+  NNT_CHECK_ARG(batch > 0 && seq > 0 && batch * seq <= kMaxTokens && d > 0 && vocab > 0 &&
                     vocab <= 65536 && ids_stride >= seq,
-                "bad size (batch*seq must be <= 16384)");
+                "bad size (batch*seq must be <= %d)", kMaxTokens);
   cudaStream_t st = (cudaStream_t)stream;
   const int T = (int)(batch * seq);
   void* keys = nullptr;
@@ -252,6 +252,11 @@ nnt_status nnt_op_gemm(const void* a_dev, int64_t lda, int32_t a_trans, const vo
   g.beta = beta != 0.f;
   if (M == 0 || N == 0) return NNT_OK;
   return gemm(g, backend, (cudaStream_t)stream);
+}
+
+nnt_status nnt_op_wait_selftest(int64_t limit_ns, int32_t arrive, void* stream) {
+  NNT_CHECK_ARG(limit_ns >= 1000 && limit_ns <= 1000000000, "limit_ns must be in [1 us, 1 s]");
+  return launch_wait_selftest((uint64_t)limit_ns, arrive != 0, (cudaStream_t)stream);
 }
 
 nnt_status nnt_op_read_error(uint32_t* code_out, void* stream) {

@@ -106,6 +106,8 @@ _SIGS = {
     "nnt_op_gemm": (C.c_int, [_P, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32, _I64, _I64, _I64, _F,
                               _F, _I32, _I32, _P]),
     "nnt_op_read_error": (C.c_int, [C.POINTER(C.c_uint32), _P]),
+    "nnt_set_fault_injection": (C.c_int, [_I32, _I64]),
+    "nnt_op_wait_selftest": (C.c_int, [_I64, _I32, _P]),
     "nnt_plan_schedule": (C.c_int, [_I32, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _I64, _P, _P, _I64]),
 }
 
@@ -348,7 +350,7 @@ def op_embedding_bwd(ids, ids_stride, dx, dwte, dwpe, batch, seq, d, vocab, stre
 
 
 def op_embedding_bwd_noalloc(ids, ids_stride, dx, dwte, dwpe, batch, seq, d, vocab, stream=None):
-    """nnt_op_embedding_bwd without any device allocation (fixed 16384-token scratch)."""
+    """nnt_op_embedding_bwd without any device allocation (fixed scratch of 16384 tokens)."""
     check(lib().nnt_op_embedding_bwd_noalloc(_ptr(ids), ids_stride, _ptr(dx), _ptr(dwte), _ptr(dwpe),
                                              batch, seq, d, vocab, _stream(stream)))
 
@@ -357,6 +359,19 @@ def op_gemm(a, lda, a_trans, b, ldb, b_trans, c, ldc, c_dtype, M, N, K, alpha=1.
             dtype=BF16, backend=0, stream=None):
     check(lib().nnt_op_gemm(_ptr(a), lda, a_trans, _ptr(b), ldb, b_trans, _ptr(c), ldc, c_dtype, M,
                             N, K, alpha, beta, dtype, backend, _stream(stream)))
+
+
+FAULT_DEVICE_ALLOC, FAULT_HOST_ALLOC, FAULT_COPY, FAULT_EVENT_WAIT = 0, 1, 2, 3
+
+
+def set_fault_injection(kind: int, nth: int):
+    """Make the nth call of ``kind`` from now on fail (host side; 0 disarms)."""
+    check(lib().nnt_set_fault_injection(kind, nth))
+
+
+def op_wait_selftest(limit_ns: int, arrive: bool, stream=None):
+    """One bounded mbarrier wait on the device (nnt_op_wait_selftest)."""
+    check(lib().nnt_op_wait_selftest(limit_ns, int(arrive), _stream(stream)))
 
 
 def read_device_error(stream=None) -> int:
