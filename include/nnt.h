@@ -100,6 +100,8 @@ typedef struct {
                                   (bf16, tensor-core GEMMs, head size 64 or 128), 1 = required
                                   (INVALID_ARG when not usable), -1 = off (materialised scores,
                                   softmax and P V as separate tasks) */
+  uint64_t host_budget_bytes;  /* pinned host bytes the model may take (offloaded AdamW moments);
+                                  0 = the host's available memory - 8 GiB */
 } nnt_options;
 
 /* AdamW hyper-parameters (README: --optimizer=fusedadamw, --optimizer-eps=1e-8,
@@ -142,10 +144,21 @@ typedef struct {
  * Errors: INVALID_ARG if n_ctx % seq_tile, n_head % head_tile,
  * batch % batch_tile or d_model % n_head is non-zero, if d_model, d_ff or the
  * head size is not a multiple of 8 (bf16: head size a multiple of 16), if vocab
- * > 65536, or if batch*n_ctx > 1048576; OOM if the tiles do not fit and offload is
- * off. *out is NULL on error. */
+ * > 65536, or if batch*n_ctx > 1048576; OOM if the allocation plan (see
+ * nnt_plan_memory) needs more device memory than is free, or more pinned host
+ * memory than host_budget_bytes -- checked before anything is allocated.
+ * *out is NULL on error. */
 nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
                             const nnt_options* opts, nnt_model** out);
+
+/* Device and pinned-host bytes nnt_create_model would allocate for this
+ * configuration, from the same allocation plan (host offload of AdamW moments
+ * included), without allocating anything. With opts->hbm_budget_bytes set no
+ * CUDA call is made; with 0 the plan starts from the current device's free
+ * memory (needs a device). Errors: as nnt_create_model's argument checks. */
+nnt_status nnt_plan_memory(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
+                           const nnt_options* opts, uint64_t* device_bytes,
+                           uint64_t* host_pinned_bytes);
 
 /* Forward pass and mean next-token cross-entropy (README --loss-reduction=mean).
  * tokens: uint16 [batch][n_ctx + 1], in host memory (tokens_on_device = 0,

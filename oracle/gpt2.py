@@ -387,11 +387,13 @@ def _forward_bf16_operands(cfg: GPT2Config, params, windows, dtype, r=None):
 
 def backward_bf16_operands(cfg: GPT2Config, params, cache, dtype=np.float64, r=None):
     """Gradients under the bfloat16 precision model: the backward of
-    :func:`backward`, with every matrix-product operand rounded by ``r``
-    (bfloat16 by default), and the gradients that the tensor-core path keeps
-    only as matrix-product operands (the logits, GELU-input and attention-score
-    gradients, the head outputs' and the fused projection's gradients) rounded
-    where they are formed. Needs the cache of ``forward(..., gemm_operands="bf16")``."""
+    :func:`backward` with every operand of every matrix product rounded by
+    ``r`` (bfloat16 by default) -- weights, activations and the gradients that
+    enter products (logits, GELU-input, attention-score, head-output and fused
+    projection gradients) -- and nothing else: the softmax backward takes the
+    unrounded probabilities (recomputed from the rounded q and k, as the
+    forward formed them) and the bias gradients sum unrounded values. Needs
+    the cache of ``forward(..., gemm_operands="bf16")``."""
     p = _cast(params, dtype)
     if r is None:
         r = lambda a: round_bf16(a).astype(dtype)  # noqa: E731
@@ -409,9 +411,10 @@ def backward_bf16_operands(cfg: GPT2Config, params, cache, dtype=np.float64, r=N
         dxa = r(dx)
         grads[q + "proj.w"] = dxa.reshape(B * S, d).T @ c["g"].reshape(B * S, -1)
         grads[q + "proj.b"] = dx.sum(axis=(0, 1))
-        du = r(gelu_backward(dxa @ r(p[q + "proj.w"]), c["u"]))
+        du_f = gelu_backward(dxa @ r(p[q + "proj.w"]), c["u"])
+        du = r(du_f)
         grads[q + "fc.w"] = du.reshape(B * S, -1).T @ c["h2"].reshape(B * S, d)
-        grads[q + "fc.b"] = du.sum(axis=(0, 1))
+        grads[q + "fc.b"] = du_f.sum(axis=(0, 1))
         dh2 = du @ r(p[q + "fc.w"])
         dln, grads[q + "ln2.g"], grads[q + "ln2.b"] = layernorm_backward(
             dh2, c["x_mid"], c["mu2"], c["r2"], p[q + "ln2.g"])
@@ -420,14 +423,15 @@ def backward_bf16_operands(cfg: GPT2Config, params, cache, dtype=np.float64, r=N
         grads[q + "o.w"] = dxa.reshape(B * S, d).T @ c["o"].reshape(B * S, d)
         grads[q + "o.b"] = dx.sum(axis=(0, 1))
         dO = split_heads(r(dxa @ r(p[q + "o.w"])), H)
-        dv = r(c["P"].transpose(0, 1, 3, 2) @ dO)
+        P = causal_softmax_forward((c["q"] @ c["k"].transpose(0, 1, 3, 2)) * scale)
+        dv = r(P).transpose(0, 1, 3, 2) @ dO
         dP = dO @ c["v"].transpose(0, 1, 3, 2)
-        dS = r(causal_softmax_backward(dP, c["P"]) * scale)
-        dq = r(dS @ c["k"])
-        dk = r(dS.transpose(0, 1, 3, 2) @ c["q"])
-        dqkv = np.concatenate([merge_heads(dq), merge_heads(dk), merge_heads(dv)], axis=-1)
+        dS = r(causal_softmax_backward(dP, P) * scale)
+        dqkv_f = np.concatenate([merge_heads(dS @ c["k"]), merge_heads(dS.transpose(0, 1, 3, 2) @ c["q"]),
+                                 merge_heads(dv)], axis=-1)
+        dqkv = r(dqkv_f)
         grads[q + "qkv.w"] = dqkv.reshape(B * S, -1).T @ c["h1"].reshape(B * S, d)
-        grads[q + "qkv.b"] = dqkv.sum(axis=(0, 1))
+        grads[q + "qkv.b"] = dqkv_f.sum(axis=(0, 1))
         dh1 = dqkv @ r(p[q + "qkv.w"])
         dln, grads[q + "ln1.g"], grads[q + "ln1.b"] = layernorm_backward(
             dh1, c["x_in"], c["mu1"], c["r1"], p[q + "ln1.g"])
@@ -568,3 +572,163 @@ def step_flops(cfg: GPT2Config) -> float:
     dense = 2.0 * T * (L * (3 * d * d + d * d + 2 * d * f) + d * V)
     attn = L * B * cfg.n_head * 2 * (2.0 * cfg.head_dim * S * (S + 1) / 2)
     return 3.0 * (dense + attn)
+
+
+# --------------------------------------------------------------------------
+# Layer-streamed bf16-operand step, for models whose parameters and gradients
+# do not fit in host memory at once (the 8-layer, 26.6B-parameter wide GPT2 of
+# the review page's "Core claim"). Same arithmetic as forward(...,
+# gemm_operands="bf16") and backward_bf16_operands in float32; only one
+# layer's parameters are held at a time, values the precision model rounds to
+# bf16 are cached as bf16 bit patterns, and attention runs one sequence at a
+# time.
+
+def bf16_bits(a):
+    """bfloat16 bit patterns (uint16) of :func:`round_bf16` of ``a``."""
+    return (round_bf16(a).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def from_bf16_bits(b):
+    """float32 values of bfloat16 bit patterns."""
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def forward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, windows):
+    """Loss and cache of the bf16-operand forward, one layer in memory at a time.
+
+    ``layer_params(l)`` returns layer l's tensors keyed without the ``h{l}.``
+    prefix (weights may already be bf16-rounded: rounding is idempotent);
+    ``head_params`` holds ``wte``, ``wpe``, ``ln_f.g``, ``ln_f.b``."""
+    r = round_bf16
+    f32 = np.float32
+    ids = windows[:, :cfg.seq].astype(np.int64)
+    tgt = windows[:, 1:cfg.seq + 1].astype(np.int64)
+    B, S, d, H = cfg.batch, cfg.seq, cfg.d_model, cfg.n_head
+    scale = 1.0 / math.sqrt(d // H)
+    wte = np.asarray(head_params["wte"], f32)
+    c = {"ids": ids, "layers": []}
+    x = embedding_forward(ids, wte, np.asarray(head_params["wpe"], f32))
+    for l in range(cfg.n_layer):
+        p = {k: np.asarray(v, f32) for k, v in layer_params(l).items()}
+        L = {"x_in": x}
+        h1, L["mu1"], L["r1"] = layernorm_forward(x, p["ln1.g"], p["ln1.b"], cfg.ln_eps)
+        h1 = r(h1)
+        L["h1"] = bf16_bits(h1)
+        qkv = linear_forward(h1, r(p["qkv.w"]), p["qkv.b"])
+        del h1
+        q = split_heads(r(qkv[..., :d]), H)
+        k = split_heads(r(qkv[..., d:2 * d]), H)
+        v = split_heads(r(qkv[..., 2 * d:]), H)
+        del qkv
+        o = np.empty((B, H, S, d // H), f32)
+        for b in range(B):
+            P = r(causal_softmax_forward((q[b:b + 1] @ k[b:b + 1].transpose(0, 1, 3, 2)) * scale))
+            o[b:b + 1] = P @ v[b:b + 1]
+            del P
+        L["q"], L["k"], L["v"] = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+        del q, k, v
+        o = r(merge_heads(o))
+        L["o"] = bf16_bits(o)
+        x = x + linear_forward(o, r(p["o.w"]), p["o.b"])
+        del o
+        L["x_mid"] = x
+        h2, L["mu2"], L["r2"] = layernorm_forward(x, p["ln2.g"], p["ln2.b"], cfg.ln_eps)
+        h2 = r(h2)
+        L["h2"] = bf16_bits(h2)
+        L["u"] = linear_forward(h2, r(p["fc.w"]), p["fc.b"])
+        del h2
+        g = r(gelu_forward(L["u"]))
+        L["g"] = bf16_bits(g)
+        x = x + linear_forward(g, r(p["proj.w"]), p["proj.b"])
+        del g, p
+        c["layers"].append(L)
+    c["x_L"] = x
+    y, c["muf"], c["rf"] = layernorm_forward(x, np.asarray(head_params["ln_f.g"], f32),
+                                              np.asarray(head_params["ln_f.b"], f32), cfg.ln_eps)
+    y = r(y)
+    c["y"] = bf16_bits(y)
+    z = linear_forward(y.reshape(B * S, d), r(wte))
+    loss, dz = cross_entropy_forward_backward(z, tgt.reshape(-1))
+    c["z"] = z
+    c["dz"] = dz
+    return loss, c
+
+
+def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, want=None):
+    """Gradients of the bf16-operand step (as :func:`backward_bf16_operands`),
+    one layer in memory at a time, from the cache of
+    :func:`forward_bf16_streamed`.
+
+    ``want``: layer indices whose parameter gradients are returned (default:
+    all). Other layers skip their weight- and bias-gradient sums, which feed
+    nothing else; the gradients of wte, wpe and ln_f are always returned."""
+    r = round_bf16
+    f32 = np.float32
+    B, S, d, H = cfg.batch, cfg.seq, cfg.d_model, cfg.n_head
+    T = B * S
+    scale = 1.0 / math.sqrt(d // H)
+    grads = {}
+    wte = np.asarray(head_params["wte"], f32)
+    dz = r(cache["dz"])
+    dwte = dz.T @ from_bf16_bits(cache["y"]).reshape(T, d)
+    dy = (dz @ r(wte)).reshape(B, S, d)
+    del dz
+    dx, grads["ln_f.g"], grads["ln_f.b"] = layernorm_backward(
+        dy, cache["x_L"], cache["muf"], cache["rf"], np.asarray(head_params["ln_f.g"], f32))
+    del dy
+    for l in reversed(range(cfg.n_layer)):
+        q = f"h{l}."
+        c = cache["layers"][l]
+        p = {k: np.asarray(v, f32) for k, v in layer_params(l).items()}
+        keep = want is None or l in want
+        dxa = r(dx)
+        if keep:
+            grads[q + "proj.w"] = dxa.reshape(T, d).T @ from_bf16_bits(c["g"]).reshape(T, -1)
+            grads[q + "proj.b"] = dx.sum(axis=(0, 1))
+        du_f = gelu_backward(dxa @ r(p["proj.w"]), c["u"])
+        du = r(du_f)
+        if keep:
+            grads[q + "fc.w"] = du.reshape(T, -1).T @ from_bf16_bits(c["h2"]).reshape(T, d)
+            grads[q + "fc.b"] = du_f.sum(axis=(0, 1))
+        del du_f
+        dh2 = du @ r(p["fc.w"])
+        del du
+        dln, g2, b2 = layernorm_backward(dh2, c["x_mid"], c["mu2"], c["r2"], p["ln2.g"])
+        del dh2
+        if keep:
+            grads[q + "ln2.g"], grads[q + "ln2.b"] = g2, b2
+        dx = dx + dln
+        dxa = r(dx)
+        if keep:
+            grads[q + "o.w"] = dxa.reshape(T, d).T @ from_bf16_bits(c["o"]).reshape(T, d)
+            grads[q + "o.b"] = dx.sum(axis=(0, 1))
+        dO = split_heads(r(dxa @ r(p["o.w"])), H)
+        del dxa
+        qh, kh, vh = from_bf16_bits(c["q"]), from_bf16_bits(c["k"]), from_bf16_bits(c["v"])
+        dqkv_f = np.empty((B, S, 3 * d), f32)
+        for b in range(B):
+            sl = slice(b, b + 1)
+            P = causal_softmax_forward((qh[sl] @ kh[sl].transpose(0, 1, 3, 2)) * scale)
+            dv = r(P).transpose(0, 1, 3, 2) @ dO[sl]
+            dS = r(causal_softmax_backward(dO[sl] @ vh[sl].transpose(0, 1, 3, 2), P) * scale)
+            del P
+            dqkv_f[sl] = np.concatenate([merge_heads(dS @ kh[sl]),
+                                         merge_heads(dS.transpose(0, 1, 3, 2) @ qh[sl]),
+                                         merge_heads(dv)], axis=-1)
+            del dS, dv
+        del dO, qh, kh, vh
+        dqkv = r(dqkv_f)
+        if keep:
+            grads[q + "qkv.w"] = dqkv.reshape(T, -1).T @ from_bf16_bits(c["h1"]).reshape(T, d)
+            grads[q + "qkv.b"] = dqkv_f.sum(axis=(0, 1))
+        del dqkv_f
+        dh1 = dqkv @ r(p["qkv.w"])
+        del dqkv
+        dln, g1, b1 = layernorm_backward(dh1, c["x_in"], c["mu1"], c["r1"], p["ln1.g"])
+        del dh1, p
+        if keep:
+            grads[q + "ln1.g"], grads[q + "ln1.b"] = g1, b1
+        dx = dx + dln
+    grads["wte"], grads["wpe"] = embedding_backward(
+        dx, cache["ids"], dwte, np.zeros_like(np.asarray(head_params["wpe"], f32)))
+    return grads

@@ -88,7 +88,11 @@ def check_step(cfg, got, seed=0, tol=2e-2, lr=3e-4):
         if sel.any():
             dw_ref = (new_p[n] - params[n])[sel]
             dw = (w_gpu - params[n])[sel]
-            assert relerr(dw, dw_ref) < tol, n
+            # the stored fp32 weight carries half an ulp (2^-24 |w|) of rounding,
+            # which the change inherits: for LayerNorm gains near 1 that is ~2e-4
+            # of the ~3e-4 step
+            ulp = 2.0 ** -24 * np.abs(new_p[n][sel]).max()
+            assert np.abs(dw - dw_ref).max() <= tol * np.abs(dw_ref).max() + ulp, n
 
 
 def test_tiny_fp32_step_matches_oracle():

@@ -1,0 +1,127 @@
+"""Wide-8 parity: the 8-layer, d_model 16384, 26.6B-parameter GPT2 step with
+host offload against the layer-streamed oracle (GPU).
+
+The configuration of the review page's "Core claim" (an 8-layer GPT2 with a
+wide embedding) at 128 heads, d_ff 65536, 4 windows of 1024 tokens. The GPU
+runs the fused backward + AdamW with the AdamW moments partly in pinned host
+memory; gradients of the layer matrices then only pass through a ring of
+device slots, so the first moment m = (1 - beta1) g of AdamW's first step
+stands in for them. The four windows are two distinct sequences, each twice
+(s0, s1, s0, s1): the loss, gradients and update equal those of the two
+sequences alone, which the oracle computes one layer at a time, with weights
+regenerated from the same seeded generator the device initialiser
+implements (it never reads a GPU value).
+
+Checked against the oracle's bf16-operand precision model (bf16 operands of
+every matrix product, fp32 everything else): the loss within 1e-3; the logits
+of both sequences, and the gradients of ln_f, wte, wpe and of every tensor of
+the first and the last block within 2e-2 normwise.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import gpt2 as O  # noqa: E402
+from tile_task_transformer_gb300 import nnt, synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+WIDE8 = O.GPT2Config(n_layer=8, d_model=16384, n_head=128, d_ff=65536, vocab=50257, seq=1024, batch=4)
+TILES = {"seq_tile": 1024, "embd_tile": 2048, "inner_tile": 4096, "head_tile": 16}
+SEED = 3
+TOL = 2e-2
+GIB = 1 << 30
+
+
+def _host_available():
+    with open("/proc/meminfo") as fh:
+        for line in fh:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
+def relerr(a, r):
+    r = np.asarray(r, np.float64)
+    return float(np.abs(np.asarray(a, np.float64) - r).max() / max(np.abs(r).max(), 1e-30))
+
+
+def test_wide8_offloaded_step_matches_streamed_oracle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cfg = WIDE8
+    L, d, f, V, S = cfg.n_layer, cfg.d_model, cfg.d_ff, cfg.vocab, cfg.seq
+    # host memory, computed before anything is allocated: the GPU phase holds
+    # the offloaded moments (at most 8 B per parameter beyond what the device
+    # keeps) plus the moments read back; the oracle phase holds bf16 copies of
+    # every layer matrix (24 d^2 B per layer), ~2.9 GB of cached activations per
+    # layer, the logits and their gradient (2 x 4 T V B) and its transients.
+    n_layer_mat = 12 * d * d
+    read_back = (2 * n_layer_mat + V * d + S * d) * 4
+    gpu_phase = 8 * (L * n_layer_mat) // 2 + read_back
+    oracle_phase = L * n_layer_mat * 2 + L * 2.9e9 + 2 * 4 * 2 * S * V + 20 * GIB + read_back
+    need = int(max(gpu_phase, oracle_phase) * 1.1)
+    have = _host_available()
+    if have < need:
+        pytest.skip(f"needs ~{need / GIB:.0f} GiB of host memory, {have / GIB:.0f} GiB available")
+
+    seqs = np.concatenate([synth.token_windows(SEED, 1, S, V), synth.token_windows(SEED + 1, 1, S, V)])
+    win = np.ascontiguousarray(np.tile(seqs, (cfg.batch // 2, 1)))
+    m = nnt.Model(L, d, cfg.n_head, f, V, S, cfg.batch, dtype=nnt.BF16, tiles=TILES, use_cuda_graph=True,
+                  n_streams=2, seed=SEED, init_std=0.02, allow_host_offload=True)
+    assert m.stats().offload_active
+    loss = m.forward(win)
+    logits = m.logits()[: 2 * S]  # windows 0 and 1: rows b * S + s
+    m.backward_adamw()
+    keep = ("h0.", f"h{L - 1}.")
+    mom = {n: m.get_adam_state(i, 0) for i, n in enumerate(m.names)
+           if n.startswith(keep) or n in ("wte", "wpe", "ln_f.g", "ln_f.b")}
+    m.close()
+    one_minus_b1 = 1.0 - float(np.float32(0.9))  # the fp32 beta1 the update used
+    grads = {n: v.astype(np.float64) / one_minus_b1 for n, v in mom.items()}
+    del mom
+
+    # oracle: parameters regenerated from the seeded generator, the layer
+    # matrices kept as bf16 bit patterns (the precision model multiplies with
+    # their bf16 rounding; rounding twice changes nothing)
+    names = synth.param_names_shapes(L, d, f, V, S)
+    index = {n: (i, sh) for i, (n, sh) in enumerate(names)}
+
+    def gen(n):
+        i, sh = index[n]
+        return synth.gpt2_tensor(SEED, i, n, sh)
+
+    head = {n: gen(n) for n in ("wte", "wpe", "ln_f.g", "ln_f.b")}
+    layers = []
+    for l in range(L):
+        t = {}
+        for k in ("ln1.g", "ln1.b", "qkv.w", "qkv.b", "o.w", "o.b", "ln2.g", "ln2.b", "fc.w", "fc.b",
+                  "proj.w", "proj.b"):
+            a = gen(f"h{l}.{k}")
+            t[k] = O.bf16_bits(a) if k.endswith(".w") else a
+            del a
+        layers.append(t)
+
+    def layer_params(l):
+        return {k: (O.from_bf16_bits(v) if k.endswith(".w") else v) for k, v in layers[l].items()}
+
+    two = O.GPT2Config(n_layer=L, d_model=d, n_head=cfg.n_head, d_ff=f, vocab=V, seq=S, batch=2)
+    bloss, cache = O.forward_bf16_streamed(two, layer_params, head, seqs)
+    assert abs(loss - bloss) < 1e-3, (loss, bloss)
+    e_logits = relerr(logits, cache["z"])
+    assert e_logits < TOL, e_logits
+    rgrads = O.backward_bf16_streamed(two, layer_params, head, cache, want={0, L - 1})
+    del cache, layers
+    worst = {}
+    for n, g in grads.items():
+        worst[n] = relerr(g, rgrads[n])
+    print(f"loss: gpu {loss:.6f} oracle {bloss:.6f}; logits {e_logits:.4f}")
+    for n, e in worst.items():
+        print(f"{n}: {e:.4f}")
+    bad = {n: e for n, e in worst.items() if not e < TOL}
+    assert not bad, bad
+    assert math.isfinite(loss)

@@ -415,6 +415,35 @@ def test_bf16_precision_model_reduces_to_exact_step_with_identity_rounding():
         assert np.abs(gb[k] - g0[k]).max() <= 3e-2 * np.abs(g0[k]).max() + 1e-12, k
 
 
+def test_streamed_bf16_step_matches_whole_model():
+    """The layer-streamed bf16-operand step (one layer's parameters at a time,
+    bf16 values cached as bit patterns, attention one sequence at a time) gives
+    the whole-model precision model's loss, logits and gradients."""
+    cfg = O.GPT2Config(n_layer=3, d_model=32, n_head=2, d_ff=64, vocab=37, seq=12, batch=3)
+    p = {k: v.astype(np.float32) for k, v in _rand_params(cfg, 46).items()}
+    win = _windows(cfg, 47)
+    head = {k: p[k] for k in ("wte", "wpe", "ln_f.g", "ln_f.b")}
+    layer = lambda l: {k[len(f"h{l}."):]: v for k, v in p.items() if k.startswith(f"h{l}.")}  # noqa: E731
+    l0, c0 = O.forward(cfg, p, win, dtype=np.float32, gemm_operands="bf16")
+    g0 = O.backward_bf16_operands(cfg, p, c0, dtype=np.float32)
+    l1, c1 = O.forward_bf16_streamed(cfg, layer, head, win)
+    assert abs(l1 - l0) < 1e-6
+    np.testing.assert_allclose(c1["z"], c0["z"], rtol=1e-5, atol=1e-6)
+    g1 = O.backward_bf16_streamed(cfg, layer, head, c1)
+    assert set(g1) == set(g0)
+    for k in g0:
+        scale = np.abs(g0[k]).max()
+        assert np.abs(g1[k] - g0[k]).max() <= 1e-4 * scale + 1e-9, k
+    # only the requested layers' parameter gradients (plus wte, wpe, ln_f)
+    g2 = O.backward_bf16_streamed(cfg, layer, head, c1, want={0, 2})
+    assert set(g2) == {k for k in g0 if not k.startswith("h1.")}
+    for k in g2:
+        np.testing.assert_array_equal(g2[k], g1[k])
+    # bf16 bit patterns round-trip
+    x = np.random.default_rng(0).standard_normal(1000).astype(np.float32)
+    np.testing.assert_array_equal(O.from_bf16_bits(O.bf16_bits(x)), O.round_bf16(x))
+
+
 # ------------------------------------- gradient accumulation and lr warm-up
 
 def test_warmup_schedule_end_points_from_readme():

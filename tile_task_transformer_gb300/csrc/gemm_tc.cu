@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "ptx_math.cuh"
 #include "tc_ptx.cuh"
 
 namespace nnt {
@@ -78,7 +79,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes: one swizzle row
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each on half of the tile's columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int BN>
 struct Cfg {
@@ -88,8 +90,9 @@ struct Cfg {
   static constexpr int STAGES = BN >= 192 ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = BN == 192 ? 512 : 2 * BN;  // two accumulators, power of two
   static constexpr int BAR_BYTES = 256;
-  // per epilogue warp: a 32x32 output chunk (4 KB) and a 32x32 fp32 GELU input chunk (4 KB)
-  static constexpr int STAGING_BYTES = 4 * 8192;
+  // per epilogue warp: one 4 KB buffer -- a 32x32 fp32 output chunk, or a
+  // 32x32 bf16 output chunk plus its 32x32 bf16 GELU input chunk
+  static constexpr int STAGING_BYTES = kEpiWarps * 4096;
   static constexpr int SMEM = STAGES * STAGE + STAGING_BYTES + BAR_BYTES + 1024;
 };
 
@@ -137,22 +140,22 @@ __device__ __forceinline__ TileCoord tile_at(const GemmArgs& g, const TileSpace&
   return c;
 }
 
-// tanh-form GELU and its derivative with the hardware tanh approximation
-// (relative error about 2^-11, below the bf16 rounding of the values these
-// epilogues produce; the CUDA-core path keeps the library tanhf).
-__device__ __forceinline__ float tanh_fast(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// tanh-form GELU and its derivative through the logistic function:
+// (1 + tanh(x)) / 2 = 1 / (1 + e^(-2x)), so with x = c (u + a u^3) and
+// s = 1 / (1 + 2^(-2x log2 e)):  gelu(u) = u s,  gelu'(u) = s + 2 u s (1 - s) x'
+// (x' = c (1 + 3 a u^2)). Nothing cancels in the negative tail (where 1 + tanh
+// would), and the error is that of ex2.approx (2^-22 relative) and one fast
+// division: fp32-accurate.
+__device__ __forceinline__ float gelu_sig_fast(float u) {
+  const float c2l = 2.0f * 0.7978845608028654f * 1.4426950408889634f, a = 0.044715f;
+  // the exponent is capped at 64 (s ~ 5e-20 there) so the division stays in its normal range
+  return __fdividef(1.0f, 1.0f + ex2f(fminf(-c2l * (u + a * u * u * u), 64.0f)));
 }
-__device__ __forceinline__ float gelu_fwd_fast(float u) {
-  const float c = 0.7978845608028654f, a = 0.044715f;
-  return 0.5f * u * (1.0f + tanh_fast(c * (u + a * u * u * u)));
-}
+__device__ __forceinline__ float gelu_fwd_fast(float u) { return u * gelu_sig_fast(u); }
 __device__ __forceinline__ float gelu_grad_fast(float u) {
   const float c = 0.7978845608028654f, a = 0.044715f;
-  const float t = tanh_fast(c * (u + a * u * u * u));
-  return 0.5f * (1.0f + t) + 0.5f * u * (1.0f - t * t) * c * (1.0f + 3.0f * a * u * u);
+  const float s = gelu_sig_fast(u);
+  return s + 2.0f * u * s * (1.0f - s) * c * (1.0f + 3.0f * a * u * u);
 }
 
 // Elementwise epilogue of one 32-column chunk of row m held in registers
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * kEpiWarps);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -383,24 +386,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+    // ---------------- epilogue: warps 2..9; warp w drains TMEM lane quarter
+    // w % 4 (the quarter a warp may access) and half (w - 2) / 4 of the tile's
+    // 32-column chunks
     const int q = warp & 3;
-    // Staging: 8 KB per warp, two 4 KB halves ping-ponged so that two
-    // bulk-store groups can be in flight; a GELU epilogue with bf16 output and
-    // bf16 u puts both 2 KB chunks in one half. With an fp32 u the whole 8 KB
-    // serves one chunk (one group in flight).
-    uint8_t* stage_base = smem + C::STAGES * C::STAGE + (warp - 2) * 8192;
+    const int nch = BN / 64;  // chunks per warp
+    const int ch0 = ((warp - 2) >> 2) * nch;
+    // Staging: one 4 KB buffer per warp (an fp32 chunk, or a bf16 chunk and
+    // its bf16 GELU-input chunk), reused once the previous bulk store has
+    // read it; the other warps' work covers that wait. A GELU epilogue with
+    // an fp32 output or fp32 u stores directly.
+    uint8_t* stage_base = smem + C::STAGES * C::STAGE + (warp - 2) * 4096;
     const bool cbf = g.c_dtype == NNT_BF16;
     const bool gelu = g.epi == EPI_GELU;
     const bool ubf = g.aux_dtype == NNT_BF16;
-    const bool single = gelu && !(cbf && ubf);
+    const bool gelu_direct = gelu && !(cbf && ubf);
     // residual (EPI_STORE) or GELU input (EPI_GELU_BWD): each chunk's 32x32
     // block is read coalesced one chunk ahead and turned into one row per lane
     // through the chunk's (free) output staging buffer
     const void* src = g.epi == EPI_GELU_BWD ? g.aux : (g.epi == EPI_STORE ? g.resid : nullptr);
     const bool src_bf = g.epi == EPI_GELU_BWD && ubf;
     const int64_t ld_src = g.epi == EPI_GELU_BWD ? g.ld_aux : g.ld_resid;
-    int buf = 0;
     int issued = 0;  // bulk store groups of this warp so far
     int acc = 0;
     uint32_t aph = 0;
@@ -440,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return whole;
       };
-      bool have = prefetch(c.n_box);
+      bool have = prefetch(c.n_box + ch0 * 32);
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int ch = ch0; ch < ch0 + nch; ++ch) {
         const int nb = c.n_box + ch * 32;
         if (nb >= c.n_end) break;  // uniform across the warp
         float v[32], u[32], pre[32];
@@ -452,16 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool tma;
         if (ts.c_mode == 1) tma = row0 >= c.m_start && nb >= c.n_start;
         else tma = ts.c_mode > 1 && rows_full && cols_full;
-        if (tma && g.epi == EPI_GELU && !ts.aux_tma) tma = false;
-        uint8_t* stage_c = stage_base + (single ? 0 : buf * 4096);
-        uint8_t* stage_u = single ? stage_base + 4096 : stage_c + 2048;
+        if (tma && gelu && (!ts.aux_tma || gelu_direct)) tma = false;
+        uint8_t* stage_c = stage_base;
+        uint8_t* stage_u = stage_base + 2048;
         const bool have_cur = have;
-        if ((tma || have_cur) && issued >= (single ? 1 : 2)) {
-          // the group that last used this buffer must have finished reading it
-          if (lane == 0) {
-            if (single) bulk_wait_read();
-            else bulk_wait_read1();
-          }
+        if ((tma || have_cur) && issued >= 1) {
+          // the group that last used the buffer must have finished reading it
+          if (lane == 0) bulk_wait_read();
           __syncwarp();
         }
         if (have_cur) {
@@ -498,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        have = ch + 1 < BN / 32 && prefetch(nb + 32);  // next chunk's block, in flight meanwhile
+        have = ch + 1 < ch0 + nch && prefetch(nb + 32);  // next chunk's block, in flight meanwhile
         epi_chunk(g, c.i, m, row_ok, nb, c.n_start, c.n_end, cols_full, v, u, have_cur ? pre : nullptr);
         if (!tma) {
           if (row_ok) {
@@ -540,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit();
         }
         ++issued;
-        buf ^= 1;
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);

@@ -14,6 +14,7 @@
 // that declare the tiles they read and write; the executor derives the
 // dependency graph and the stream schedule once, at creation.
 #include <math.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -105,6 +106,9 @@ struct nnt_model {
   // memory
   std::vector<void*> dev_allocs;
   uint64_t device_bytes = 0, host_bytes = 0;
+  // dry run: plan the allocations (count bytes, allocate nothing)
+  bool dry = false;
+  uint64_t free_device = 0;  // free device memory the plan assumes
 
   // parameters (flat fp32 buffers + bf16 copy, same offsets)
   std::vector<ParamInfo> params;
@@ -118,7 +122,8 @@ struct nnt_model {
   uint16_t* tokens_dev = nullptr;
   std::vector<float*> x, xmid, mu1, r1, mu2, r2;
   std::vector<void*> h1, qkvh, P, O, h2, g;
-  std::vector<void*> u;  // FC pre-activation (GELU input), activation dtype
+  std::vector<void*> u;  // FC pre-activation (GELU input), u_dtype
+  int u_dtype = NNT_BF16;
   float* scores = nullptr;  // [B*H][S][S] fp32, reused by every layer (fwd scores, bwd dP)
   // fused attention (flash): per-layer row log-sum-exp [B*H][S] and the
   // backward's D = rowsum(dO * O) scratch [B*H][S]; no P or scores buffers
@@ -206,6 +211,11 @@ template <typename Ptr>
 nnt_status dalloc(nnt_model* m, Ptr*& p, size_t bytes) {
   void* q = nullptr;
   if (bytes == 0) bytes = 16;
+  if (m->dry) {
+    m->device_bytes += bytes;
+    p = nullptr;
+    return NNT_OK;
+  }
   if (fault_hit(FAULT_DEVICE_ALLOC)) {
     set_thread_error("cudaMalloc of %zu bytes failed (injected); %llu bytes already held", bytes,
                      (unsigned long long)m->device_bytes);
@@ -364,9 +374,11 @@ nnt_status alloc_param_state(nnt_model* m, uint64_t budget) {
     NNT_TRY(dalloc(m, m->grad, pf));
     NNT_TRY(dalloc(m, m->mom1, pf));
     NNT_TRY(dalloc(m, m->mom2, pf));
-    NNT_CUDA_TRY(cudaMemset(m->grad, 0, pf));
-    NNT_CUDA_TRY(cudaMemset(m->mom1, 0, pf));
-    NNT_CUDA_TRY(cudaMemset(m->mom2, 0, pf));
+    if (!m->dry) {
+      NNT_CUDA_TRY(cudaMemset(m->grad, 0, pf));
+      NNT_CUDA_TRY(cudaMemset(m->mom1, 0, pf));
+      NNT_CUDA_TRY(cudaMemset(m->mom2, 0, pf));
+    }
     m->n_grad = m->n_dev_mv = m->n_flat;
     for (ParamInfo& p : m->params) p.goff = p.off;
     for (Chunk& c : m->chunks) {
@@ -394,7 +406,7 @@ nnt_status alloc_param_state(nnt_model* m, uint64_t budget) {
   }
   m->n_grad = n_grad;
   NNT_TRY(dalloc(m, m->grad, (size_t)std::max<int64_t>(n_grad, 64) * 4));
-  NNT_CUDA_TRY(cudaMemset(m->grad, 0, (size_t)n_grad * 4));
+  if (!m->dry) NNT_CUDA_TRY(cudaMemset(m->grad, 0, (size_t)n_grad * 4));
   m->n_ring = max_ring ? 4 : 0;
   m->ring_elems = round_up(max_ring, 64);
   if (m->n_ring) NNT_TRY(dalloc(m, m->ring, (size_t)m->n_ring * m->ring_elems * 4));
@@ -427,6 +439,10 @@ nnt_status alloc_param_state(nnt_model* m, uint64_t budget) {
   m->n_host_mv = host_mv;
   NNT_TRY(dalloc(m, m->mom1, (size_t)std::max<int64_t>(dev_mv, 64) * 4));
   NNT_TRY(dalloc(m, m->mom2, (size_t)std::max<int64_t>(dev_mv, 64) * 4));
+  if (m->dry) {
+    m->host_bytes += (uint64_t)host_mv * 8;
+    return NNT_OK;
+  }
   NNT_CUDA_TRY(cudaMemset(m->mom1, 0, (size_t)dev_mv * 4));
   NNT_CUDA_TRY(cudaMemset(m->mom2, 0, (size_t)dev_mv * 4));
   if (host_mv) {
@@ -491,14 +507,16 @@ nnt_status alloc_all(nnt_model* m) {
   }
   add_param("ln_f.g", d, 0, 2);
   add_param("ln_f.b", d, 0, 3);
-  size_t free_b = 0, total_b = 0;
-  NNT_CUDA_TRY(cudaMemGetInfo(&free_b, &total_b));
+  size_t free_b = m->free_device, total_b = 0;
+  if (!m->dry) NNT_CUDA_TRY(cudaMemGetInfo(&free_b, &total_b));
   const size_t pf = (size_t)m->n_flat * 4;
   NNT_TRY(dalloc(m, m->master, pf));
   NNT_TRY(dalloc(m, m->wbf, (size_t)m->n_flat * 2));
   NNT_TRY(dalloc(m, m->hyper_dev, sizeof(AdamHyperDev)));
-  NNT_CUDA_TRY(cudaMemset(m->master, 0, pf));
-  NNT_CUDA_TRY(cudaMemset(m->wbf, 0, (size_t)m->n_flat * 2));
+  if (!m->dry) {
+    NNT_CUDA_TRY(cudaMemset(m->master, 0, pf));
+    NNT_CUDA_TRY(cudaMemset(m->wbf, 0, (size_t)m->n_flat * 2));
+  }
 
   NNT_TRY(dalloc(m, m->tokens_dev, (size_t)B * (S + 1) * 2));
   m->x.resize(L + 1);
@@ -531,7 +549,7 @@ nnt_status alloc_all(nnt_model* m) {
       NNT_TRY(dalloc(m, m->P[l], (size_t)B * H * S * S * as));
     NNT_TRY(dalloc(m, m->O[l], Td * as));
     NNT_TRY(dalloc(m, m->h2[l], Td * as));
-    NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * as));
+    NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * (m->u_dtype == NNT_F32 ? 4 : 2)));
     NNT_TRY(dalloc(m, m->g[l], (size_t)T * f * as));
   }
   if (m->flash) {
@@ -563,6 +581,13 @@ nnt_status alloc_all(nnt_model* m) {
     NNT_TRY(dalloc(m, m->splitk_ws, (size_t)m->splitk_elems * 4));
   }
   NNT_TRY(dalloc(m, m->sort_keys, (size_t)T * 4));
+  const uint64_t budget = m->opts.hbm_budget_bytes
+                              ? m->opts.hbm_budget_bytes
+                              : (free_b > (2ull << 30) ? free_b - (2ull << 30) : 0);
+  if (m->dry) {
+    m->host_bytes += 64;
+    return alloc_param_state(m, budget);
+  }
   // padding columns of the logits must stay finite: zero them once
   NNT_CUDA_TRY(cudaMemset(m->z, 0, (size_t)T * m->ldz * 4));
   NNT_CUDA_TRY(cudaMemset(m->dz, 0, (size_t)T * m->lddz * as));
@@ -575,9 +600,6 @@ nnt_status alloc_all(nnt_model* m) {
   m->loss_host = (float*)lh;
   m->host_bytes += 64;
   // gradients and AdamW moments last, once everything else is placed
-  const uint64_t budget = m->opts.hbm_budget_bytes
-                              ? m->opts.hbm_budget_bytes
-                              : (free_b > (2ull << 30) ? free_b - (2ull << 30) : 0);
   return alloc_param_state(m, budget);
 }
 
@@ -861,7 +883,7 @@ void build_forward(nnt_model* m) {
         g.B = pw(m, P_(m, l, FCW)); g.ldb = d;
         g.C = m->g[l]; g.ldc = f; g.c_dtype = act;
         g.bias = pm(m, P_(m, l, FCB));
-        g.epi = EPI_GELU; g.aux = m->u[l]; g.ld_aux = f; g.aux_dtype = act;
+        g.epi = EPI_GELU; g.aux = m->u[l]; g.ld_aux = f; g.aux_dtype = m->u_dtype;
         std::vector<TileUse> u;
         box(u, m->gh2[l], ACC_R, rt, rt + 1);
         box(u, m->gu[l], ACC_W, rt, rt + 1, t0, t1);
@@ -1185,7 +1207,7 @@ void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
         GemmArgs proto = b.base();
         proto.epi = EPI_GELU_BWD;
         proto.aux = m->u[l];
-        proto.aux_dtype = act;
+        proto.aux_dtype = m->u_dtype;
         proto.ld_aux = f;
         std::vector<TileUse> u;
         box(u, m->gdres_act, ACC_R, rt, rt + 1);
@@ -1596,23 +1618,9 @@ nnt_status run_backward(nnt_model* m, bool acc, const char* who) {
   return NNT_OK;
 }
 
-}  // namespace
-
-// ====================================================================== C ABI
-
-extern "C" {
-
-nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
-                            const nnt_options* opts, nnt_model** out) {
-  if (!out) {
-    set_thread_error("out is NULL");
-    t_model_err = thread_error();
-    return NNT_ERR_INVALID_ARG;
-  }
-  *out = nullptr;
-  nnt_status s = validate(cfg, tiles);
-  if (s != NNT_OK) return fail(nullptr, s);
-  nnt_model* m = new nnt_model();
+// Model fields that follow from the config, tile sizes and options.
+nnt_status setup_fields(nnt_model* m, const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
+                        const nnt_options* opts) {
   m->cfg = *cfg;
   nnt_tiles zt{};
   m->tiles = tiles ? *tiles : zt;
@@ -1620,6 +1628,8 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
   m->opts = opts ? *opts : zo;
   m->act = cfg->dtype;
   m->act_size = m->act == NNT_BF16 ? 2 : 4;
+  m->u_dtype = m->act;
+  if (getenv("NNT_U_F32")) m->u_dtype = NNT_F32;
   m->L = cfg->n_layer; m->d = cfg->d_model; m->H = cfg->n_head; m->hd = m->d / m->H;
   m->f = cfg->d_ff; m->V = cfg->vocab; m->S = cfg->n_ctx; m->B = cfg->batch; m->T = m->B * m->S;
   m->tb = m->tiles.batch_tile ? m->tiles.batch_tile : m->B;
@@ -1643,10 +1653,92 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
     if (m->opts.flash_attention > 0 && !usable) {
       set_thread_error("flash attention needs bf16, tensor-core GEMMs and head size 64 or 128 "
                        "(head size %d)", m->hd);
-      delete m;
-      return fail(nullptr, NNT_ERR_INVALID_ARG);
+      return NNT_ERR_INVALID_ARG;
     }
     m->flash = m->opts.flash_attention >= 0 && usable;
+  }
+
+  return NNT_OK;
+}
+
+uint64_t host_mem_available() {
+  FILE* fh = fopen("/proc/meminfo", "r");
+  if (!fh) return 0;
+  char line[256];
+  unsigned long long kb = 0;
+  while (fgets(line, sizeof line, fh))
+    if (sscanf(line, "MemAvailable: %llu kB", &kb) == 1) break;
+  fclose(fh);
+  return (uint64_t)kb * 1024;
+}
+
+// Device and pinned-host bytes of the model's allocations, from a dry run of
+// the allocation plan; free_device is the free device memory the default
+// device budget is taken from.
+nnt_status plan_bytes(const nnt_gpt2_config* cfg, const nnt_tiles* tiles, const nnt_options* opts,
+                      uint64_t free_device, uint64_t* dev, uint64_t* host) {
+  nnt_model tmp;
+  NNT_TRY(setup_fields(&tmp, cfg, tiles, opts));
+  tmp.dry = true;
+  tmp.free_device = free_device;
+  NNT_TRY(alloc_all(&tmp));
+  *dev = tmp.device_bytes;
+  *host = tmp.host_bytes;
+  return NNT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+
+nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
+                            const nnt_options* opts, nnt_model** out) {
+  if (!out) {
+    set_thread_error("out is NULL");
+    t_model_err = thread_error();
+    return NNT_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  nnt_status s = validate(cfg, tiles);
+  if (s != NNT_OK) return fail(nullptr, s);
+  nnt_model* m = new nnt_model();
+  s = setup_fields(m, cfg, tiles, opts);
+  if (s != NNT_OK) {
+    delete m;
+    return fail(nullptr, s);
+  }
+  {
+    // the whole allocation plan must fit before anything is allocated
+    size_t free_b = 0, total_b = 0;
+    cudaError_t e = cudaMemGetInfo(&free_b, &total_b);
+    if (e != cudaSuccess) {
+      set_thread_error("cudaMemGetInfo: %s", cudaGetErrorString(e));
+      delete m;
+      return fail(nullptr, NNT_ERR_CUDA);
+    }
+    uint64_t dev = 0, host = 0;
+    s = plan_bytes(cfg, tiles, opts, free_b, &dev, &host);
+    if (s != NNT_OK) {
+      delete m;
+      return fail(nullptr, s);
+    }
+    const uint64_t avail = host_mem_available();
+    const uint64_t host_budget = m->opts.host_budget_bytes
+                                     ? m->opts.host_budget_bytes
+                                     : (avail > (8ull << 30) ? avail - (8ull << 30) : avail);
+    if (dev > free_b) {
+      set_thread_error("the model needs %.2f GiB of device memory, %.2f GiB are free", dev / 1073741824.0,
+                       free_b / 1073741824.0);
+      delete m;
+      return fail(nullptr, NNT_ERR_OOM);
+    }
+    if (host > 64 && host_budget && host > host_budget) {
+      set_thread_error("the model needs %.2f GiB of pinned host memory, the budget is %.2f GiB",
+                       host / 1073741824.0, host_budget / 1073741824.0);
+      delete m;
+      return fail(nullptr, NNT_ERR_OOM);
+    }
   }
 
   cudaStream_t main = (cudaStream_t)m->opts.stream;
@@ -1689,6 +1781,28 @@ nnt_status nnt_create_model(const nnt_gpt2_config* cfg, const nnt_tiles* tiles,
   return NNT_OK;
 }
 
+nnt_status nnt_plan_memory(const nnt_gpt2_config* cfg, const nnt_tiles* tiles, const nnt_options* opts,
+                           uint64_t* device_bytes, uint64_t* host_pinned_bytes) {
+  if (!device_bytes || !host_pinned_bytes) {
+    set_thread_error("NULL output");
+    return fail(nullptr, NNT_ERR_INVALID_ARG);
+  }
+  nnt_status s = validate(cfg, tiles);
+  if (s != NNT_OK) return fail(nullptr, s);
+  size_t free_b = 0, total_b = 0;
+  if (!(opts && opts->hbm_budget_bytes)) {
+    cudaError_t e = cudaMemGetInfo(&free_b, &total_b);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_thread_error("cudaMemGetInfo: %s (set hbm_budget_bytes to plan without a device)",
+                       cudaGetErrorString(e));
+      return fail(nullptr, NNT_ERR_CUDA);
+    }
+  }
+  s = plan_bytes(cfg, tiles, opts, free_b, device_bytes, host_pinned_bytes);
+  return s == NNT_OK ? s : fail(nullptr, s);
+}
+
 nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_device,
                        float* loss_out) {
   if (!m || !tokens) {
@@ -1707,6 +1821,7 @@ nnt_status nnt_forward(nnt_model* m, const uint16_t* tokens, int32_t tokens_on_d
   m->state = 1;
   if (loss_out || m->opts.trace) {
     s = copy_async(m->loss_host, m->loss_dev, 4, cudaMemcpyDeviceToHost, st, "loss read-back");
+    if (s == NNT_OK) s = sync_model(m);  // bounded wait for the step and the copy
     if (s != NNT_OK) {
       m->state = 0;
       return fail(m, s);

@@ -46,7 +46,8 @@ class Options(C.Structure):
                 ("init_std", C.c_float), ("init_zero_bias", C.c_int32), ("n_streams", C.c_int32),
                 ("use_cuda_graph", C.c_int32), ("timeout_ms", C.c_uint32),
                 ("gemm_backend", C.c_int32), ("trace", C.c_int32),
-                ("gemm_min_task_cols", C.c_int32), ("flash_attention", C.c_int32)]
+                ("gemm_min_task_cols", C.c_int32), ("flash_attention", C.c_int32),
+                ("host_budget_bytes", C.c_uint64)]
 
 
 class AdamW(C.Structure):
@@ -72,6 +73,8 @@ _I32 = C.c_int32
 _F = C.c_float
 _SIGS = {
     "nnt_create_model": (C.c_int, [C.POINTER(Config), C.POINTER(Tiles), C.POINTER(Options), C.POINTER(_P)]),
+    "nnt_plan_memory": (C.c_int, [C.POINTER(Config), C.POINTER(Tiles), C.POINTER(Options),
+                                  C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]),
     "nnt_forward": (C.c_int, [_P, _P, _I32, C.POINTER(_F)]),
     "nnt_backward": (C.c_int, [_P]),
     "nnt_backward_accumulate": (C.c_int, [_P]),
@@ -171,14 +174,15 @@ class Model:
                  ln_eps=1e-5, tiles=None, seed=0, init_std=0.0, zero_bias=False, stream=None,
                  n_streams=2, use_cuda_graph=False, timeout_ms=0, gemm_backend=0, trace=False,
                  allow_host_offload=False, hbm_budget_bytes=0, gemm_min_task_cols=0,
-                 flash_attention=0):
+                 flash_attention=0, host_budget_bytes=0):
         self.cfg = Config(n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype, ln_eps)
         t = tiles or {}
         self.tiles = Tiles(t.get("batch_tile", 0), t.get("seq_tile", 0), t.get("embd_tile", 0),
                            t.get("inner_tile", 0), t.get("head_tile", 0), t.get("vocab_tile", 0))
         self.opts = Options(_stream(stream), hbm_budget_bytes, int(allow_host_offload), seed,
                             init_std, int(zero_bias), n_streams, int(use_cuda_graph), timeout_ms,
-                            gemm_backend, int(trace), gemm_min_task_cols, flash_attention)
+                            gemm_backend, int(trace), gemm_min_task_cols, flash_attention,
+                            host_budget_bytes)
         h = C.c_void_p()
         check(lib().nnt_create_model(C.byref(self.cfg), C.byref(self.tiles), C.byref(self.opts),
                                      C.byref(h)))
@@ -359,6 +363,22 @@ def op_gemm(a, lda, a_trans, b, ldb, b_trans, c, ldc, c_dtype, M, N, K, alpha=1.
             dtype=BF16, backend=0, stream=None):
     check(lib().nnt_op_gemm(_ptr(a), lda, a_trans, _ptr(b), ldb, b_trans, _ptr(c), ldc, c_dtype, M,
                             N, K, alpha, beta, dtype, backend, _stream(stream)))
+
+
+def plan_memory(n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype=BF16, ln_eps=1e-5,
+                tiles=None, allow_host_offload=False, hbm_budget_bytes=0, flash_attention=0):
+    """(device bytes, pinned host bytes) nnt_create_model would allocate (nnt_plan_memory)."""
+    cfg = Config(n_layer, d_model, n_head, d_ff, vocab, n_ctx, batch, dtype, ln_eps)
+    t = tiles or {}
+    tl = Tiles(t.get("batch_tile", 0), t.get("seq_tile", 0), t.get("embd_tile", 0),
+               t.get("inner_tile", 0), t.get("head_tile", 0), t.get("vocab_tile", 0))
+    opts = Options()
+    opts.allow_host_offload = int(allow_host_offload)
+    opts.hbm_budget_bytes = hbm_budget_bytes
+    opts.flash_attention = flash_attention
+    dev, host = C.c_uint64(0), C.c_uint64(0)
+    check(lib().nnt_plan_memory(C.byref(cfg), C.byref(tl), C.byref(opts), C.byref(dev), C.byref(host)))
+    return dev.value, host.value
 
 
 FAULT_DEVICE_ALLOC, FAULT_HOST_ALLOC, FAULT_COPY, FAULT_EVENT_WAIT = 0, 1, 2, 3

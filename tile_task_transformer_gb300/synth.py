@@ -121,25 +121,31 @@ def param_names_shapes(n_layer: int, d_model: int, d_ff: int, vocab: int, n_ctx:
     return out
 
 
+def gpt2_tensor(seed: int, index: int, name: str, shape, std: float = 0.02,
+                zero_bias: bool = False) -> np.ndarray:
+    """Parameter tensor ``index`` (named ``name``) of :func:`param_names_shapes`:
+    LayerNorm gains 1 and shifts 0, other tensors N(0, std) from stream ``index``
+    (biases 0 with ``zero_bias``)."""
+    n = int(np.prod(shape))
+    if name.endswith(".g") and ("ln" in name):
+        a = np.ones(n, dtype=np.float32)
+    elif name.endswith(".b") and ("ln" in name):
+        a = np.zeros(n, dtype=np.float32)
+    elif zero_bias and name.endswith(".b"):
+        a = np.zeros(n, dtype=np.float32)
+    else:
+        a = normal_f32(seed, index, n, std)
+    return a.reshape(shape)
+
+
 def gpt2_params(seed: int, n_layer: int, d_model: int, d_ff: int, vocab: int, n_ctx: int,
                 std: float = 0.02, zero_bias: bool = False) -> dict:
     """Seeded fp32 GPT2 parameters: N(0, std) weights and biases, LayerNorm g=1, b=0.
 
     Tensor ``i`` of :func:`param_names_shapes` draws from stream ``i``.
     """
-    params = {}
-    for i, (name, shape) in enumerate(param_names_shapes(n_layer, d_model, d_ff, vocab, n_ctx)):
-        n = int(np.prod(shape))
-        if name.endswith(".g") and ("ln" in name):
-            a = np.ones(n, dtype=np.float32)
-        elif name.endswith(".b") and ("ln" in name):
-            a = np.zeros(n, dtype=np.float32)
-        elif zero_bias and name.endswith(".b"):
-            a = np.zeros(n, dtype=np.float32)
-        else:
-            a = normal_f32(seed, i, n, std)
-        params[name] = a.reshape(shape)
-    return params
+    return {name: gpt2_tensor(seed, i, name, shape, std, zero_bias)
+            for i, (name, shape) in enumerate(param_names_shapes(n_layer, d_model, d_ff, vocab, n_ctx))}
 
 
 def normal_matrix(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
