@@ -370,6 +370,95 @@ def run_gpu(args):
 
 
 # --------------------------------------------------------------------------
+# capacity sweep: the largest wide GPT2 that completes a step on one GPU
+# --------------------------------------------------------------------------
+
+# (layers, d_model) at the 8-layer, 26.6B-parameter wide-8 scale and deeper;
+# d_ff = 4 d, 128-wide heads, 4 x 1024 tokens, tiles as wide-8
+CAPACITY_POINTS = ((8, 16384), (9, 16384), (12, 14336), (16, 12288), (11, 15360), (13, 14336),
+                   (10, 16384))
+
+
+def host_available():
+    with open("/proc/meminfo") as fh:
+        for line in fh:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
+def run_capacity(args):
+    """Each point's device and pinned-host footprint comes from the library's
+    allocation plan first; only points inside both budgets are created and
+    stepped (forward + backward with the fused AdamW). Also measures the
+    pinned cudaMemcpyAsync peaks of the host link."""
+    import numpy as np
+    import torch
+
+    from tile_task_transformer_gb300 import nnt, synth
+
+    gib = 1 << 30
+    # host link: pinned copies of 1 GiB, best of 5, CUDA events
+    h = torch.empty(1 << 28, dtype=torch.float32, pin_memory=True)
+    dbuf = torch.empty(1 << 28, dtype=torch.float32, device="cuda")
+    link = {}
+    for name, (dst, src) in (("h2d_gbs", (dbuf, h)), ("d2h_gbs", (h, dbuf))):
+        best = 1e9
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dst.copy_(src, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        link[name] = h.numel() * 4 / (best / 1e3) / 1e9
+    del h, dbuf
+    torch.cuda.empty_cache()
+    print(json.dumps({"capacity": "host_link", "pinned_copy_1gib": link}), flush=True)
+    points = CAPACITY_POINTS
+    if args.capacity_points:
+        points = [tuple(int(v) for v in p.split("x")) for p in args.capacity_points.split(",")]
+    for L, d in points:
+        H, f, V, S, B = d // 128, 4 * d, 50257, 1024, 4
+        ht = 16 if H % 16 == 0 else 8
+        tiles = {"seq_tile": 1024, "embd_tile": 2048, "inner_tile": 4096, "head_tile": ht}
+        n = sum(int(np.prod(sh)) for _, sh in synth.param_names_shapes(L, d, f, V, S))
+        free, _ = torch.cuda.mem_get_info()
+        dev_budget = free - 2 * gib
+        host_budget = max(host_available() - 16 * gib, 0)
+        dev, host = nnt.plan_memory(L, d, H, f, V, S, B, tiles=tiles, allow_host_offload=True,
+                                    hbm_budget_bytes=dev_budget)
+        line = {"capacity": f"L{L} d{d} H{H} ff{f} V{V} S{S} B{B}", "params": n,
+                "plan_device_gib": dev / gib, "plan_host_gib": host / gib,
+                "device_budget_gib": dev_budget / gib, "host_budget_gib": host_budget / gib,
+                "admitted": bool(dev <= dev_budget and host <= host_budget)}
+        if line["admitted"]:
+            t0 = time.perf_counter()
+            m = nnt.Model(L, d, H, f, V, S, B, dtype=nnt.BF16, tiles=tiles, seed=3, use_cuda_graph=True,
+                          n_streams=2, allow_host_offload=True, hbm_budget_bytes=dev_budget,
+                          host_budget_bytes=host_budget)
+            line["create_s"] = time.perf_counter() - t0
+            win = synth.token_windows(3, B, S, V)
+            stream = torch.cuda.current_stream()
+            times, losses = [], []
+            for _ in range(2):  # the first step also captures the graphs
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                losses.append(m.forward(win))
+                m.backward_adamw()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) / 1e3)
+            st = m.stats()
+            line.update(completed=bool(np.isfinite(losses).all()), loss=losses, step_s=times[-1],
+                        tokens_per_s=B * S / times[-1], device_gib=st["device_bytes"] / gib,
+                        pinned_gib=st["host_pinned_bytes"] / gib)
+            m.close()
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
 # tile-kernel sweep: the step's tile kernels alone on synthetic tiles
 # --------------------------------------------------------------------------
 
@@ -539,6 +628,9 @@ def main():
     ap.add_argument("--fused", action="store_true", help="backward with AdamW fused in")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="tile-kernel sweep instead of the step")
+    ap.add_argument("--capacity", action="store_true",
+                    help="largest wide GPT2 that completes a step (plan first, then create and step)")
+    ap.add_argument("--capacity-points", default="", help="comma list of LAYERSxD_MODEL")
     ap.add_argument("--sweep-kernel", default="", help="comma list (default: all)")
     ap.add_argument("--sweep-dtype", default="", choices=["", "f32", "bf16"])
     ap.add_argument("--sweep-rows", default="")
@@ -551,6 +643,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.capacity:
+        return run_capacity(args)
     return run_gpu(args)
 
 

@@ -257,9 +257,9 @@ def test_adamw():
     # w_new = w - lr wd w - lr mhat / (sqrt(vhat) + eps): the terms can cancel
     upd_terms = hp.lr * (hp.weight_decay * np.abs(w64) + np.abs(rm / bc1) / (np.sqrt(rv / bc2) + hp.eps))
     close32(n(W), rw, terms=np.abs(w64) + upd_terms)
-    # the update w_new - w itself to 1e-4 of its terms; w_new's own fp32
-    # rounding (2^-24 |w_new|) is part of the difference
-    close32(n(W) - w64, rw - w64, rtol=1e-4, terms=upd_terms + 2.0 ** -24 * np.abs(rw) / 1e-4)
+    # the update w_new - w itself to 1e-4 of its terms; the fp32 roundings of
+    # w - lr wd w and of w_new (half an ulp each) are part of the difference
+    close32(n(W) - w64, rw - w64, rtol=1e-4, terms=upd_terms + 2.0 ** -23 * (np.abs(w64) + np.abs(rw)) / 1e-4)
     assert torch.equal(Wb, W.to(torch.bfloat16))
 
 

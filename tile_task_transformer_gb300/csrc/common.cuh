@@ -70,6 +70,34 @@ const char* thread_error();
     }                                             \
   } while (0)
 
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch: the library's kernels are launched with
+// launch_pdl, which lets a kernel start (and run its prologue) while the
+// previous kernel on its stream finishes. Each kernel calls pdl_wait() before
+// its first access to global memory -- griddepcontrol.wait returns once the
+// preceding grids have completed and their writes are visible -- and then
+// pdl_trigger(), after which the next kernel may launch. NNT_PDL=0 in the
+// environment launches without the attribute (the waits are then no-ops).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- types
 typedef __nv_bfloat16 bf16;
 

@@ -2,6 +2,8 @@
 // makes its Nth call from now fail as the real failure would (the allocation
 // returns OOM, the copy submission or the wait returns its error), without
 // touching the GPU. Off by default; nothing on the device is ever faulted.
+#include <stdlib.h>
+
 #include <atomic>
 
 #include "common.cuh"
@@ -18,6 +20,14 @@ bool fault_hit(FaultKind kind) {
     if (c.compare_exchange_weak(v, v - 1, std::memory_order_relaxed)) return v == 1;
   }
   return false;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("NNT_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 }  // namespace nnt

@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the prologue above overlaps the previous kernel
+  pdl_trigger();
   const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_v = smem_u32(sm + C::OFF_V), s_p = smem_u32(sm + C::OFF_P);
   constexpr int HC = FB / 2;  // score columns per thread
@@ -375,6 +377,8 @@ __device__ __forceinline__ float dot8_bf16(uint4 x, uint4 y) {
 // D[z][s] = sum_j dO[z][s][j] * O(z, s, j). CTA: 32 rows of item blockIdx.y;
 // eight lanes per row, 16 bytes of dO and of O each per step.
 __global__ void __launch_bounds__(256) flash_bwd_d_kernel(const bf16* __restrict__ dO, const FlashArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int item = blockIdx.y;
   const int s = blockIdx.x * 32 + warp * 4 + (lane >> 3);
@@ -453,6 +457,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the prologue above overlaps the previous kernel
+  pdl_trigger();
   const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t s_k = smem_u32(sm + C::OFF_K), s_v = smem_u32(sm + C::OFF_V);
   const uint32_t s_pt = smem_u32(sm + C::OFF_PT), s_ds = smem_u32(sm + C::OFF_DS);
@@ -690,6 +696,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the prologue above overlaps the previous kernel
+  pdl_trigger();
   const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_do = smem_u32(sm + C::OFF_DO);
   const uint32_t s_ds = smem_u32(sm + C::OFF_DS);
@@ -875,7 +883,7 @@ nnt_status fwd_hd(const bf16* q, const bf16* k, const bf16* v, const FlashArgs& 
   NNT_CHECK_ARG(err != nullptr, "device error word unavailable");
   const int nqb = (int)ceil_div(a.S, FB);
   const float c2 = (float)(1.4426950408889634 / sqrt((double)HD));
-  kern<<<(unsigned)(nqb * a.nz), kThreads, FwdCfg<HD>::SMEM, st>>>(mq, mk, mv, a, nqb, c2, err);
+  launch_pdl(kern, (unsigned)(nqb * a.nz), kThreads, FwdCfg<HD>::SMEM, st, mq, mk, mv, a, nqb, c2, err);
   return launch_check("flash_fwd");
 }
 
@@ -896,16 +904,16 @@ nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, c
   const int nqb = (int)ceil_div(a.S, FB);
   const double scale = 1.0 / sqrt((double)HD);
   const float c2 = (float)(1.4426950408889634 * scale);
-  flash_bwd_d_kernel<<<dim3((unsigned)ceil_div(a.S, 32), (unsigned)a.nz), 256, 0, st>>>(dO, a);
+  launch_pdl(flash_bwd_d_kernel, dim3((unsigned)ceil_div(a.S, 32), (unsigned)a.nz), 256, 0, st, dO, a);
   NNT_TRY(launch_check("flash_bwd_d"));
   const bool via_gemm = a.ds && a.S % 8 == 0;
   CUtensorMap mds = mq;  // unused unless via_gemm
   if (via_gemm) NNT_TRY(make_map(&mds, a.ds, a.S, a.S, a.S, (int64_t)a.S * a.S, a.z_total, 64, FB));
-  kv<<<(unsigned)(nqb * a.nz), kBwdThreads, KvCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a,
+  launch_pdl(kv, (unsigned)(nqb * a.nz), kBwdThreads, KvCfg<HD>::SMEM, st, mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a,
                                                                    nqb, c2, (float)scale, err);
   NNT_TRY(launch_check("flash_bwd_kv"));
   if (!via_gemm) {
-    qk<<<(unsigned)(nqb * a.nz), kBwdThreads, QCfg<HD>::SMEM, st>>>(mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
+    launch_pdl(qk, (unsigned)(nqb * a.nz), kBwdThreads, QCfg<HD>::SMEM, st, mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
     return launch_check("flash_bwd_q");
   }
   // dQ[q] = sum_{k <= q} dS[q][k] K[k]: A = dS^T read MN-major, causal key range per query tile

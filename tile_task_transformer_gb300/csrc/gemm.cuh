@@ -10,8 +10,8 @@ namespace nnt {
 
 enum EpiKind : int {
   EPI_STORE = 0,     // C = alpha*acc (+ bias[n]) (+ resid[m, n]) (+ C if beta)
-  EPI_GELU = 1,      // u = alpha*acc + bias[n] -> aux (aux_dtype); C = gelu(u)
-  EPI_GELU_BWD = 2,  // C = alpha*acc * gelu'(aux[m, n])
+  EPI_GELU = 1,      // u = alpha*acc + bias[n]; C = gelu(u), aux = gelu'(u) (aux_dtype)
+  EPI_GELU_BWD = 2,  // C = alpha*acc * aux[m, n] (aux = gelu'(u) from the EPI_GELU launch)
 };
 
 enum OutMode : int {
@@ -59,7 +59,7 @@ struct GemmArgs {
   const float* bias = nullptr;
   const float* resid = nullptr;
   int64_t ld_resid = 0;
-  void* aux = nullptr;  // GELU input u: written by EPI_GELU, read by EPI_GELU_BWD
+  void* aux = nullptr;  // GELU derivative gelu'(u): written by EPI_GELU, read by EPI_GELU_BWD
   int64_t ld_aux = 0;
   int aux_dtype = NNT_F32;  // NNT_F32 or NNT_BF16
   int causal = CAUSAL_NONE;
@@ -114,10 +114,10 @@ __device__ __forceinline__ void epilogue_one(const GemmArgs& g, int i, int m, in
     if (g.beta) v += static_cast<const float*>(g.C)[o];
   } else if (g.epi == EPI_GELU) {
     if (g.bias) v += g.bias[n];
-    aux_store(g, (int64_t)m * g.ld_aux + n, v);
+    aux_store(g, (int64_t)m * g.ld_aux + n, gelu_grad_dev(v));
     v = gelu_fwd_dev(v);
   } else {  // EPI_GELU_BWD
-    v *= gelu_grad_dev(aux_load(g, (int64_t)m * g.ld_aux + n));
+    v *= aux_load(g, (int64_t)m * g.ld_aux + n);
   }
   if (g.c_dtype == NNT_BF16)
     static_cast<bf16*>(g.C)[o] = __float2bfloat16_rn(v);

@@ -14,6 +14,8 @@ __device__ __forceinline__ float ld_op(const T* p, int64_t i) { return to_f(p[i]
 
 template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   // tiles sit on absolute multiples of BM/BN (so no tile straddles a causal block)
@@ -83,9 +85,9 @@ nnt_status gemm_simt(const GemmArgs& g, cudaStream_t st) {
             (unsigned)((g.m0 + g.mt - 1) / BM - g.m0 / BM + 1), (unsigned)g.nbatch);
   NNT_CHECK_ARG(grid.y < 65536 && grid.z < 65536, "gemm: grid too large");
   if (g.op_dtype == NNT_BF16)
-    gemm_simt_kernel<bf16><<<grid, 256, 0, st>>>(g);
+    launch_pdl(gemm_simt_kernel<bf16>, grid, 256, 0, st, g);
   else
-    gemm_simt_kernel<float><<<grid, 256, 0, st>>>(g);
+    launch_pdl(gemm_simt_kernel<float>, grid, 256, 0, st, g);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_thread_error("gemm_simt launch: %s", cudaGetErrorString(e));

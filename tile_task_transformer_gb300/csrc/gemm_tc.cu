@@ -151,17 +151,15 @@ __device__ __forceinline__ float gelu_sig_fast(float u) {
   // the exponent is capped at 64 (s ~ 5e-20 there) so the division stays in its normal range
   return __fdividef(1.0f, 1.0f + ex2f(fminf(-c2l * (u + a * u * u * u), 64.0f)));
 }
-__device__ __forceinline__ float gelu_fwd_fast(float u) { return u * gelu_sig_fast(u); }
-__device__ __forceinline__ float gelu_grad_fast(float u) {
+__device__ __forceinline__ float gelu_grad_from_sig(float u, float s) {
   const float c = 0.7978845608028654f, a = 0.044715f;
-  const float s = gelu_sig_fast(u);
   return s + 2.0f * u * s * (1.0f - s) * c * (1.0f + 3.0f * a * u * u);
 }
 
 // Elementwise epilogue of one 32-column chunk of row m held in registers
 // (columns nb..nb+31; `full`: all of them inside the window). Bias loads are
 // the same address across the warp (broadcast). `pre` holds this row's 32
-// residual (EPI_STORE) or GELU-input (EPI_GELU_BWD) values when the chunk lies
+// residual (EPI_STORE) or GELU-derivative (EPI_GELU_BWD) values when the chunk lies
 // wholly inside the window (loaded coalesced and transposed through shared
 // memory by the caller); otherwise they are read here element by element.
 __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool row_ok, int nb,
@@ -202,18 +200,19 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int i, int m, bool 
   } else if (g.epi == EPI_GELU) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      u_out[j] = v[j];
-      v[j] = gelu_fwd_fast(v[j]);
+      const float s = gelu_sig_fast(v[j]);
+      u_out[j] = gelu_grad_from_sig(v[j], s);  // aux: gelu'(u) for the backward
+      v[j] *= s;
     }
-  } else if (row_ok) {  // EPI_GELU_BWD
+  } else if (row_ok) {  // EPI_GELU_BWD: times the stored gelu'(u)
     if (pre) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_fast(pre[j]);
+      for (int j = 0; j < 32; ++j) v[j] *= pre[j];
     } else {
       const int64_t ub = (int64_t)m * g.ld_aux;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= gelu_grad_fast(aux_load(g, ub + nb + j));
+        if (nb + j >= n_lo && nb + j < n_hi) v[j] *= aux_load(g, ub + nb + j);
     }
   }
 }
@@ -282,6 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above (barriers, TMEM, descriptor prefetch) overlaps the
+  // previous kernel; from here on global memory is read and written
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool gelu = g.epi == EPI_GELU;
     const bool ubf = g.aux_dtype == NNT_BF16;
     const bool gelu_direct = gelu && !(cbf && ubf);
-    // residual (EPI_STORE) or GELU input (EPI_GELU_BWD): each chunk's 32x32
+    // residual (EPI_STORE) or GELU derivative (EPI_GELU_BWD): each chunk's 32x32
     // block is read coalesced one chunk ahead and turned into one row per lane
     // through the chunk's (free) output staging buffer
     const void* src = g.epi == EPI_GELU_BWD ? g.aux : (g.epi == EPI_STORE ? g.resid : nullptr);
@@ -413,17 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < ts.total && !*abort_flag; t += gridDim.x) {
       const TileCoord c = tile_at<BN>(g, ts, t);
       if (!c.needed) continue;
-      if (!mbar_wait(&tfull[acc], aph, g.wait_ns)) {
-        atomicOr(err, DEVERR_WAIT_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
       const int row0 = c.m_box + q * 32;
       const int m = row0 + lane;
       const bool row_ok = m >= c.m_start && m < c.m_end;
       const bool rows_full = row0 >= c.m_start && row0 + 32 <= c.m_end;
-      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       // fp32: lane reads rows 4*rr + lane/8 of the block, 16 bytes at column
       // 4*(lane%8); bf16: rows 8*rr + lane/4, 16 bytes at column 8*(lane%4)
       uint4 pf[8];
@@ -446,7 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return whole;
       };
+      // the first chunk's residual / GELU-derivative block does not depend on
+      // the accumulator: its loads are in flight while the MMAs finish
       bool have = prefetch(c.n_box + ch0 * 32);
+      if (!mbar_wait(&tfull[acc], aph, g.wait_ns)) {
+        atomicOr(err, DEVERR_WAIT_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int ch = ch0; ch < ch0 + nch; ++ch) {
         const int nb = c.n_box + ch * 32;
@@ -692,7 +697,7 @@ nnt_status launch_tc(const GemmArgs& g, cudaStream_t st) {
     set_thread_error("device error word unavailable");
     return NNT_ERR_CUDA;
   }
-  gemm_tc_kernel<BN, A_MN, B_MN><<<grid, kThreads, C::SMEM, st>>>(ma, mb, mc, mu, g, ts, err);
+  launch_pdl(gemm_tc_kernel<BN, A_MN, B_MN>, grid, kThreads, C::SMEM, st, ma, mb, mc, mu, g, ts, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_thread_error("gemm_tc launch: %s", cudaGetErrorString(e));
@@ -779,6 +784,8 @@ nnt_status gemm_tc_one(const GemmArgs& g, cudaStream_t st) {
 // ws[s][m - m0][n - n0], for the window rows m and columns n.
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int split, int64_t mt, int nt,
                                      float* C, int64_t ldc, int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n4 = (int64_t)mt * (nt / 4);
   const int64_t win = (int64_t)mt * nt;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
@@ -820,7 +827,7 @@ nnt_status gemm_tc_split(const GemmArgs& g, int split, cudaStream_t st) {
   float* out = static_cast<float*>(g.C) + (int64_t)(g.m0 - g.c_row0) * g.ldc + g.n0;
   const int64_t n4 = (int64_t)g.mt * (g.nt / 4);
   const int grid = (int)std::min<int64_t>((n4 + 255) / 256, 4 * num_sms());
-  splitk_reduce_kernel<<<grid, 256, 0, st>>>(g.ws, split, g.mt, g.nt, out, g.ldc, g.beta);
+  launch_pdl(splitk_reduce_kernel, grid, 256, 0, st, g.ws, split, g.mt, g.nt, out, g.ldc, g.beta);
   return launch_check("splitk_reduce");
 }
 
@@ -836,6 +843,8 @@ nnt_status gemm_tc(const GemmArgs& g, cudaStream_t st) {
 
 namespace {
 __global__ void wait_selftest_kernel(uint64_t limit_ns, int arrive, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x != 0) return;
   mbar_init(&bar, 1);
@@ -851,7 +860,7 @@ nnt_status launch_wait_selftest(uint64_t limit_ns, bool arrive, cudaStream_t st)
     set_thread_error("device error word unavailable");
     return NNT_ERR_CUDA;
   }
-  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, arrive ? 1 : 0, err);
+  launch_pdl(wait_selftest_kernel, 1, 32, 0, st, limit_ns, arrive ? 1 : 0, err);
   return launch_check("wait_selftest");
 }
 

@@ -59,6 +59,8 @@ __global__ void embedding_fwd_kernel(const uint16_t* __restrict__ ids, int64_t i
                                      const float* __restrict__ wte, const float* __restrict__ wpe,
                                      float* __restrict__ x, int d, int vocab, TokMap tm, int b0,
                                      int nb, int s0, int ns) {
+  pdl_wait();
+  pdl_trigger();
   const int nv = d >> 2;
   const int64_t total = (int64_t)nb * ns * nv;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -87,7 +89,7 @@ nnt_status launch_embedding_fwd(const uint16_t* ids, int64_t ids_stride, const f
   int64_t total = (int64_t)nb * ns * (d / 4);
   if (total == 0) return NNT_OK;
   int grid = (int)std::min<int64_t>(ceil_div(total, 256), 152 * 16);
-  embedding_fwd_kernel<<<grid, 256, 0, st>>>(ids, ids_stride, wte, wpe, x, d, vocab, tm, b0, nb, s0,
+  launch_pdl(embedding_fwd_kernel, grid, 256, 0, st, ids, ids_stride, wte, wpe, x, d, vocab, tm, b0, nb, s0,
                                              ns);
   return launch_check("embedding_fwd");
 }
@@ -100,6 +102,8 @@ nnt_status launch_embedding_fwd(const uint16_t* ids, int64_t ids_stride, const f
 // the blocks themselves are in token order.
 __global__ void token_sort_kernel(const uint16_t* __restrict__ ids, int64_t ids_stride, int B,
                                   int S, uint32_t* __restrict__ keys_out, int Bs, int npow2) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t sk[];
   const int T = B * S;
   const int t0 = blockIdx.x * Bs;
@@ -147,7 +151,7 @@ nnt_status launch_token_sort(const uint16_t* ids, int64_t ids_stride, int B, int
   if (smem > 48 * 1024)
     NNT_CUDA_TRY(cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
-  token_sort_kernel<<<(T + Bs - 1) / Bs, 1024, smem, st>>>(ids, ids_stride, B, S, keys_out, Bs, npow2);
+  launch_pdl(token_sort_kernel, (T + Bs - 1) / Bs, 1024, smem, st, ids, ids_stride, B, S, keys_out, Bs, npow2);
   return launch_check("token_sort");
 }
 
@@ -171,6 +175,8 @@ constexpr int kScatterMaxBlocks = kMaxTokens / kTokenSortBlock;
 __global__ void embedding_scatter_kernel(const uint32_t* __restrict__ keys, int T, int Bs,
                                          const float* __restrict__ dx, TokMap tm, int S,
                                          float* __restrict__ dwte, int d, int vocab) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int run_lo[kScatterMaxBlocks], run_hi[kScatterMaxBlocks];
   __shared__ int in_earlier;
   const int p = blockIdx.x;
@@ -216,13 +222,15 @@ nnt_status launch_embedding_scatter(const uint32_t* keys, int T, const float* dx
   NNT_CHECK_ARG(T >= 0 && T <= kMaxTokens, "embedding scatter: too many tokens (%d)", T);
   if (T == 0) return NNT_OK;
   int threads = std::min(256, std::max(32, (d / 4 + 31) / 32 * 32));
-  embedding_scatter_kernel<<<T, threads, 0, st>>>(keys, T, token_sort_block(T), dx, tm, S, dwte, d,
+  launch_pdl(embedding_scatter_kernel, T, threads, 0, st, keys, T, token_sort_block(T), dx, tm, S, dwte, d,
                                                   vocab);
   return launch_check("embedding_scatter");
 }
 
 __global__ void wpe_grad_kernel(const float* __restrict__ dx, TokMap tm, int B, int s0, int ns,
                                 int d, float* __restrict__ dwpe, int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   const int nv = d >> 2;
   const int64_t total = (int64_t)ns * nv;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -245,7 +253,7 @@ nnt_status launch_wpe_grad(const float* dx, TokMap tm, int B, int s0, int ns, in
   int64_t total = (int64_t)ns * (d / 4);
   if (total == 0) return NNT_OK;
   int grid = (int)std::min<int64_t>(ceil_div(total, 256), 152 * 8);
-  wpe_grad_kernel<<<grid, 256, 0, st>>>(dx, tm, B, s0, ns, d, dwpe, accumulate);
+  launch_pdl(wpe_grad_kernel, grid, 256, 0, st, dx, tm, B, s0, ns, d, dwpe, accumulate);
   return launch_check("wpe_grad");
 }
 
@@ -259,6 +267,8 @@ __global__ void ln_fwd_kernel(const float* __restrict__ x, const float* __restri
                               const float* __restrict__ b, T* __restrict__ y,
                               float* __restrict__ mean, float* __restrict__ rstd, int64_t rows,
                               int cols, float eps) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   const int rpc = blockDim.x / TPR;
   const int lane = threadIdx.x % TPR;
@@ -359,9 +369,9 @@ nnt_status launch_layernorm_fwd(const float* x, const float* g, const float* b, 
   const int mv = row_maxv(cols, tpr);
   NNT_TPR_DISPATCH(tpr, NNT_MAXV_DISPATCH(mv, {
     if (act_dtype == NNT_BF16)
-      ln_fwd_kernel<TPR, MV, bf16><<<grid, block, 0, st>>>(x, g, b, (bf16*)y, mean, rstd, rows, cols, eps);
+      launch_pdl(ln_fwd_kernel<TPR, MV, bf16>, grid, block, 0, st, x, g, b, (bf16*)y, mean, rstd, rows, cols, eps);
     else
-      ln_fwd_kernel<TPR, MV, float><<<grid, block, 0, st>>>(x, g, b, (float*)y, mean, rstd, rows, cols, eps);
+      launch_pdl(ln_fwd_kernel<TPR, MV, float>, grid, block, 0, st, x, g, b, (float*)y, mean, rstd, rows, cols, eps);
   }));
   return launch_check("layernorm_fwd");
 }
@@ -373,6 +383,8 @@ __global__ void ln_bwd_kernel(const float* __restrict__ dy, const float* __restr
                               const float* __restrict__ mean, const float* __restrict__ rstd,
                               const float* __restrict__ g, const float* resid, float* dx,
                               T* __restrict__ dx_act, int64_t rows, int cols) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   const int rpc = blockDim.x / TPR;
   const int lane = threadIdx.x % TPR;
@@ -438,9 +450,9 @@ nnt_status launch_layernorm_bwd(const float* dy, const float* x, const float* me
   const int mv = row_maxv(cols, tpr);
   NNT_TPR_DISPATCH(tpr, NNT_MAXV_DISPATCH(mv, {
     if (act_dtype == NNT_BF16)
-      ln_bwd_kernel<TPR, MV, bf16><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols);
+      launch_pdl(ln_bwd_kernel<TPR, MV, bf16>, grid, block, 0, st, dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols);
     else
-      ln_bwd_kernel<TPR, MV, float><<<grid, block, 0, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols);
+      launch_pdl(ln_bwd_kernel<TPR, MV, float>, grid, block, 0, st, dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols);
   }));
   return launch_check("layernorm_bwd");
 }
@@ -460,6 +472,8 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_fused_kernel(
     const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ mean,
     const float* __restrict__ rstd, const float* __restrict__ g, const float* resid, float* dx,
     T* __restrict__ dx_act, int64_t rows, int cols, float* __restrict__ part, int want_out) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int G = 8 / RW;  // row groups per CTA
   extern __shared__ float red[];  // [G][3][cols]
   __shared__ float xch[2][8][2];  // pair exchange: [parity][warp][s1, s2]
@@ -589,14 +603,14 @@ nnt_status launch_ln_bwd_fused(const float* dy, const float* x, const float* mea
       static const cudaError_t attr =                                                            \
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 / RWV * 3 * 1024 * 4); \
       NNT_CUDA_TRY(attr);                                                                        \
-      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols, part, \
+      launch_pdl(k, grid, 256, smem, st, dy, x, mean, rstd, g, resid, dx, (bf16*)dx_act, rows, cols, part, \
                                  want_out);                                                      \
     } else {                                                                                     \
       auto k = ln_bwd_fused_kernel<RWV, MV, float>;                                             \
       static const cudaError_t attr =                                                            \
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 / RWV * 3 * 1024 * 4); \
       NNT_CUDA_TRY(attr);                                                                        \
-      k<<<grid, 256, smem, st>>>(dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols,      \
+      launch_pdl(k, grid, 256, smem, st, dy, x, mean, rstd, g, resid, dx, (float*)dx_act, rows, cols,      \
                                  part, want_out);                                                \
     }                                                                                            \
   })
@@ -620,6 +634,8 @@ __global__ void ln_bwd_colsums_kernel(const float* __restrict__ dy, const float*
                                       const float* __restrict__ rstd, const float* __restrict__ out,
                                       int64_t rows, int cols, int64_t rows_per_chunk,
                                       float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float4 red[3][8][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = (blockIdx.x * 32 + lane) * 4;
@@ -668,7 +684,7 @@ nnt_status launch_ln_bwd_colsums(const float* dy, const float* x, const float* m
   const int64_t nch = ln_colsum_chunks(rows);
   const int64_t rpc = ceil_div(rows, nch);
   dim3 grid((unsigned)ceil_div(cols, 128), (unsigned)nch);
-  ln_bwd_colsums_kernel<<<grid, 256, 0, st>>>(dy, x, mean, rstd, out, rows, cols, rpc, part);
+  launch_pdl(ln_bwd_colsums_kernel, grid, 256, 0, st, dy, x, mean, rstd, out, rows, cols, rpc, part);
   NNT_TRY(launch_check("ln_bwd_colsums"));
   return launch_sum_parts3(part, nch, cols, dg, db, out ? dbias : nullptr, accumulate, st);
 }
@@ -681,6 +697,8 @@ constexpr int kSumWarps = 32;
 
 __global__ void __launch_bounds__(32 * kSumWarps) sum_parts_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
                                  int64_t ld, float* __restrict__ out, int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[kSumWarps][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = blockIdx.x * 32ll + lane;
@@ -709,6 +727,8 @@ __global__ void __launch_bounds__(32 * kSumWarps) sum_parts_kernel(const float* 
 
 __global__ void __launch_bounds__(32 * kSumWarps) sum_parts3_kernel(const float* __restrict__ part, int64_t nparts, int64_t cols,
                                   float* o0, float* o1, float* o2, int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   float* outs[3] = {o0, o1, o2};
   float* out = outs[blockIdx.y];
   if (!out) return;
@@ -745,14 +765,14 @@ nnt_status launch_sum_parts3(const float* part, int64_t nparts, int64_t cols, fl
                              float* o2, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
   dim3 grid((unsigned)ceil_div(cols, 32), 3);
-  sum_parts3_kernel<<<grid, 32 * kSumWarps, 0, st>>>(part, nparts, cols, o0, o1, o2, accumulate);
+  launch_pdl(sum_parts3_kernel, grid, 32 * kSumWarps, 0, st, part, nparts, cols, o0, o1, o2, accumulate);
   return launch_check("sum_parts3");
 }
 
 nnt_status launch_sum_parts(const float* part, int64_t nparts, int64_t cols, int64_t ld,
                             float* out, int accumulate, cudaStream_t st) {
   if (cols == 0) return NNT_OK;
-  sum_parts_kernel<<<(unsigned)ceil_div(cols, 32), 32 * kSumWarps, 0, st>>>(part, nparts, cols, ld, out,
+  launch_pdl(sum_parts_kernel, (unsigned)ceil_div(cols, 32), 32 * kSumWarps, 0, st, part, nparts, cols, ld, out,
                                                                   accumulate);
   return launch_check("sum_parts");
 }
@@ -766,6 +786,8 @@ int64_t colsum_nparts(int64_t rows) { return ceil_div(rows, kColRows); }
 template <typename T>
 __global__ void colsum_part_kernel(const T* __restrict__ a, int64_t rows, int64_t cols, int64_t ld,
                                    float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float4 red[8][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = ((int64_t)blockIdx.x * 32 + lane) * 4;
@@ -800,9 +822,9 @@ nnt_status launch_colsum(const void* a, int a_dtype, int64_t rows, int64_t cols,
   NNT_CHECK_ARG(np < 65536, "colsum: too many rows");
   dim3 grid((unsigned)ceil_div(cols, 128), (unsigned)np);
   if (a_dtype == NNT_BF16)
-    colsum_part_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)a, rows, cols, ld, part);
+    launch_pdl(colsum_part_kernel<bf16>, grid, 256, 0, st, (const bf16*)a, rows, cols, ld, part);
   else
-    colsum_part_kernel<float><<<grid, 256, 0, st>>>((const float*)a, rows, cols, ld, part);
+    launch_pdl(colsum_part_kernel<float>, grid, 256, 0, st, (const float*)a, rows, cols, ld, part);
   NNT_TRY(launch_check("colsum_part"));
   return launch_sum_parts(part, np, cols, cols, out, accumulate, st);
 }
@@ -820,6 +842,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) softmax_fwd_kernel(const float* __restrict__ s,
                                                           T* __restrict__ p, int64_t S, ZMap zm,
                                                           int nz, int q0, int nq) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= (int64_t)nz * nq) return;
@@ -926,6 +950,8 @@ __global__ void __launch_bounds__(256, 3) softmax_bwd_kernel(const T* __restrict
                                                              const float* __restrict__ dp,
                                                              T* __restrict__ ds, int64_t S, ZMap zm,
                                                              int nz, int q0, int nq, float scale) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= (int64_t)nz * nq) return;
@@ -1007,9 +1033,9 @@ nnt_status launch_softmax_fwd(const float* s, void* p, int64_t S, ZMap zm, int n
   if (rows == 0) return NNT_OK;
   const int64_t grid = ceil_div(rows, 8);
   if (act_dtype == NNT_BF16)
-    softmax_fwd_kernel<bf16><<<grid, 256, 0, st>>>(s, (bf16*)p, S, zm, nz, q0, nq);
+    launch_pdl(softmax_fwd_kernel<bf16>, grid, 256, 0, st, s, (bf16*)p, S, zm, nz, q0, nq);
   else
-    softmax_fwd_kernel<float><<<grid, 256, 0, st>>>(s, (float*)p, S, zm, nz, q0, nq);
+    launch_pdl(softmax_fwd_kernel<float>, grid, 256, 0, st, s, (float*)p, S, zm, nz, q0, nq);
   return launch_check("softmax_fwd");
 }
 
@@ -1020,9 +1046,9 @@ nnt_status launch_softmax_bwd(const void* p, const float* dp, void* ds, int64_t 
   if (rows == 0) return NNT_OK;
   const int64_t grid = ceil_div(rows, 8);
   if (act_dtype == NNT_BF16)
-    softmax_bwd_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
+    launch_pdl(softmax_bwd_kernel<bf16>, grid, 256, 0, st, (const bf16*)p, dp, (bf16*)ds, S, zm, nz, q0, nq, scale);
   else
-    softmax_bwd_kernel<float><<<grid, 256, 0, st>>>((const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
+    launch_pdl(softmax_bwd_kernel<float>, grid, 256, 0, st, (const float*)p, dp, (float*)ds, S, zm, nz, q0, nq, scale);
   return launch_check("softmax_bwd");
 }
 
@@ -1042,6 +1068,8 @@ __device__ __forceinline__ float gelu_grad_f(float u) {
 
 template <typename T>
 __global__ void gelu_fwd_kernel(const float* __restrict__ u, T* __restrict__ g, int64_t n4) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 x = load4_stream(u + 4 * i);
@@ -1051,6 +1079,8 @@ __global__ void gelu_fwd_kernel(const float* __restrict__ u, T* __restrict__ g, 
 template <typename T>
 __global__ void gelu_bwd_kernel(const T* __restrict__ dg, const float* __restrict__ u,
                                 T* __restrict__ du, int64_t n4) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 x = load4_stream(u + 4 * i);
@@ -1068,9 +1098,9 @@ nnt_status launch_gelu_fwd(const float* u, void* g, int64_t n, int act_dtype, cu
   NNT_CHECK_ARG(n % 4 == 0, "gelu: n must be a multiple of 4");
   if (n == 0) return NNT_OK;
   if (act_dtype == NNT_BF16)
-    gelu_fwd_kernel<bf16><<<elementwise_grid(n / 4), 256, 0, st>>>(u, (bf16*)g, n / 4);
+    launch_pdl(gelu_fwd_kernel<bf16>, elementwise_grid(n / 4), 256, 0, st, u, (bf16*)g, n / 4);
   else
-    gelu_fwd_kernel<float><<<elementwise_grid(n / 4), 256, 0, st>>>(u, (float*)g, n / 4);
+    launch_pdl(gelu_fwd_kernel<float>, elementwise_grid(n / 4), 256, 0, st, u, (float*)g, n / 4);
   return launch_check("gelu_fwd");
 }
 nnt_status launch_gelu_bwd(const void* dg, const float* u, void* du, int64_t n, int act_dtype,
@@ -1078,9 +1108,9 @@ nnt_status launch_gelu_bwd(const void* dg, const float* u, void* du, int64_t n, 
   NNT_CHECK_ARG(n % 4 == 0, "gelu bwd: n must be a multiple of 4");
   if (n == 0) return NNT_OK;
   if (act_dtype == NNT_BF16)
-    gelu_bwd_kernel<bf16><<<elementwise_grid(n / 4), 256, 0, st>>>((const bf16*)dg, u, (bf16*)du, n / 4);
+    launch_pdl(gelu_bwd_kernel<bf16>, elementwise_grid(n / 4), 256, 0, st, (const bf16*)dg, u, (bf16*)du, n / 4);
   else
-    gelu_bwd_kernel<float><<<elementwise_grid(n / 4), 256, 0, st>>>((const float*)dg, u, (float*)du, n / 4);
+    launch_pdl(gelu_bwd_kernel<float>, elementwise_grid(n / 4), 256, 0, st, (const float*)dg, u, (float*)du, n / 4);
   return launch_check("gelu_bwd");
 }
 
@@ -1097,6 +1127,8 @@ __global__ void __launch_bounds__(512) cross_entropy_kernel(
     const uint16_t* __restrict__ tok_ids, TokMap tm, const uint16_t* __restrict__ tgt,
     int64_t tgt_stride, T* __restrict__ dz, int64_t lddz, float* __restrict__ row_loss,
     float inv_rows) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red_m[32], red_s[32];
   for (int64_t rr = blockIdx.x; rr < nrows; rr += gridDim.x) {
   const int64_t r = r0 + rr;
@@ -1214,10 +1246,10 @@ nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t
   // two CTAs per SM walk the rows, so the rows being re-read (pass 2) stay in L2
   const unsigned grid = (unsigned)std::min<int64_t>(nrows, 2 * 152);
   if (act_dtype == NNT_BF16)
-    cross_entropy_kernel<bf16><<<grid, 512, 0, st>>>(
+    launch_pdl(cross_entropy_kernel<bf16>, grid, 512, 0, st, 
         z, ldz, r0, nrows, cols, tok_ids, tm, tgt, tgt_stride, (bf16*)dz, lddz, row_loss, inv_rows);
   else
-    cross_entropy_kernel<float><<<grid, 512, 0, st>>>(
+    launch_pdl(cross_entropy_kernel<float>, grid, 512, 0, st, 
         z, ldz, r0, nrows, cols, tok_ids, tm, tgt, tgt_stride, (float*)dz, lddz, row_loss, inv_rows);
   return launch_check("cross_entropy");
 }
@@ -1225,6 +1257,8 @@ nnt_status launch_cross_entropy(const float* z, int64_t ldz, int64_t r0, int64_t
 // loss = (sum of row losses in a fixed order, in double) / rows
 __global__ void mean_loss_kernel(const float* __restrict__ row_loss, int64_t rows,
                                  float* __restrict__ loss) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ double red[1024];
   double s = 0.0;
   for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) s += (double)row_loss[i];
@@ -1238,7 +1272,7 @@ __global__ void mean_loss_kernel(const float* __restrict__ row_loss, int64_t row
 }
 
 nnt_status launch_mean_loss(const float* row_loss, int64_t rows, float* loss, cudaStream_t st) {
-  mean_loss_kernel<<<1, 1024, 0, st>>>(row_loss, rows, loss);
+  launch_pdl(mean_loss_kernel, 1, 1024, 0, st, row_loss, rows, loss);
   return launch_check("mean_loss");
 }
 
@@ -1272,6 +1306,8 @@ __global__ void adamw_kernel(float* __restrict__ w, const float* __restrict__ g,
                              float* __restrict__ m, float* __restrict__ v, bf16* __restrict__ wb,
                              int64_t n, float lr, float b1, float b2, float eps, float wd,
                              float bc1, float bc2, const float* __restrict__ hyper) {
+  pdl_wait();
+  pdl_trigger();
   float gs = 1.f;
   if (hyper) {
     lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; eps = hyper[3]; wd = hyper[4];
@@ -1326,7 +1362,7 @@ nnt_status launch_adamw(float* w, const float* g, float* m, float* v, bf16* w_bf
                     ((uintptr_t)w_bf16) % 8 == 0,
                 "adamw: buffers must be 16-byte aligned (bf16 copy 8-byte)");
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
-  adamw_kernel<1><<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, lr, b1, b2, eps, wd, bc1, bc2, nullptr);
+  launch_pdl(adamw_kernel<1>, grid, 256, 0, st, w, g, m, v, w_bf16, n, lr, b1, b2, eps, wd, bc1, bc2, nullptr);
   return launch_check("adamw");
 }
 
@@ -1335,10 +1371,10 @@ nnt_status launch_adamw_dev(float* w, const float* g, float* m, float* v, bf16* 
   if (n == 0) return NNT_OK;
   if (max_ctas > 0) {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256 * 4), max_ctas));
-    adamw_kernel<4><<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
+    launch_pdl(adamw_kernel<4>, grid, 256, 0, st, w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
   } else {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n / 4 + 1, 256), 152 * 8));
-    adamw_kernel<1><<<grid, 256, 0, st>>>(w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
+    launch_pdl(adamw_kernel<1>, grid, 256, 0, st, w, g, m, v, w_bf16, n, 0, 0, 0, 0, 0, 1, 1, hyper_dev);
   }
   return launch_check("adamw");
 }
@@ -1357,6 +1393,8 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
 }
 
 __global__ void init_normal_kernel(float* __restrict__ w, int64_t n, uint64_t key, double std) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t npairs = (n + 1) / 2;
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < npairs;
        j += (int64_t)gridDim.x * blockDim.x) {
@@ -1385,40 +1423,46 @@ nnt_status launch_init_normal(float* w, int64_t n, uint64_t seed, uint64_t strea
   if (n == 0) return NNT_OK;
   const uint64_t key = host_splitmix64(host_splitmix64(seed) ^ stream_id);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div((n + 1) / 2, 256), 152 * 16));
-  init_normal_kernel<<<grid, 256, 0, st>>>(w, n, key, std);
+  launch_pdl(init_normal_kernel, grid, 256, 0, st, w, n, key, std);
   return launch_check("init_normal");
 }
 
 __global__ void fill_kernel(float* __restrict__ w, int64_t n, float value) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     w[i] = value;
 }
 nnt_status launch_fill(float* w, int64_t n, float value, cudaStream_t st) {
   if (n == 0) return NNT_OK;
-  fill_kernel<<<(int)std::min<int64_t>(ceil_div(n, 256), 152 * 16), 256, 0, st>>>(w, n, value);
+  launch_pdl(fill_kernel, (int)std::min<int64_t>(ceil_div(n, 256), 152 * 16), 256, 0, st, w, n, value);
   return launch_check("fill");
 }
 
 __global__ void cast_bf16_kernel(const float* __restrict__ s, bf16* __restrict__ d, int64_t n) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     d[i] = __float2bfloat16_rn(s[i]);
 }
 nnt_status launch_cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t st) {
   if (n == 0) return NNT_OK;
-  cast_bf16_kernel<<<(int)std::min<int64_t>(ceil_div(n, 256), 152 * 16), 256, 0, st>>>(src, dst, n);
+  launch_pdl(cast_bf16_kernel, (int)std::min<int64_t>(ceil_div(n, 256), 152 * 16), 256, 0, st, src, dst, n);
   return launch_check("cast_bf16");
 }
 
 __global__ void check_tokens_kernel(const uint16_t* __restrict__ ids, int64_t n, int vocab) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     if (ids[i] >= vocab) atomicOr(&g_device_error, DEVERR_TOKEN_RANGE);
 }
 nnt_status launch_check_tokens(const uint16_t* ids, int64_t n, int vocab, cudaStream_t st) {
   if (n == 0) return NNT_OK;
-  check_tokens_kernel<<<(int)std::min<int64_t>(ceil_div(n, 256), 152), 256, 0, st>>>(ids, n, vocab);
+  launch_pdl(check_tokens_kernel, (int)std::min<int64_t>(ceil_div(n, 256), 152), 256, 0, st, ids, n, vocab);
   return launch_check("check_tokens");
 }
 

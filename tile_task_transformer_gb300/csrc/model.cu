@@ -122,8 +122,9 @@ struct nnt_model {
   uint16_t* tokens_dev = nullptr;
   std::vector<float*> x, xmid, mu1, r1, mu2, r2;
   std::vector<void*> h1, qkvh, P, O, h2, g;
-  std::vector<void*> u;  // FC pre-activation (GELU input), u_dtype
-  int u_dtype = NNT_BF16;
+  // gelu'(u) of the FC pre-activation u (activation dtype), written by the FC
+  // epilogue for the GELU backward
+  std::vector<void*> u;
   float* scores = nullptr;  // [B*H][S][S] fp32, reused by every layer (fwd scores, bwd dP)
   // fused attention (flash): per-layer row log-sum-exp [B*H][S] and the
   // backward's D = rowsum(dO * O) scratch [B*H][S]; no P or scores buffers
@@ -549,7 +550,7 @@ nnt_status alloc_all(nnt_model* m) {
       NNT_TRY(dalloc(m, m->P[l], (size_t)B * H * S * S * as));
     NNT_TRY(dalloc(m, m->O[l], Td * as));
     NNT_TRY(dalloc(m, m->h2[l], Td * as));
-    NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * (m->u_dtype == NNT_F32 ? 4 : 2)));
+    NNT_TRY(dalloc(m, m->u[l], (size_t)T * f * as));
     NNT_TRY(dalloc(m, m->g[l], (size_t)T * f * as));
   }
   if (m->flash) {
@@ -883,7 +884,7 @@ void build_forward(nnt_model* m) {
         g.B = pw(m, P_(m, l, FCW)); g.ldb = d;
         g.C = m->g[l]; g.ldc = f; g.c_dtype = act;
         g.bias = pm(m, P_(m, l, FCB));
-        g.epi = EPI_GELU; g.aux = m->u[l]; g.ld_aux = f; g.aux_dtype = m->u_dtype;
+        g.epi = EPI_GELU; g.aux = m->u[l]; g.ld_aux = f; g.aux_dtype = act;
         std::vector<TileUse> u;
         box(u, m->gh2[l], ACC_R, rt, rt + 1);
         box(u, m->gu[l], ACC_W, rt, rt + 1, t0, t1);
@@ -1207,7 +1208,7 @@ void build_backward(nnt_model* m, Program& P, bool fused, bool acc = false) {
         GemmArgs proto = b.base();
         proto.epi = EPI_GELU_BWD;
         proto.aux = m->u[l];
-        proto.aux_dtype = m->u_dtype;
+        proto.aux_dtype = act;
         proto.ld_aux = f;
         std::vector<TileUse> u;
         box(u, m->gdres_act, ACC_R, rt, rt + 1);
@@ -1628,8 +1629,6 @@ nnt_status setup_fields(nnt_model* m, const nnt_gpt2_config* cfg, const nnt_tile
   m->opts = opts ? *opts : zo;
   m->act = cfg->dtype;
   m->act_size = m->act == NNT_BF16 ? 2 : 4;
-  m->u_dtype = m->act;
-  if (getenv("NNT_U_F32")) m->u_dtype = NNT_F32;
   m->L = cfg->n_layer; m->d = cfg->d_model; m->H = cfg->n_head; m->hd = m->d / m->H;
   m->f = cfg->d_ff; m->V = cfg->vocab; m->S = cfg->n_ctx; m->B = cfg->batch; m->T = m->B * m->S;
   m->tb = m->tiles.batch_tile ? m->tiles.batch_tile : m->B;

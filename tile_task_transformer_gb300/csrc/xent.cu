@@ -79,6 +79,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCeThreads, 2) cross
     const uint16_t* __restrict__ tok_ids, TokMap tm, const uint16_t* __restrict__ tgt,
     int64_t tgt_stride, T* __restrict__ dz, int64_t lddz, float* __restrict__ row_loss,
     float inv_rows, int half, int cf, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) float rowbuf[];  // this CTA's half row
   __shared__ __align__(8) uint64_t full[kCeChunks];
   __shared__ __align__(8) uint64_t xbar[2];         // the peer's (max, sum) landed, by row parity
@@ -266,7 +268,7 @@ nnt_status launch_pair(const float* z, int64_t ldz, int64_t r0, int64_t nrows, i
   NNT_CUDA_TRY(attr);
   const int half = (int)ce_half(cols), cf = ce_chunk(half);
   const unsigned clusters = (unsigned)std::min<int64_t>(nrows, sms);
-  kern<<<2 * clusters, kCeThreads, (size_t)half * 4, st>>>(z, ldz, r0, nrows, cols, tok_ids, tm, tgt,
+  launch_pdl(kern, 2 * clusters, kCeThreads, (size_t)half * 4, st, z, ldz, r0, nrows, cols, tok_ids, tm, tgt,
                                                           tgt_stride, dz, lddz, row_loss, inv_rows,
                                                           half, cf, err);
   return launch_check("cross_entropy_pair");
