@@ -8,7 +8,9 @@
   the oracle computes; with wte = 0 every logit is 0 and the loss is ln V
   exactly.
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -79,15 +81,17 @@ def test_wide4_zero_embedding_loss_is_log_vocab():
     assert abs(loss - math.log(cfg.vocab)) < 1e-4
 
 
-def _step_checks(grads, new, mom1, params, rgrads, rnew, rm, norm=relerr):
+def _step_checks(grads, new, mom1, params, rgrads, rnew, rm, norm=relerr, allow=None):
     """Normwise gradient, first-moment and updated-weight errors of one step
-    (gradients and moments in the given norm, updated weights in the max norm)."""
+    (gradients and moments in the given norm, updated weights in the max norm).
+    ``allow[n]`` adds to the gradient and moment tolerance of tensor n."""
     worst = {}
     for n in rgrads:
+        tol = TOL + (allow[n] if allow else 0.0)
         e = norm(grads[n], rgrads[n])
         worst[n] = e
-        assert e < TOL, (n, e)
-        assert norm(mom1[n], rm[n]) < TOL, n
+        assert e < tol, (n, e, tol)
+        assert norm(mom1[n], rm[n]) < tol, n
         w0 = params[n].astype(np.float64)
         if np.abs(w0).max() > 0:
             assert relerr(new[n], rnew[n]) < TOL, n
@@ -107,14 +111,17 @@ def test_wide4_step_matches_bf16_operand_oracle():
 
     The reference is the oracle with every matrix-product operand rounded to
     bf16 (the stated precision: bf16 GEMM operands, fp32 accumulation and fp32
-    everything else): loss within 1e-3 of it, updated weights within 2e-2 in
-    the max norm, gradients and first moments within 2e-2 in the relative
-    2-norm. At d_model 8192 the max-norm error of a gradient is not determined
-    by the precision to 2e-2: the oracle's own bf16-operand step evaluated with
-    fp32 and with fp64 accumulation differs by up to 1.7% in that norm (most
-    in the embedding and first-block gradients), so the max-norm errors are
-    printed, not asserted, as are the departures from the unrounded oracle
-    (except the logits, asserted in the max norm)."""
+    everything else): loss within 1e-3 of it and updated weights within 2e-2
+    in the max norm. At d_model 8192 a gradient is not determined by that
+    precision to 2e-2: the oracle's own bf16-operand step evaluated with fp32
+    and with fp64 accumulation differs by up to 1.7% per tensor (relative
+    2-norm; tests/golden/wide4_accumulation_spread.json, written by the oracle
+    alone). Gradients and first moments are therefore checked in the relative
+    2-norm within 2e-2 plus that spread, and, as a check of their structure,
+    within twice the spread (plus 2e-3): an implementation that only sums in
+    another fp32 order stays near 1.3 times it. Max-norm errors and the
+    departures from the unrounded oracle are printed (the logits are asserted
+    in the max norm)."""
     cfg = WIDE4
     two = O.GPT2Config(n_layer=cfg.n_layer, d_model=cfg.d_model, n_head=cfg.n_head, d_ff=cfg.d_ff,
                        vocab=cfg.vocab, seq=cfg.seq, batch=2)
@@ -138,7 +145,11 @@ def test_wide4_step_matches_bf16_operand_oracle():
     del bcache
     bnew, bm, _ = O.adamw_step(params, bgrads, None, None, 1, O.AdamWHyper(), np.float32)
     assert abs(loss - bloss) < 1e-3, (loss, bloss)
-    worst = _step_checks(grads, new, mom1, params, bgrads, bnew, bm, norm=relerr2)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "wide4_accumulation_spread.json")) as fh:
+        spread = {n: v["two_norm"] for n, v in json.load(fh)["tensors"].items()}
+    worst = _step_checks(grads, new, mom1, params, bgrads, bnew, bm, norm=relerr2, allow=spread)
+    for n, e in worst.items():
+        assert e <= 2 * spread[n] + 2e-3, (n, e, spread[n])
     worst_max = {n: relerr(grads[n], bgrads[n]) for n in bgrads}
     del bnew, bm
 
@@ -148,6 +159,7 @@ def test_wide4_step_matches_bf16_operand_oracle():
     del cache
     print(f"loss: gpu {loss:.6f} bf16-operand oracle {bloss:.6f} unrounded oracle {rloss:.6f}")
     for n in rgrads:
-        print(f"{n}: gpu-vs-bf16 2-norm {worst[n]:.4f} max-norm {worst_max[n]:.4f}; "
+        print(f"{n}: gpu-vs-bf16 2-norm {worst[n]:.4f} (oracle fp32/fp64 spread {spread[n]:.4f}) "
+              f"max-norm {worst_max[n]:.4f}; "
               f"gpu-vs-unrounded max-norm {relerr(grads[n], rgrads[n]):.4f}; "
               f"bf16-vs-unrounded max-norm {relerr(bgrads[n], rgrads[n]):.4f}")

@@ -119,16 +119,16 @@ def test_wide8_offloaded_step_matches_streamed_oracle():
 
     two = O.GPT2Config(n_layer=L, d_model=d, n_head=cfg.n_head, d_ff=f, vocab=V, seq=S, batch=2)
     bloss, cache = O.forward_bf16_streamed(two, layer_params, head, seqs)
-    assert abs(loss - bloss) < 1e-3, (loss, bloss)
     e_logits = relerr(logits, cache["z"])
-    assert e_logits < TOL, e_logits
     rgrads = O.backward_bf16_streamed(two, layer_params, head, cache, want={0, L - 1})
     del cache, layers
     worst = {}
     for n, g in grads.items():
         worst[n] = relerr2(g, rgrads[n])
         print(f"{n}: 2-norm {worst[n]:.4f} max-norm {relerr(g, rgrads[n]):.4f}")
-    print(f"loss: gpu {loss:.6f} oracle {bloss:.6f}; logits {e_logits:.4f}")
+    print(f"loss: gpu {loss:.6f} oracle {bloss:.6f} diff {loss - bloss:.2e}; logits max-norm {e_logits:.4f}")
+    assert math.isfinite(loss)
+    assert abs(loss - bloss) < 1e-3, (loss, bloss)
+    assert e_logits < TOL, e_logits
     bad = {n: e for n, e in worst.items() if not e < TOL}
     assert not bad, bad
-    assert math.isfinite(loss)

@@ -46,3 +46,19 @@ def test_param_recipe():
 def test_parameter_counts_match_the_stated_model_sizes(L, d, f, V, S, stated, half_unit):
     n = sum(int(np.prod(s)) for _, s in synth.param_names_shapes(L, d, f, V, S))
     assert abs(n - stated) <= half_unit, (n, stated)  # equal after rounding to the stated digits
+
+
+def test_wide4_spread_golden_covers_every_parameter():
+    """The stored accumulation spread of the wide-4 parity inputs (written by
+    tests/golden/make_wide4_spread.py from the oracle alone) names every
+    parameter tensor once, with spreads in (0, 5%)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "wide4_accumulation_spread.json")
+    with open(path) as fh:
+        d = json.load(fh)
+    names = [n for n, _ in synth.param_names_shapes(4, 8192, 32768, 50257, 1024)]
+    assert sorted(d["tensors"]) == sorted(names)
+    for n, v in d["tensors"].items():
+        assert 0 < v["two_norm"] < 0.05 and 0 < v["max_norm"] < 0.05, n
+    assert abs(d["loss_fp32"] - d["loss_fp64"]) < 1e-3
