@@ -593,14 +593,16 @@ def from_bf16_bits(b):
     return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def forward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, windows):
+def forward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, windows, dtype=np.float32):
     """Loss and cache of the bf16-operand forward, one layer in memory at a time.
 
     ``layer_params(l)`` returns layer l's tensors keyed without the ``h{l}.``
     prefix (weights may already be bf16-rounded: rounding is idempotent);
-    ``head_params`` holds ``wte``, ``wpe``, ``ln_f.g``, ``ln_f.b``."""
-    r = round_bf16
-    f32 = np.float32
+    ``head_params`` holds ``wte``, ``wpe``, ``ln_f.g``, ``ln_f.b``. ``dtype``
+    is the arithmetic (float32, or float64 to measure what fp32 accumulation
+    leaves undetermined)."""
+    f32 = dtype
+    r = lambda a: round_bf16(a).astype(f32)  # noqa: E731
     ids = windows[:, :cfg.seq].astype(np.int64)
     tgt = windows[:, 1:cfg.seq + 1].astype(np.int64)
     B, S, d, H = cfg.batch, cfg.seq, cfg.d_model, cfg.n_head
@@ -654,23 +656,34 @@ def forward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, windows):
     return loss, c
 
 
-def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, want=None):
+def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, want=None,
+                           dtype=np.float32, grad_dtype=None):
     """Gradients of the bf16-operand step (as :func:`backward_bf16_operands`),
     one layer in memory at a time, from the cache of
     :func:`forward_bf16_streamed`.
 
     ``want``: layer indices whose parameter gradients are returned (default:
     all). Other layers skip their weight- and bias-gradient sums, which feed
-    nothing else; the gradients of wte, wpe and ln_f are always returned."""
-    r = round_bf16
-    f32 = np.float32
+    nothing else; the gradients of wte, wpe and ln_f are always returned.
+    ``dtype`` as in :func:`forward_bf16_streamed`; ``grad_dtype`` (default
+    ``dtype``) is the type the returned gradients are stored in as soon as each
+    is formed (float32 keeps an fp64 run's memory down)."""
+    f32 = dtype
+    r = lambda a: round_bf16(a).astype(f32)  # noqa: E731
+    unpack = lambda b: from_bf16_bits(b).astype(f32)  # noqa: E731
     B, S, d, H = cfg.batch, cfg.seq, cfg.d_model, cfg.n_head
     T = B * S
     scale = 1.0 / math.sqrt(d // H)
-    grads = {}
+    gdt = grad_dtype or dtype
+
+    class _Grads(dict):
+        def __setitem__(self, k, v):
+            super().__setitem__(k, np.asarray(v).astype(gdt, copy=False))
+
+    grads = _Grads()
     wte = np.asarray(head_params["wte"], f32)
     dz = r(cache["dz"])
-    dwte = dz.T @ from_bf16_bits(cache["y"]).reshape(T, d)
+    dwte = dz.T @ unpack(cache["y"]).reshape(T, d)
     dy = (dz @ r(wte)).reshape(B, S, d)
     del dz
     dx, grads["ln_f.g"], grads["ln_f.b"] = layernorm_backward(
@@ -683,12 +696,12 @@ def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, wa
         keep = want is None or l in want
         dxa = r(dx)
         if keep:
-            grads[q + "proj.w"] = dxa.reshape(T, d).T @ from_bf16_bits(c["g"]).reshape(T, -1)
+            grads[q + "proj.w"] = dxa.reshape(T, d).T @ unpack(c["g"]).reshape(T, -1)
             grads[q + "proj.b"] = dx.sum(axis=(0, 1))
         du_f = gelu_backward(dxa @ r(p["proj.w"]), c["u"])
         du = r(du_f)
         if keep:
-            grads[q + "fc.w"] = du.reshape(T, -1).T @ from_bf16_bits(c["h2"]).reshape(T, d)
+            grads[q + "fc.w"] = du.reshape(T, -1).T @ unpack(c["h2"]).reshape(T, d)
             grads[q + "fc.b"] = du_f.sum(axis=(0, 1))
         del du_f
         dh2 = du @ r(p["fc.w"])
@@ -700,11 +713,11 @@ def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, wa
         dx = dx + dln
         dxa = r(dx)
         if keep:
-            grads[q + "o.w"] = dxa.reshape(T, d).T @ from_bf16_bits(c["o"]).reshape(T, d)
+            grads[q + "o.w"] = dxa.reshape(T, d).T @ unpack(c["o"]).reshape(T, d)
             grads[q + "o.b"] = dx.sum(axis=(0, 1))
         dO = split_heads(r(dxa @ r(p["o.w"])), H)
         del dxa
-        qh, kh, vh = from_bf16_bits(c["q"]), from_bf16_bits(c["k"]), from_bf16_bits(c["v"])
+        qh, kh, vh = unpack(c["q"]), unpack(c["k"]), unpack(c["v"])
         dqkv_f = np.empty((B, S, 3 * d), f32)
         for b in range(B):
             sl = slice(b, b + 1)
@@ -719,7 +732,7 @@ def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, wa
         del dO, qh, kh, vh
         dqkv = r(dqkv_f)
         if keep:
-            grads[q + "qkv.w"] = dqkv.reshape(T, -1).T @ from_bf16_bits(c["h1"]).reshape(T, d)
+            grads[q + "qkv.w"] = dqkv.reshape(T, -1).T @ unpack(c["h1"]).reshape(T, d)
             grads[q + "qkv.b"] = dqkv_f.sum(axis=(0, 1))
         del dqkv_f
         dh1 = dqkv @ r(p["qkv.w"])
@@ -731,4 +744,4 @@ def backward_bf16_streamed(cfg: GPT2Config, layer_params, head_params, cache, wa
         dx = dx + dln
     grads["wte"], grads["wpe"] = embedding_backward(
         dx, cache["ids"], dwte, np.zeros_like(np.asarray(head_params["wpe"], f32)))
-    return grads
+    return dict(grads)

@@ -58,6 +58,22 @@ def relerr2(a, r):
     return float(np.linalg.norm(np.asarray(a, np.float64) - r) / max(np.linalg.norm(r), 1e-30))
 
 
+def test_wide8_zero_embedding_loss_is_log_vocab():
+    """With wte = 0 every logit is 0 and the mean cross-entropy is ln V exactly,
+    whatever the rest of the 26.6B-parameter model computes (full size, host
+    offload active)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cfg = WIDE8
+    m = nnt.Model(cfg.n_layer, cfg.d_model, cfg.n_head, cfg.d_ff, cfg.vocab, cfg.seq, cfg.batch, dtype=nnt.BF16,
+                  tiles=TILES, use_cuda_graph=True, n_streams=2, seed=SEED, init_std=0.02,
+                  allow_host_offload=True)
+    m.set_param(0, np.zeros((cfg.vocab, cfg.d_model), np.float32))
+    loss = m.forward(synth.token_windows(SEED, cfg.batch, cfg.seq, cfg.vocab))
+    m.close()
+    assert abs(loss - math.log(cfg.vocab)) < 1e-4, loss
+
+
 def test_wide8_offloaded_step_matches_streamed_oracle():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")

@@ -439,6 +439,14 @@ def test_streamed_bf16_step_matches_whole_model():
     assert set(g2) == {k for k in g0 if not k.startswith("h1.")}
     for k in g2:
         np.testing.assert_array_equal(g2[k], g1[k])
+    # the same in fp64 arithmetic (used to measure what fp32 accumulation leaves open)
+    l64, c64 = O.forward(cfg, p, win, dtype=np.float64, gemm_operands="bf16")
+    g64 = O.backward_bf16_operands(cfg, p, c64, dtype=np.float64)
+    l3, c3 = O.forward_bf16_streamed(cfg, layer, head, win, dtype=np.float64)
+    assert abs(l3 - l64) < 1e-12
+    g3 = O.backward_bf16_streamed(cfg, layer, head, c3, dtype=np.float64)
+    for k in g64:
+        assert np.abs(g3[k] - g64[k]).max() <= 1e-10 * np.abs(g64[k]).max() + 1e-15, k
     # bf16 bit patterns round-trip
     x = np.random.default_rng(0).standard_normal(1000).astype(np.float32)
     np.testing.assert_array_equal(O.from_bf16_bits(O.bf16_bits(x)), O.round_bf16(x))

@@ -540,13 +540,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool diag = i == kb;
     uint8_t* pt = sm + C::OFF_PT;
     uint8_t* dst = sm + C::OFF_DS;
+    // this thread's 64 query columns, two chunks of 32: the second chunk's
+    // TMEM loads are in flight while the first chunk is computed
+    uint32_t svc[2][32], dvc[2][32];
+    tmem_ld32_nw(t_row + 32 * (2 * hf), svc[0]);
+    tmem_ld32_nw(t_row + FB + 32 * (2 * hf), dvc[0]);
+    tmem_wait_ld();
+    tmem_ld32_nw(t_row + 32 * (2 * hf + 1), svc[1]);
+    tmem_ld32_nw(t_row + FB + 32 * (2 * hf + 1), dvc[1]);
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {  // this thread's 64 query columns
+    for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * hf + cc;
-      uint32_t sv[32], dv[32];
-      tmem_ld32_nw(t_row + 32 * c, sv);
-      tmem_ld32_nw(t_row + FB + 32 * c, dv);
-      tmem_wait_ld();
+      if (cc == 1) tmem_wait_ld();
+      const uint32_t* sv = svc[cc];
+      const uint32_t* dv = dvc[cc];
       // the chunk's 32 lse and D values: the same addresses across the warp (broadcast)
       float ls[32], dd[32];
 #pragma unroll
