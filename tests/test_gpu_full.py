@@ -81,13 +81,15 @@ def test_wide4_zero_embedding_loss_is_log_vocab():
     assert abs(loss - math.log(cfg.vocab)) < 1e-4
 
 
-def _step_checks(grads, new, mom1, params, rgrads, rnew, rm, norm=relerr, allow=None):
+def _step_checks(grads, new, mom1, params, rgrads, rnew, rm, norm=relerr, spread=None):
     """Normwise gradient, first-moment and updated-weight errors of one step
     (gradients and moments in the given norm, updated weights in the max norm).
-    ``allow[n]`` adds to the gradient and moment tolerance of tensor n."""
+    With ``spread`` (per tensor: how far the oracle's own result moves between
+    fp32 and fp64 accumulation), a gradient or moment may be off by twice its
+    spread where that exceeds the tolerance."""
     worst = {}
     for n in rgrads:
-        tol = TOL + (allow[n] if allow else 0.0)
+        tol = max(TOL, 2 * spread[n]) if spread else TOL
         e = norm(grads[n], rgrads[n])
         worst[n] = e
         assert e < tol, (n, e, tol)
@@ -112,16 +114,16 @@ def test_wide4_step_matches_bf16_operand_oracle():
     The reference is the oracle with every matrix-product operand rounded to
     bf16 (the stated precision: bf16 GEMM operands, fp32 accumulation and fp32
     everything else): loss within 1e-3 of it and updated weights within 2e-2
-    in the max norm. At d_model 8192 a gradient is not determined by that
-    precision to 2e-2: the oracle's own bf16-operand step evaluated with fp32
-    and with fp64 accumulation differs by up to 1.7% per tensor (relative
-    2-norm; tests/golden/wide4_accumulation_spread.json, written by the oracle
-    alone). Gradients and first moments are therefore checked in the relative
-    2-norm within 2e-2 plus that spread, and, as a check of their structure,
-    within twice the spread (plus 2e-3): an implementation that only sums in
-    another fp32 order stays near 1.3 times it. Max-norm errors and the
-    departures from the unrounded oracle are printed (the logits are asserted
-    in the max norm)."""
+    in the max norm. At d_model 8192 a gradient is not fully determined by that
+    precision: the oracle's own bf16-operand step evaluated with fp32 and with
+    fp64 accumulation differs by up to 1.7% per tensor (relative 2-norm;
+    tests/golden/wide4_accumulation_spread.json, written by the oracle alone),
+    and two evaluations that differ only in fp32 summation order are expected
+    about sqrt(2) times that apart. Gradients and first moments are therefore
+    checked in the relative 2-norm within 2e-2, or twice their spread where
+    that is larger, and, as a check of their structure, within twice the
+    spread plus 2e-3. Max-norm errors and the departures from the unrounded
+    oracle are printed (the logits are asserted in the max norm)."""
     cfg = WIDE4
     two = O.GPT2Config(n_layer=cfg.n_layer, d_model=cfg.d_model, n_head=cfg.n_head, d_ff=cfg.d_ff,
                        vocab=cfg.vocab, seq=cfg.seq, batch=2)
@@ -147,7 +149,7 @@ def test_wide4_step_matches_bf16_operand_oracle():
     assert abs(loss - bloss) < 1e-3, (loss, bloss)
     with open(os.path.join(os.path.dirname(__file__), "golden", "wide4_accumulation_spread.json")) as fh:
         spread = {n: v["two_norm"] for n, v in json.load(fh)["tensors"].items()}
-    worst = _step_checks(grads, new, mom1, params, bgrads, bnew, bm, norm=relerr2, allow=spread)
+    worst = _step_checks(grads, new, mom1, params, bgrads, bnew, bm, norm=relerr2, spread=spread)
     for n, e in worst.items():
         assert e <= 2 * spread[n] + 2e-3, (n, e, spread[n])
     worst_max = {n: relerr(grads[n], bgrads[n]) for n in bgrads}

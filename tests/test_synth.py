@@ -62,3 +62,20 @@ def test_wide4_spread_golden_covers_every_parameter():
     for n, v in d["tensors"].items():
         assert 0 < v["two_norm"] < 0.05 and 0 < v["max_norm"] < 0.05, n
     assert abs(d["loss_fp32"] - d["loss_fp64"]) < 1e-3
+
+
+def test_wide8_spread_golden_covers_the_compared_tensors():
+    """The stored accumulation spread of the wide-8 parity inputs (written by
+    tests/golden/make_wide8_spread.py from the oracle alone) covers ln_f, wte,
+    wpe and the first and last blocks, with spreads in (0, 20%)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "wide8_accumulation_spread.json")
+    with open(path) as fh:
+        d = json.load(fh)
+    names = [n for n, _ in synth.param_names_shapes(8, 16384, 65536, 50257, 1024)
+             if n.startswith(("h0.", "h7.")) or n in ("wte", "wpe", "ln_f.g", "ln_f.b")]
+    assert sorted(d["tensors"]) == sorted(names)
+    for n, v in d["tensors"].items():
+        assert 0 < v["two_norm"] < 0.2 and 0 < v["max_norm"] < 0.2, n
+    assert 0 < d["logits"]["max_norm"] < 0.1

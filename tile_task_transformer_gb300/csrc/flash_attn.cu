@@ -400,7 +400,10 @@ __global__ void __launch_bounds__(256) flash_bwd_d_kernel(const bf16* __restrict
 template <int HD>
 struct KvCfg {
   static constexpr int TILE = FB * HD * 2;
-  static constexpr int NS = HD <= 64 ? 2 : 1;  // stages of (Q, dO)
+  // head size 64: three stages of (Q, dO), and the next query block's S^T and
+  // dP^T are issued as soon as this block's are in registers (EARLY)
+  static constexpr bool EARLY = HD <= 64;
+  static constexpr int NS = HD <= 64 ? 3 : 1;  // stages of (Q, dO)
   static constexpr int OFF_K = 0, OFF_V = TILE, OFF_ST = 2 * TILE;  // stage s: Q, then dO
   static constexpr int OFF_PT = OFF_ST + NS * 2 * TILE, OFF_DS = OFF_PT + 2 * CHUNK;
   static constexpr int OFF_ROW = OFF_DS + 2 * CHUNK;  // lse and D of the current query block
@@ -424,12 +427,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_kv = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint64_t* bar_ld = bar_kv + 1;    // [2]
-  uint64_t* bar_free = bar_kv + 3;  // [2]
-  uint64_t* bar_s = bar_kv + 5;
-  uint64_t* bar_o = bar_kv + 6;
-  uint64_t* bar_x = bar_kv + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kv + 8);
+  uint64_t* bar_ld = bar_kv + 1;    // [3]
+  uint64_t* bar_free = bar_kv + 4;  // [3]
+  uint64_t* bar_s = bar_kv + 7;
+  uint64_t* bar_o = bar_kv + 8;
+  uint64_t* bar_x = bar_kv + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kv + 10);
   float* lse_s = reinterpret_cast<float*>(sm + C::OFF_ROW);
   float* d_s = lse_s + FB;
 
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int key = kb * FB + r;
 
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(bar_kv + i, 1);
+    for (int i = 0; i < 10; ++i) mbar_init(bar_kv + i, 1);
     mbar_fence_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     load_tile<HD>(&tmQ, dst, &bar_ld[s], i * FB, z);
     load_tile<HD>(&tmdO, dst + C::TILE, &bar_ld[s], i * FB, z);
   };
-  int n_ld[2] = {0, 0}, w_ld[2] = {0, 0}, w_kv = 0;
+  int n_ld[3] = {0, 0, 0}, w_ld[3] = {0, 0, 0}, w_kv = 0;
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
     load_tile<HD>(&tmK, sm + C::OFF_K, bar_kv, kb * FB, z);
@@ -499,6 +502,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   };
+  // S^T = K Q_i^T and dP^T = V dO_i^T of iteration it_ into TMEM columns 0..255
+  // (thread 0; the operands' stage must have landed)
+  auto issue_s = [&](int it_) {
+    const int st_ = it_ % NS;
+    if (ok) {
+      ok = mbar_wait(&bar_ld[st_], (uint32_t)((it_ / NS) & 1));
+      if (ok) ++w_ld[st_];
+    }
+    if (ok) {
+      tc_fence_after();
+      const uint32_t s_qt = smem_u32(sm + C::OFF_ST + st_ * 2 * C::TILE), s_do = s_qt + C::TILE;
+      constexpr uint32_t idesc = make_idesc(FB, FB, false, false);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem, desc_k(s_k, kk), desc_k(s_qt, kk), idesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + FB, desc_k(s_v, kk), desc_k(s_do, kk), idesc, kk > 0 ? 1u : 0u);
+      umma_commit(bar_s);
+    }
+  };
+  if (C::EARLY && tid == 0) {
+    ok = mbar_wait(bar_kv, 0);
+    w_kv = ok ? 1 : 0;
+    issue_s(0);
+  }
   float row_next = row_val(kb);
   for (int it = 0; it < n; ++it) {
     const int i = kb + it, st = it % NS;
@@ -506,28 +535,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (it + 1 < n) row_next = row_val(i + 1);
     // the previous dS^T tile must have left shared memory before it is rewritten
     if (store_ds && tid == 32 && it > 0) bulk_wait_read();
-    if (tid == 0) {
+    if (!C::EARLY && tid == 0) {
       if (it == 0) {
         ok = mbar_wait(bar_kv, 0);
         w_kv = ok ? 1 : 0;
       }
       if (NS == 1) refill(it);  // single stage: the operands of this iteration
-      if (ok) {
-        ok = mbar_wait(&bar_ld[st], (uint32_t)((it / NS) & 1));
-        if (ok) ++w_ld[st];
-      }
-      if (ok) {
-        tc_fence_after();
-        const uint32_t s_qt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE), s_do = s_qt + C::TILE;
-        constexpr uint32_t idesc = make_idesc(FB, FB, false, false);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem, desc_k(s_k, kk), desc_k(s_qt, kk), idesc, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + FB, desc_k(s_v, kk), desc_k(s_do, kk), idesc, kk > 0 ? 1u : 0u);
-        umma_commit(bar_s);
-      }
+      issue_s(it);
       if (NS > 1) refill(it);  // after the issue, so the MMAs queue back to back
     }
     (hf ? d_s : lse_s)[r] = row_c;
@@ -540,18 +554,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool diag = i == kb;
     uint8_t* pt = sm + C::OFF_PT;
     uint8_t* dst = sm + C::OFF_DS;
-    // this thread's 64 query columns, two chunks of 32: the second chunk's
-    // TMEM loads are in flight while the first chunk is computed
+    // this thread's 64 query columns, two chunks of 32
     uint32_t svc[2][32], dvc[2][32];
     tmem_ld32_nw(t_row + 32 * (2 * hf), svc[0]);
     tmem_ld32_nw(t_row + FB + 32 * (2 * hf), dvc[0]);
-    tmem_wait_ld();
-    tmem_ld32_nw(t_row + 32 * (2 * hf + 1), svc[1]);
-    tmem_ld32_nw(t_row + FB + 32 * (2 * hf + 1), dvc[1]);
+    if constexpr (C::EARLY) {
+      // all of this block's S^T and dP^T into registers; then TMEM columns
+      // 0..255 are free and the next block's products run while this one is
+      // computed. P^T and dS^T (one buffer) are rewritten only once the
+      // previous block's dV, dK products have consumed them.
+      tmem_ld32_nw(t_row + 32 * (2 * hf + 1), svc[1]);
+      tmem_ld32_nw(t_row + FB + 32 * (2 * hf + 1), dvc[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        if (it + 1 < n) issue_s(it + 1);
+        refill(it);
+      }
+      if (it > 0 && ok && !mbar_wait(&bar_free[(it - 1) % NS], (uint32_t)(((it - 1) / NS) & 1))) ok = false;
+    } else {
+      // the second chunk's TMEM loads are in flight while the first is computed
+      tmem_wait_ld();
+      tmem_ld32_nw(t_row + 32 * (2 * hf + 1), svc[1]);
+      tmem_ld32_nw(t_row + FB + 32 * (2 * hf + 1), dvc[1]);
+    }
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * hf + cc;
-      if (cc == 1) tmem_wait_ld();
+      if (!C::EARLY && cc == 1) tmem_wait_ld();
       const uint32_t* sv = svc[cc];
       const uint32_t* dv = dvc[cc];
       // the chunk's 32 lse and D values: the same addresses across the warp (broadcast)
@@ -631,8 +663,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (tid == 0) {
     atomicOr(err, DEVERR_WAIT_TIMEOUT);
     drain(bar_kv, 1, &w_kv);
-    drain(&bar_ld[0], n_ld[0], &w_ld[0]);
-    drain(&bar_ld[1], n_ld[1], &w_ld[1]);
+    for (int s2 = 0; s2 < NS; ++s2) drain(&bar_ld[s2], n_ld[s2], &w_ld[s2]);
     umma_commit(bar_x);
     mbar_wait(bar_x, 0);
   }
