@@ -44,7 +44,8 @@ namespace {
 
 constexpr int FB = 128;              // queries or keys per block
 constexpr int kThreads = 256;     // forward: two threads per row, one per half of the columns
-constexpr int kBwdThreads = 256;  // backward: the same split
+constexpr int kBwdThreads = 256;  // backward dQ kernel: the same split
+constexpr int kKvThreads = 512;   // backward dK/dV kernel: four threads per key row, 32 columns each
 constexpr int CHUNK = FB * 128;      // one [128 rows][64 bf16] swizzled chunk: 16 KB
 
 // Descriptor of K step kk (16 elements) of a [128][*] tile used K-major.
@@ -417,7 +418,7 @@ struct KvCfg {
 //   P^T = 2^(S^T c2 - lse), dS^T = scale * P^T (dP^T - D)   (rows = keys, in smem)
 //   dV += P^T dO_i, dK += dS^T Q_i              (TMEM columns 256.., 256+HD..)
 template <int HD>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     flash_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                         const __grid_constant__ CUtensorMap tmDS, int store_ds, const FlashArgs a,
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* d_s = lse_s + FB;
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int r = tid & (FB - 1), hf = tid >> 7;  // row of the tile, column half
+  const int r = tid & (FB - 1), hf = tid >> 7;  // row of the tile, column quarter
   const int kb = (int)(blockIdx.x / a.nz);
   const int item = (int)(blockIdx.x % a.nz);
   const int z = (int)a.zm.z(item);
@@ -486,10 +487,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bool ok = true, aborted = false;
   // column r of query block i: lse (first half of the threads) or D (second);
   // the next block's value is loaded one iteration ahead
-  const float* rowsrc = hf ? a.D : a.lse;
+  const float* rowsrc = hf == 1 ? a.D : a.lse;  // quarters 0 and 1 stage lse and D
   auto row_val = [&](int i) {
     const int qc = i * FB + r;
-    return qc < a.S ? rowsrc[(int64_t)z * a.S + qc] : 0.f;
+    return hf < 2 && qc < a.S ? rowsrc[(int64_t)z * a.S + qc] : 0.f;
   };
   // refill the stage freed by iteration it-1 with the operands of iteration it+NS-1
   auto refill = [&](int it) {
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       issue_s(it);
       if (NS > 1) refill(it);  // after the issue, so the MMAs queue back to back
     }
-    (hf ? d_s : lse_s)[r] = row_c;
+    if (hf < 2) (hf ? d_s : lse_s)[r] = row_c;
     if (ok) ok = mbar_wait(bar_s, (uint32_t)(it & 1));
     if (__syncthreads_or(!ok)) {
       aborted = true;
@@ -554,18 +555,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool diag = i == kb;
     uint8_t* pt = sm + C::OFF_PT;
     uint8_t* dst = sm + C::OFF_DS;
-    // this thread's 64 query columns, two chunks of 32
-    uint32_t svc[2][32], dvc[2][32];
-    tmem_ld32_nw(t_row + 32 * (2 * hf), svc[0]);
-    tmem_ld32_nw(t_row + FB + 32 * (2 * hf), dvc[0]);
+    // this thread's 32 query columns
+    uint32_t sv[32], dv[32];
+    tmem_ld32_nw(t_row + 32 * hf, sv);
+    tmem_ld32_nw(t_row + FB + 32 * hf, dv);
+    tmem_wait_ld();
     if constexpr (C::EARLY) {
-      // all of this block's S^T and dP^T into registers; then TMEM columns
-      // 0..255 are free and the next block's products run while this one is
-      // computed. P^T and dS^T (one buffer) are rewritten only once the
-      // previous block's dV, dK products have consumed them.
-      tmem_ld32_nw(t_row + 32 * (2 * hf + 1), svc[1]);
-      tmem_ld32_nw(t_row + FB + 32 * (2 * hf + 1), dvc[1]);
-      tmem_wait_ld();
+      // this block's S^T and dP^T are in registers: TMEM columns 0..255 are
+      // free and the next block's products run while this one is computed.
+      // P^T and dS^T (one buffer) are rewritten only once the previous
+      // block's dV, dK products have consumed them.
       tc_fence_before();
       __syncthreads();
       if (tid == 0) {
@@ -574,37 +573,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         refill(it);
       }
       if (it > 0 && ok && !mbar_wait(&bar_free[(it - 1) % NS], (uint32_t)(((it - 1) / NS) & 1))) ok = false;
-    } else {
-      // the second chunk's TMEM loads are in flight while the first is computed
-      tmem_wait_ld();
-      tmem_ld32_nw(t_row + 32 * (2 * hf + 1), svc[1]);
-      tmem_ld32_nw(t_row + FB + 32 * (2 * hf + 1), dvc[1]);
     }
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * hf + cc;
-      if (!C::EARLY && cc == 1) tmem_wait_ld();
-      const uint32_t* sv = svc[cc];
-      const uint32_t* dv = dvc[cc];
-      // the chunk's 32 lse and D values: the same addresses across the warp (broadcast)
-      float ls[32], dd[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 x = reinterpret_cast<const float4*>(lse_s + 32 * c)[k];
-        const float4 y = reinterpret_cast<const float4*>(d_s + 32 * c)[k];
-        ls[4 * k] = x.x; ls[4 * k + 1] = x.y; ls[4 * k + 2] = x.z; ls[4 * k + 3] = x.w;
-        dd[4 * k] = y.x; dd[4 * k + 1] = y.y; dd[4 * k + 2] = y.z; dd[4 * k + 3] = y.w;
-      }
-      float p[32], ds[32];
+    {
+      const int c = hf;
+      // the chunk's lse and D values are read from shared memory as they are
+      // needed (the same addresses across the warp: broadcast); P^T and dS^T
+      // overwrite the registers that held S^T and dP^T
+      const float* lsr = lse_s + 32 * c;
+      const float* ddr = d_s + 32 * c;
+      float* p = reinterpret_cast<float*>(sv);
+      float* ds = reinterpret_cast<float*>(dv);
       if (!diag && i * FB + 32 * c + 32 <= a.S) {  // every entry of the chunk is causal and in range
         const float2 c22 = make_float2(c2, c2), sc2 = make_float2(scale, scale);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
+          const float2 ls2 = *reinterpret_cast<const float2*>(lsr + e);
+          const float2 dd2 = *reinterpret_cast<const float2*>(ddr + e);
           const float2 t = fma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22,
-                                make_float2(-ls[e], -ls[e + 1]));
+                                make_float2(-ls2.x, -ls2.y));
           const float2 pv = make_float2(ex2f(t.x), ex2f(t.y));
           const float2 dq = add2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
-                                 make_float2(-dd[e], -dd[e + 1]));
+                                 make_float2(-dd2.x, -dd2.y));
           const float2 d2 = mul2(mul2(pv, sc2), dq);
           p[e] = pv.x; p[e + 1] = pv.y;
           ds[e] = d2.x; ds[e + 1] = d2.y;
@@ -614,9 +603,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 32; ++e) {
           const int qq = 32 * c + e;
           const bool valid = i * FB + qq < a.S && (!diag || qq >= r);
-          const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -ls[e])) : 0.f;
+          const float pv = valid ? ex2f(fmaf(__uint_as_float(sv[e]), c2, -lsr[e])) : 0.f;
+          const float dsv = pv * scale * (__uint_as_float(dv[e]) - ddr[e]);
           p[e] = pv;
-          ds[e] = pv * scale * (__uint_as_float(dv[e]) - dd[e]);
+          ds[e] = dsv;
         }
       }
 #pragma unroll
@@ -657,9 +647,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int b = a.zm.b(item), h = a.zm.h(item);
     const bool row_ok = key < a.S;
     const int64_t row = row_ok ? a.tm.row(b, key) * a.ldd : 0;
-    const int c0 = hf * (HD / 2);  // this thread's half of the columns
-    store_row<HD / 2>(t_row + 2 * FB + c0, row_ok, a.dv + row + a.dv_col + (int64_t)h * HD + c0, 1.f);
-    store_row<HD / 2>(t_row + 2 * FB + HD + c0, row_ok, a.dk + row + a.dk_col + (int64_t)h * HD + c0, 1.f);
+    // quarters 0, 1: the two halves of dV; quarters 2, 3: of dK
+    const int c0 = (hf & 1) * (HD / 2);
+    if (hf < 2)
+      store_row<HD / 2>(t_row + 2 * FB + c0, row_ok, a.dv + row + a.dv_col + (int64_t)h * HD + c0, 1.f);
+    else
+      store_row<HD / 2>(t_row + 2 * FB + HD + c0, row_ok, a.dk + row + a.dk_col + (int64_t)h * HD + c0, 1.f);
   } else if (tid == 0) {
     atomicOr(err, DEVERR_WAIT_TIMEOUT);
     drain(bar_kv, 1, &w_kv);
@@ -947,7 +940,7 @@ nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, c
   const bool via_gemm = a.ds && a.S % 8 == 0;
   CUtensorMap mds = mq;  // unused unless via_gemm
   if (via_gemm) NNT_TRY(make_map(&mds, a.ds, a.S, a.S, a.S, (int64_t)a.S * a.S, a.z_total, 64, FB));
-  launch_pdl(kv, (unsigned)(nqb * a.nz), kBwdThreads, KvCfg<HD>::SMEM, st, mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a,
+  launch_pdl(kv, (unsigned)(nqb * a.nz), kKvThreads, KvCfg<HD>::SMEM, st, mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a,
                                                                    nqb, c2, (float)scale, err);
   NNT_TRY(launch_check("flash_bwd_kv"));
   if (!via_gemm) {
