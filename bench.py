@@ -322,7 +322,7 @@ def run_gpu(args):
         tok, sec, cores = oracle_sample(name, 1 + rank)
         cpu = {"value": tok / sec, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"one {name} training step on 1 sequence x {S} tokens (fp64 numpy, "
-                         f"{sec:.1f} s)"}
+                         f"{sec:.1f} s; the GPU step above runs {B} sequences, both rates are per token)"}
 
     type_table = {k: {"ms_per_step": v["ms"] / 2, "launches_per_step": v["launches"] // 2,
                       **({"tflops": v["flops"] / (v["ms"] / 1e3) / 1e12} if v["flops"] else {}),
@@ -623,7 +623,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="gpt2-small", choices=sorted(WORKLOADS))
-    ap.add_argument("--streams", type=int, default=2)
+    ap.add_argument("--streams", type=int, default=3)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--fused", action="store_true", help="backward with AdamW fused in")
     ap.add_argument("--no-cpu-baseline", action="store_true")
