@@ -213,8 +213,14 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     name = args.workload
     L, d, H, f, V, S, B, dtype, tiles = WORKLOADS[name]
+    if args.tiles:
+        tiles = {**tiles, **json.loads(args.tiles)}
     dt = nnt.BF16 if dtype == "bf16" else nnt.F32
     stream = torch.cuda.Stream()
+    link = None
+    if nnt.plan_memory(L, d, H, f, V, S, B, dtype=dt, tiles=tiles, allow_host_offload=True)[1]:
+        # moments in pinned host memory: the host link bounds their AdamW tasks
+        link = host_link_peaks(torch)
     t_create = time.perf_counter()
     model = nnt.Model(L, d, H, f, V, S, B, dtype=dt, tiles=tiles, seed=1 + rank, stream=stream,
                       n_streams=args.streams, use_cuda_graph=not args.no_graph,
@@ -297,7 +303,18 @@ def run_gpu(args):
     total_ms = sum(a["ms"] for a in by_kernel.values())
     dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
     a = by_kernel[dom]
-    if a["flops"] > 0:
+    if dom == "adamw_host_moments" and link:
+        # m and v of the host-resident chunks cross the host link both ways
+        # (8 B each way per parameter); peak: pinned copies, both ways at once
+        st_now = model.stats()
+        link_bytes = (st_now["h2d_bytes"] + st_now["d2h_bytes"]) - (st["h2d_bytes"] + st["d2h_bytes"])
+        steps_run = max(args.warmup, 1) + 2 * args.steps + 2
+        achieved = link_bytes / steps_run / (a["ms"] / 2 / 1e3) / 1e9
+        roof = {"bound": "host_link", "achieved": achieved, "peak": link["both_gbs"],
+                "unit": "GB/s", "frac": achieved / link["both_gbs"], "traffic": None,
+                "kernel": dom, "peak_kind": "measured in this run: pinned cudaMemcpyAsync, "
+                "1 GiB each way at once", "host_link_gbs": link}
+    elif a["flops"] > 0:
         achieved = a["flops"] / (a["ms"] / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -387,6 +404,40 @@ def host_available():
     return 0
 
 
+def host_link_peaks(torch):
+    """Pinned cudaMemcpyAsync throughput of the host link, 1 GiB per copy, best
+    of 5 by CUDA events: host to device, device to host, and both at once (one
+    copy each way on two streams; bytes of both over the time of the pair)."""
+    n = 1 << 28
+    h_in = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    h_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    d_in = torch.empty(n, dtype=torch.float32, device="cuda")
+    d_out = torch.empty(n, dtype=torch.float32, device="cuda")
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+    link = {}
+    for name, pairs in (("h2d_gbs", ((d_in, h_in, s_up),)), ("d2h_gbs", ((h_out, d_out, s_down),)),
+                        ("both_gbs", ((d_in, h_in, s_up), (h_out, d_out, s_down)))):
+        best = 1e9
+        for _ in range(5):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _, _, st in pairs:
+                st.wait_event(e0)
+            for dst, src, st in pairs:
+                with torch.cuda.stream(st):
+                    dst.copy_(src, non_blocking=True)
+            for _, _, st in pairs:
+                torch.cuda.current_stream().wait_stream(st)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        link[name] = len(pairs) * n * 4 / (best / 1e3) / 1e9
+    del h_in, h_out, d_in, d_out
+    torch.cuda.empty_cache()
+    return link
+
+
 def run_capacity(args):
     """Each point's device and pinned-host footprint comes from the library's
     allocation plan first; only points inside both budgets are created and
@@ -398,22 +449,7 @@ def run_capacity(args):
     from tile_task_transformer_gb300 import nnt, synth
 
     gib = 1 << 30
-    # host link: pinned copies of 1 GiB, best of 5, CUDA events
-    h = torch.empty(1 << 28, dtype=torch.float32, pin_memory=True)
-    dbuf = torch.empty(1 << 28, dtype=torch.float32, device="cuda")
-    link = {}
-    for name, (dst, src) in (("h2d_gbs", (dbuf, h)), ("d2h_gbs", (h, dbuf))):
-        best = 1e9
-        for _ in range(5):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            dst.copy_(src, non_blocking=True)
-            e1.record()
-            torch.cuda.synchronize()
-            best = min(best, e0.elapsed_time(e1))
-        link[name] = h.numel() * 4 / (best / 1e3) / 1e9
-    del h, dbuf
-    torch.cuda.empty_cache()
+    link = host_link_peaks(torch)
     print(json.dumps({"capacity": "host_link", "pinned_copy_1gib": link}), flush=True)
     points = CAPACITY_POINTS
     if args.capacity_points:
@@ -624,6 +660,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="gpt2-small", choices=sorted(WORKLOADS))
     ap.add_argument("--streams", type=int, default=3)
+    ap.add_argument("--tiles", default="", help='JSON object of tile sizes that override the '
+                    'workload\'s, e.g. {"batch_tile": 2}')
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--fused", action="store_true", help="backward with AdamW fused in")
     ap.add_argument("--no-cpu-baseline", action="store_true")
