@@ -669,6 +669,320 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- dK/dV, warp-specialised (head size 64)
+
+// Sixteen compute warps (four threads per key row, 32 query columns each) and one
+// warp whose lane 0 issues every TMA copy and tensor-core product, handing off
+// through mbarriers instead of block-wide barriers, so the products of one
+// query block run while the next block's arithmetic runs:
+//
+//   issuer, block it:  S^T, dP^T of block it+1 once the compute warps hold
+//                      block it's in registers; the (Q, dO) stage of block
+//                      it-1 refilled with block it+2 once dV, dK of it-1 are
+//                      done; dV += P^T dO and dK += dS^T Q of block it once
+//                      P^T (tensor memory) and dS^T (shared memory) are
+//                      written; dS^T of block it stored to global by TMA.
+//   compute, block it: block it+1's -lse and -scale D staged in shared memory
+//                      (three buffers, so no block-wide barrier); S^T, dP^T
+//                      to registers; P^T and dS^T computed, then written
+//                      once the products of block it-1 (and the store of
+//                      block it-2's dS^T buffer) are done.
+//
+// The products are bound by shared-memory bandwidth at these sizes (N of 64
+// or 128), so the operands that can live in tensor memory do: K and V (the A
+// operands of S^T and dP^T, copied there once) and P^T (the A operand of dV).
+// Tensor memory (512 columns): S^T 0..127, dP^T 128..255, dV 256..319,
+// dK 320..383, P^T 384..447, K 448..479, V 480..511 (16-bit pairs).
+struct KvWsCfg {
+  static constexpr int HD = 64;
+  static constexpr int TILE = FB * HD * 2;
+  static constexpr int NS = 3;  // (Q, dO) stages
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_ST = 2 * TILE;
+  static constexpr int OFF_DS = OFF_ST + NS * 2 * TILE;  // two [128][128] bf16 dS^T tiles
+  static constexpr int OFF_ROW = OFF_DS + 2 * 2 * CHUNK;  // [3][-lse, -scale D][FB] floats
+  static constexpr int OFF_BAR = OFF_ROW + 3 * 2 * FB * 4;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr uint32_t T_DV = 2 * FB, T_DK = 2 * FB + HD, T_P = 2 * FB + 2 * HD;
+  static constexpr uint32_t T_K = T_P + FB / 2, T_V = T_K + HD / 2;
+};
+constexpr int kKvWsCompute = 512;
+constexpr int kKvWsThreads = kKvWsCompute + 32;
+
+__global__ void __launch_bounds__(kKvWsThreads, 1)
+    flash_bwd_kv_ws_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                           const __grid_constant__ CUtensorMap tmDS, int store_ds, const FlashArgs a,
+                           int nqb, float c2, float scale, uint32_t* err) {
+  using C = KvWsCfg;
+  constexpr int HD = C::HD, NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_kv = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* bar_ld = bar_kv + 1;      // [NS] (Q, dO) stage landed
+  uint64_t* bar_s = bar_kv + 4;       // S^T, dP^T of the current block done
+  uint64_t* bar_sfree = bar_kv + 5;   // compute warps hold S^T, dP^T in registers (16 arrivals)
+  uint64_t* bar_pready = bar_kv + 6;  // [2] P^T, dS^T of block it written (16 arrivals), by it % 2
+  uint64_t* bar_free = bar_kv + 8;    // [NS] dV, dK of a block done: its stage and buffers are free
+  uint64_t* bar_dsread = bar_kv + 11; // [2] the store of dS^T buffer b has read it
+  uint64_t* bar_o = bar_kv + 13;
+  uint64_t* bar_x = bar_kv + 14;
+  uint64_t* bar_kvt = bar_kv + 15;    // K and V copied into tensor memory (16 arrivals)
+  uint64_t* bar_rows = bar_kv + 16;   // [3] -lse, -scale D of a query block staged (16 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kv + 19);
+  float* rows = reinterpret_cast<float*>(sm + C::OFF_ROW);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kb = (int)(blockIdx.x / a.nz);
+  const int item = (int)(blockIdx.x % a.nz);
+  const int z = (int)a.zm.z(item);
+  const int n = nqb - kb;
+
+  if (tid == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_ld[s], 1);
+      mbar_init(&bar_free[s], 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, kKvWsCompute / 32);
+    mbar_init(&bar_pready[0], kKvWsCompute / 32);
+    mbar_init(&bar_pready[1], kKvWsCompute / 32);
+    mbar_init(&bar_dsread[0], 1);
+    mbar_init(&bar_dsread[1], 1);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_x, 1);
+    mbar_init(bar_kvt, kKvWsCompute / 32);
+    for (int q = 0; q < 3; ++q) mbar_init(&bar_rows[q], kKvWsCompute / 32);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the prologue above overlaps the previous kernel
+  pdl_trigger();
+
+  bool ok = true;
+  int n_ld[NS] = {0, 0, 0}, w_ld[NS] = {0, 0, 0}, w_kv = 0;  // issuer: copies issued / waited per stage
+  const bool issuer = warp == kKvWsCompute / 32;
+  const int r = tid & (FB - 1), h = (tid >> 7) & 3;  // compute warps: key row, quarter of the columns
+  const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  if (issuer) {
+    // ------------------------------------------------ TMA / MMA issue (lane 0)
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmdO);
+      auto load_qdo = [&](int s, int i) {
+        uint8_t* dst = sm + C::OFF_ST + s * 2 * C::TILE;
+        mbar_arrive_expect_tx(&bar_ld[s], 2 * C::TILE);
+        load_tile<HD>(&tmQ, dst, &bar_ld[s], i * FB, z);
+        load_tile<HD>(&tmdO, dst + C::TILE, &bar_ld[s], i * FB, z);
+        ++n_ld[s];
+      };
+      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
+      load_tile<HD>(&tmK, sm + C::OFF_K, bar_kv, kb * FB, z);
+      load_tile<HD>(&tmV, sm + C::OFF_V, bar_kv, kb * FB, z);
+      for (int it = 0; it < NS && it < n; ++it) load_qdo(it, kb + it);
+      // S^T = K Q^T and dP^T = V dO^T of block it_ into columns 0..255 (K, V from tensor memory)
+      auto issue_s = [&](int it_) {
+        const int s = it_ % NS;
+        ok = ok && mbar_wait(&bar_ld[s], (uint32_t)((it_ / NS) & 1));
+        if (!ok) return;
+        ++w_ld[s];
+        tc_fence_after();
+        const uint32_t s_qt = smem_u32(sm + C::OFF_ST + s * 2 * C::TILE), s_do = s_qt + C::TILE;
+        constexpr uint32_t idesc = make_idesc(FB, FB, false, false);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ta(tmem, tmem + C::T_K + 8 * kk, desc_k(s_qt, kk), idesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ta(tmem + FB, tmem + C::T_V + 8 * kk, desc_k(s_do, kk), idesc, kk > 0 ? 1u : 0u);
+        umma_commit(bar_s);
+      };
+      ok = mbar_wait(bar_kvt, 0);
+      issue_s(0);
+      for (int it = 0; it < n && ok; ++it) {
+        const int st = it % NS, b = it & 1;
+        if (it + 1 < n) {
+          ok = mbar_wait(bar_sfree, (uint32_t)(it & 1));
+          if (ok) {
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+        }
+        if (ok && it >= 1 && it + 2 < n) {  // stage of block it-1 <- operands of block it+2
+          ok = mbar_wait(&bar_free[(it - 1) % NS], (uint32_t)(((it - 1) / NS) & 1));
+          if (ok) load_qdo((it + 2) % NS, kb + it + 2);
+        }
+        if (ok && store_ds && it >= 1) {  // the store of dS^T(it-1) has read its buffer
+          bulk_wait_read();
+          mbar_arrive(&bar_dsread[(it - 1) & 1]);
+        }
+        if (ok) ok = mbar_wait(&bar_pready[b], (uint32_t)((it >> 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t s_qt = smem_u32(sm + C::OFF_ST + st * 2 * C::TILE), s_do = s_qt + C::TILE;
+        const uint32_t s_ds = smem_u32(sm + C::OFF_DS + b * 2 * CHUNK);
+        constexpr uint32_t idesc = make_idesc(FB, HD, false, true);
+#pragma unroll
+        for (int kk = 0; kk < FB / 16; ++kk)
+          umma_bf16_ta(tmem + C::T_DV, tmem + C::T_P + 8 * kk, desc_mn(s_do, kk), idesc,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < FB / 16; ++kk)
+          umma_bf16(tmem + C::T_DK, desc_k(s_ds, kk), desc_mn(s_qt, kk), idesc, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar_free[st]);
+        if (store_ds) {  // dS^T tile to global: rows kb*128.., columns (kb+it)*128..
+          uint8_t* dsb = sm + C::OFF_DS + b * 2 * CHUNK;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tma_store_3d(&tmDS, dsb + c * CHUNK, (kb + it) * FB + 64 * c, kb * FB, z);
+          bulk_commit();
+        }
+      }
+      if (ok) umma_commit(bar_o);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ compute warps
+    // K and V rows into tensor memory (quarters 0, 1: head columns 32h.. of K's
+    // row r; quarters 2, 3: of V's)
+    ok = mbar_wait(bar_kv, 0);
+    __syncwarp();
+    {
+      uint32_t w[16];
+      const int half = h & 1;
+      const uint8_t* src = sm + (h < 2 ? C::OFF_K : C::OFF_V) + r * 128;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int piece = (4 * half + k) ^ (r & 7);  // 128-byte swizzle of the TMA tile
+        const uint4 x = *reinterpret_cast<const uint4*>(src + (piece << 4));
+        w[4 * k] = x.x; w[4 * k + 1] = x.y; w[4 * k + 2] = x.z; w[4 * k + 3] = x.w;
+      }
+      tmem_st16(t_row + (h < 2 ? C::T_K : C::T_V) + 16 * half, w);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_kvt);
+    }
+    // -lse (quarter 0) or -scale * D (quarter 1) of query column r of block i
+    auto row_val = [&](int i) {
+      const int qc = i * FB + r;
+      if (qc >= a.S || h > 1) return 0.f;
+      const int64_t o = (int64_t)z * a.S + qc;
+      return h ? -scale * a.D[o] : -a.lse[o];
+    };
+    const float2 c22 = make_float2(c2, c2), sc2 = make_float2(scale, scale);
+    if (h < 2) rows[(2 * 0 + h) * FB + r] = row_val(kb);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_rows[0]);
+    float row_next = n > 1 ? row_val(kb + 1) : 0.f;
+    for (int it = 0; it < n; ++it) {
+      const int i = kb + it, b = it % 3;
+      if (it + 1 < n) {  // block it+1's values into buffer (it+1) % 3 (last read in block it-2)
+        if (h < 2) rows[(2 * ((it + 1) % 3) + h) * FB + r] = row_next;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_rows[(it + 1) % 3]);
+        if (it + 2 < n) row_next = row_val(i + 2);
+      }
+      ok = ok && mbar_wait(&bar_rows[b], (uint32_t)((it / 3) & 1));
+      uint32_t sv[32], dv[32];
+      ok = ok && mbar_wait(bar_s, (uint32_t)(it & 1));
+      __syncwarp();
+      tc_fence_after();
+      tmem_ld32_nw(t_row + 32 * h, sv);
+      tmem_ld32_nw(t_row + FB + 32 * h, dv);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfree);
+      // P^T = 2^(S^T c2 - lse), dS^T = P^T (scale dP^T - scale D), in place
+      const float* nls = rows + (2 * b) * FB + 32 * h;
+      const float* nds = rows + (2 * b + 1) * FB + 32 * h;
+      const int bd = it & 1;
+      float* p = reinterpret_cast<float*>(sv);
+      float* ds = reinterpret_cast<float*>(dv);
+      if (i != kb && i * FB + 32 * h + 32 <= a.S) {  // every entry causal and in range
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(nls + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(nds + e);
+          const float2 t0 = fma2(make_float2(p[e], p[e + 1]), c22, make_float2(l4.x, l4.y));
+          const float2 t1 = fma2(make_float2(p[e + 2], p[e + 3]), c22, make_float2(l4.z, l4.w));
+          const float2 p0 = make_float2(ex2f(t0.x), ex2f(t0.y)), p1 = make_float2(ex2f(t1.x), ex2f(t1.y));
+          const float2 q0 = fma2(make_float2(ds[e], ds[e + 1]), sc2, make_float2(d4.x, d4.y));
+          const float2 q1 = fma2(make_float2(ds[e + 2], ds[e + 3]), sc2, make_float2(d4.z, d4.w));
+          const float2 g0 = mul2(p0, q0), g1 = mul2(p1, q1);
+          p[e] = p0.x; p[e + 1] = p0.y; p[e + 2] = p1.x; p[e + 3] = p1.y;
+          ds[e] = g0.x; ds[e + 1] = g0.y; ds[e + 2] = g1.x; ds[e + 3] = g1.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qq = 32 * h + e;
+          const bool valid = i * FB + qq < a.S && (i != kb || qq >= r);
+          const float pv = valid ? ex2f(fmaf(p[e], c2, nls[e])) : 0.f;
+          p[e] = pv;
+          ds[e] = pv * fmaf(ds[e], scale, nds[e]);
+        }
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = pack_bf2(p[2 * e], p[2 * e + 1]);
+      // P^T's buffer was read by dV of block it-1; dS^T buffer b by dK and the store of block it-2
+      if (it >= 1) ok = ok && mbar_wait(&bar_free[(it - 1) % NS], (uint32_t)(((it - 1) / NS) & 1));
+      if (it >= 2 && store_ds) ok = ok && mbar_wait(&bar_dsread[bd], (uint32_t)(((it - 2) >> 1) & 1));
+      __syncwarp();
+      tc_fence_after();
+      tmem_st16(t_row + C::T_P + 16 * h, pk);
+      uint8_t* dsb = sm + C::OFF_DS + bd * 2 * CHUNK;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) put8(dsb, r, 4 * h + g, ds + 8 * g);
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pready[bd]);
+    }
+    ok = ok && mbar_wait(bar_o, 0);
+    __syncwarp();
+  }
+  if (__syncthreads_or(!ok)) {
+    if (issuer && lane == 0) {
+      atomicOr(err, DEVERR_WAIT_TIMEOUT);
+      drain(bar_kv, 1, &w_kv);
+      for (int s = 0; s < NS; ++s) drain(&bar_ld[s], n_ld[s], &w_ld[s]);
+      umma_commit(bar_x);
+      mbar_wait(bar_x, 0);
+    }
+  } else if (!issuer) {
+    tc_fence_after();
+    const int key = kb * FB + r;
+    const int bb = a.zm.b(item), hh = a.zm.h(item);
+    const bool row_ok = key < a.S;
+    const int64_t row = row_ok ? a.tm.row(bb, key) * a.ldd : 0;
+    // quarters 0, 1: the two halves of dV; quarters 2, 3: of dK
+    const int c0 = (h & 1) * (HD / 2);
+    if (h < 2)
+      store_row<HD / 2>(t_row + C::T_DV + c0, row_ok, a.dv + row + a.dv_col + (int64_t)hh * HD + c0, 1.f);
+    else
+      store_row<HD / 2>(t_row + C::T_DK + c0, row_ok, a.dk + row + a.dk_col + (int64_t)hh * HD + c0, 1.f);
+  }
+  if (issuer && lane == 0 && store_ds) bulk_wait_all();  // stores finished before shared memory goes
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int HD>
 struct QCfg {
   static constexpr int TILE = FB * HD * 2;
@@ -921,11 +1235,15 @@ nnt_status fwd_hd(const bf16* q, const bf16* k, const bf16* v, const FlashArgs& 
 template <int HD>
 nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, const FlashArgs& a,
                   cudaStream_t st) {
-  auto kv = flash_bwd_kv_kernel<HD>;
+  // head size 64: the warp-specialised dK/dV kernel; 128 leaves no tensor
+  // memory for the P^T buffers and takes the block-synchronous one
+  auto kv = HD == 64 ? flash_bwd_kv_ws_kernel : flash_bwd_kv_kernel<HD>;
+  const int kv_smem = HD == 64 ? KvWsCfg::SMEM : KvCfg<HD>::SMEM;
+  const int kv_threads = HD == 64 ? kKvWsThreads : kKvThreads;
   auto qk = flash_bwd_q_kernel<HD>;
   static std::once_flag once_kv, once_q;
   static cudaError_t attr_kv = cudaSuccess, attr_q = cudaSuccess;
-  NNT_TRY(allow_smem(kv, KvCfg<HD>::SMEM, once_kv, attr_kv));
+  NNT_TRY(allow_smem(kv, kv_smem, once_kv, attr_kv));
   NNT_TRY(allow_smem(qk, QCfg<HD>::SMEM, once_q, attr_q));
   CUtensorMap mq, mk, mv, mdo;
   NNT_TRY(qkv_maps(a, q, k, v, &mq, &mk, &mv));
@@ -940,8 +1258,8 @@ nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, c
   const bool via_gemm = a.ds && a.S % 8 == 0;
   CUtensorMap mds = mq;  // unused unless via_gemm
   if (via_gemm) NNT_TRY(make_map(&mds, a.ds, a.S, a.S, a.S, (int64_t)a.S * a.S, a.z_total, 64, FB));
-  launch_pdl(kv, (unsigned)(nqb * a.nz), kKvThreads, KvCfg<HD>::SMEM, st, mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a,
-                                                                   nqb, c2, (float)scale, err);
+  launch_pdl(kv, (unsigned)(nqb * a.nz), kv_threads, kv_smem, st, mq, mk, mv, mdo, mds, via_gemm ? 1 : 0, a, nqb,
+             c2, (float)scale, err);
   NNT_TRY(launch_check("flash_bwd_kv"));
   if (!via_gemm) {
     launch_pdl(qk, (unsigned)(nqb * a.nz), kBwdThreads, QCfg<HD>::SMEM, st, mq, mk, mv, mdo, a, nqb, c2, (float)scale, err);
