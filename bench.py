@@ -227,7 +227,7 @@ def run_gpu(args):
                       allow_host_offload=True)
     t_create = time.perf_counter() - t_create
     st = model.stats()
-    fused = args.fused or st["offload_active"] == 1
+    fused = not args.separate or st["offload_active"] == 1
     T = B * S
     win_host = synth.token_windows(1 + rank, B, S, V)
     tok_dev = torch.as_tensor(win_host.view(np.int16)).to("cuda")
@@ -659,11 +659,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="gpt2-small", choices=sorted(WORKLOADS))
-    ap.add_argument("--streams", type=int, default=3)
+    ap.add_argument("--streams", type=int, default=4)
     ap.add_argument("--tiles", default="", help='JSON object of tile sizes that override the '
                     'workload\'s, e.g. {"batch_tile": 2}')
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--fused", action="store_true", help="backward with AdamW fused in")
+    ap.add_argument("--separate", action="store_true",
+                    help="backward, then AdamW over all parameters (default: AdamW fused into the "
+                    "backward, each parameter chunk updated once its gradient is final)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="tile-kernel sweep instead of the step")
     ap.add_argument("--capacity", action="store_true",

@@ -9,19 +9,22 @@
 // memory, and nothing of size S x S is written to HBM. The backward pass
 // recomputes P from the per-row log-sum-exp saved by the forward.
 //
-// The tensor-core kernels run 256 threads (8 warps): threads t and t+128 own
-// row t of the current tile, which is TMEM lane t (warp w reads lanes
-// 32(w%4)..32(w%4)+31), each taking one half of the row's columns. Thread 0
-// also issues the TMA copies and the tcgen05.mma instructions; the other
-// threads only wait for their results. Tiles are [128 rows][hd] bf16 loaded by TMA
-// with a 128-byte swizzle as hd/64 chunks of 16 KB; the same smem tile serves
+// The forward and the head-size-128 backward kernels are block-synchronous:
+// threads t, t+128, ... own row t of the current tile, which is TMEM lane t
+// (warp w reads lanes 32(w%4)..32(w%4)+31), each taking a share of the row's
+// columns; thread 0 also issues the TMA copies and the tcgen05.mma
+// instructions. The head-size-64 dK/dV kernel is warp-specialised (one issuing
+// warp, sixteen compute warps, mbarrier hand-offs). Tiles are [128 rows][hd]
+// bf16 loaded by TMA with a 128-byte swizzle as hd/64 chunks of 16 KB; the same
+// smem tile serves
 // as a K-major operand (rows = M or N, K = hd) or an MN-major one (N = hd,
 // K = rows) through its descriptor. P and dS tiles written by the threads use
 // the K-major layout TMA would produce.
 //
 //   flash_fwd_kernel     item x query block: O and the log-sum-exp
 //   flash_bwd_d_kernel   D = rowsum(dO * O)
-//   flash_bwd_kv_kernel  item x key block: dK, dV over the query blocks at or after it,
+//   flash_bwd_kv_ws_kernel / flash_bwd_kv_kernel (head size 64 / 128)
+//                        item x key block: dK, dV over the query blocks at or after it,
 //                        and (given a dS^T buffer) each dS^T tile stored by TMA, after
 //                        which dQ = dS K is the causal tensor-core GEMM
 //   flash_bwd_q_kernel   item x query block: dQ over the key blocks at or before it
@@ -401,10 +404,9 @@ __global__ void __launch_bounds__(256) flash_bwd_d_kernel(const bf16* __restrict
 template <int HD>
 struct KvCfg {
   static constexpr int TILE = FB * HD * 2;
-  // head size 64: three stages of (Q, dO), and the next query block's S^T and
-  // dP^T are issued as soon as this block's are in registers (EARLY)
-  static constexpr bool EARLY = HD <= 64;
-  static constexpr int NS = HD <= 64 ? 3 : 1;  // stages of (Q, dO)
+  // head size 128 (64 takes the warp-specialised kernel): one (Q, dO) stage,
+  // tensor memory full with S^T, dP^T, dV and dK
+  static constexpr int NS = 1;
   static constexpr int OFF_K = 0, OFF_V = TILE, OFF_ST = 2 * TILE;  // stage s: Q, then dO
   static constexpr int OFF_PT = OFF_ST + NS * 2 * TILE, OFF_DS = OFF_PT + 2 * CHUNK;
   static constexpr int OFF_ROW = OFF_DS + 2 * CHUNK;  // lse and D of the current query block
@@ -524,11 +526,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       umma_commit(bar_s);
     }
   };
-  if (C::EARLY && tid == 0) {
-    ok = mbar_wait(bar_kv, 0);
-    w_kv = ok ? 1 : 0;
-    issue_s(0);
-  }
   float row_next = row_val(kb);
   for (int it = 0; it < n; ++it) {
     const int i = kb + it, st = it % NS;
@@ -536,14 +533,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (it + 1 < n) row_next = row_val(i + 1);
     // the previous dS^T tile must have left shared memory before it is rewritten
     if (store_ds && tid == 32 && it > 0) bulk_wait_read();
-    if (!C::EARLY && tid == 0) {
+    if (tid == 0) {
       if (it == 0) {
         ok = mbar_wait(bar_kv, 0);
         w_kv = ok ? 1 : 0;
       }
-      if (NS == 1) refill(it);  // single stage: the operands of this iteration
+      refill(it);  // single stage: the operands of this iteration
       issue_s(it);
-      if (NS > 1) refill(it);  // after the issue, so the MMAs queue back to back
     }
     if (hf < 2) (hf ? d_s : lse_s)[r] = row_c;
     if (ok) ok = mbar_wait(bar_s, (uint32_t)(it & 1));
@@ -560,20 +556,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     tmem_ld32_nw(t_row + 32 * hf, sv);
     tmem_ld32_nw(t_row + FB + 32 * hf, dv);
     tmem_wait_ld();
-    if constexpr (C::EARLY) {
-      // this block's S^T and dP^T are in registers: TMEM columns 0..255 are
-      // free and the next block's products run while this one is computed.
-      // P^T and dS^T (one buffer) are rewritten only once the previous
-      // block's dV, dK products have consumed them.
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
-        if (it + 1 < n) issue_s(it + 1);
-        refill(it);
-      }
-      if (it > 0 && ok && !mbar_wait(&bar_free[(it - 1) % NS], (uint32_t)(((it - 1) / NS) & 1))) ok = false;
-    }
     {
       const int c = hf;
       // the chunk's lse and D values are read from shared memory as they are
@@ -1236,10 +1218,19 @@ template <int HD>
 nnt_status bwd_hd(const bf16* q, const bf16* k, const bf16* v, const bf16* dO, const FlashArgs& a,
                   cudaStream_t st) {
   // head size 64: the warp-specialised dK/dV kernel; 128 leaves no tensor
-  // memory for the P^T buffers and takes the block-synchronous one
-  auto kv = HD == 64 ? flash_bwd_kv_ws_kernel : flash_bwd_kv_kernel<HD>;
-  const int kv_smem = HD == 64 ? KvWsCfg::SMEM : KvCfg<HD>::SMEM;
-  const int kv_threads = HD == 64 ? kKvWsThreads : kKvThreads;
+  // memory for K, V and P^T and takes the block-synchronous one
+  void (*kv)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, int, FlashArgs, int, float,
+             float, uint32_t*);
+  int kv_smem, kv_threads;
+  if constexpr (HD == 64) {
+    kv = flash_bwd_kv_ws_kernel;
+    kv_smem = KvWsCfg::SMEM;
+    kv_threads = kKvWsThreads;
+  } else {
+    kv = flash_bwd_kv_kernel<HD>;
+    kv_smem = KvCfg<HD>::SMEM;
+    kv_threads = kKvThreads;
+  }
   auto qk = flash_bwd_q_kernel<HD>;
   static std::once_flag once_kv, once_q;
   static cudaError_t attr_kv = cudaSuccess, attr_q = cudaSuccess;
