@@ -75,6 +75,8 @@ def inputs(seed, Z, S, hd, qscale=1.0):
     (3, 128, 64),     # one block
     (2, 200, 64),     # ragged tail inside the second block
     (4, 513, 64),     # five blocks, one-row tail
+    (3, 1024, 64),    # eight blocks: every operand stage and buffer of the pipelined
+                      # dK/dV kernel is reused (S a multiple of 8: dS^T stored, dQ by GEMM)
     (2, 384, 128),    # head size 128, three blocks
     (2, 257, 128),    # head size 128, ragged
     (1, 1, 64),       # a single position: O = v, all gradients but dv zero
