@@ -5,8 +5,8 @@
 // "Minimal working GPT example", flag list). Here it is a tile task of its
 // own: the score tile S = Q K^T / sqrt(hd) of one (sequence, head) and 128
 // queries lives in tensor memory, the causal softmax is taken row by row with
-// a running maximum and sum (online softmax), P reaches P V through shared
-// memory, and nothing of size S x S is written to HBM. The backward pass
+// a running maximum and sum (online softmax), P reaches P V through tensor
+// memory (the product's A operand), and nothing of size S x S is written to HBM. The backward pass
 // recomputes P from the per-row log-sum-exp saved by the forward.
 //
 // The forward and the head-size-128 backward kernels are block-synchronous:
@@ -115,8 +115,8 @@ __device__ __forceinline__ void drain(uint64_t* bar, int n, int* w) {
 template <int HD>
 struct FwdCfg {
   static constexpr int TILE = FB * HD * 2;
-  // Q, K (two stages), V (two stages), P. The halves' row maxima and sums
-  // ([2][128] floats) borrow the start of P while P is free.
+  // Q, K (two stages), V (two stages), and scratch for the halves' row maxima
+  // and sums ([2][128] floats).
   static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE;
   static constexpr int OFF_RED = OFF_P;
   static constexpr int OFF_BAR = OFF_P + 2 * CHUNK;
@@ -124,7 +124,9 @@ struct FwdCfg {
   // on an SM; the kernel then requires a 1024-byte aligned dynamic base
   static constexpr bool FIXED_BASE = HD <= 64;
   static constexpr int SMEM = OFF_BAR + 128 + (FIXED_BASE ? 0 : 1024);
-  static constexpr uint32_t TMEM_COLS = FB + HD <= 256 ? 256 : 512;  // S: 128 columns, O: HD
+  // S: 128 columns, O: HD, P (bf16 pairs, the A operand of P V): 64
+  static constexpr uint32_t T_O = FB, T_P = FB + HD;
+  static constexpr uint32_t TMEM_COLS = FB + HD + FB / 2 <= 256 ? 256 : 512;
 };
 
 // Per CTA: item blockIdx % nz, query block nqb-1 - blockIdx / nz (largest
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
   pdl_wait();  // the prologue above overlaps the previous kernel
   pdl_trigger();
   const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_v = smem_u32(sm + C::OFF_V), s_p = smem_u32(sm + C::OFF_P);
+  const uint32_t s_q = smem_u32(sm + C::OFF_Q), s_v = smem_u32(sm + C::OFF_V);
   constexpr int HC = FB / 2;  // score columns per thread
   constexpr int HO = HD / 2;  // O columns per thread
 
@@ -299,22 +301,18 @@ __global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
     }
     float2 sum2 = make_float2(0.f, 0.f);
     const float2 c22 = make_float2(c2, c2), mm = make_float2(-m_used, -m_used);
-    uint8_t* pt = sm + C::OFF_P;
+    // P in bf16 pairs into tensor memory (this thread: keys hf*HC.., columns T_P + hf*HC/2..)
+    uint32_t pk[HC / 2];
 #pragma unroll
-    for (int g = 0; g < HC / 8; ++g) {
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const float2 t = fma2(make_float2(__uint_as_float(u[8 * g + e]), __uint_as_float(u[8 * g + e + 1])), c22, mm);
-        const float2 pv = make_float2(ex2f(t.x), ex2f(t.y));
-        v[e] = pv.x;
-        v[e + 1] = pv.y;
-        sum2 = add2(sum2, pv);
-      }
-      put8(pt, r, hf * (HC / 8) + g, v);
+    for (int e = 0; e < HC; e += 2) {
+      const float2 t = fma2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), c22, mm);
+      const float2 pv = make_float2(ex2f(t.x), ex2f(t.y));
+      sum2 = add2(sum2, pv);
+      pk[e / 2] = pack_bf2(pv.x, pv.y);
     }
+    tmem_st32(t_row + C::T_P + hf * (HC / 2), pk);
     l += sum2.x + sum2.y;
-    fence_async_smem();
+    tmem_wait_st();
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
@@ -326,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, HD <= 64 ? 2 : 1)
         constexpr uint32_t idesc = make_idesc(FB, HD, false, true);
 #pragma unroll
         for (int kk = 0; kk < FB / 16; ++kk)
-          umma_bf16(tmem + FB, desc_k(s_p, kk), desc_mn(s_vt, kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ta(tmem + C::T_O, tmem + C::T_P + 8 * kk, desc_mn(s_vt, kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
       }
     }
   }
